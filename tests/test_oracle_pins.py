@@ -1,0 +1,469 @@
+"""Pins for the fp64 oracle against what the pages and mathematics fix.
+
+Each test ties one oracle function to something other than itself: values
+printed on the pages (tests/golden/), closed forms, exact rational
+enumeration, chi-square tests over seeded draws, and finite differences.
+"""
+
+import itertools
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import spec_oracle as so
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "worked_examples.json")
+
+
+def _rand_dist(rng, V, spiky=1.0):
+    z = rng.standard_normal(V) * spiky
+    return so.softmax_t(z, 1.0)
+
+
+# ---------------------------------------------------------------------------
+# softmax
+# ---------------------------------------------------------------------------
+
+def test_softmax_sums_to_one_and_is_shift_invariant():
+    rng = np.random.default_rng(1)
+    for V in (1, 2, 7, 1000):
+        z = rng.standard_normal(V) * 3
+        for T in (0.3, 1.0, 2.5):
+            p = so.softmax_t(z, T)
+            assert abs(p.sum() - 1.0) < 1e-12
+            assert np.all(p >= 0)
+            assert np.allclose(so.softmax_t(z + 17.25, T), p, rtol=1e-12, atol=0)
+
+
+def test_softmax_closed_form_two_tokens():
+    # p(0) = 1 / (1 + exp((z1 - z0)/T)) (logistic function)
+    for d, T in ((0.0, 1.0), (1.5, 0.7), (-3.0, 2.0)):
+        p = so.softmax_t(np.array([0.0, d]), T)
+        assert abs(p[0] - 1.0 / (1.0 + math.exp(d / T))) < 1e-15
+
+
+def test_softmax_rejects_zero_temperature():
+    with pytest.raises(ValueError):
+        so.softmax_t(np.zeros(3), 0.0)
+
+
+# ---------------------------------------------------------------------------
+# overlap / TV
+# ---------------------------------------------------------------------------
+
+def test_overlap_equals_one_minus_tv():
+    rng = np.random.default_rng(2)
+    for V in (2, 5, 300):
+        for _ in range(20):
+            p, q = _rand_dist(rng, V, 2.0), _rand_dist(rng, V, 2.0)
+            a = so.overlap(p, q)
+            assert abs(a - (1.0 - so.tv_distance(p, q))) < 1e-12
+            assert 0.0 <= a <= 1.0 + 1e-15
+            assert abs(a - so.overlap(q, p)) < 1e-15
+
+
+def test_overlap_one_iff_equal_and_zero_for_disjoint():
+    p = np.array([0.25, 0.25, 0.5, 0.0])
+    assert so.overlap(p, p) == pytest.approx(1.0, abs=1e-15)
+    assert so.overlap(np.array([1.0, 0.0]), np.array([0.0, 1.0])) == 0.0
+    q = np.array([0.25, 0.25, 0.25, 0.25])
+    assert so.overlap(p, q) == pytest.approx(0.75, abs=1e-15)
+
+
+def test_overlap_is_expected_acceptance_exact():
+    # alpha_RS = E_{y~q}[min(1, p(y)/q(y))] = sum min(p, q), in exact rationals
+    p = np.array([Fraction(1, 2), Fraction(1, 3), Fraction(1, 6), Fraction(0)], dtype=object)
+    q = np.array([Fraction(1, 5), Fraction(1, 5), Fraction(1, 5), Fraction(2, 5)], dtype=object)
+    e = sum(q[y] * min(Fraction(1), p[y] / q[y]) for y in range(4))
+    assert so.overlap(p, q) == e == Fraction(1, 5) + Fraction(1, 5) + Fraction(1, 6)
+    assert so.tv_distance(p, q) == 1 - e
+
+
+def test_residual_decomposition_recovers_target():
+    # accepted path min(p,q) plus rejected path (1-alpha) * residual equals p
+    rng = np.random.default_rng(3)
+    for V in (3, 50, 4000):
+        p, q = _rand_dist(rng, V, 1.5), _rand_dist(rng, V, 1.5)
+        a = so.overlap(p, q)
+        rho = so.residual(p, q)
+        assert abs(rho.sum() - (1.0 - a)) < 1e-12
+        assert np.allclose(np.minimum(p, q) + (1.0 - a) * rho / rho.sum(), p, rtol=0, atol=1e-15)
+    pf = np.array([Fraction(3, 10), Fraction(3, 10), Fraction(2, 5)], dtype=object)
+    qf = np.array([Fraction(1, 2), Fraction(1, 4), Fraction(1, 4)], dtype=object)
+    rf = so.residual(pf, qf)
+    af = so.overlap(pf, qf)
+    assert list(np.minimum(pf, qf) + (1 - af) * rf / rf.sum()) == list(pf)
+
+
+# ---------------------------------------------------------------------------
+# inverse CDF
+# ---------------------------------------------------------------------------
+
+def test_inverse_cdf_uniform_weights_closed_form():
+    # equal weights: index floor(u * V)
+    V = 7
+    for u in (0.0, 0.01, 0.2, 0.5, 0.86, 0.999):
+        v, _ = so.inverse_cdf(np.ones(V), u)
+        assert v == math.floor(u * V)
+
+
+def test_inverse_cdf_skips_zero_weights_and_one_hot():
+    w = np.array([0.0, 0.0, 2.0, 0.0, 1.0, 0.0])
+    for u in np.linspace(0, 0.999, 50):
+        v, _ = so.inverse_cdf(w, u)
+        assert w[v] > 0
+        assert v == (2 if u < 2.0 / 3.0 else 4)
+    assert so.inverse_cdf(np.array([0.0, 5.0, 0.0]), 0.9999)[0] == 1
+
+
+def test_inverse_cdf_near_flag():
+    w = np.array([1.0, 1.0])
+    assert so.inverse_cdf(w, 0.5 - 1e-7)[1]
+    assert not so.inverse_cdf(w, 0.25)[1]
+
+
+# ---------------------------------------------------------------------------
+# worked examples printed on the pages
+# ---------------------------------------------------------------------------
+
+def test_worked_examples_expected_emitted():
+    g = json.load(open(GOLDEN))
+    for ex in g["expected_emitted"]:
+        assert np.allclose(so.prefix_survival(ex["alpha"]), ex["prefix_survival"], atol=1e-12), ex["cite"]
+        assert abs(so.expected_emitted(ex["alpha"]) - ex["value"]) < 1e-12, ex["cite"]
+        assert abs(so.expected_accepted(ex["alpha"]) - (ex["value"] - 1)) < 1e-12
+
+
+def test_worked_examples_speedup():
+    g = json.load(open(GOLDEN))
+    for ex in g["speedup"]:
+        s = so.speedup_estimate(ex["alpha"], ex["t_ar"], ex["t_draft"], ex["t_verify"], ex["t_overhead"])
+        assert abs(s - ex["value"]) < ex["tol"], ex["cite"]
+
+
+# ---------------------------------------------------------------------------
+# exact rational enumeration of the verify sampler
+# ---------------------------------------------------------------------------
+
+def _enumerate_outputs(p, q):
+    """Exact output distribution of oracle.accept_and_correct, by evaluating it
+    at one representative uniform inside every interval on which its decisions
+    are constant, weighted by the interval's length and by prod q_k(y_k)."""
+    K = len(q)
+    V = len(q[0])
+    dist = {}
+    for ys in itertools.product(range(V), repeat=K):
+        py = Fraction(1)
+        for k in range(K):
+            py *= q[k][ys[k]]
+        if py == 0:
+            continue
+        # acceptance uniform: accept on [0, r], reject on (r, 1)
+        choices = []
+        for k in range(K):
+            r = p[k][ys[k]] / q[k][ys[k]]
+            opts = []
+            if r > 0:
+                m = min(r, Fraction(1))
+                opts.append((m / 2, m))
+            if r < 1:
+                opts.append(((r + 1) / 2, 1 - r))
+            choices.append(opts)
+        for combo in itertools.product(*choices):
+            us = [c[0] for c in combo]
+            wu = Fraction(1)
+            for c in combo:
+                wu *= c[1]
+            # final uniform: midpoints of the 4V intervals between every CDF
+            # boundary that any draw could use (fine enough for all of them)
+            bounds = set([Fraction(0), Fraction(1)])
+            for k in range(K + 1):
+                w = p[k] if k == K else so.residual(p[k], q[k])
+                tot = w.sum()
+                if tot > 0:
+                    c = Fraction(0)
+                    for x in w:
+                        c += x
+                        bounds.add(c / tot)
+            bl = sorted(bounds)
+            for lo, hi in zip(bl[:-1], bl[1:]):
+                if hi == lo:
+                    continue
+                uf = (lo + hi) / 2
+                toks, n, *_ = so.accept_and_correct(p, q, list(ys), us, uf)
+                key = (tuple(toks), n)
+                dist[key] = dist.get(key, Fraction(0)) + py * wu * (hi - lo)
+    return dist
+
+
+def _frac_dist(vals):
+    vals = [int(v) for v in vals]
+    s = sum(vals)
+    return np.array([Fraction(v, s) for v in vals], dtype=object)
+
+
+@pytest.mark.parametrize("K", [1, 2, 3])
+def test_exact_enumeration_matches_target(K):
+    V = 3 if K == 3 else 4
+    rng = np.random.default_rng(10 + K)
+    p = [_frac_dist(list(rng.integers(0, 6, V) + (np.arange(V) == k))) for k in range(K + 1)]
+    q = [_frac_dist(list(rng.integers(1, 6, V))) for k in range(K)]
+    dist = _enumerate_outputs(p, q)
+    assert sum(dist.values()) == 1
+    alpha = [so.overlap(p[k], q[k]) for k in range(K)]
+    # P(n >= j) = prod_{k<=j} alpha_k exactly (positions independent here)
+    for j in range(K + 1):
+        pj = sum(w for (toks, n), w in dist.items() if n >= j)
+        want = Fraction(1)
+        for k in range(j):
+            want *= alpha[k]
+        assert pj == want
+    # the token emitted at position j, given the cycle reaches j, follows p_j
+    for j in range(K + 1):
+        reach = sum(w for (toks, n), w in dist.items() if n >= j)
+        for v in range(V):
+            pv = sum(w for (toks, n), w in dist.items() if n >= j and toks[j] == v)
+            assert pv == reach * p[j][v]
+
+
+def test_exact_enumeration_detects_full_p_resample(monkeypatch):
+    # planted mistake: resample the correction from the full target p
+    p = [_frac_dist([1, 2, 3]), _frac_dist([3, 2, 1])]
+    q = [_frac_dist([3, 2, 1])]
+    monkeypatch.setattr(so, "residual", lambda pp, qq: pp.copy())
+    dist = _enumerate_outputs(p, q)
+    p0 = sum(w for (toks, n), w in dist.items() if toks[0] == 2)
+    assert p0 != p[0][2]
+
+
+# ---------------------------------------------------------------------------
+# chi-square over 1e6 seeded draws
+# ---------------------------------------------------------------------------
+
+N_DRAWS = 1_000_000
+
+
+def _draws(p, q, n, seed):
+    rng = np.random.default_rng(seed)
+    K = len(q)
+    cq = [np.cumsum(qk) for qk in q]
+    ys = np.stack([np.minimum(np.searchsorted(cq[k], rng.random(n), side="right"), len(q[k]) - 1)
+                   for k in range(K)], axis=1)
+    ua = rng.random((n, K))
+    uf = rng.random(n)
+    toks = np.full((n, K + 1), -1, dtype=np.int64)
+    ns = np.zeros(n, dtype=np.int64)
+    for i in range(n):
+        t, m, *_ = so.accept_and_correct(p, q, ys[i], ua[i], uf[i])
+        toks[i] = t
+        ns[i] = m
+    return toks, ns
+
+
+@pytest.fixture(scope="module")
+def chi_case():
+    rng = np.random.default_rng(42)
+    V, K = 4, 2
+    p = [_rand_dist(rng, V, 1.0) for _ in range(K + 1)]
+    q = [_rand_dist(rng, V, 1.0) for _ in range(K)]
+    toks, ns = _draws(p, q, N_DRAWS, seed=2024)
+    return p, q, toks, ns
+
+
+def _chi2_pvalue(counts, probs):
+    from scipy.stats import chisquare
+    counts = np.asarray(counts, dtype=np.float64)
+    exp = np.asarray(probs, dtype=np.float64) * counts.sum()
+    keep = exp > 0
+    assert counts[~keep].sum() == 0
+    return chisquare(counts[keep], exp[keep]).pvalue
+
+
+@pytest.mark.slow
+def test_chi_square_output_distribution(chi_case):
+    p, q, toks, ns = chi_case
+    K = len(q)
+    V = len(p[0])
+    alpha = [so.overlap(p[k], q[k]) for k in range(K)]
+    # first emitted token ~ p_1
+    assert _chi2_pvalue(np.bincount(toks[:, 0], minlength=V), p[0]) > 1e-3
+    # emitted token at position j given the cycle reaches j ~ p_j
+    for j in range(1, K + 1):
+        sel = ns >= j
+        assert _chi2_pvalue(np.bincount(toks[sel, j], minlength=V), p[j]) > 1e-3
+    # number accepted: P(n = j) = prod_{k<=j} alpha_k * (1 - alpha_{j+1})
+    surv = [1.0] + so.prefix_survival(alpha)
+    pn = [surv[j] - (surv[j + 1] if j < K else 0.0) for j in range(K + 1)]
+    assert _chi2_pvalue(np.bincount(ns, minlength=K + 1), pn) > 1e-3
+    # mean emitted length matches 1 + sum prod alpha within 3 sigma
+    emitted = ns + 1
+    se = emitted.std() / math.sqrt(len(emitted))
+    assert abs(emitted.mean() - so.expected_emitted(alpha)) < 3 * se
+
+
+@pytest.mark.slow
+def test_chi_square_rejects_full_p_resample(monkeypatch):
+    # planted mistake in the oracle: after a rejection, resample from full p
+    rng = np.random.default_rng(7)
+    V, K = 4, 1
+    p = [_rand_dist(rng, V, 1.5) for _ in range(K + 1)]
+    q = [_rand_dist(rng, V, 1.5) for _ in range(K)]
+    monkeypatch.setattr(so, "residual", lambda pp, qq: pp.copy())
+    toks, ns = _draws(p, q, 200_000, seed=5)
+    assert _chi2_pvalue(np.bincount(toks[:, 0], minlength=V), p[0]) < 1e-6
+
+
+# ---------------------------------------------------------------------------
+# greedy
+# ---------------------------------------------------------------------------
+
+def test_greedy_equals_argmax_and_first_mismatch():
+    rng = np.random.default_rng(4)
+    K, V = 4, 50
+    zt = rng.standard_normal((1, K + 1, V))
+    am = zt[0].argmax(axis=1)
+    draft = am[:K].copy()
+    draft[2] = (am[2] + 1) % V
+    r = oracle.verify(zt, None, draft[None], np.zeros((1, K)), np.zeros(1), 0.0)
+    assert r.n_accepted[0] == 2
+    assert list(r.tokens[0]) == [am[0], am[1], am[2], -1, -1]
+    r2 = oracle.verify(zt, None, am[None, :K], np.zeros((1, K)), np.zeros(1), 0.0)
+    assert r2.n_accepted[0] == K and list(r2.tokens[0]) == list(am)
+
+
+def test_greedy_ties_take_smallest_index():
+    z = np.array([[[1.0, 3.0, 3.0, 0.0], [2.0, 2.0, 1.0, 2.0]]])
+    r = oracle.verify(z, None, np.array([[2]]), np.zeros((1, 1)), np.zeros(1), 0.0)
+    assert list(r.tokens[0]) == [1, -1] and r.n_accepted[0] == 0
+    r = oracle.verify(z, None, np.array([[1]]), np.zeros((1, 1)), np.zeros(1), 0.0)
+    assert list(r.tokens[0]) == [1, 0]
+
+
+def test_greedy_is_zero_temperature_limit():
+    rng = np.random.default_rng(5)
+    B, K, V = 20, 3, 12
+    # well separated logits: at T=0.01 every distribution is one-hot to 1e-40
+    zt = np.stack([np.stack([rng.permutation(V).astype(np.float64) for _ in range(K + 1)])
+                   for _ in range(B)])
+    zd = np.where(rng.random((B, K, 1)) < 0.5, zt[:, :K], zt[:, :K][:, :, ::-1])
+    draft = zd.argmax(axis=2)
+    ua = rng.random((B, K)).astype(np.float32)
+    uf = rng.random(B).astype(np.float32)
+    g = oracle.verify(zt, zd, draft, ua, uf, 0.0)
+    s = oracle.verify(zt, zd, draft, ua, uf, 0.01)
+    assert (g.tokens == s.tokens).all() and (g.n_accepted == s.n_accepted).all()
+    assert np.allclose(g.alpha, s.alpha, atol=1e-12)
+
+
+def test_identical_logits_accept_everything():
+    rng = np.random.default_rng(6)
+    B, K, V = 8, 5, 30
+    zt = rng.standard_normal((B, K + 1, V)) * 2
+    zd = zt[:, :K].copy()
+    draft = rng.integers(0, V, (B, K))
+    ua = rng.random((B, K)).astype(np.float32)
+    uf = rng.random(B).astype(np.float32)
+    r = oracle.verify(zt, zd, draft, ua, uf, 0.8)
+    assert (r.n_accepted == K).all()
+    assert (r.tokens[:, :K] == draft).all()
+    assert np.allclose(r.alpha, 1.0, atol=1e-12)
+    # the bonus follows p_{K+1}'s inverse CDF at u'
+    for b in range(B):
+        v, _ = so.inverse_cdf(so.softmax_t(zt[b, K], 0.8), float(uf[b]))
+        assert r.tokens[b, K] == v
+
+
+def test_zero_draft_probability_always_accepts():
+    p = [np.array([0.5, 0.5]), np.array([1.0, 0.0])]
+    q = [np.array([1.0, 0.0])]
+    toks, n, *_ = so.accept_and_correct(p, q, [1], [0.999], 0.3)
+    assert n == 1 and toks[0] == 1
+
+
+def test_K_zero_is_plain_sampling():
+    z = np.log(np.array([[[0.1, 0.2, 0.7]]]))
+    # CDF of p = (0.1, 0.3, 1.0): u' = 0.25 -> index 1, u' = 0.35 -> index 2
+    for uf, want in ((0.05, 0), (0.25, 1), (0.35, 2)):
+        r = oracle.verify(z, np.zeros((1, 0, 3)), np.zeros((1, 0), dtype=np.int64),
+                          np.zeros((1, 0)), np.array([uf]), 1.0)
+        assert r.n_accepted[0] == 0 and list(r.tokens[0]) == [want]
+
+
+# ---------------------------------------------------------------------------
+# overlap statistics
+# ---------------------------------------------------------------------------
+
+def test_overlap_stats_prefix_products():
+    rng = np.random.default_rng(8)
+    zt = rng.standard_normal((3, 4, 20))
+    zd = zt + rng.standard_normal((3, 4, 20)) * 0.5
+    o = oracle.overlap_stats(zt, zd, 1.0)
+    assert np.allclose(o.alpha, 1 - o.tv, atol=1e-12)
+    assert np.allclose(o.prefix_survival, np.cumprod(o.alpha, axis=1), atol=1e-15)
+    assert np.allclose(o.expected_accepted, o.prefix_survival.sum(axis=1), atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# E2E-TV loss and gradient
+# ---------------------------------------------------------------------------
+
+def test_e2e_loss_single_position_is_alpha():
+    rng = np.random.default_rng(9)
+    zt = rng.standard_normal((5, 1, 40))
+    zd = rng.standard_normal((5, 1, 40))
+    L, a = oracle.e2e_tv_loss(zt, zd, 1.3)
+    assert abs(L - a[:, 0].mean()) < 1e-15
+    for b in range(5):
+        p, q = so.softmax_t(zt[b, 0], 1.3), so.softmax_t(zd[b, 0], 1.3)
+        assert abs(a[b, 0] - (1 - so.tv_distance(p, q))) < 1e-12
+
+
+def test_e2e_loss_worked_example_structure():
+    # with constant alpha the loss is sum_j alpha^j (page's prefix-product form)
+    zt = np.zeros((2, 4, 6))
+    zd = np.zeros((2, 4, 6))
+    L, a = oracle.e2e_tv_loss(zt, zd, 1.0)
+    assert np.allclose(a, 1.0) and abs(L - 4.0) < 1e-12
+
+
+@pytest.mark.parametrize("T", [1.0, 0.6])
+def test_e2e_grad_matches_finite_differences(T):
+    rng = np.random.default_rng(11)
+    B, K, V = 2, 3, 6
+    zt = rng.standard_normal((B, K, V)) * 1.5
+    zd = zt + rng.standard_normal((B, K, V)) * 0.8
+    g, amb = oracle.e2e_tv_grad(zt, zd, T, grad_scale=-1.0)
+    assert not amb.any()
+    h = 1e-6
+    num = np.zeros_like(zd)
+    for idx in np.ndindex(*zd.shape):
+        zp = zd.copy()
+        zp[idx] += h
+        zm = zd.copy()
+        zm[idx] -= h
+        num[idx] = -(oracle.e2e_tv_loss(zt, zp, T)[0] - oracle.e2e_tv_loss(zt, zm, T)[0]) / (2 * h)
+    assert np.allclose(g, num, rtol=1e-6, atol=1e-9)
+
+
+def test_e2e_grad_rows_sum_to_zero_and_subset():
+    rng = np.random.default_rng(12)
+    zt = rng.standard_normal((3, 4, 50))
+    zd = zt + rng.standard_normal((3, 4, 50)) * 0.3
+    g, _ = oracle.e2e_tv_grad(zt, zd, 0.9)
+    assert np.allclose(g.sum(axis=2), 0.0, atol=1e-15)
+    g1, _ = oracle.e2e_tv_grad(zt, zd, 0.9, rows=[2])
+    assert np.array_equal(g1[0], g[2])
+
+
+def test_inverse_cdf_strict_boundary_reading():
+    # reading: the chosen index is the first whose running sum is strictly
+    # above u * total, so u landing exactly on a boundary moves to the next
+    # token (u in [0, 1) never selects past the last positive weight)
+    assert so.inverse_cdf(np.array([1.0, 1.0]), 0.5)[0] == 1
+    assert so.inverse_cdf(np.array([1.0, 1.0]), 0.0)[0] == 0
+    assert so.inverse_cdf(np.array([0.0, 1.0, 1.0]), 0.0)[0] == 1
