@@ -1,0 +1,185 @@
+/*
+ * spec_verify.h -- C ABI of the speculative-sampling verify library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * One vocabulary sweep per (batch row, drafted position) computes the
+ * temperature softmax of target and draft logits, the overlap
+ * alpha = sum_v min(p, q) = 1 - d_TV(p, q), the min(1, p/q) acceptance, the
+ * residual max(0, p - q) correction and the bonus draw; the E2E-TV entry
+ * point turns the same sweep into a loss and its draft-logit gradient.
+ *
+ * Citations name the page and the section that defines each operation:
+ *   "Speculative Decoding 与 MTP：先猜多个 token，再让大模型一次验完"
+ *   "读 Qwen Bebop 与 DeepSeek DSpark：Speculative Decoding 正在从技巧变成系统工程"
+ *   "SpecOPD: Branch-Parallel On-Policy Distillation for Speculative Decoding"
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every buffer argument is a DEVICE pointer owned by the caller.  The
+ *    library allocates no device memory; scratch space is the caller's
+ *    `workspace` (size from the matching *_workspace_bytes function).
+ *  - Logit tensors are row-major and contiguous: element v of position k of
+ *    batch row b sits at base + ((b * P + k) * V + v) * elem_size, where P is
+ *    the number of positions stored per batch row.  Bulk (TMA) loads are used
+ *    when V * elem_size is a multiple of 16 bytes and the base is 16-byte
+ *    aligned; other shapes take a slower element-wise staging path.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  The host return value covers argument checks
+ *    and the launch only.  Problems found in the data are OR-ed into the
+ *    caller's 32-bit device word `dev_status` (may be NULL) and become visible
+ *    once the caller synchronises the stream; kernels never trap.
+ *  - The workspace must be zero-filled before its first use (for instance by
+ *    cudaMemsetAsync); every call that completes leaves it zero-filled again.
+ *    Two calls that may run at the same time on the GPU must not share a
+ *    workspace.
+ *  - Temperatures are float32; T == 0 selects greedy decoding where allowed.
+ *  - Limits: B >= 0, 0 <= K <= 64, 1 <= V, and 2 * V * elem_size may not
+ *    exceed 16 CTAs' worth of shared memory (V up to about 900k for bf16).
+ */
+#ifndef SPEC_VERIFY_H_
+#define SPEC_VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SPEC_OK = 0,
+  SPEC_ERR_INVALID_ARG = 1, /* a pointer, size, dtype or temperature is invalid */
+  SPEC_ERR_UNSUPPORTED = 2, /* valid request beyond this build's limits */
+  SPEC_ERR_CUDA = 3         /* the CUDA runtime reported an error */
+} spec_status_t;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define SPEC_DEV_BAD_TOKEN 1u      /* a drafted token outside [0, V) (treated as rejected) */
+#define SPEC_DEV_BAD_LOGITS 2u     /* NaN or +inf logit, or no finite logit in a row */
+#define SPEC_DEV_BAD_UNIFORM 4u    /* a uniform outside [0, 1) */
+#define SPEC_DEV_TIMEOUT 8u        /* a bounded wait inside a kernel gave up */
+#define SPEC_DEV_EMPTY_RESIDUAL 16u /* rejection with zero residual mass: drawn from p */
+
+/* Version of this ABI (bumped on any signature change). */
+int spec_abi_version(void);
+
+/* Human-readable name of a status code (static string). */
+const char* spec_status_string(spec_status_t status);
+
+/* ------------------------------------------------------------------------ */
+/* Batched verify step.
+ *
+ * Defined by "Speculative Decoding 与 MTP", section 2 (draft/verify loop: K
+ * candidates, target distributions p_1..p_K plus the bonus distribution, the
+ * first rejection ends the block), section 3 (accept with min(1, p/q); after
+ * a rejection draw from the residual max(0, p - q), never from the full p)
+ * and section 4 (greedy T == 0 compares with the target argmax; p and q use
+ * the same temperature).  The overlap written to alpha_out is alpha_RS of
+ * "读 Qwen Bebop 与 DeepSeek DSpark", section "用公式看".
+ *
+ * target_logits  [B, K+1, V] dtype: p_k = softmax(target[b,k] / T); row K is
+ *                the bonus distribution.
+ * draft_logits   [B, K, V] dtype: q_k = softmax(draft[b,k] / T).  May be NULL
+ *                only when T == 0 and alpha_out == NULL.
+ * draft_tokens   [B, K] int32: the drafted tokens y_k (sampled by the caller).
+ * u_accept       [B, K] float32 in [0, 1): draft k is accepted iff
+ *                u_accept <= p_k(y_k) / q_k(y_k).  Unused when T == 0.
+ * u_final        [B] float32 in [0, 1): inverse-CDF uniform for the one
+ *                correction or bonus token of the row.  Unused when T == 0.
+ * out_tokens     [B, K+1] int32 (written): the n accepted drafts, then the
+ *                correction (n < K) or bonus (n == K) token, then -1.
+ * n_accepted     [B] int32 (written): n in [0, K]; tokens emitted = n + 1.
+ * alpha_out      [B, K] float32 or NULL: per-position overlap alpha_k
+ *                (at T == 0 the indicator [argmax p_k == argmax q_k]).
+ * Inverse CDF: the smallest token v whose running sum in vocabulary order
+ * exceeds u_final times the total mass.
+ */
+size_t spec_verify_workspace_bytes(int B, int K, int V);
+
+spec_status_t spec_verify(const void* target_logits, const void* draft_logits,
+                          spec_dtype_t dtype, int B, int K, int V,
+                          float temperature, const int32_t* draft_tokens,
+                          const float* u_accept, const float* u_final,
+                          int32_t* out_tokens, int32_t* n_accepted,
+                          float* alpha_out, uint32_t* dev_status,
+                          void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Overlap statistics of K drafted positions.
+ *
+ * alpha_k = sum_v min(p_k, q_k) = 1 - d_TV(p_k, q_k), prefix survival
+ * a_j = prod_{k<=j} alpha_k and E[tau] = sum_j a_j: "读 Qwen Bebop 与
+ * DeepSeek DSpark", section "用公式看" (alpha_RS, d_TV, P(tau >= j), E[tau])
+ * and section "DSpark 的第二块拼图" (soft label c*_k = 1 - d_TV, a_j).
+ *
+ * target_logits  [B, KT, V] dtype, KT >= K: position k < K of each row is used
+ *                (pass KT = K + 1 to reuse a verify batch's target tensor).
+ * draft_logits   [B, K, V] dtype.
+ * temperature    T >= 0 (T == 0: alpha_k = [argmax p_k == argmax q_k]).
+ * alpha          [B, K] float32 (written, required).
+ * tv             [B, K] float32 or NULL: 1 - alpha_k.
+ * prefix_survival [B, K] float32 or NULL.
+ * expected_accepted [B] float32 or NULL: E[tau] (add 1 for emitted tokens).
+ */
+size_t spec_overlap_workspace_bytes(int B, int K, int V);
+
+spec_status_t spec_overlap(const void* target_logits, const void* draft_logits,
+                           spec_dtype_t dtype, int B, int K, int KT, int V,
+                           float temperature, float* alpha, float* tv,
+                           float* prefix_survival, float* expected_accepted,
+                           uint32_t* dev_status, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* E2E-TV loss and its gradient with respect to the draft logits.
+ *
+ * L = (1/B) sum_b sum_{j=1..K} prod_{k<=j} alpha_{b,k}: "读 Qwen Bebop 与
+ * DeepSeek DSpark", section "Bebop 的解法" (E[tau] written with
+ * 1 - d_TV(p_k, q_k)); "SpecOPD", method step (6): prefix products of the
+ * per-position overlap, only the draft probabilities are differentiated and
+ * the target is a constant.  The loss is the expected accepted length (to be
+ * maximised); pass grad_scale = -1 to get the gradient of -L.
+ *
+ * grad[b,k,v] = grad_scale * dL/dalpha_{b,k} * (q_v / T) * (1[q_v < p_v] - S),
+ * S = sum_{u: q_u < p_u} q_u, with
+ * dL/dalpha_k = (1/B) prod_{i<k} alpha_i (1 + alpha_{k+1} + alpha_{k+1} alpha_{k+2} + ...).
+ *
+ * target_logits  [B, KT, V] dtype, KT >= K (first K positions used).
+ * draft_logits   [B, K, V] dtype.
+ * temperature    T > 0.
+ * loss_out       [1] float32 (written).
+ * alpha_out      [B, K] float32 or NULL.
+ * grad_draft_logits [B, K, V] float32 (overwritten).
+ */
+size_t spec_e2e_tv_workspace_bytes(int B, int K, int V);
+
+spec_status_t spec_e2e_tv_fwd_bwd(const void* target_logits,
+                                  const void* draft_logits, spec_dtype_t dtype,
+                                  int B, int K, int KT, int V,
+                                  float temperature, float grad_scale,
+                                  float* loss_out, float* alpha_out,
+                                  float* grad_draft_logits,
+                                  uint32_t* dev_status, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Launch shape the library picks for a sweep over V (for benchmarks and
+ * diagnostics): CTAs per (row, position) cluster, threads per CTA and dynamic
+ * shared memory per CTA.  Returns SPEC_ERR_UNSUPPORTED if V does not fit. */
+spec_status_t spec_launch_shape(spec_dtype_t dtype, int units, int V,
+                                int* cluster_ctas, int* threads,
+                                int* smem_bytes);
+
+/* Forces the number of CTAs per cluster (1..16) for later launches of this
+ * process, for launch-shape sweeps in benchmarks; 0 restores the automatic
+ * choice.  Process-wide; not synchronised with launches in flight. */
+void spec_set_cluster_override(int cluster_ctas);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H_ */

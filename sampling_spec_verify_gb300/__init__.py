@@ -1,0 +1,328 @@
+"""Speculative-sampling verify on GB300: Python binding of the C ABI.
+
+The functions here only marshal arguments: every step of the verify, overlap
+and E2E-TV computations runs in the CUDA kernels of ``libspec_verify.so``.
+PyTorch provides device memory and streams.  There is no CPU fallback: if the
+library is missing, every call raises.
+
+Entry points (same names as the C ABI, see include/spec_verify.h):
+
+* ``verify``          -- batched draft/verify step (acceptance, residual
+                         correction, bonus token, greedy at T == 0);
+* ``overlap``         -- alpha = sum min(p, q), TV, prefix survival, E[tau];
+* ``e2e_tv_fwd_bwd``  -- E2E-TV loss and its draft-logit gradient.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "SpecError", "lib", "verify", "overlap", "e2e_tv_fwd_bwd", "launch_shape",
+    "set_cluster_override", "VerifyOutput", "OverlapOutput", "E2EOutput", "HostVerifier",
+    "DEV_BAD_TOKEN", "DEV_BAD_LOGITS", "DEV_BAD_UNIFORM", "DEV_TIMEOUT", "DEV_EMPTY_RESIDUAL",
+    "SPEC_OK", "SPEC_ERR_INVALID_ARG", "SPEC_ERR_UNSUPPORTED", "SPEC_ERR_CUDA",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libspec_verify.so")
+
+SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA = 0, 1, 2, 3
+SPEC_F32, SPEC_BF16 = 0, 1
+DEV_BAD_TOKEN, DEV_BAD_LOGITS, DEV_BAD_UNIFORM, DEV_TIMEOUT, DEV_EMPTY_RESIDUAL = 1, 2, 4, 8, 16
+
+_lib = None
+
+
+class SpecError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        msg = lib().spec_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{what}: {msg} (status {status})")
+
+
+def lib():
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` "
+            "(or sampling_spec_verify_gb300.build.build())")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.spec_abi_version.restype = i32
+    L.spec_status_string.restype = ctypes.c_char_p
+    L.spec_status_string.argtypes = [i32]
+    L.spec_verify_workspace_bytes.restype = sz
+    L.spec_verify_workspace_bytes.argtypes = [i32, i32, i32]
+    L.spec_verify.restype = i32
+    L.spec_verify.argtypes = [vp, vp, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.spec_overlap_workspace_bytes.restype = sz
+    L.spec_overlap_workspace_bytes.argtypes = [i32, i32, i32]
+    L.spec_overlap.restype = i32
+    L.spec_overlap.argtypes = [vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.spec_e2e_tv_workspace_bytes.restype = sz
+    L.spec_e2e_tv_workspace_bytes.argtypes = [i32, i32, i32]
+    L.spec_e2e_tv_fwd_bwd.restype = i32
+    L.spec_e2e_tv_fwd_bwd.argtypes = [vp, vp, i32, i32, i32, i32, i32, f32, f32, vp, vp, vp, vp, vp, sz, vp]
+    L.spec_launch_shape.restype = i32
+    L.spec_launch_shape.argtypes = [i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    L.spec_set_cluster_override.restype = None
+    L.spec_set_cluster_override.argtypes = [i32]
+    _lib = L
+    return L
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}")
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device):
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream), s
+
+
+_WS = {}
+
+
+def _workspace(nbytes: int, device, stream) -> torch.Tensor:
+    """A zero-filled workspace cached per (device, stream).  The library
+    leaves it zero-filled after every completed call."""
+    key = (device.index, stream.cuda_stream)
+    ws = _WS.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _WS[key] = ws
+    return ws
+
+
+def _check(status: int, what: str):
+    if status != SPEC_OK:
+        raise SpecError(status, what)
+
+
+def set_cluster_override(cluster_ctas: int) -> None:
+    """Force the CTAs per cluster (1..16) of later launches; 0 = automatic."""
+    lib().spec_set_cluster_override(int(cluster_ctas))
+
+
+def launch_shape(dtype: torch.dtype, units: int, V: int):
+    """(cluster CTAs, threads per CTA, dynamic shared bytes) for a sweep."""
+    a, b, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    code = SPEC_BF16 if dtype == torch.bfloat16 else SPEC_F32
+    _check(lib().spec_launch_shape(code, units, V, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
+           "spec_launch_shape")
+    return a.value, b.value, c.value
+
+
+# ---------------------------------------------------------------------------
+# verify
+# ---------------------------------------------------------------------------
+
+@dataclass
+class VerifyOutput:
+    tokens: torch.Tensor       # int32 [B, K+1]
+    n_accepted: torch.Tensor   # int32 [B]
+    alpha: Optional[torch.Tensor]  # float32 [B, K]
+    status: torch.Tensor       # int32 [1] device status word
+
+
+def verify(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: torch.Tensor,
+           u_accept: Optional[torch.Tensor], u_final: Optional[torch.Tensor], temperature: float, *,
+           want_alpha: bool = True, out: Optional[VerifyOutput] = None,
+           workspace: Optional[torch.Tensor] = None,
+           stream: Optional[torch.cuda.Stream] = None) -> VerifyOutput:
+    """Batched verify of K drafted tokens per row (see spec_verify in the C
+    header).  target [B, K+1, V], draft [B, K, V] (bf16 or fp32),
+    draft_tokens int32 [B, K], u_accept float32 [B, K], u_final float32 [B]."""
+    L = lib()
+    _need(target, "target")
+    B, K1, V = target.shape
+    K = K1 - 1
+    dev = target.device
+    greedy = float(temperature) == 0.0
+    if draft is not None:
+        _need(draft, "draft", dtype=target.dtype, shape=(B, K, V), device=dev)
+    _need(draft_tokens, "draft_tokens", dtype=torch.int32, shape=(B, K), device=dev)
+    if not greedy:
+        _need(u_accept, "u_accept", dtype=torch.float32, shape=(B, K), device=dev)
+        _need(u_final, "u_final", dtype=torch.float32, shape=(B,), device=dev)
+    want_alpha = want_alpha and draft is not None
+    if out is None:
+        out = VerifyOutput(
+            torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+            torch.empty((B,), dtype=torch.int32, device=dev),
+            torch.empty((B, K), dtype=torch.float32, device=dev) if want_alpha else None,
+            torch.zeros((1,), dtype=torch.int32, device=dev))
+    sh, s = _stream_handle(stream, dev)
+    need = L.spec_verify_workspace_bytes(B, K, V)
+    ws = workspace if workspace is not None else _workspace(need, dev, s)
+    st = L.spec_verify(_ptr(target), _ptr(draft), _dtype_code(target), B, K, V, float(temperature),
+                       _ptr(draft_tokens), _ptr(u_accept), _ptr(u_final), _ptr(out.tokens),
+                       _ptr(out.n_accepted), _ptr(out.alpha), _ptr(out.status), _ptr(ws),
+                       ws.numel() * ws.element_size(), sh)
+    _check(st, "spec_verify")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# overlap
+# ---------------------------------------------------------------------------
+
+@dataclass
+class OverlapOutput:
+    alpha: torch.Tensor
+    tv: Optional[torch.Tensor]
+    prefix_survival: Optional[torch.Tensor]
+    expected_accepted: Optional[torch.Tensor]
+    status: torch.Tensor
+
+
+def overlap(target: torch.Tensor, draft: torch.Tensor, temperature: float, *, K: Optional[int] = None,
+            want_tv: bool = True, want_survival: bool = True, out: Optional[OverlapOutput] = None,
+            workspace: Optional[torch.Tensor] = None,
+            stream: Optional[torch.cuda.Stream] = None) -> OverlapOutput:
+    """Per-position overlap statistics.  target [B, KT, V] with KT >= K (the
+    first K positions are used), draft [B, K, V]."""
+    L = lib()
+    _need(target, "target")
+    _need(draft, "draft", dtype=target.dtype)
+    B, KT, V = target.shape
+    K = draft.shape[1] if K is None else K
+    if tuple(draft.shape) != (B, K, V) or KT < K:
+        raise ValueError("draft must be [B, K, V] with K <= target.shape[1]")
+    dev = target.device
+    if out is None:
+        f = lambda *shape: torch.empty(shape, dtype=torch.float32, device=dev)  # noqa: E731
+        out = OverlapOutput(f(B, K), f(B, K) if want_tv else None, f(B, K) if want_survival else None,
+                            f(B) if want_survival else None, torch.zeros((1,), dtype=torch.int32, device=dev))
+    sh, s = _stream_handle(stream, dev)
+    need = L.spec_overlap_workspace_bytes(B, K, V)
+    ws = workspace if workspace is not None else _workspace(need, dev, s)
+    st = L.spec_overlap(_ptr(target), _ptr(draft), _dtype_code(target), B, K, KT, V, float(temperature),
+                        _ptr(out.alpha), _ptr(out.tv), _ptr(out.prefix_survival),
+                        _ptr(out.expected_accepted), _ptr(out.status), _ptr(ws),
+                        ws.numel() * ws.element_size(), sh)
+    _check(st, "spec_overlap")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# E2E-TV
+# ---------------------------------------------------------------------------
+
+@dataclass
+class E2EOutput:
+    loss: torch.Tensor            # float32 [1]
+    alpha: Optional[torch.Tensor]  # float32 [B, K]
+    grad: torch.Tensor            # float32 [B, K, V]
+    status: torch.Tensor
+
+
+def e2e_tv_fwd_bwd(target: torch.Tensor, draft: torch.Tensor, temperature: float, grad_scale: float = 1.0, *,
+                   K: Optional[int] = None, want_alpha: bool = True, out: Optional[E2EOutput] = None,
+                   workspace: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None) -> E2EOutput:
+    """E2E-TV loss mean_b sum_j prod_{k<=j} alpha_{b,k} and grad_scale times
+    its gradient with respect to the draft logits (target held constant)."""
+    L = lib()
+    _need(target, "target")
+    _need(draft, "draft", dtype=target.dtype)
+    B, KT, V = target.shape
+    K = draft.shape[1] if K is None else K
+    if tuple(draft.shape) != (B, K, V) or KT < K:
+        raise ValueError("draft must be [B, K, V] with K <= target.shape[1]")
+    dev = target.device
+    if out is None:
+        out = E2EOutput(torch.empty((1,), dtype=torch.float32, device=dev),
+                        torch.empty((B, K), dtype=torch.float32, device=dev) if want_alpha else None,
+                        torch.empty((B, K, V), dtype=torch.float32, device=dev),
+                        torch.zeros((1,), dtype=torch.int32, device=dev))
+    sh, s = _stream_handle(stream, dev)
+    need = L.spec_e2e_tv_workspace_bytes(B, K, V)
+    ws = workspace if workspace is not None else _workspace(need, dev, s)
+    st = L.spec_e2e_tv_fwd_bwd(_ptr(target), _ptr(draft), _dtype_code(target), B, K, KT, V, float(temperature),
+                               float(grad_scale), _ptr(out.loss), _ptr(out.alpha), _ptr(out.grad),
+                               _ptr(out.status), _ptr(ws), ws.numel() * ws.element_size(), sh)
+    _check(st, "spec_e2e_tv_fwd_bwd")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# host-buffer convenience: one verify step from pinned host memory
+# ---------------------------------------------------------------------------
+
+class HostVerifier:
+    """Runs verify steps whose inputs and outputs live in (pinned) host
+    memory: each ``run`` copies the step's inputs to the device, launches the
+    verify kernel and copies tokens, accepted counts and overlaps back, all on
+    one stream, then waits for the stream."""
+
+    def __init__(self, B: int, K: int, V: int, dtype=torch.bfloat16, device="cuda",
+                 stream: Optional[torch.cuda.Stream] = None):
+        self.device = torch.device(device)
+        self.stream = stream or torch.cuda.Stream(self.device)
+        d = self.device
+        self.target = torch.empty((B, K + 1, V), dtype=dtype, device=d)
+        self.draft = torch.empty((B, K, V), dtype=dtype, device=d)
+        self.tokens_in = torch.empty((B, K), dtype=torch.int32, device=d)
+        self.ua = torch.empty((B, K), dtype=torch.float32, device=d)
+        self.uf = torch.empty((B,), dtype=torch.float32, device=d)
+        self.out = VerifyOutput(torch.empty((B, K + 1), dtype=torch.int32, device=d),
+                                torch.empty((B,), dtype=torch.int32, device=d),
+                                torch.empty((B, K), dtype=torch.float32, device=d),
+                                torch.zeros((1,), dtype=torch.int32, device=d))
+        self.ws = torch.zeros(max(lib().spec_verify_workspace_bytes(B, K, V), 256), dtype=torch.uint8, device=d)
+        self.h2d_bytes = sum(t.numel() * t.element_size()
+                             for t in (self.target, self.draft, self.tokens_in, self.ua, self.uf))
+        self.d2h_bytes = sum(t.numel() * t.element_size() for t in (self.out.tokens, self.out.n_accepted,
+                                                                   self.out.alpha))
+
+    def run(self, target_h, draft_h, tokens_h, ua_h, uf_h, temperature, tokens_out_h, n_acc_out_h, alpha_out_h):
+        with torch.cuda.stream(self.stream):
+            self.target.copy_(target_h, non_blocking=True)
+            self.draft.copy_(draft_h, non_blocking=True)
+            self.tokens_in.copy_(tokens_h, non_blocking=True)
+            self.ua.copy_(ua_h, non_blocking=True)
+            self.uf.copy_(uf_h, non_blocking=True)
+            verify(self.target, self.draft, self.tokens_in, self.ua, self.uf, temperature,
+                   out=self.out, workspace=self.ws, stream=self.stream)
+            tokens_out_h.copy_(self.out.tokens, non_blocking=True)
+            n_acc_out_h.copy_(self.out.n_accepted, non_blocking=True)
+            alpha_out_h.copy_(self.out.alpha, non_blocking=True)
+        self.stream.synchronize()

@@ -1,0 +1,377 @@
+// C ABI of the verify library: argument checks, workspace layout, launch
+// shape and kernel launches.  No entry point allocates device memory or
+// synchronises the stream.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "spec_verify.h"
+#include "sweep.cuh"
+
+namespace {
+
+using ssv::Bf16;
+using ssv::E2EStats;
+using ssv::F32;
+using ssv::SweepParams;
+using ssv::VerifyRecord;
+
+constexpr int kMaxK = 64;
+constexpr int kMaxCluster = 16;
+constexpr int kMaxDevices = 64;
+constexpr int kStaticSmemReserve = 4096;
+constexpr long long kCtaTargetBytes = 64 * 1024;  // both rows of one CTA's slice
+
+std::atomic<int> g_cluster_override{0};
+
+struct DevInfo {
+  int sms = 0;
+  int smem_optin = 0;
+};
+
+DevInfo g_dev[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
+
+bool device_info(DevInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::call_once(g_dev_once[dev], [dev]() {
+    DevInfo d;
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    g_dev[dev] = d;
+  });
+  *out = g_dev[dev];
+  return out->sms > 0 && out->smem_optin > 0;
+}
+
+// Per-device "attributes already set" flags for each kernel instantiation.
+template <class Fn>
+cudaError_t prepare_kernel(Fn fn, std::atomic<uint64_t>& done_mask) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done_mask.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  DevInfo di;
+  if (!device_info(&di)) return cudaErrorInvalidDevice;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin - kStaticSmemReserve);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  done_mask.fetch_or(bit, std::memory_order_release);
+  return cudaSuccess;
+}
+
+struct Shape {
+  int S = 0;
+  int L = 0;
+  int smem = 0;
+};
+
+int elem_size(spec_dtype_t dt) { return dt == SPEC_BF16 ? 2 : 4; }
+
+// CTAs per cluster S and slice length L (elements, a multiple of 8) such that
+// both rows of a slice fit in one CTA's shared memory.
+bool pick_shape(int es, long long units, int V, Shape* out) {
+  DevInfo di;
+  if (!device_info(&di)) return false;
+  const long long smem_max = di.smem_optin - kStaticSmemReserve;
+  const long long pair_bytes = 2LL * V * es;
+  int S = (int)((pair_bytes + kCtaTargetBytes - 1) / kCtaTargetBytes);
+  S = S < 1 ? 1 : (S > kMaxCluster ? kMaxCluster : S);
+  // Few units: split the vocabulary further so more SMs share the work.
+  while (S < kMaxCluster && units * S < di.sms && (long long)V / (2LL * S) >= 4096) S = (S * 2 > kMaxCluster) ? kMaxCluster : S * 2;
+  const int ov = g_cluster_override.load();
+  if (ov > 0) S = ov;
+  for (;; ++S) {
+    if (S > kMaxCluster) return false;
+    long long L = ((long long)V + S - 1) / S;
+    L = (L + 7) / 8 * 8;
+    const long long smem = 2 * L * es;
+    if (smem <= smem_max) {
+      out->S = S;
+      out->L = (int)L;
+      out->smem = (int)smem;
+      return true;
+    }
+    if (ov > 0) return false;
+  }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+spec_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA; }
+
+template <class E, int MODE>
+cudaError_t launch_sweep(const SweepParams& P, const Shape& sh, cudaStream_t stream) {
+  static std::atomic<uint64_t> prepared{0};
+  auto fn = ssv::sweep_kernel<E, MODE>;
+  cudaError_t e = prepare_kernel(fn, prepared);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(P.units * P.S), 1, 1);
+  cfg.blockDim = dim3(ssv::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)sh.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)P.S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, P);
+}
+
+template <int MODE>
+cudaError_t launch_sweep_dt(spec_dtype_t dt, const SweepParams& P, const Shape& sh, cudaStream_t stream) {
+  return dt == SPEC_BF16 ? launch_sweep<Bf16, MODE>(P, sh, stream) : launch_sweep<F32, MODE>(P, sh, stream);
+}
+
+template <class E>
+cudaError_t launch_grad(const ssv::GradParams& G, cudaStream_t stream) {
+  const int nvec = G.aligned ? G.V / E::PV : G.V;
+  int gx = (nvec + 256 * 2 - 1) / (256 * 2);
+  gx = gx < 1 ? 1 : gx;
+  const int gy = G.units < 65535 ? G.units : 65535;
+  ssv::e2e_grad_kernel<E><<<dim3(gx, gy, 1), 256, 0, stream>>>(G);
+  return cudaGetLastError();
+}
+
+// Workspace layouts (all offsets 256-byte aligned).
+struct VerifyWs {
+  size_t rec = 0, cnt = 0, total = 0;
+};
+VerifyWs verify_ws(int B, int K) {
+  VerifyWs w;
+  w.rec = 0;
+  w.cnt = align256((size_t)B * (K + 1) * sizeof(VerifyRecord));
+  w.total = w.cnt + align256((size_t)B * sizeof(uint32_t));
+  return w;
+}
+struct E2EWs {
+  size_t stats = 0, row_loss = 0, cnt = 0, glob = 0, total = 0;
+};
+E2EWs e2e_ws(int B, int K) {
+  E2EWs w;
+  w.stats = 0;
+  w.row_loss = align256((size_t)B * K * sizeof(E2EStats));
+  w.cnt = w.row_loss + align256((size_t)B * sizeof(float));
+  w.glob = w.cnt + align256((size_t)B * sizeof(uint32_t));
+  w.total = w.glob + 256;
+  return w;
+}
+
+bool dims_ok(int B, int K, int V) { return B >= 0 && K >= 0 && K <= kMaxK && V >= 1; }
+
+bool dtype_ok(spec_dtype_t dt) { return dt == SPEC_F32 || dt == SPEC_BF16; }
+
+}  // namespace
+
+extern "C" {
+
+int spec_abi_version(void) { return 1; }
+
+const char* spec_status_string(spec_status_t s) {
+  switch (s) {
+    case SPEC_OK:
+      return "ok";
+    case SPEC_ERR_INVALID_ARG:
+      return "invalid argument";
+    case SPEC_ERR_UNSUPPORTED:
+      return "unsupported size or configuration";
+    case SPEC_ERR_CUDA:
+      return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+void spec_set_cluster_override(int cluster_ctas) {
+  g_cluster_override.store(cluster_ctas > 0 && cluster_ctas <= kMaxCluster ? cluster_ctas : 0);
+}
+
+spec_status_t spec_launch_shape(spec_dtype_t dtype, int units, int V, int* cluster_ctas, int* threads,
+                                int* smem_bytes) {
+  if (!dtype_ok(dtype) || units < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
+  Shape sh;
+  if (!pick_shape(elem_size(dtype), units, V, &sh)) return SPEC_ERR_UNSUPPORTED;
+  if (cluster_ctas) *cluster_ctas = sh.S;
+  if (threads) *threads = ssv::kThreads;
+  if (smem_bytes) *smem_bytes = sh.smem;
+  return SPEC_OK;
+}
+
+size_t spec_verify_workspace_bytes(int B, int K, int V) {
+  if (!dims_ok(B, K, V)) return 0;
+  return verify_ws(B, K).total;
+}
+
+spec_status_t spec_verify(const void* target_logits, const void* draft_logits, spec_dtype_t dtype, int B, int K,
+                          int V, float temperature, const int32_t* draft_tokens, const float* u_accept,
+                          const float* u_final, int32_t* out_tokens, int32_t* n_accepted, float* alpha_out,
+                          uint32_t* dev_status, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!dims_ok(B, K, V) || !dtype_ok(dtype)) return SPEC_ERR_INVALID_ARG;
+  if (!(temperature >= 0.0f) || !std::isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  const bool greedy = temperature == 0.0f;
+  if (!target_logits || !out_tokens || !n_accepted || !workspace) return SPEC_ERR_INVALID_ARG;
+  if (K > 0 && !draft_tokens) return SPEC_ERR_INVALID_ARG;
+  if (K > 0 && !draft_logits && (!greedy || alpha_out)) return SPEC_ERR_INVALID_ARG;
+  if (!greedy && (!u_final || (K > 0 && !u_accept))) return SPEC_ERR_INVALID_ARG;
+  const VerifyWs ws = verify_ws(B, K);
+  if (workspace_bytes < ws.total || !aligned16(workspace)) return SPEC_ERR_INVALID_ARG;
+  const long long units = (long long)B * (K + 1);
+  const int es = elem_size(dtype);
+  Shape sh;
+  if (!pick_shape(es, units, V, &sh)) return SPEC_ERR_UNSUPPORTED;
+  if (units * sh.S > 0x7FFFFFFFLL) return SPEC_ERR_UNSUPPORTED;
+
+  SweepParams P = {};
+  P.target = target_logits;
+  P.draft = draft_logits;
+  P.B = B;
+  P.K = K;
+  P.KT = K + 1;
+  P.V = V;
+  P.units = (int)units;
+  P.S = sh.S;
+  P.L = sh.L;
+  P.aligned = aligned16(target_logits) && (!draft_logits || aligned16(draft_logits)) && ((long long)V * es) % 16 == 0;
+  P.s = greedy ? 0.0f : (float)(1.4426950408889634 / (double)temperature);
+  P.inv_t = greedy ? 0.0f : (float)(1.0 / (double)temperature);
+  P.draft_tokens = draft_tokens;
+  P.u_accept = u_accept;
+  P.u_final = u_final;
+  P.out_tokens = out_tokens;
+  P.n_accepted = n_accepted;
+  P.alpha = alpha_out;
+  P.rec = reinterpret_cast<VerifyRecord*>(static_cast<char*>(workspace) + ws.rec);
+  P.row_cnt = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + ws.cnt);
+  P.status = dev_status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = greedy ? launch_sweep_dt<ssv::kVerifyGreedy>(dtype, P, sh, st)
+                         : launch_sweep_dt<ssv::kVerify>(dtype, P, sh, st);
+  return from_cuda(e);
+}
+
+size_t spec_overlap_workspace_bytes(int B, int K, int V) {
+  if (!dims_ok(B, K, V)) return 0;
+  return align256((size_t)B * sizeof(uint32_t));
+}
+
+spec_status_t spec_overlap(const void* target_logits, const void* draft_logits, spec_dtype_t dtype, int B, int K,
+                           int KT, int V, float temperature, float* alpha, float* tv, float* prefix_survival,
+                           float* expected_accepted, uint32_t* dev_status, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  if (!dims_ok(B, K, V) || !dtype_ok(dtype) || KT < K) return SPEC_ERR_INVALID_ARG;
+  if (!(temperature >= 0.0f) || !std::isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (B == 0) return SPEC_OK;
+  if (K == 0) {
+    if (expected_accepted) return from_cuda(cudaMemsetAsync(expected_accepted, 0, (size_t)B * sizeof(float), st));
+    return SPEC_OK;
+  }
+  if (!target_logits || !draft_logits || !alpha) return SPEC_ERR_INVALID_ARG;
+  const bool need_ws = prefix_survival || expected_accepted;
+  if (need_ws && (!workspace || workspace_bytes < spec_overlap_workspace_bytes(B, K, V) || !aligned16(workspace)))
+    return SPEC_ERR_INVALID_ARG;
+  const long long units = (long long)B * K;
+  const int es = elem_size(dtype);
+  Shape sh;
+  if (!pick_shape(es, units, V, &sh)) return SPEC_ERR_UNSUPPORTED;
+  if (units * sh.S > 0x7FFFFFFFLL) return SPEC_ERR_UNSUPPORTED;
+  const bool greedy = temperature == 0.0f;
+  SweepParams P = {};
+  P.target = target_logits;
+  P.draft = draft_logits;
+  P.B = B;
+  P.K = K;
+  P.KT = KT;
+  P.V = V;
+  P.units = (int)units;
+  P.S = sh.S;
+  P.L = sh.L;
+  P.aligned = aligned16(target_logits) && aligned16(draft_logits) && ((long long)V * es) % 16 == 0;
+  P.s = greedy ? 0.0f : (float)(1.4426950408889634 / (double)temperature);
+  P.inv_t = greedy ? 0.0f : (float)(1.0 / (double)temperature);
+  P.alpha = alpha;
+  P.tv = tv;
+  P.surv = prefix_survival;
+  P.exp_acc = expected_accepted;
+  P.row_cnt = need_ws ? static_cast<uint32_t*>(workspace) : nullptr;
+  P.status = dev_status;
+  cudaError_t e = greedy ? launch_sweep_dt<ssv::kOverlapGreedy>(dtype, P, sh, st)
+                         : launch_sweep_dt<ssv::kOverlap>(dtype, P, sh, st);
+  return from_cuda(e);
+}
+
+size_t spec_e2e_tv_workspace_bytes(int B, int K, int V) {
+  if (!dims_ok(B, K, V)) return 0;
+  return e2e_ws(B, K).total;
+}
+
+spec_status_t spec_e2e_tv_fwd_bwd(const void* target_logits, const void* draft_logits, spec_dtype_t dtype, int B,
+                                  int K, int KT, int V, float temperature, float grad_scale, float* loss_out,
+                                  float* alpha_out, float* grad_draft_logits, uint32_t* dev_status, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (!dims_ok(B, K, V) || !dtype_ok(dtype) || KT < K) return SPEC_ERR_INVALID_ARG;
+  if (!(temperature > 0.0f) || !std::isfinite(temperature) || !std::isfinite(grad_scale)) return SPEC_ERR_INVALID_ARG;
+  if (!loss_out) return SPEC_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (B == 0 || K == 0) return from_cuda(cudaMemsetAsync(loss_out, 0, sizeof(float), st));
+  if (!target_logits || !draft_logits || !grad_draft_logits || !workspace) return SPEC_ERR_INVALID_ARG;
+  const E2EWs ws = e2e_ws(B, K);
+  if (workspace_bytes < ws.total || !aligned16(workspace)) return SPEC_ERR_INVALID_ARG;
+  const long long units = (long long)B * K;
+  const int es = elem_size(dtype);
+  Shape sh;
+  if (!pick_shape(es, units, V, &sh)) return SPEC_ERR_UNSUPPORTED;
+  if (units * sh.S > 0x7FFFFFFFLL) return SPEC_ERR_UNSUPPORTED;
+  char* w = static_cast<char*>(workspace);
+  SweepParams P = {};
+  P.target = target_logits;
+  P.draft = draft_logits;
+  P.B = B;
+  P.K = K;
+  P.KT = KT;
+  P.V = V;
+  P.units = (int)units;
+  P.S = sh.S;
+  P.L = sh.L;
+  P.aligned = aligned16(target_logits) && aligned16(draft_logits) && ((long long)V * es) % 16 == 0;
+  P.s = (float)(1.4426950408889634 / (double)temperature);
+  P.inv_t = (float)(1.0 / (double)temperature);
+  P.grad_scale = grad_scale;
+  P.alpha = alpha_out;
+  P.loss = loss_out;
+  P.stats = reinterpret_cast<E2EStats*>(w + ws.stats);
+  P.row_loss = reinterpret_cast<float*>(w + ws.row_loss);
+  P.row_cnt = reinterpret_cast<uint32_t*>(w + ws.cnt);
+  P.glob_cnt = reinterpret_cast<uint32_t*>(w + ws.glob);
+  P.status = dev_status;
+  cudaError_t e = launch_sweep_dt<ssv::kE2E>(dtype, P, sh, st);
+  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  ssv::GradParams G = {};
+  G.target = target_logits;
+  G.draft = draft_logits;
+  G.B = B;
+  G.K = K;
+  G.KT = KT;
+  G.V = V;
+  G.units = (int)units;
+  G.aligned = P.aligned && aligned16(grad_draft_logits);
+  G.s = P.s;
+  G.stats = P.stats;
+  G.grad = grad_draft_logits;
+  e = dtype == SPEC_BF16 ? launch_grad<Bf16>(G, st) : launch_grad<F32>(G, st);
+  return from_cuda(e);
+}
+
+}  // extern "C"

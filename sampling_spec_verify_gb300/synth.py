@@ -90,9 +90,11 @@ def _uniforms(rng, B, K):
 
 
 def gaussian(B, K, V, *, sigma=2.0, noise=0.5, dtype=torch.bfloat16,
-             temperature=1.0, seed=0, bonus=True, name="gaussian"):
+             temperature=1.0, seed=0, bonus=True, name="gaussian", draft_tokens=True):
     """z_t ~ N(0, sigma^2) (sigma a scalar or one value per batch row),
-    z_d = z_t + N(0, noise^2); both rounded to ``dtype``."""
+    z_d = z_t + N(0, noise^2); both rounded to ``dtype``.  With
+    ``draft_tokens=False`` no tokens are drafted (all zero), as for the
+    E2E-TV loss, which consumes logits only."""
     rng = np.random.Generator(np.random.PCG64(seed))
     KT = K + 1 if bonus else K
     sig = np.broadcast_to(np.asarray(sigma, dtype=np.float32).reshape(-1, 1, 1)
@@ -103,7 +105,7 @@ def gaussian(B, K, V, *, sigma=2.0, noise=0.5, dtype=torch.bfloat16,
     draft = _round(zd32, dtype)
     del zt32, zd32
     t = fp32_temperature(temperature)
-    y = _gumbel_draft(rng, draft, t)
+    y = _gumbel_draft(rng, draft, t) if draft_tokens else torch.zeros((B, K), dtype=torch.int32)
     ua, uf = _uniforms(rng, B, K)
     return Workload(name, target, draft, y, ua, uf, t)
 
@@ -155,7 +157,7 @@ def zipf(seed=0, B=128, K=7, V=129280, temperature=1.0, low_frac=0.2, bonus=True
 def e2e(seed=0, B=256, K=7, V=151936):
     """E2E-TV training batch: target and draft logits [B, K, V] (no bonus row)."""
     return gaussian(B, K, V, sigma=2.0, noise=0.5, dtype=torch.bfloat16,
-                    temperature=1.0, seed=seed, bonus=False, name="e2e")
+                    temperature=1.0, seed=seed, bonus=False, name="e2e", draft_tokens=False)
 
 
 def sweep(B, K, seed=0, V=151936):

@@ -1,0 +1,88 @@
+"""The C-ABI library loads, exports every symbol the header declares, and
+rejects bad arguments before touching the GPU (CPU-only tests)."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    import sampling_spec_verify_gb300 as ssv
+    if not os.path.exists(ssv.LIB_PATH):
+        from sampling_spec_verify_gb300 import build
+        build.build()
+    return ssv.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(spec_[a-z0-9_]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("spec_verify", "spec_overlap", "spec_e2e_tv_fwd_bwd", "spec_status_string",
+                 "spec_verify_workspace_bytes", "spec_overlap_workspace_bytes", "spec_e2e_tv_workspace_bytes"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    import sampling_spec_verify_gb300 as ssv
+    out = subprocess.run(["nm", "-D", "--defined-only", ssv.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(L, name)
+
+
+def test_status_strings_and_version(L):
+    assert L.spec_abi_version() == 1
+    assert L.spec_status_string(0) == b"ok"
+    assert L.spec_status_string(1) == b"invalid argument"
+    assert L.spec_status_string(99) == b"unknown status"
+
+
+def test_workspace_sizes(L):
+    assert L.spec_verify_workspace_bytes(32, 4, 151936) >= 32 * 5 * 16 + 32 * 4
+    assert L.spec_verify_workspace_bytes(-1, 4, 10) == 0
+    assert L.spec_verify_workspace_bytes(1, 65, 10) == 0
+    assert L.spec_e2e_tv_workspace_bytes(256, 7, 151936) >= 256 * 7 * 32
+    assert L.spec_overlap_workspace_bytes(8, 4, 100) >= 32
+
+
+def test_argument_validation_without_gpu(L):
+    fake = ctypes.c_void_p(0x1000)
+    ws = ctypes.c_void_p(0x2000)
+    # bad dims and dtype
+    assert L.spec_verify(fake, fake, 1, 2, -1, 10, 1.0, fake, fake, fake, fake, fake, None, None, ws, 1 << 20, None) == 1
+    assert L.spec_verify(fake, fake, 7, 2, 2, 10, 1.0, fake, fake, fake, fake, fake, None, None, ws, 1 << 20, None) == 1
+    assert L.spec_verify(fake, fake, 1, 2, 2, 0, 1.0, fake, fake, fake, fake, fake, None, None, ws, 1 << 20, None) == 1
+    # negative / NaN temperature
+    assert L.spec_verify(fake, fake, 1, 2, 2, 10, -1.0, fake, fake, fake, fake, fake, None, None, ws, 1 << 20, None) == 1
+    assert L.spec_verify(fake, fake, 1, 2, 2, 10, float("nan"), fake, fake, fake, fake, fake, None, None, ws, 1 << 20,
+                         None) == 1
+    # empty batch: nothing to do
+    assert L.spec_verify(None, None, 1, 0, 2, 10, 1.0, None, None, None, None, None, None, None, None, 0, None) == 0
+    # missing outputs, missing draft at T > 0, missing uniforms
+    assert L.spec_verify(fake, fake, 1, 2, 2, 10, 1.0, fake, fake, fake, None, fake, None, None, ws, 1 << 20, None) == 1
+    assert L.spec_verify(fake, None, 1, 2, 2, 10, 1.0, fake, fake, fake, fake, fake, None, None, ws, 1 << 20, None) == 1
+    assert L.spec_verify(fake, fake, 1, 2, 2, 10, 1.0, fake, None, fake, fake, fake, None, None, ws, 1 << 20, None) == 1
+    # workspace too small / unaligned
+    assert L.spec_verify(fake, fake, 1, 2, 2, 10, 1.0, fake, fake, fake, fake, fake, None, None, ws, 8, None) == 1
+    assert L.spec_verify(fake, fake, 1, 2, 2, 10, 1.0, fake, fake, fake, fake, fake, None, None,
+                         ctypes.c_void_p(0x2004), 1 << 20, None) == 1
+    # E2E needs T > 0 and a loss pointer
+    assert L.spec_e2e_tv_fwd_bwd(fake, fake, 1, 2, 2, 2, 10, 0.0, 1.0, fake, None, fake, None, ws, 1 << 20, None) == 1
+    assert L.spec_e2e_tv_fwd_bwd(fake, fake, 1, 2, 2, 2, 10, 1.0, 1.0, None, None, fake, None, ws, 1 << 20, None) == 1
+    # overlap: KT < K, missing alpha
+    assert L.spec_overlap(fake, fake, 1, 2, 3, 2, 10, 1.0, fake, None, None, None, None, ws, 1 << 20, None) == 1
+    assert L.spec_overlap(fake, fake, 1, 2, 3, 3, 10, 1.0, None, None, None, None, None, ws, 1 << 20, None) == 1
