@@ -371,7 +371,10 @@ spec_status_t spec_e2e_tv_fwd_bwd(const void* target_logits, const void* draft_l
   G.stats = P.stats;
   G.grad = grad_draft_logits;
   e = dtype == SPEC_BF16 ? launch_grad<Bf16>(G, st) : launch_grad<F32>(G, st);
-  return from_cuda(e);
+  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  // The per-position statistics are consumed by the gradient kernel; clear
+  // them so the workspace is zero-filled again when the call completes.
+  return from_cuda(cudaMemsetAsync(w + ws.stats, 0, (size_t)B * K * sizeof(E2EStats), st));
 }
 
 }  // extern "C"

@@ -840,6 +840,10 @@ __global__ void __launch_bounds__(kThreads) sweep_kernel(const SweepParams P) {
       P.out_tokens[(long long)b * (K + 1) + kk] = tokv;
       if (kk < K && P.alpha) P.alpha[b * K + kk] = __ldcg(&rr[kk].alpha);
     }
+    __syncwarp();
+    // Leave the workspace zero-filled: the records of this row are consumed.
+    VerifyRecord* rw = P.rec + (long long)b * (K + 1);
+    for (int kk = lane; kk <= K; kk += 32) rw[kk] = VerifyRecord{0, 0, 0.0f, 0u};
     if (lane == 0) {
       P.n_accepted[b] = nacc;
       P.row_cnt[b] = 0;
@@ -888,7 +892,10 @@ __global__ void __launch_bounds__(kThreads) sweep_kernel(const SweepParams P) {
     __syncthreads();
     if (!s_glast || warp != 0) return;
     float acc_l = 0.0f;
-    for (int i = lane; i < P.B; i += 32) acc_l = __fadd_rn(acc_l, __ldcg(&P.row_loss[i]));
+    for (int i = lane; i < P.B; i += 32) {
+      acc_l = __fadd_rn(acc_l, __ldcg(&P.row_loss[i]));
+      P.row_loss[i] = 0.0f;  // consumed: leave the workspace zero-filled
+    }
     acc_l = warp_sum(acc_l);
     if (lane == 0) {
       *P.loss = acc_l / (float)P.B;

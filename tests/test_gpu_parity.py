@@ -178,7 +178,7 @@ def test_zipf_full_size(ssv):
 
 
 def test_sweep_points_sampled_rows(ssv):
-    for B, K in ((1, 1), (8, 2), (64, 7), (256, 16)):
+    for B, K in ((1, 1), (8, 2), (64, 7), (64, 16), (256, 4)):
         w = synth.sweep(B, K, seed=1238 + B + K)
         out = ssv.verify(*to_dev(w), w.temperature)
         torch.cuda.synchronize()
@@ -366,15 +366,24 @@ def test_deterministic_and_workspace_left_zero(ssv):
     w = synth.gaussian(16, 5, 60000, sigma=2.0, noise=0.7, dtype=torch.bfloat16, temperature=1.0, seed=9)
     args = to_dev(w)
     L = ssv.lib()
-    ws = torch.zeros(L.spec_verify_workspace_bytes(16, 5, 60000), dtype=torch.uint8, device=DEV)
+    nbytes = max(L.spec_verify_workspace_bytes(16, 5, 60000), L.spec_e2e_tv_workspace_bytes(16, 5, 60000))
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
     a = ssv.verify(*args, 1.0, workspace=ws)
     b = ssv.verify(*args, 1.0, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(a.tokens, b.tokens) and torch.equal(a.n_accepted, b.n_accepted)
     assert torch.equal(a.alpha, b.alpha)
-    # the arrival counters are zero again; records may hold data
-    cnt_off = ((16 * 6 * 16 + 255) // 256) * 256
-    assert int(ws[cnt_off:].sum().item()) == 0
+    # every call leaves the whole workspace zero-filled
+    assert int(ws.count_nonzero().item()) == 0
+    # shared between entry points and shapes without re-zeroing
+    e = ssv.e2e_tv_fwd_bwd(args[0], args[1], 1.0, K=5, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(ws.count_nonzero().item()) == 0
+    c = ssv.verify(args[0][:3].contiguous(), args[1][:3].contiguous(), args[2][:3].contiguous(),
+                   args[3][:3].contiguous(), args[4][:3].contiguous(), 1.0, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(c.tokens, a.tokens[:3]) and int(ws.count_nonzero().item()) == 0
+    assert np.isfinite(float(e.loss.item()))
 
 
 def test_unaligned_rows_match_aligned(ssv):
