@@ -108,6 +108,37 @@ spec_status_t spec_verify(const void* target_logits, const void* draft_logits,
                           void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Allocation-free verify.  The pages have no counterpart: this entry point
+ * exists for callers that cannot allocate device memory when they run a
+ * verify step -- code inside a CUDA stream capture (where cudaMalloc is not
+ * allowed), runtimes whose pool owns all device memory, plugin hosts that
+ * provide buffers but no allocator.
+ *
+ * Same arguments and results as spec_verify, without the workspace: the
+ * scratch is a fixed device array of SPEC_NOALLOC_SCRATCH_BYTES inside the
+ * library, held by every GPU that loads the library until the process exits.
+ * Sizes whose spec_verify_workspace_bytes(B, K, V) exceeds it are rejected with
+ * SPEC_ERR_UNSUPPORTED (at K = 4 that is about 12,000 rows).  No call
+ * allocates or frees memory; each clears the part of the array it uses with
+ * cudaMemsetAsync on `stream`.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the one array: calls that may overlap on
+ *    the GPU (different streams without ordering between them) race and give
+ *    wrong results.  Serialise them. */
+#define SPEC_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+spec_status_t spec_verify_noalloc(const void* target_logits,
+                                  const void* draft_logits, spec_dtype_t dtype,
+                                  int B, int K, int V, float temperature,
+                                  const int32_t* draft_tokens,
+                                  const float* u_accept, const float* u_final,
+                                  int32_t* out_tokens, int32_t* n_accepted,
+                                  float* alpha_out, uint32_t* dev_status,
+                                  void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Overlap statistics of K drafted positions.
  *
  * alpha_k = sum_v min(p_k, q_k) = 1 - d_TV(p_k, q_k), prefix survival
