@@ -197,17 +197,20 @@ spec_status_t spec_e2e_tv_fwd_bwd(const void* target_logits,
                                   size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
-/* Launch shape the library picks for a sweep over V (for benchmarks and
- * diagnostics): CTAs per (row, position) cluster, threads per CTA and dynamic
- * shared memory per CTA.  Returns SPEC_ERR_UNSUPPORTED if V does not fit. */
+/* Launch shape the library picks for a verify sweep over `units` (row,
+ * position) pairs of V logits (for benchmarks and diagnostics): CTAs per
+ * cluster, threads per CTA, dynamic shared memory per CTA, the number of
+ * persistent clusters launched and the shared-memory stages per CTA.  Needs a current CUDA device.  Returns
+ * SPEC_ERR_UNSUPPORTED if V does not fit.  Any output pointer may be NULL. */
 spec_status_t spec_launch_shape(spec_dtype_t dtype, int units, int V,
                                 int* cluster_ctas, int* threads,
-                                int* smem_bytes);
+                                int* smem_bytes, int* clusters, int* stages);
 
-/* Forces the number of CTAs per cluster (1..16) for later launches of this
- * process, for launch-shape sweeps in benchmarks; 0 restores the automatic
- * choice.  Process-wide; not synchronised with launches in flight. */
-void spec_set_cluster_override(int cluster_ctas);
+/* Forces the CTAs per cluster (1..16) and the shared-memory stages per CTA
+ * (1 or 2) of later launches in this process, for launch-shape sweeps in
+ * benchmarks; 0 restores the automatic choice of either.  Process-wide; not
+ * synchronised with launches in flight. */
+void spec_set_launch_override(int cluster_ctas, int stages);
 
 #ifdef __cplusplus
 }

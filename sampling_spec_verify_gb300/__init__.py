@@ -24,7 +24,7 @@ import torch
 
 __all__ = [
     "SpecError", "lib", "verify", "overlap", "e2e_tv_fwd_bwd", "launch_shape",
-    "set_cluster_override", "VerifyOutput", "OverlapOutput", "E2EOutput", "HostVerifier",
+    "set_launch_override", "VerifyOutput", "OverlapOutput", "E2EOutput", "HostVerifier",
     "DEV_BAD_TOKEN", "DEV_BAD_LOGITS", "DEV_BAD_UNIFORM", "DEV_TIMEOUT", "DEV_EMPTY_RESIDUAL",
     "SPEC_OK", "SPEC_ERR_INVALID_ARG", "SPEC_ERR_UNSUPPORTED", "SPEC_ERR_CUDA",
 ]
@@ -74,9 +74,9 @@ def lib():
     L.spec_e2e_tv_fwd_bwd.restype = i32
     L.spec_e2e_tv_fwd_bwd.argtypes = [vp, vp, i32, i32, i32, i32, i32, f32, f32, vp, vp, vp, vp, vp, sz, vp]
     L.spec_launch_shape.restype = i32
-    L.spec_launch_shape.argtypes = [i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i32)]
-    L.spec_set_cluster_override.restype = None
-    L.spec_set_cluster_override.argtypes = [i32]
+    L.spec_launch_shape.argtypes = [i32, i32, i32] + [ctypes.POINTER(i32)] * 5
+    L.spec_set_launch_override.restype = None
+    L.spec_set_launch_override.argtypes = [i32, i32]
     _lib = L
     return L
 
@@ -136,18 +136,19 @@ def _check(status: int, what: str):
         raise SpecError(status, what)
 
 
-def set_cluster_override(cluster_ctas: int) -> None:
-    """Force the CTAs per cluster (1..16) of later launches; 0 = automatic."""
-    lib().spec_set_cluster_override(int(cluster_ctas))
+def set_launch_override(cluster_ctas: int = 0, stages: int = 0) -> None:
+    """Force the CTAs per cluster (1..16) and shared-memory stages (1 or 2)
+    of later launches; 0 = automatic."""
+    lib().spec_set_launch_override(int(cluster_ctas), int(stages))
 
 
 def launch_shape(dtype: torch.dtype, units: int, V: int):
-    """(cluster CTAs, threads per CTA, dynamic shared bytes) for a sweep."""
-    a, b, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    """(cluster CTAs, threads per CTA, dynamic shared bytes, clusters, stages)
+    of a verify sweep over `units` (row, position) pairs."""
+    v = [ctypes.c_int() for _ in range(5)]
     code = SPEC_BF16 if dtype == torch.bfloat16 else SPEC_F32
-    _check(lib().spec_launch_shape(code, units, V, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
-           "spec_launch_shape")
-    return a.value, b.value, c.value
+    _check(lib().spec_launch_shape(code, units, V, *[ctypes.byref(x) for x in v]), "spec_launch_shape")
+    return tuple(x.value for x in v)
 
 
 # ---------------------------------------------------------------------------

@@ -7,7 +7,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "spec_verify.h"
 #include "sweep.cuh"
@@ -24,9 +26,9 @@ constexpr int kMaxK = 64;
 constexpr int kMaxCluster = 16;
 constexpr int kMaxDevices = 64;
 constexpr int kStaticSmemReserve = 4096;
-constexpr long long kCtaTargetBytes = 64 * 1024;  // both rows of one CTA's slice
 
 std::atomic<int> g_cluster_override{0};
+std::atomic<int> g_stage_override{0};
 
 struct DevInfo {
   int sms = 0;
@@ -68,39 +70,90 @@ cudaError_t prepare_kernel(Fn fn, std::atomic<uint64_t>& done_mask) {
 }
 
 struct Shape {
-  int S = 0;
-  int L = 0;
-  int smem = 0;
+  int S = 0;     // CTAs per cluster
+  int L = 0;     // slice length (elements)
+  int nst = 0;   // shared-memory stages per CTA (2: the next unit is prefetched)
+  int smem = 0;  // dynamic shared memory per CTA: nst stages of both rows
+  int G = 0;     // clusters launched (persistent)
 };
 
 int elem_size(spec_dtype_t dt) { return dt == SPEC_BF16 ? 2 : 4; }
 
-// CTAs per cluster S and slice length L (elements, a multiple of 8) such that
-// both rows of a slice fit in one CTA's shared memory.
-bool pick_shape(int es, long long units, int V, Shape* out) {
+std::mutex g_occ_mu;
+std::map<std::tuple<const void*, int, int, int>, int> g_occ;  // (kernel, S, smem, device) -> clusters
+
+// Clusters of S CTAs with `smem` dynamic bytes each that fit on the device at once.
+template <class Fn>
+int max_active_clusters(Fn fn, int S, int smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const auto key = std::make_tuple((const void*)fn, S, smem, dev);
+  {
+    std::lock_guard<std::mutex> g(g_occ_mu);
+    auto itc = g_occ.find(key);
+    if (itc != g_occ.end()) return itc->second;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)S, 1, 1);
+  cfg.blockDim = dim3(ssv::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> g(g_occ_mu);
+  g_occ[key] = n;
+  return n;
+}
+
+// Picks the cluster size S and the stage count for a sweep over V: the
+// stages must fit in shared memory, and among the shapes that fit the one
+// with the lowest estimated time wins -- (units per cluster, rounded up) x
+// (rounds of 32 vectors per warp + a fixed per-unit allowance for the
+// exchanges, larger when the load of a unit is not prefetched).
+template <class Fn>
+bool pick_shape(Fn fn, int es, long long units, int V, int rows, Shape* out) {
   DevInfo di;
   if (!device_info(&di)) return false;
   const long long smem_max = di.smem_optin - kStaticSmemReserve;
-  const long long pair_bytes = 2LL * V * es;
-  int S = (int)((pair_bytes + kCtaTargetBytes - 1) / kCtaTargetBytes);
-  S = S < 1 ? 1 : (S > kMaxCluster ? kMaxCluster : S);
-  // Few units: split the vocabulary further so more SMs share the work.
-  while (S < kMaxCluster && units * S < di.sms && (long long)V / (2LL * S) >= 4096) S = (S * 2 > kMaxCluster) ? kMaxCluster : S * 2;
+  const int pv = 16 / es;
   const int ov = g_cluster_override.load();
-  if (ov > 0) S = ov;
-  for (;; ++S) {
-    if (S > kMaxCluster) return false;
-    long long L = ((long long)V + S - 1) / S;
-    L = (L + 7) / 8 * 8;
-    const long long smem = 2 * L * es;
-    if (smem <= smem_max) {
-      out->S = S;
-      out->L = (int)L;
-      out->smem = (int)smem;
-      return true;
+  const int ovs = g_stage_override.load();
+  double best_cost = -1.0;
+  for (int nst = 2; nst >= 1; --nst) {
+    if (ovs > 0 && nst != ovs) continue;
+    for (int S = (ov > 0 ? ov : 1); S <= (ov > 0 ? ov : kMaxCluster); ++S) {
+      long long L = ((long long)V + S - 1) / S;
+      L = (L + 7) / 8 * 8;
+      const long long smem = (long long)rows * nst * L * es;
+      if (smem > smem_max) continue;
+      const long long nvec = L / pv;
+      const long long per_warp = (nvec + ssv::kWarps - 1) / ssv::kWarps;
+      const long long rounds = (per_warp + 31) / 32;
+      if (rounds > ssv::kMaxRounds) continue;
+      const int G = max_active_clusters(fn, S, (int)smem);
+      if (G <= 0) continue;
+      const long long Ge = units < G ? units : G;
+      const double cost = (double)((units + Ge - 1) / Ge) * ((double)rounds + (nst == 2 ? 2.0 : 4.0));
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        out->S = S;
+        out->L = (int)L;
+        out->nst = nst;
+        out->smem = (int)smem;
+        out->G = (int)Ge;
+      }
     }
-    if (ov > 0) return false;
   }
+  return best_cost >= 0;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -110,13 +163,31 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 spec_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA; }
 
 template <class E, int MODE>
-cudaError_t launch_sweep(const SweepParams& P, const Shape& sh, cudaStream_t stream) {
-  static std::atomic<uint64_t> prepared{0};
+std::atomic<uint64_t>& prepared_mask() {
+  static std::atomic<uint64_t> m{0};
+  return m;
+}
+
+// Sets the kernel's attributes (once per device) and picks its launch shape.
+template <class E, int MODE>
+spec_status_t shape_for(long long units, int V, int rows, Shape* sh) {
   auto fn = ssv::sweep_kernel<E, MODE>;
-  cudaError_t e = prepare_kernel(fn, prepared);
-  if (e != cudaSuccess) return e;
+  if (prepare_kernel(fn, prepared_mask<E, MODE>()) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (!pick_shape(fn, E::ES, units, V, rows, sh)) return SPEC_ERR_UNSUPPORTED;
+  return SPEC_OK;
+}
+
+// rows: logit rows staged per unit (2, or 1 when no draft row is read).
+template <int MODE>
+spec_status_t shape_for_dt(spec_dtype_t dt, long long units, int V, int rows, Shape* sh) {
+  return dt == SPEC_BF16 ? shape_for<Bf16, MODE>(units, V, rows, sh) : shape_for<F32, MODE>(units, V, rows, sh);
+}
+
+template <class E, int MODE>
+cudaError_t launch_sweep(const SweepParams& P, const Shape& sh, cudaStream_t stream) {
+  auto fn = ssv::sweep_kernel<E, MODE>;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(P.units * P.S), 1, 1);
+  cfg.gridDim = dim3((unsigned)(sh.G * sh.S), 1, 1);
   cfg.blockDim = dim3(ssv::kThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)sh.smem;
   cfg.stream = stream;
@@ -146,23 +217,40 @@ cudaError_t launch_grad(const ssv::GradParams& G, cudaStream_t stream) {
 }
 
 // Workspace layouts (all offsets 256-byte aligned).
+size_t part_bytes(long long units) { return align256((size_t)units * ssv::kPartStride * sizeof(float)); }
+
 struct VerifyWs {
-  size_t rec = 0, cnt = 0, total = 0;
+  size_t rec = 0, part = 0, cnt = 0, total = 0;
 };
 VerifyWs verify_ws(int B, int K) {
+  const long long units = (long long)B * (K + 1);
   VerifyWs w;
   w.rec = 0;
-  w.cnt = align256((size_t)B * (K + 1) * sizeof(VerifyRecord));
+  w.part = align256((size_t)units * sizeof(VerifyRecord));
+  w.cnt = w.part + part_bytes(units);
+  w.total = w.cnt + align256((size_t)B * sizeof(uint32_t));
+  return w;
+}
+struct OverlapWs {
+  size_t part = 0, cnt = 0, total = 0;
+};
+OverlapWs overlap_ws(int B, int K) {
+  OverlapWs w;
+  w.part = 0;
+  w.cnt = part_bytes((long long)B * K);
   w.total = w.cnt + align256((size_t)B * sizeof(uint32_t));
   return w;
 }
 struct E2EWs {
-  size_t stats = 0, row_loss = 0, cnt = 0, glob = 0, total = 0;
+  size_t stats = 0, part = 0, part2 = 0, row_loss = 0, cnt = 0, glob = 0, total = 0;
 };
 E2EWs e2e_ws(int B, int K) {
+  const long long units = (long long)B * K;
   E2EWs w;
   w.stats = 0;
-  w.row_loss = align256((size_t)B * K * sizeof(E2EStats));
+  w.part = align256((size_t)units * sizeof(E2EStats));
+  w.part2 = w.part + part_bytes(units);
+  w.row_loss = w.part2 + part_bytes(units);
   w.cnt = w.row_loss + align256((size_t)B * sizeof(float));
   w.glob = w.cnt + align256((size_t)B * sizeof(uint32_t));
   w.total = w.glob + 256;
@@ -177,7 +265,7 @@ bool dtype_ok(spec_dtype_t dt) { return dt == SPEC_F32 || dt == SPEC_BF16; }
 
 extern "C" {
 
-int spec_abi_version(void) { return 1; }
+int spec_abi_version(void) { return 2; }
 
 const char* spec_status_string(spec_status_t s) {
   switch (s) {
@@ -193,18 +281,22 @@ const char* spec_status_string(spec_status_t s) {
   return "unknown status";
 }
 
-void spec_set_cluster_override(int cluster_ctas) {
+void spec_set_launch_override(int cluster_ctas, int stages) {
   g_cluster_override.store(cluster_ctas > 0 && cluster_ctas <= kMaxCluster ? cluster_ctas : 0);
+  g_stage_override.store(stages == 1 || stages == 2 ? stages : 0);
 }
 
 spec_status_t spec_launch_shape(spec_dtype_t dtype, int units, int V, int* cluster_ctas, int* threads,
-                                int* smem_bytes) {
+                                int* smem_bytes, int* clusters, int* stages) {
   if (!dtype_ok(dtype) || units < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
   Shape sh;
-  if (!pick_shape(elem_size(dtype), units, V, &sh)) return SPEC_ERR_UNSUPPORTED;
+  const spec_status_t r = shape_for_dt<ssv::kVerify>(dtype, units, V, 2, &sh);
+  if (r != SPEC_OK) return r;
   if (cluster_ctas) *cluster_ctas = sh.S;
   if (threads) *threads = ssv::kThreads;
   if (smem_bytes) *smem_bytes = sh.smem;
+  if (clusters) *clusters = sh.G;
+  if (stages) *stages = sh.nst;
   return SPEC_OK;
 }
 
@@ -228,10 +320,15 @@ spec_status_t spec_verify(const void* target_logits, const void* draft_logits, s
   const VerifyWs ws = verify_ws(B, K);
   if (workspace_bytes < ws.total || !aligned16(workspace)) return SPEC_ERR_INVALID_ARG;
   const long long units = (long long)B * (K + 1);
+  if (units > 0x7FFFFFFFLL) return SPEC_ERR_UNSUPPORTED;
   const int es = elem_size(dtype);
+  const int rows = (greedy && !alpha_out) ? 1 : 2;  // greedy without overlap reads no draft row
   Shape sh;
-  if (!pick_shape(es, units, V, &sh)) return SPEC_ERR_UNSUPPORTED;
-  if (units * sh.S > 0x7FFFFFFFLL) return SPEC_ERR_UNSUPPORTED;
+  {
+    const spec_status_t r = greedy ? shape_for_dt<ssv::kVerifyGreedy>(dtype, units, V, rows, &sh)
+                                   : shape_for_dt<ssv::kVerify>(dtype, units, V, rows, &sh);
+    if (r != SPEC_OK) return r;
+  }
 
   SweepParams P = {};
   P.target = target_logits;
@@ -243,9 +340,12 @@ spec_status_t spec_verify(const void* target_logits, const void* draft_logits, s
   P.units = (int)units;
   P.S = sh.S;
   P.L = sh.L;
+  P.nst = sh.nst;
+  P.rows = 2;
   P.aligned = aligned16(target_logits) && (!draft_logits || aligned16(draft_logits)) && ((long long)V * es) % 16 == 0;
   P.s = greedy ? 0.0f : (float)(1.4426950408889634 / (double)temperature);
   P.inv_t = greedy ? 0.0f : (float)(1.0 / (double)temperature);
+  P.rows = rows;
   P.draft_tokens = draft_tokens;
   P.u_accept = u_accept;
   P.u_final = u_final;
@@ -253,6 +353,7 @@ spec_status_t spec_verify(const void* target_logits, const void* draft_logits, s
   P.n_accepted = n_accepted;
   P.alpha = alpha_out;
   P.rec = reinterpret_cast<VerifyRecord*>(static_cast<char*>(workspace) + ws.rec);
+  P.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.part);
   P.row_cnt = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + ws.cnt);
   P.status = dev_status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -263,7 +364,7 @@ spec_status_t spec_verify(const void* target_logits, const void* draft_logits, s
 
 size_t spec_overlap_workspace_bytes(int B, int K, int V) {
   if (!dims_ok(B, K, V)) return 0;
-  return align256((size_t)B * sizeof(uint32_t));
+  return overlap_ws(B, K).total;
 }
 
 spec_status_t spec_overlap(const void* target_logits, const void* draft_logits, spec_dtype_t dtype, int B, int K,
@@ -279,15 +380,18 @@ spec_status_t spec_overlap(const void* target_logits, const void* draft_logits, 
     return SPEC_OK;
   }
   if (!target_logits || !draft_logits || !alpha) return SPEC_ERR_INVALID_ARG;
-  const bool need_ws = prefix_survival || expected_accepted;
-  if (need_ws && (!workspace || workspace_bytes < spec_overlap_workspace_bytes(B, K, V) || !aligned16(workspace)))
-    return SPEC_ERR_INVALID_ARG;
+  const OverlapWs ws = overlap_ws(B, K);
+  if (!workspace || workspace_bytes < ws.total || !aligned16(workspace)) return SPEC_ERR_INVALID_ARG;
   const long long units = (long long)B * K;
+  if (units > 0x7FFFFFFFLL) return SPEC_ERR_UNSUPPORTED;
   const int es = elem_size(dtype);
-  Shape sh;
-  if (!pick_shape(es, units, V, &sh)) return SPEC_ERR_UNSUPPORTED;
-  if (units * sh.S > 0x7FFFFFFFLL) return SPEC_ERR_UNSUPPORTED;
   const bool greedy = temperature == 0.0f;
+  Shape sh;
+  {
+    const spec_status_t r = greedy ? shape_for_dt<ssv::kOverlapGreedy>(dtype, units, V, 2, &sh)
+                                   : shape_for_dt<ssv::kOverlap>(dtype, units, V, 2, &sh);
+    if (r != SPEC_OK) return r;
+  }
   SweepParams P = {};
   P.target = target_logits;
   P.draft = draft_logits;
@@ -298,6 +402,8 @@ spec_status_t spec_overlap(const void* target_logits, const void* draft_logits, 
   P.units = (int)units;
   P.S = sh.S;
   P.L = sh.L;
+  P.nst = sh.nst;
+  P.rows = 2;
   P.aligned = aligned16(target_logits) && aligned16(draft_logits) && ((long long)V * es) % 16 == 0;
   P.s = greedy ? 0.0f : (float)(1.4426950408889634 / (double)temperature);
   P.inv_t = greedy ? 0.0f : (float)(1.0 / (double)temperature);
@@ -305,7 +411,8 @@ spec_status_t spec_overlap(const void* target_logits, const void* draft_logits, 
   P.tv = tv;
   P.surv = prefix_survival;
   P.exp_acc = expected_accepted;
-  P.row_cnt = need_ws ? static_cast<uint32_t*>(workspace) : nullptr;
+  P.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.part);
+  P.row_cnt = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + ws.cnt);
   P.status = dev_status;
   cudaError_t e = greedy ? launch_sweep_dt<ssv::kOverlapGreedy>(dtype, P, sh, st)
                          : launch_sweep_dt<ssv::kOverlap>(dtype, P, sh, st);
@@ -330,10 +437,13 @@ spec_status_t spec_e2e_tv_fwd_bwd(const void* target_logits, const void* draft_l
   const E2EWs ws = e2e_ws(B, K);
   if (workspace_bytes < ws.total || !aligned16(workspace)) return SPEC_ERR_INVALID_ARG;
   const long long units = (long long)B * K;
+  if (units > 0x7FFFFFFFLL) return SPEC_ERR_UNSUPPORTED;
   const int es = elem_size(dtype);
   Shape sh;
-  if (!pick_shape(es, units, V, &sh)) return SPEC_ERR_UNSUPPORTED;
-  if (units * sh.S > 0x7FFFFFFFLL) return SPEC_ERR_UNSUPPORTED;
+  {
+    const spec_status_t r = shape_for_dt<ssv::kE2E>(dtype, units, V, 2, &sh);
+    if (r != SPEC_OK) return r;
+  }
   char* w = static_cast<char*>(workspace);
   SweepParams P = {};
   P.target = target_logits;
@@ -345,6 +455,8 @@ spec_status_t spec_e2e_tv_fwd_bwd(const void* target_logits, const void* draft_l
   P.units = (int)units;
   P.S = sh.S;
   P.L = sh.L;
+  P.nst = sh.nst;
+  P.rows = 2;
   P.aligned = aligned16(target_logits) && aligned16(draft_logits) && ((long long)V * es) % 16 == 0;
   P.s = (float)(1.4426950408889634 / (double)temperature);
   P.inv_t = (float)(1.0 / (double)temperature);
@@ -352,6 +464,8 @@ spec_status_t spec_e2e_tv_fwd_bwd(const void* target_logits, const void* draft_l
   P.alpha = alpha_out;
   P.loss = loss_out;
   P.stats = reinterpret_cast<E2EStats*>(w + ws.stats);
+  P.part = reinterpret_cast<float*>(w + ws.part);
+  P.part2 = reinterpret_cast<float*>(w + ws.part2);
   P.row_loss = reinterpret_cast<float*>(w + ws.row_loss);
   P.row_cnt = reinterpret_cast<uint32_t*>(w + ws.cnt);
   P.glob_cnt = reinterpret_cast<uint32_t*>(w + ws.glob);

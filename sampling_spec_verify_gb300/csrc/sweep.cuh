@@ -1,32 +1,37 @@
 // Vocabulary sweep kernels for sm_103a.
 //
-// One thread-block cluster of S CTAs owns one (batch row b, position k) unit.
-// CTA r of the cluster holds the slice [r*L, min((r+1)*L, V)) of the target
-// row (and of the draft row) in shared memory, loaded ONCE from HBM by 1-D
-// bulk copies (one per warp segment, completing on a per-warp mbarrier).
-// Every later pass reads shared memory only:
+// A (row b, position k) "unit" is one target row (and, for drafted positions,
+// one draft row) of V logits.  A thread-block cluster of S CTAs works on one
+// unit at a time: CTA r of the cluster owns the slice [r*L, min((r+1)*L, V)).
+// The kernel is persistent: cluster c processes units c, c+G, c+2G, ... and
+// every CTA keeps two shared-memory stages, so the 1-D bulk (TMA) copies of
+// the next unit's slice are in flight while the current unit is computed.
+// Each warp owns a contiguous segment of 16-byte vectors in both stages,
+// issues the bulk copies for that segment itself (completing on its own
+// mbarrier) and is the only reader of it, so no block-wide barrier orders the
+// staging against the compute.
 //
-//   pass A  max of each row                  -> DSMEM exchange 1
-//   pass B  sum of 2^((z - M) s), s = log2e/T -> DSMEM exchange 2
-//   pass C  overlap sum_v min(p, q) (one exp per element through
-//           min(log p, log q)), or, at a rejected / bonus position, the
-//           residual max(0, p - q) (or p) with per-round warp scans
-//                                            -> DSMEM exchange 3
-//   search  the CTA / warp / lane / element holding u' * total mass
-//                                            -> DSMEM exchange 4
-//
-// Rank 0 then publishes a per-unit record in the workspace and bumps a
-// per-row arrival counter; the CTA that arrives last for a row runs the
-// prefix-order decision over the row's K+1 records (first rejection, tokens,
-// overlap) with one warp and re-zeroes the counter.
-//
-// Data in shared memory is laid out by element index, so thread (warp w,
-// lane l) always sees the same vocabulary entries of the target and draft
-// rows; a warp only ever reads its own segment of vectors, so no block-wide
-// barrier separates the staging from the compute.
+// Per unit (sampling, T > 0):
+//   pass A  thread-local maxima (packed bf16x2 compares)
+//   pass B  thread-local sums of 2^((z - m) s), s = log2(e)/T
+//           -> block and cluster combine of (max, sum) pairs   [exchange 1]
+//   decide  accept iff u * q(y) <= p(y) (identical in every CTA)
+//   pass C  accepted drafts: sum_v min(p, q) through min(log p, log q), one
+//           exp per element; the CTA's partial goes to the workspace.
+//           rejected drafts / bonus: weights max(0, p - q) (or p) with per
+//           round warp scans; CTA totals are exchanged           [exchange 2]
+//           and the owning CTA / warp / round / lane / element of
+//           u' * total is located; one warp recomputes one round.
+// Thread 0 of each CTA writes the unit's record / overlap partial and queues
+// an arrival for the unit's row.  Arrivals are published in batches (one
+// release fence, then up to 32 counter updates in parallel by warp 0) when
+// 32 rows are queued and at the end; the CTA completing a row decides the
+// prefix-order outcome, sums the overlap partials in rank order and re-zeroes
+// the workspace it used.
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cstddef>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -35,18 +40,19 @@ namespace ssv {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kMaxRounds = 16;     // rounds of 32 vectors per warp segment
+constexpr int kPartStride = 16;    // partial slots per unit (max cluster size)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s bound on any wait
+constexpr unsigned kFull = 0xFFFFFFFFu;
 
-constexpr uint32_t kBadToken = 1u, kBadLogits = 2u, kBadUniform = 4u, kTimeout = 8u,
-                   kEmptyResidual = 16u;
+constexpr uint32_t kBadToken = 1u, kBadLogits = 2u, kBadUniform = 4u, kTimeout = 8u, kEmptyResidual = 16u;
 
 enum Mode : int { kVerify = 0, kVerifyGreedy = 1, kOverlap = 2, kOverlapGreedy = 3, kE2E = 4 };
 
 struct VerifyRecord {  // one per (b, k), k = 0..K
   int32_t acc;         // 1 accepted, 0 rejected (draft positions)
   int32_t token;       // correction / bonus / greedy choice; -1 if none
-  float alpha;         // overlap of the position
-  uint32_t pad;
+  uint32_t pad0, pad1;
 };
 
 struct E2EStats {  // one per (b, k), k = 0..K-1
@@ -67,6 +73,8 @@ struct SweepParams {
   int S;        // CTAs per cluster
   int L;        // slice length in elements (multiple of 8)
   int aligned;  // rows start on 16-byte boundaries: bulk copies allowed
+  int nst;      // shared-memory stages per CTA (1 or 2)
+  int rows;     // logit rows staged per unit: 2 (target and draft) or 1 (target only)
   float s;      // log2(e) / T
   float inv_t;  // 1 / T
   float grad_scale;
@@ -82,6 +90,8 @@ struct SweepParams {
   float* loss;
   VerifyRecord* rec;
   E2EStats* stats;
+  float* part;   // [units][kPartStride] overlap partials
+  float* part2;  // [units][kPartStride] E2E S-mass partials
   float* row_loss;
   uint32_t* row_cnt;
   uint32_t* glob_cnt;
@@ -106,19 +116,27 @@ struct Bf16 {
     x[7] = __uint_as_float(w.w & 0xFFFF0000u);
   }
   __device__ static __forceinline__ float to_f32(Raw r) { return __uint_as_float(uint32_t(r) << 16); }
-  // Running maximum kept packed (bf16x2); max needs no rounding.
-  struct MaxAcc {
-    __nv_bfloat162 m;
-    __device__ MaxAcc() { m = __bfloat162bfloat162(__ushort_as_bfloat16(kNegInf)); }
-    __device__ __forceinline__ void add(const uint4& w) {
-      const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&w.x);
-      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w.y);
-      const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&w.z);
-      const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&w.w);
-      m = __hmax2(m, __hmax2(__hmax2(a, b), __hmax2(c, d)));
-    }
-    __device__ __forceinline__ float get() const { return fmaxf(__low2float(m), __high2float(m)); }
-  };
+  // Maximum of the 8 values of a vector (packed compares; max needs no rounding).
+  __device__ static __forceinline__ float vmax(const uint4& w) {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&w.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w.y);
+    const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&w.z);
+    const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&w.w);
+    const __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
+    return fmaxf(__low2float(m), __high2float(m));
+  }
+  // Maximum of a vector ignoring NaN, and whether the vector holds a NaN.
+  __device__ static __forceinline__ float vmax_nan(const uint4& w, bool& nan) {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&w.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w.y);
+    const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&w.z);
+    const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&w.w);
+    const __nv_bfloat162 mn = __hmax2_nan(__hmax2_nan(a, b), __hmax2_nan(c, d));
+    const float lo = __low2float(mn), hi = __high2float(mn);
+    nan = (lo != lo) || (hi != hi);
+    const __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
+    return fmaxf(__low2float(m), __high2float(m));
+  }
 };
 
 struct F32 {
@@ -133,15 +151,17 @@ struct F32 {
     x[3] = __uint_as_float(w.w);
   }
   __device__ static __forceinline__ float to_f32(Raw r) { return __uint_as_float(r); }
-  struct MaxAcc {
-    float m = -INFINITY;
-    __device__ __forceinline__ void add(const uint4& w) {
-      m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
-                         fmaxf(__uint_as_float(w.z), __uint_as_float(w.w))));
-    }
-    __device__ __forceinline__ float get() const { return m; }
-  };
+  __device__ static __forceinline__ float vmax(const uint4& w) {
+    return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)), fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
+  }
+  __device__ static __forceinline__ float vmax_nan(const uint4& w, bool& nan) {
+    const float a = __uint_as_float(w.x), b = __uint_as_float(w.y), c = __uint_as_float(w.z), d = __uint_as_float(w.w);
+    nan = (a != a) || (b != b) || (c != c) || (d != d);
+    return fmaxf(fmaxf(a, b), fmaxf(c, d));
+  }
 };
+
+// ---- small reductions (fixed association: identical in every CTA) ------------------
 
 template <int N>
 __device__ __forceinline__ float tree_sum(const float (&x)[N]) {
@@ -155,54 +175,59 @@ __device__ __forceinline__ float tree_sum(const float (&x)[N]) {
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-  return v;
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(kFull, v, o));
   return v;
 }
 
 __device__ __forceinline__ float warp_incl_scan(float v, int lane) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const float t = __shfl_up_sync(0xFFFFFFFFu, v, o);
+    const float t = __shfl_up_sync(kFull, v, o);
     if (lane >= o) v = __fadd_rn(v, t);
   }
   return v;
 }
 
-// (value, index) argmax reduction: larger value wins, ties to the smaller index.
-__device__ __forceinline__ void arg_better(float& v, int& i, float v2, int i2) {
-  if (v2 > v || (v2 == v && i2 < i)) {
-    v = v2;
-    i = i2;
-  }
-}
-
-__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+// Two rows at once: the maxima in one warp instruction each, then the
+// rescaled sums through one shuffle tree whose two chains overlap.
+__device__ __forceinline__ void warp_combine_mz2(float& m1, float& z1, float& m2, float& z2, float s) {
+  const float M1 = redux_max_f32(m1), M2 = redux_max_f32(m2);
+  const float f1 = (m1 > -INFINITY) ? ex2(__fadd_rn(__fmul_rn(m1, s), -__fmul_rn(M1, s))) : 0.0f;
+  const float f2 = (m2 > -INFINITY) ? ex2(__fadd_rn(__fmul_rn(m2, s), -__fmul_rn(M2, s))) : 0.0f;
+  float a = __fmul_rn(z1, f1), b = __fmul_rn(z2, f2);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const float v2 = __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    const int i2 = __shfl_xor_sync(0xFFFFFFFFu, i, o);
-    arg_better(v, i, v2, i2);
+    const float ta = __shfl_xor_sync(kFull, a, o);
+    const float tb = __shfl_xor_sync(kFull, b, o);
+    a = __fadd_rn(a, ta);
+    b = __fadd_rn(b, tb);
   }
+  z1 = a;
+  z2 = b;
+  m1 = M1;
+  m2 = M2;
 }
 
-// Per-element weights of the residual / bonus draws.  The same function runs
-// in the first pass and in the replay of the owning warp, with every rounding
-// pinned (__fmul_rn / __fadd_rn / fmaf), so both see bit-identical values.
+// Warp argmax in two warp instructions: the largest value, then the smallest
+// index among the lanes holding it.
+__device__ __forceinline__ void warp_argmax_redux(float& v, int& i) {
+  const float M = redux_max_f32(v);
+  const uint32_t cand = (v == M) ? (uint32_t)i : 0xFFFFFFFFu;
+  i = (int)redux_min_u32(cand);
+  v = M;
+}
+
+// Per-element weights of the residual / target draws.  The first pass and the
+// owner's recomputation call this same function with every rounding pinned
+// (fmaf / __fadd_rn), so both see bit-identical values.
 template <class E, bool kResidual>
 __device__ __forceinline__ float draw_weights(const uint4& wt, const uint4& wd, float s, float c1t, float c1d,
                                               float ratio, float (&w)[E::PV], float& min_mass) {
   float t[E::PV];
   E::unpack(wt, t);
   if constexpr (kResidual) {
-    float d[E::PV];
+    float d[E::PV], m[E::PV];
     E::unpack(wd, d);
-    float m[E::PV];
 #pragma unroll
     for (int i = 0; i < E::PV; ++i) {
       const float et = ex2(fmaf(t[i], s, -c1t));
@@ -222,51 +247,46 @@ __device__ __forceinline__ float draw_weights(const uint4& wt, const uint4& wd, 
 
 // ---- the sweep kernel ----------------------------------------------------------
 
+struct SweepSmem {
+  uint64_t mbar[2][kWarps];
+  float wred[kWarps][4];
+  int wredi[kWarps][2];
+  float wrun[kWarps][kMaxRounds + 1];  // per-round prefix of a warp's draw weights
+  float wtot[kWarps];
+  float woff[kWarps + 1];
+  alignas(16) float mbox[2][kPartStride][8];  // pushed by peers: [exchange slot][sender rank][field]
+  float bcf[8];
+  int bci[8];
+  int pend_row[32];  // rows with arrivals not yet published (thread 0)
+  int pend_cnt[32];
+  int npend;
+};
+
+// 16-byte remote vector stores into the mailbox need 16-byte alignment.
+static_assert(offsetof(SweepSmem, mbox) % 16 == 0, "mailbox must be 16-byte aligned");
+static_assert(sizeof(float) * 8 % 16 == 0, "mailbox rows must be 16-byte multiples");
+
 template <class E, int MODE>
-__global__ void __launch_bounds__(kThreads) sweep_kernel(const SweepParams P) {
+__global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P) {
   extern __shared__ __align__(128) uint8_t dyn_smem[];
-  __shared__ __align__(8) uint64_t mbar[kWarps];
-  __shared__ float red_a[kWarps], red_b[kWarps], red_c[kWarps];
-  __shared__ int red_i[kWarps], red_j[kWarps];
-  __shared__ float warp_total[kWarps];
-  // Cluster mailboxes: written by this CTA, read by peers after a barrier.
-  __shared__ float mail_f[8];
-  __shared__ int mail_i[4];
-  __shared__ uint32_t mail_tok;
-  // Block-wide broadcast of values thread 0 computed.
-  __shared__ float bc_f[8];
-  __shared__ int bc_i[8];
+  __shared__ __align__(16) SweepSmem sm;
 
   constexpr int PV = E::PV;
+  using Raw = typename E::Raw;
   constexpr bool kGreedy = (MODE == kVerifyGreedy || MODE == kOverlapGreedy);
   constexpr bool kVerifyMode = (MODE == kVerify || MODE == kVerifyGreedy);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int S = P.S;
   const uint32_t rank = cluster_rank();
-  const int unit = blockIdx.x / S;
+  const int cl = blockIdx.x / S;
+  const int G = gridDim.x / S;
   const int K = P.K, V = P.V;
+  const int per_row = kVerifyMode ? K + 1 : K;
+  const float s = P.s;
+  const int nst = P.nst;  // shared-memory stages: 1, or 2 (next unit prefetched)
 
-  int b, k;
-  bool bonus = false;
-  if constexpr (kVerifyMode) {
-    b = unit / (K + 1);
-    k = unit - b * (K + 1);
-    bonus = (k == K);
-  } else {
-    b = unit / K;
-    k = unit - b * K;
-  }
-  const long long trow = (long long)b * P.KT + k;
-  const long long drow = (long long)b * K + k;
-  bool has_draft = !bonus;
-  if constexpr (MODE == kVerifyGreedy) has_draft = !bonus && P.alpha != nullptr;
-
-  const typename E::Raw* tg = reinterpret_cast<const typename E::Raw*>(P.target) + trow * V;
-  const typename E::Raw* dg =
-      has_draft ? reinterpret_cast<const typename E::Raw*>(P.draft) + drow * V : nullptr;
-
-  // ---- slice and warp segment ----
+  // slice of this CTA, segment of this warp
   const int e0 = (int)rank * P.L;
   const int e1 = min(e0 + P.L, V);
   const int n = max(e1 - e0, 0);
@@ -275,301 +295,531 @@ __global__ void __launch_bounds__(kThreads) sweep_kernel(const SweepParams P) {
   const int seg = (nvec + kWarps - 1) / kWarps;
   const int v_lo = min(warp * seg, nvec);
   const int v_hi = min(v_lo + seg, nvec);
-  uint4* st = reinterpret_cast<uint4*>(dyn_smem);
-  uint4* sd = st + nvec_alloc;
+  const int nrounds = (v_hi - v_lo + 31) >> 5;
+  const bool bulk = P.aligned && v_hi > v_lo;
+  const size_t stage_bytes = (size_t)P.rows * (size_t)nvec_alloc * 16u;
+  auto stage_t = [&](int st) { return reinterpret_cast<uint4*>(dyn_smem + st * stage_bytes); };
 
-  // Scalars of the decision, fetched early so their latency hides under the
-  // staging: drafted token, its two logits, the uniforms.
-  int y = -1;
-  float u = 0.0f, uf = 0.0f, zt_y = 0.0f, zd_y = 0.0f;
-  bool tok_ok = true;
-  if constexpr (MODE == kVerify || MODE == kVerifyGreedy) {
-    if (!bonus) {
-      y = P.draft_tokens[b * K + k];
-      tok_ok = (y >= 0 && y < V);
-      if constexpr (MODE == kVerify) {
-        u = P.u_accept[b * K + k];
-        if (tok_ok) {
-          zt_y = E::to_f32(tg[y]);
-          zd_y = E::to_f32(dg[y]);
+  if (bulk && lane == 0) {
+    mbar_init(smem_addr(&sm.mbar[0][warp]), 1);
+    mbar_init(smem_addr(&sm.mbar[1][warp]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const uint64_t pol = l2_evict_first_policy();
+
+  struct Unit {
+    int b, k;
+    bool bonus, has_draft;
+    const Raw* tg;
+    const Raw* dg;
+  };
+  auto decode = [&](int u) {
+    Unit x;
+    if constexpr (kVerifyMode) {
+      x.b = u / (K + 1);
+      x.k = u - x.b * (K + 1);
+      x.bonus = (x.k == K);
+    } else {
+      x.b = u / K;
+      x.k = u - x.b * K;
+      x.bonus = false;
+    }
+    x.has_draft = !x.bonus;
+    if constexpr (MODE == kVerifyGreedy) x.has_draft = !x.bonus && P.alpha != nullptr;
+    x.tg = reinterpret_cast<const Raw*>(P.target) + ((long long)x.b * P.KT + x.k) * V;
+    x.dg = x.has_draft ? reinterpret_cast<const Raw*>(P.draft) + ((long long)x.b * K + x.k) * V : nullptr;
+    return x;
+  };
+
+  // Bulk copies of this warp's segment of unit u into stage st (lane 0).
+  auto issue = [&](int u, int st) {
+    if (!bulk || lane != 0) return;
+    const Unit x = decode(u);
+    const uint32_t bar = smem_addr(&sm.mbar[st][warp]);
+    const uint32_t bytes = (uint32_t)(v_hi - v_lo) * 16u;
+    fence_proxy_async_smem();  // earlier generic reads of this segment come first
+    mbar_arrive_expect_tx(bar, x.has_draft ? 2u * bytes : bytes);
+    uint4* dt = stage_t(st);
+    bulk_load(smem_addr(dt + v_lo), x.tg + e0 + (long long)v_lo * PV, bytes, bar, pol);
+    if (x.has_draft) bulk_load(smem_addr(dt + nvec_alloc + v_lo), x.dg + e0 + (long long)v_lo * PV, bytes, bar, pol);
+  };
+
+  // Warp 0 pushes eight values (held by every lane) into slot `slot` of every
+  // CTA's mailbox; after the next cluster barrier each CTA reads them locally.
+  auto push8 = [&](int slot, float f0, float f1, float f2, float f3, float f4, float f5, float f6, float f7) {
+    if (lane < S) {
+      const uint32_t a = map_rank(smem_addr(&sm.mbox[slot][rank][0]), (uint32_t)lane);
+      st_cluster_v4(a, f0, f1, f2, f3);
+      st_cluster_v4(a + 16u, f4, f5, f6, f7);
+    }
+  };
+  auto mb = [&](int slot, int f, float dflt) { return lane < S ? sm.mbox[slot][lane][f] : dflt; };
+
+  // ---- per-row completion (warp 0 of the CTA that arrives last) ----
+  auto complete_row = [&](int b) {
+    const float* pp0 = P.part + (long long)b * per_row * kPartStride;
+    // overlap of position kk: partials summed in rank order
+    auto alpha_of = [&](int kk) {
+      const float* pp = pp0 + kk * kPartStride;
+      float a = 0.0f;
+      for (int r = 0; r < S; ++r) a = __fadd_rn(a, __ldcg(pp + r));
+      return a;
+    };
+    if constexpr (kVerifyMode) {
+      const VerifyRecord* rr = P.rec + (long long)b * (K + 1);
+      int nacc = K;
+      for (int base = 0; base < K; base += 32) {
+        const int kk = base + lane;
+        const bool rej = (kk < K) && (__ldcg(&rr[kk].acc) == 0);
+        const unsigned m = __ballot_sync(kFull, rej);
+        if (m) {
+          nacc = base + __ffs(m) - 1;
+          break;
+        }
+      }
+      const int corr = __ldcg(&rr[nacc].token);
+      for (int kk = lane; kk <= K; kk += 32) {
+        int tokv = -1;
+        if (kk < nacc) tokv = P.draft_tokens[b * K + kk];
+        else if (kk == nacc) tokv = corr;
+        P.out_tokens[(long long)b * (K + 1) + kk] = tokv;
+        if (kk < K && P.alpha) P.alpha[b * K + kk] = alpha_of(kk);
+      }
+      __syncwarp();
+      VerifyRecord* rw = P.rec + (long long)b * (K + 1);
+      float* pw = P.part + (long long)b * per_row * kPartStride;
+      for (int kk = lane; kk <= K; kk += 32) rw[kk] = VerifyRecord{0, 0, 0u, 0u};
+      for (int i = lane; i < per_row * kPartStride; i += 32) pw[i] = 0.0f;
+      if (lane == 0) {
+        P.n_accepted[b] = nacc;
+        P.row_cnt[b] = 0;
+      }
+    } else if constexpr (MODE == kOverlap || MODE == kOverlapGreedy) {
+      float al[2];
+      for (int h = 0; h < 2; ++h) {
+        const int kk = lane + 32 * h;
+        al[h] = (kk < K) ? alpha_of(kk) : 0.0f;
+        if (kk < K) {
+          P.alpha[b * K + kk] = al[h];
+          if (P.tv) P.tv[b * K + kk] = 1.0f - al[h];
+        }
+      }
+      // prefix products in position order
+      float pr = 1.0f, sum = 0.0f;
+      for (int kk = 0; kk < K; ++kk) {
+        const float a = __shfl_sync(kFull, al[kk >> 5], kk & 31);
+        pr = __fmul_rn(pr, a);
+        sum = __fadd_rn(sum, pr);
+        if (lane == 0 && P.surv) P.surv[b * K + kk] = pr;
+      }
+      __syncwarp();
+      float* pw = P.part + (long long)b * per_row * kPartStride;
+      for (int i = lane; i < per_row * kPartStride; i += 32) pw[i] = 0.0f;
+      if (lane == 0) {
+        if (P.exp_acc) P.exp_acc[b] = sum;
+        P.row_cnt[b] = 0;
+      }
+    } else {  // kE2E
+      E2EStats* sr = P.stats + (long long)b * K;
+      const float* qq0 = P.part2 + (long long)b * K * kPartStride;
+      float al[2], sm2[2];
+      for (int h = 0; h < 2; ++h) {
+        const int kk = lane + 32 * h;
+        al[h] = 0.0f;
+        sm2[h] = 0.0f;
+        if (kk < K) {
+          al[h] = alpha_of(kk);
+          const float* qq = qq0 + kk * kPartStride;
+          for (int r = 0; r < S; ++r) sm2[h] = __fadd_rn(sm2[h], __ldcg(qq + r));
+          if (P.alpha) P.alpha[b * K + kk] = al[h];
+        }
+      }
+      // prefix products P_{k-1}, suffix sums G_k = 1 + alpha_{k+1} G_{k+1}
+      float pre[2] = {1.0f, 1.0f}, suf[2] = {1.0f, 1.0f};
+      float pr = 1.0f, rowl = 0.0f;
+      for (int kk = 0; kk < K; ++kk) {
+        if ((kk & 31) == lane) pre[kk >> 5] = pr;
+        pr = __fmul_rn(pr, __shfl_sync(kFull, al[kk >> 5], kk & 31));
+        rowl = __fadd_rn(rowl, pr);
+      }
+      float g = 1.0f;
+      for (int kk = K - 1; kk >= 0; --kk) {
+        if ((kk & 31) == lane) suf[kk >> 5] = g;
+        g = fmaf(__shfl_sync(kFull, al[kk >> 5], kk & 31), g, 1.0f);
+      }
+      const float scale = P.grad_scale / (float)P.B;
+      for (int h = 0; h < 2; ++h) {
+        const int kk = lane + 32 * h;
+        if (kk < K) {
+          const float coef = __fmul_rn(__fmul_rn(scale, pre[h]), suf[h]);
+          const float A = __fmul_rn(__fmul_rn(coef, __ldcg(&sr[kk].izt)), P.inv_t);
+          sr[kk].smass = sm2[h];
+          sr[kk].alpha = al[h];
+          sr[kk].b1 = __fmul_rn(A, 1.0f - sm2[h]);
+          sr[kk].b0 = __fmul_rn(A, -sm2[h]);
+        }
+      }
+      __syncwarp();
+      float* pw = P.part + (long long)b * K * kPartStride;
+      float* pw2 = P.part2 + (long long)b * K * kPartStride;
+      for (int i = lane; i < K * kPartStride; i += 32) {
+        pw[i] = 0.0f;
+        pw2[i] = 0.0f;
+      }
+      int glast = 0;
+      if (lane == 0) {
+        P.row_loss[b] = rowl;
+        P.row_cnt[b] = 0;
+        __threadfence();
+        const uint32_t old = atomicAdd(P.glob_cnt, 1u);
+        glast = (old == (uint32_t)P.B - 1) ? 1 : 0;
+        if (glast) __threadfence();
+      }
+      glast = __shfl_sync(kFull, glast, 0);
+      if (glast) {
+        float acc_l = 0.0f;
+        for (int i = lane; i < P.B; i += 32) {
+          acc_l = __fadd_rn(acc_l, __ldcg(&P.row_loss[i]));
+          P.row_loss[i] = 0.0f;
+        }
+        acc_l = warp_sum(acc_l);
+        if (lane == 0) {
+          *P.loss = acc_l / (float)P.B;
+          *P.glob_cnt = 0;
         }
       }
     }
-    if constexpr (MODE == kVerify) uf = P.u_final[b];
-  }
+  };
 
-  // ---- staging: one bulk copy per row per warp segment ----
-  bool staged = true;
-  if (v_hi > v_lo) {
-    if (P.aligned) {
-      const uint32_t bar = smem_addr(&mbar[warp]);
-      const uint32_t bytes = (uint32_t)(v_hi - v_lo) * 16u;
-      if (lane == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
-        mbar_arrive_expect_tx(bar, has_draft ? 2u * bytes : bytes);
-        const uint64_t pol = l2_evict_first_policy();
-        bulk_load(smem_addr(st + v_lo), tg + e0 + (long long)v_lo * PV, bytes, bar, pol);
-        if (has_draft) bulk_load(smem_addr(sd + v_lo), dg + e0 + (long long)v_lo * PV, bytes, bar, pol);
-      }
-      __syncwarp();
-      staged = mbar_wait_bounded(bar, 0, kWaitLimitNs);
+  // Publishes the queued arrivals (warp 0, converged): one release fence, one
+  // counter update per queued row (lanes in parallel), then the rows whose
+  // arrivals are complete are finished by the whole warp.
+  auto flush = [&]() {
+    __syncwarp();
+    const int np = __shfl_sync(kFull, sm.npend, 0);  // lane 0 (thread 0) owns the queue
+    if (np == 0) return;
+    if (lane == 0) __threadfence();
+    __syncwarp();
+    int row = -1, last = 0;
+    if (lane < np) {
+      row = sm.pend_row[lane];
+      const uint32_t c = (uint32_t)sm.pend_cnt[lane];
+      const uint32_t old = atomicAdd(&P.row_cnt[row], c);
+      last = (old + c == (uint32_t)(per_row * S)) ? 1 : 0;
+    }
+    unsigned m = __ballot_sync(kFull, last);
+    if (m) __threadfence();
+    while (m) {
+      const int l = __ffs(m) - 1;
+      m &= m - 1;
+      complete_row(__shfl_sync(kFull, row, l));
+    }
+    __syncwarp();
+    if (lane == 0) sm.npend = 0;
+    __syncwarp();
+  };
+  // Queues one arrival for row b (thread 0).
+  auto queue_arrival = [&](int b) {
+    const int np = sm.npend;
+    if (np > 0 && sm.pend_row[np - 1] == b) {
+      sm.pend_cnt[np - 1] += 1;
     } else {
-      // Element-wise staging for rows that do not start on 16-byte
-      // boundaries; the tail of the last vector is padded with -inf.
-      typename E::Raw* rt = reinterpret_cast<typename E::Raw*>(st);
-      typename E::Raw* rd = reinterpret_cast<typename E::Raw*>(sd);
+      sm.pend_row[np] = b;
+      sm.pend_cnt[np] = 1;
+      sm.npend = np + 1;
+    }
+  };
+
+  int xc = 0;  // exchange counter: mailbox slot xc & 1
+  if (tid == 0) sm.npend = 0;
+  if (cl < P.units) issue(cl, 0);
+
+  // decision scalars of a unit (thread 0): drafted token and uniforms,
+  // fetched one unit ahead
+  auto fetch_scalars = [&](int u, int& y_, float& ua_, float& uf_) {
+    y_ = -1;
+    ua_ = 0.0f;
+    uf_ = 0.0f;
+    if constexpr (kVerifyMode) {
+      const Unit x = decode(u);
+      if (!x.bonus) y_ = P.draft_tokens[x.b * K + x.k];
+      if constexpr (MODE == kVerify) {
+        if (!x.bonus) ua_ = P.u_accept[x.b * K + x.k];
+        uf_ = P.u_final[x.b];
+      }
+    }
+  };
+  int y_next = -1;
+  float ua_next = 0.0f, uf_next = 0.0f;
+  if (tid == 0 && cl < P.units) fetch_scalars(cl, y_next, ua_next, uf_next);
+
+  for (int it = 0;; ++it) {
+    const int u = cl + it * G;
+    if (u >= P.units) break;
+    const int stg = (nst == 2) ? (it & 1) : 0;
+    const uint32_t par = (nst == 2) ? ((uint32_t)(it >> 1) & 1u) : ((uint32_t)it & 1u);
+    if (nst == 2) {
+      if (u + G < P.units) issue(u + G, stg ^ 1);
+    } else if (it > 0) {
+      issue(u, 0);  // this warp finished reading its segment of the previous unit
+    }
+    const Unit x = decode(u);
+
+    // this unit's scalars (thread 0), and the next unit's in flight
+    const int y = y_next;
+    const float ua = ua_next, uf = uf_next;
+    if (tid == 0 && u + G < P.units) fetch_scalars(u + G, y_next, ua_next, uf_next);
+    const bool tok_ok = x.bonus || (y >= 0 && y < V);
+
+    // queued arrivals are published when the queue is full
+    if (warp == 0 && __shfl_sync(kFull, sm.npend, 0) == 32) flush();
+
+    uint4* st = stage_t(stg);
+    uint4* sd = st + nvec_alloc;
+    bool ok = true;
+    if (bulk) {
+      ok = mbar_wait_bounded(smem_addr(&sm.mbar[stg][warp]), par, kWaitLimitNs);
+    } else if (v_hi > v_lo) {
+      // element-wise staging for rows off 16-byte boundaries (-inf padding)
+      Raw* rt = reinterpret_cast<Raw*>(st);
+      Raw* rd = reinterpret_cast<Raw*>(sd);
       const int lo = v_lo * PV, hi = v_hi * PV;
       for (int i = lo + lane; i < hi; i += 32) {
         const bool in = (e0 + i) < e1;
-        rt[i] = in ? tg[e0 + i] : E::kNegInf;
-        if (has_draft) rd[i] = in ? dg[e0 + i] : E::kNegInf;
+        rt[i] = in ? x.tg[e0 + i] : E::kNegInf;
+        if (x.has_draft) rd[i] = in ? x.dg[e0 + i] : E::kNegInf;
       }
       __syncwarp();
     }
-  }
-  if (!staged && lane == 0) atomicOr(P.status, kTimeout);
-  const bool work = staged;
+    if (!ok && lane == 0 && P.status) atomicOr(P.status, kTimeout);
 
-  // Reads a value of field `slot` from every CTA of the cluster, in rank order.
-  auto gather_f = [&](float* slot, float* out) {
-    for (int r = 0; r < S; ++r) out[r] = ld_cluster_f32(map_rank(smem_addr(slot), r));
-  };
-
-  uint32_t flags = 0;
-  if (tid == 0) mail_tok = 0xFFFFFFFFu;  // peers write it only after exchange 3
-
-  if constexpr (kGreedy) {
-    // ================= greedy: argmax of target (and draft) =================
-    float bt = -INFINITY, bd = -INFINITY;
-    int jt = -1, jd = -1;
-    bool nan_seen = false;
-    if (work) {
-      for (int j = v_lo + lane; j < v_hi; j += 32) {
-        float x[PV];
-        E::unpack(st[j], x);
-        float vm = x[0];
-#pragma unroll
-        for (int i = 1; i < PV; ++i) vm = fmaxf(vm, x[i]);
-#pragma unroll
-        for (int i = 0; i < PV; ++i) nan_seen |= (x[i] != x[i]);
-        if (vm > bt) {
-          bt = vm;
-          jt = j;
-        }
-        if (has_draft) {
-          E::unpack(sd[j], x);
-          vm = x[0];
-#pragma unroll
-          for (int i = 1; i < PV; ++i) vm = fmaxf(vm, x[i]);
-#pragma unroll
-          for (int i = 0; i < PV; ++i) nan_seen |= (x[i] != x[i]);
-          if (vm > bd) {
-            bd = vm;
-            jd = j;
+    if constexpr (kGreedy) {
+      // ============ greedy: argmax of target (and draft) ============
+      float bt = -INFINITY, bd = -INFINITY;
+      int jt = -1, jd = -1;
+      bool nan_seen = false;
+      if (ok) {
+        // packed maximum per vector; only the winning vector is unpacked later
+        for (int j = v_lo + lane; j < v_hi; j += 32) {
+          bool nn;
+          float vm = E::vmax_nan(st[j], nn);
+          nan_seen |= nn;
+          if (vm > bt) {
+            bt = vm;
+            jt = j;
+          }
+          if (x.has_draft) {
+            vm = E::vmax_nan(sd[j], nn);
+            nan_seen |= nn;
+            if (vm > bd) {
+              bd = vm;
+              jd = j;
+            }
           }
         }
       }
-    }
-    int it = 0x7FFFFFFF, id = 0x7FFFFFFF;
-    if (jt >= 0) {
-      float x[PV];
-      E::unpack(st[jt], x);
-      for (int i = PV - 1; i >= 0; --i)
-        if (x[i] == bt) it = e0 + jt * PV + i;
-    }
-    if (jd >= 0) {
-      float x[PV];
-      E::unpack(sd[jd], x);
-      for (int i = PV - 1; i >= 0; --i)
-        if (x[i] == bd) id = e0 + jd * PV + i;
-    }
-    warp_argmax(bt, it);
-    warp_argmax(bd, id);
-    nan_seen = __any_sync(0xFFFFFFFFu, nan_seen);
-    if (lane == 0) {
-      red_a[warp] = bt;
-      red_i[warp] = it;
-      red_b[warp] = bd;
-      red_j[warp] = id;
-      red_c[warp] = nan_seen ? 1.0f : 0.0f;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float v1 = red_a[0], v2 = red_b[0], nn = red_c[0];
-      int i1 = red_i[0], i2 = red_j[0];
-      for (int w = 1; w < kWarps; ++w) {
-        arg_better(v1, i1, red_a[w], red_i[w]);
-        arg_better(v2, i2, red_b[w], red_j[w]);
-        nn = fmaxf(nn, red_c[w]);
+      int it_ = 0x7FFFFFFF, id_ = 0x7FFFFFFF;
+      if (jt >= 0) {
+        float xv[PV];
+        E::unpack(st[jt], xv);
+        for (int i = PV - 1; i >= 0; --i)
+          if (xv[i] == bt) it_ = e0 + jt * PV + i;
       }
-      mail_f[0] = v1;
-      mail_i[0] = i1;
-      mail_f[1] = v2;
-      mail_i[1] = i2;
-      mail_f[2] = nn;
-    }
-    cluster_sync();  // ---- exchange 1
-    if (rank == 0 && tid == 0) {
-      float v1 = -INFINITY, v2 = -INFINITY, nn = 0.0f;
-      int i1 = 0x7FFFFFFF, i2 = 0x7FFFFFFF;
-      for (int r = 0; r < S; ++r) {
-        arg_better(v1, i1, ld_cluster_f32(map_rank(smem_addr(&mail_f[0]), r)),
-                   (int)ld_cluster_u32(map_rank(smem_addr(&mail_i[0]), r)));
-        arg_better(v2, i2, ld_cluster_f32(map_rank(smem_addr(&mail_f[1]), r)),
-                   (int)ld_cluster_u32(map_rank(smem_addr(&mail_i[1]), r)));
-        nn = fmaxf(nn, ld_cluster_f32(map_rank(smem_addr(&mail_f[2]), r)));
+      if (jd >= 0) {
+        float xv[PV];
+        E::unpack(sd[jd], xv);
+        for (int i = PV - 1; i >= 0; --i)
+          if (xv[i] == bd) id_ = e0 + jd * PV + i;
       }
-      const bool bad = nn != 0.0f || !(v1 < INFINITY) || i1 == 0x7FFFFFFF ||
-                       (has_draft && (!(v2 < INFINITY) || i2 == 0x7FFFFFFF));
-      if (bad) flags |= kBadLogits;
-      const int am_t = bad ? -1 : i1;
-      const float al = has_draft ? ((am_t >= 0 && am_t == i2) ? 1.0f : 0.0f) : 0.0f;
-      bc_i[0] = am_t;
-      bc_f[0] = al;
-    }
-    cluster_sync();  // ---- peers may exit once rank 0 has read their mailboxes
-    if (rank != 0) return;
-    if constexpr (MODE == kVerifyGreedy) {
-      if (tid == 0) {
-        if (!bonus && !tok_ok) flags |= kBadToken;
-        VerifyRecord r;
-        r.acc = (!bonus && tok_ok && y == bc_i[0]) ? 1 : 0;
-        r.token = bc_i[0];
-        r.alpha = bc_f[0];
-        r.pad = 0;
-        P.rec[unit] = r;
-      }
-    } else {
-      if (tid == 0) {
-        P.alpha[b * K + k] = bc_f[0];
-        if (P.tv) P.tv[b * K + k] = 1.0f - bc_f[0];
-      }
-    }
-  } else {
-    // ================= sampling path: T > 0 =================
-    const float s = P.s;
-    // ---- pass A: maxima ----
-    typename E::MaxAcc mt, md;
-    if (work) {
-      for (int j = v_lo + lane; j < v_hi; j += 32) {
-        mt.add(st[j]);
-        if (has_draft) md.add(sd[j]);
-      }
-    }
-    {
-      const float a = warp_max(mt.get());
-      const float d = warp_max(md.get());
+      warp_argmax_redux(bt, it_);
+      warp_argmax_redux(bd, id_);
+      const bool nan_w = __any_sync(kFull, nan_seen);
       if (lane == 0) {
-        red_a[warp] = a;
-        red_b[warp] = d;
+        sm.wred[warp][0] = bt;
+        sm.wred[warp][1] = bd;
+        sm.wred[warp][2] = nan_w ? 1.0f : 0.0f;
+        sm.wredi[warp][0] = it_;
+        sm.wredi[warp][1] = id_;
       }
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float a = red_a[0], d = red_b[0];
-      for (int w = 1; w < kWarps; ++w) {
-        a = fmaxf(a, red_a[w]);
-        d = fmaxf(d, red_b[w]);
+      __syncthreads();
+      const int slot = xc & 1;
+      if (warp == 0) {
+        float v1 = -INFINITY, v2 = -INFINITY, nn = 0.0f;
+        int i1 = 0x7FFFFFFF, i2 = 0x7FFFFFFF;
+        if (lane < kWarps) {
+          v1 = sm.wred[lane][0];
+          v2 = sm.wred[lane][1];
+          nn = sm.wred[lane][2];
+          i1 = sm.wredi[lane][0];
+          i2 = sm.wredi[lane][1];
+        }
+        warp_argmax_redux(v1, i1);
+        warp_argmax_redux(v2, i2);
+        nn = redux_max_f32(nn);
+        push8(slot, v1, v2, nn, __int_as_float(i1), __int_as_float(i2), 0.0f, 0.0f, 0.0f);
       }
-      mail_f[0] = a;
-      mail_f[1] = d;
-    }
-    cluster_sync();  // ---- exchange 1
-    if (tid == 0) {
-      float a = -INFINITY, d = -INFINITY;
-      for (int r = 0; r < S; ++r) {
-        a = fmaxf(a, ld_cluster_f32(map_rank(smem_addr(&mail_f[0]), r)));
-        d = fmaxf(d, ld_cluster_f32(map_rank(smem_addr(&mail_f[1]), r)));
+      cluster_sync();  // ---- exchange 1
+      ++xc;
+      if (warp == 0) {
+        float v1 = mb(slot, 0, -INFINITY), v2 = mb(slot, 1, -INFINITY), nn = mb(slot, 2, 0.0f);
+        int i1 = lane < S ? __float_as_int(sm.mbox[slot][lane][3]) : 0x7FFFFFFF;
+        int i2 = lane < S ? __float_as_int(sm.mbox[slot][lane][4]) : 0x7FFFFFFF;
+        warp_argmax_redux(v1, i1);
+        warp_argmax_redux(v2, i2);
+        nn = redux_max_f32(nn);
+        if (rank == 0 && lane == 0) {
+          uint32_t flags = 0;
+          const bool bad = nn != 0.0f || !(v1 < INFINITY) || i1 == 0x7FFFFFFF ||
+                           (x.has_draft && (!(v2 < INFINITY) || i2 == 0x7FFFFFFF));
+          if (bad) flags |= kBadLogits;
+          const int am_t = bad ? -1 : i1;
+          const float al = x.has_draft ? ((am_t >= 0 && am_t == i2) ? 1.0f : 0.0f) : 0.0f;
+          if constexpr (MODE == kVerifyGreedy) {
+            if (!x.bonus && !tok_ok) flags |= kBadToken;
+            VerifyRecord r;
+            r.acc = (!x.bonus && tok_ok && y == am_t) ? 1 : 0;
+            r.token = am_t;
+            r.pad0 = r.pad1 = 0;
+            P.rec[u] = r;
+          }
+          P.part[(long long)u * kPartStride] = al;
+          if (flags && P.status) atomicOr(P.status, flags);
+        }
+        if (lane == 0) queue_arrival(x.b);
       }
-      bc_f[0] = __fmul_rn(a, s);  // c1t
-      bc_f[1] = __fmul_rn(d, s);  // c1d
-    }
-    __syncthreads();
-    const float c1t = bc_f[0], c1d = bc_f[1];
-
-    // ---- pass B: normalisers ----
-    float zt = 0.0f, zd = 0.0f;
-    if (work) {
-      for (int j = v_lo + lane; j < v_hi; j += 32) {
-        float x[PV], e[PV];
-        E::unpack(st[j], x);
+      continue;
+    } else {
+      // ============ sampling path: T > 0 ============
+      // ---- pass A: one sweep, running max per thread, sums rescaled when it grows ----
+      float mt = -INFINITY, md = -INFINITY, zt = 0.0f, zd = 0.0f;
+      if (ok && v_hi > v_lo) {
+        float ct = 0.0f, cd = 0.0f;  // fl(m * s) of the running maxima
+        for (int j = v_lo + lane; j < v_hi; j += 32) {
+          float xv[PV], e[PV];
+          const uint4 wt = st[j];
+          const float vt = E::vmax(wt);
+          if (vt > mt) {
+            const float cn = __fmul_rn(vt, s);
+            zt = (mt > -INFINITY) ? __fmul_rn(zt, ex2(__fadd_rn(ct, -cn))) : 0.0f;
+            ct = cn;
+            mt = vt;
+          }
+          if (mt > -INFINITY) {
+            E::unpack(wt, xv);
 #pragma unroll
-        for (int i = 0; i < PV; ++i) e[i] = ex2(fmaf(x[i], s, -c1t));
-        zt = __fadd_rn(zt, tree_sum(e));
-        if (has_draft) {
-          E::unpack(sd[j], x);
+            for (int i = 0; i < PV; ++i) e[i] = ex2(fmaf(xv[i], s, -ct));
+            zt = __fadd_rn(zt, tree_sum(e));
+          }
+          if (x.has_draft) {
+            const uint4 wd = sd[j];
+            const float vd = E::vmax(wd);
+            if (vd > md) {
+              const float cn = __fmul_rn(vd, s);
+              zd = (md > -INFINITY) ? __fmul_rn(zd, ex2(__fadd_rn(cd, -cn))) : 0.0f;
+              cd = cn;
+              md = vd;
+            }
+            if (md > -INFINITY) {
+              E::unpack(wd, xv);
 #pragma unroll
-          for (int i = 0; i < PV; ++i) e[i] = ex2(fmaf(x[i], s, -c1d));
-          zd = __fadd_rn(zd, tree_sum(e));
+              for (int i = 0; i < PV; ++i) e[i] = ex2(fmaf(xv[i], s, -cd));
+              zd = __fadd_rn(zd, tree_sum(e));
+            }
+          }
         }
       }
-    }
-    zt = warp_sum(zt);
-    zd = warp_sum(zd);
-    __syncthreads();  // red_* reuse
-    if (lane == 0) {
-      red_a[warp] = zt;
-      red_b[warp] = zd;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float a = 0.0f, d = 0.0f;
-      for (int w = 0; w < kWarps; ++w) {
-        a = __fadd_rn(a, red_a[w]);
-        d = __fadd_rn(d, red_b[w]);
+      warp_combine_mz2(mt, zt, md, zd, s);
+      if (lane == 0) {
+        sm.wred[warp][0] = mt;
+        sm.wred[warp][1] = zt;
+        sm.wred[warp][2] = md;
+        sm.wred[warp][3] = zd;
       }
-      mail_f[2] = a;
-      mail_f[3] = d;
-    }
-    cluster_sync();  // ---- exchange 2
-    if (tid == 0) {
-      float a = 0.0f, d = 0.0f;
-      for (int r = 0; r < S; ++r) {
-        a = __fadd_rn(a, ld_cluster_f32(map_rank(smem_addr(&mail_f[2]), r)));
-        d = __fadd_rn(d, ld_cluster_f32(map_rank(smem_addr(&mail_f[3]), r)));
-      }
-      const bool valid = (a > 0.0f && a < INFINITY) && (!has_draft || (d > 0.0f && d < INFINITY));
-      int mode_c = 0;  // 0: overlap only, 1: residual draw, 2: draw from p
-      int acc = 1;
-      if constexpr (MODE == kVerify) {
-        if (bonus) {
-          mode_c = 2;
-        } else {
-          // Acceptance: u * q(y) <= p(y), with p(y), q(y) formed exactly like
-          // the per-element values of the residual pass.
-          const float py = __fmul_rn(ex2(fmaf(zt_y, s, -c1t)), 1.0f / a);
-          const float qy = __fmul_rn(ex2(fmaf(zd_y, s, -c1d)), 1.0f / d);
-          acc = (tok_ok && __fmul_rn(u, qy) <= py) ? 1 : 0;
-          mode_c = acc ? 0 : 1;
+      __syncthreads();
+      int slot = xc & 1;
+      if (warp == 0) {
+        float a = -INFINITY, za = 0.0f, d = -INFINITY, zda = 0.0f;
+        if (lane < kWarps) {
+          a = sm.wred[lane][0];
+          za = sm.wred[lane][1];
+          d = sm.wred[lane][2];
+          zda = sm.wred[lane][3];
         }
-        if (!(u >= 0.0f && u < 1.0f) && !bonus) flags |= kBadUniform;
-        if (!(uf >= 0.0f && uf < 1.0f)) flags |= kBadUniform;
-        if (!tok_ok) flags |= kBadToken;
+        warp_combine_mz2(a, za, d, zda, s);
+        // the CTA holding the drafted token publishes its two logits
+        float gt = 0.0f, gd = 0.0f;
+        if constexpr (MODE == kVerify) {
+          if (lane == 0 && !x.bonus && tok_ok && y >= e0 && y < e1) {
+            gt = E::to_f32(reinterpret_cast<const Raw*>(st)[y - e0]);
+            gd = E::to_f32(reinterpret_cast<const Raw*>(sd)[y - e0]);
+          }
+          gt = __shfl_sync(kFull, gt, 0);
+          gd = __shfl_sync(kFull, gd, 0);
+        }
+        push8(slot, a, za, d, zda, gt, gd, 0.0f, 0.0f);
       }
-      if (!valid) {
-        flags |= kBadLogits;
-        mode_c = 3;  // skip: invalid row
+      cluster_sync();  // ---- exchange 1: (max, sum) of both rows
+      ++xc;
+      if (warp == 0) {
+        float a = mb(slot, 0, -INFINITY), za = mb(slot, 1, 0.0f);
+        float d = mb(slot, 2, -INFINITY), zda = mb(slot, 3, 0.0f);
+        float zty = 0.0f, zdy = 0.0f;
+        if constexpr (MODE == kVerify) {
+          const int yy = __shfl_sync(kFull, y, 0);
+          const bool ok_y = __shfl_sync(kFull, (int)tok_ok, 0) != 0;
+          const int own = (ok_y && !x.bonus) ? yy / P.L : 0;
+          zty = sm.mbox[slot][own][4];
+          zdy = sm.mbox[slot][own][5];
+        }
+        warp_combine_mz2(a, za, d, zda, s);
+        if (lane == 0) {
+          const float Zt = za, Zd = zda;
+          const float c1t = __fmul_rn(a, s), c1d = __fmul_rn(d, s);
+          const bool valid = (Zt > 0.0f && Zt < INFINITY) && (!x.has_draft || (Zd > 0.0f && Zd < INFINITY));
+          const float izt = __frcp_rn(Zt), izd = __frcp_rn(Zd);
+          uint32_t flags = 0;
+          int mode_c = 0;  // 0: overlap only, 1: residual draw, 2: draw from p, 3: invalid
+          int acc = 1;
+          if constexpr (MODE == kVerify) {
+            if (x.bonus) {
+              mode_c = 2;
+            } else {
+              // u * q(y) <= p(y), with p(y), q(y) formed like the per-element values
+              const float py = __fmul_rn(ex2(fmaf(zty, s, -c1t)), izt);
+              const float qy = __fmul_rn(ex2(fmaf(zdy, s, -c1d)), izd);
+              acc = (tok_ok && __fmul_rn(ua, qy) <= py) ? 1 : 0;
+              mode_c = acc ? 0 : 1;
+              if (!(ua >= 0.0f && ua < 1.0f)) flags |= kBadUniform;
+              if (!tok_ok) flags |= kBadToken;
+            }
+            if (!(uf >= 0.0f && uf < 1.0f)) flags |= kBadUniform;
+          }
+          if (!valid) {
+            flags |= kBadLogits;
+            mode_c = 3;
+          }
+          if (flags && rank == 0 && P.status) atomicOr(P.status, flags);
+          sm.bcf[0] = c1t;
+          sm.bcf[1] = c1d;
+          sm.bcf[2] = (x.has_draft && valid) ? c1d + __log2f(__fmul_rn(Zd, izt)) : 0.0f;  // c1d + log2(Z_d / Z_t)
+          sm.bcf[3] = izt;
+          sm.bcf[4] = __fmul_rn(Zt, izd);
+          sm.bcf[5] = uf;
+          sm.bci[0] = mode_c;
+          sm.bci[1] = acc;
+        }
       }
-      bc_f[2] = a;
-      bc_f[3] = d;
-      bc_f[5] = has_draft && valid ? c1d + log2f(d / a) : 0.0f;  // c1d + log2(Z_d / Z_t)
-      bc_i[0] = mode_c;
-      bc_i[1] = acc;
-    }
-    __syncthreads();
-    const float Zt = bc_f[2], Zd = bc_f[3], cd2 = bc_f[5];
-    int mode_c = bc_i[0];
-    const int acc = bc_i[1];
+      __syncthreads();
+      const float c1t = sm.bcf[0], c1d = sm.bcf[1], cd2 = sm.bcf[2], izt = sm.bcf[3], ratio = sm.bcf[4];
+      const float ufin = sm.bcf[5];
+      int mode_c = sm.bci[0];
+      const int acc = sm.bci[1];
 
-    // ---- pass C ----
-    float alpha_part = 0.0f, smass_part = 0.0f;
-    float a_sum = 0.0f, s_sum = 0.0f;  // cluster totals (thread 0 of rank 0)
-    int token = -1;
-    for (int attempt = 0; attempt < 2; ++attempt) {
-      if (mode_c == 0 && attempt == 0) {
-        // overlap through min(log2 p, log2 q): one exp per element
-        if (work && has_draft) {
+      if (mode_c == 0 || mode_c == 3) {
+        // ---- pass C: overlap (and E2E S-mass) partials, no exchange ----
+        float a = 0.0f, m2 = 0.0f;
+        if (mode_c == 0 && ok && x.has_draft) {
           for (int j = v_lo + lane; j < v_hi; j += 32) {
             float t[PV], d[PV], e[PV], g[PV];
             E::unpack(st[j], t);
@@ -581,149 +831,160 @@ __global__ void __launch_bounds__(kThreads) sweep_kernel(const SweepParams P) {
               e[i] = ex2(fminf(xt, xd));
               if constexpr (MODE == kE2E) g[i] = (xd < xt) ? e[i] : 0.0f;
             }
-            alpha_part = __fadd_rn(alpha_part, tree_sum(e));
-            if constexpr (MODE == kE2E) smass_part = __fadd_rn(smass_part, tree_sum(g));
+            a = __fadd_rn(a, tree_sum(e));
+            if constexpr (MODE == kE2E) m2 = __fadd_rn(m2, tree_sum(g));
           }
         }
-        alpha_part = warp_sum(alpha_part);
-        smass_part = warp_sum(smass_part);
-        __syncthreads();
+        a = warp_sum(a);
+        if constexpr (MODE == kE2E) m2 = warp_sum(m2);
         if (lane == 0) {
-          red_a[warp] = alpha_part;
-          red_b[warp] = smass_part;
+          sm.wred[warp][0] = a;
+          sm.wred[warp][1] = m2;
         }
         __syncthreads();
-        if (tid == 0) {
-          float a = 0.0f, m = 0.0f;
-          for (int w = 0; w < kWarps; ++w) {
-            a = __fadd_rn(a, red_a[w]);
-            m = __fadd_rn(m, red_b[w]);
-          }
-          mail_f[4] = a;
-          mail_f[5] = m;
-        }
-        cluster_sync();  // ---- exchange 3
-        if (rank == 0 && tid == 0) {
-          for (int r = 0; r < S; ++r) {
-            a_sum = __fadd_rn(a_sum, ld_cluster_f32(map_rank(smem_addr(&mail_f[4]), r)));
-            s_sum = __fadd_rn(s_sum, ld_cluster_f32(map_rank(smem_addr(&mail_f[5]), r)));
-          }
-        }
-        break;
-      }
-      if (mode_c == 3) {
-        cluster_sync();  // keep the barrier count of the other branches
-        break;
-      }
-      // ---- residual (mode 1) or target (mode 2) draw ----
-      const bool resid = (mode_c == 1);
-      const float ratio = __fdiv_rn(Zt, Zd);
-      float run = 0.0f, mmass = 0.0f;
-      const int nrounds = (v_hi - v_lo + 31) >> 5;
-      if (work) {
-        for (int rr = 0; rr < nrounds; ++rr) {
-          const int j = v_lo + rr * 32 + lane;
-          float rs = 0.0f;
-          if (j < v_hi) {
-            float w[PV];
-            rs = resid ? draw_weights<E, true>(st[j], sd[j], s, c1t, c1d, ratio, w, mmass)
-                       : draw_weights<E, false>(st[j], st[j], s, c1t, c1d, ratio, w, mmass);
-          }
-          const float incl = warp_incl_scan(rs, lane);
-          run = __fadd_rn(run, __shfl_sync(0xFFFFFFFFu, incl, 31));
-        }
-      }
-      mmass = warp_sum(mmass);
-      __syncthreads();
-      if (lane == 0) {
-        warp_total[warp] = run;
-        red_a[warp] = mmass;
-      }
-      __syncthreads();
-      if (tid == 0) {
-        float tot = 0.0f, a = 0.0f;
-        for (int w = 0; w < kWarps; ++w) {
-          tot = __fadd_rn(tot, warp_total[w]);
-          a = __fadd_rn(a, red_a[w]);
-        }
-        mail_f[6 + attempt] = tot;  // own slot per attempt: no reuse race
-        if (attempt == 0) mail_f[4] = a;
-      }
-      cluster_sync();  // ---- exchange 3
-      if (tid == 0) {
-        // Locate the CTA whose slice holds u' * total (vocabulary order).
-        float off = 0.0f, tot_all = 0.0f, my_off = 0.0f, my_tot = 0.0f;
-        int owner = -1, last_pos = -1;
-        float parts[16];
-        for (int r = 0; r < S; ++r) parts[r] = ld_cluster_f32(map_rank(smem_addr(&mail_f[6 + attempt]), r));
-        for (int r = 0; r < S; ++r) tot_all = __fadd_rn(tot_all, parts[r]);
-        const float thr = __fmul_rn(uf, tot_all);
-        for (int r = 0; r < S; ++r) {
-          const float nxt = __fadd_rn(off, parts[r]);
-          if (owner < 0 && nxt > thr) owner = r;
-          if (parts[r] > 0.0f) last_pos = r;
-          if (r == (int)rank) {
-            my_off = off;
-            my_tot = parts[r];
-          }
-          off = nxt;
-        }
-        bool fallback = false;
-        if (owner < 0) {
-          owner = last_pos;
-          fallback = true;
-        }
-        if (attempt == 0 && rank == 0)
-          for (int r = 0; r < S; ++r) a_sum = __fadd_rn(a_sum, ld_cluster_f32(map_rank(smem_addr(&mail_f[4]), r)));
-        bc_i[2] = (tot_all > 0.0f) ? 1 : 0;
-        bc_i[3] = (owner == (int)rank) ? 1 : 0;
-        bc_f[4] = fallback ? INFINITY : __fadd_rn(thr, -my_off);
-        (void)my_tot;
-      }
-      __syncthreads();
-      if (!bc_i[2]) {
-        // Rejection with no residual mass (rounding only): draw from p.
-        if (attempt == 0 && resid) {
-          flags |= kEmptyResidual;
-          mode_c = 2;
-          continue;
-        }
-        break;  // no mass at all: no token
-      }
-      if (bc_i[3]) {
-        // This CTA owns the threshold: warp offsets, then the owning warp
-        // replays its rounds bit-identically to find the element.
-        __shared__ int s_warp;
-        __shared__ float s_thr;
-        if (tid == 0) {
-          const float th = bc_f[4];
-          float off = 0.0f;
-          int wsel = -1, wlast = -1;
-          float wthr = INFINITY;
-          for (int w = 0; w < kWarps; ++w) {
-            const float nxt = __fadd_rn(off, warp_total[w]);
-            if (wsel < 0 && nxt > th) {
-              wsel = w;
-              wthr = __fadd_rn(th, -off);
+        if (warp == 0) {
+          float A = lane < kWarps ? sm.wred[lane][0] : 0.0f;
+          float M2 = lane < kWarps ? sm.wred[lane][1] : 0.0f;
+          A = warp_sum(A);
+          if constexpr (MODE == kE2E) M2 = warp_sum(M2);
+          if (lane == 0) {
+            const float nanv = __int_as_float(0x7FC00000);
+            P.part[(long long)u * kPartStride + rank] = (mode_c == 3) ? nanv : __fmul_rn(A, izt);
+            if constexpr (MODE == kE2E) {
+              P.part2[(long long)u * kPartStride + rank] = (mode_c == 3) ? nanv : __fmul_rn(M2, izt);
+              if (rank == 0) {
+                E2EStats e2;
+                e2.c1t = c1t;
+                e2.cd = cd2;
+                e2.izt = izt;
+                e2.smass = e2.alpha = e2.b1 = e2.b0 = e2.pad = 0.0f;
+                P.stats[u] = e2;
+              }
             }
-            if (warp_total[w] > 0.0f) wlast = w;
-            off = nxt;
+            if constexpr (MODE == kVerify) {
+              if (rank == 0) {
+                VerifyRecord r;
+                r.acc = (mode_c == 3) ? 0 : acc;
+                r.token = -1;
+                r.pad0 = r.pad1 = 0;
+                P.rec[u] = r;
+              }
+            }
+            queue_arrival(x.b);
           }
-          if (wsel < 0) {
-            wsel = wlast;
-            wthr = INFINITY;
+        }
+        continue;
+      }
+
+      // ---- pass C': residual (mode 1) or target (mode 2) draw ----
+      for (int attempt = 0; attempt < 2; ++attempt) {
+        const bool resid = (mode_c == 1);
+        float run = 0.0f, mm = 0.0f;
+        if (ok) {
+          for (int r = 0; r < nrounds; ++r) {
+            const int j = v_lo + r * 32 + lane;
+            float rs = 0.0f, w[PV];
+            if (j < v_hi)
+              rs = resid ? draw_weights<E, true>(st[j], sd[j], s, c1t, c1d, ratio, w, mm)
+                         : draw_weights<E, false>(st[j], st[j], s, c1t, c1d, ratio, w, mm);
+            const float incl = warp_incl_scan(rs, lane);
+            if (lane == 0) sm.wrun[warp][r] = run;
+            run = __fadd_rn(run, __shfl_sync(kFull, incl, 31));
           }
-          s_warp = wsel;
-          s_thr = wthr;
+        }
+        mm = warp_sum(mm);
+        if (lane == 0) {
+          sm.wrun[warp][ok ? nrounds : 0] = run;
+          sm.wtot[warp] = run;
+          sm.wred[warp][0] = mm;
         }
         __syncthreads();
-        if (warp == s_warp) {
-          const float th = s_thr;
-          float rrun = 0.0f;
-          int found = -1;
-          int last_el = -1;
-          for (int rr = 0; rr < nrounds && found < 0; ++rr) {
-            const int j = v_lo + rr * 32 + lane;
+        slot = xc & 1;
+        if (warp == 0) {
+          // warp offsets inside the CTA (one scan, so every later comparison
+          // uses the same numbers), the CTA total, and the overlap partial
+          const float wt = lane < kWarps ? sm.wtot[lane] : 0.0f;
+          const float incl = warp_incl_scan(wt, lane);
+          if (lane < kWarps) sm.woff[lane + 1] = incl;
+          if (lane == 0) sm.woff[0] = 0.0f;
+          const float tot = __shfl_sync(kFull, incl, kWarps - 1);
+          float A = lane < kWarps ? sm.wred[lane][0] : 0.0f;
+          A = warp_sum(A);
+          if (lane == 0 && attempt == 0 && resid) P.part[(long long)u * kPartStride + rank] = __fmul_rn(A, izt);
+          push8(slot, tot, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f);
+        }
+        cluster_sync();  // ---- exchange 2: CTA totals of the draw weights
+        ++xc;
+        if (warp == 0) {
+          const float tr = mb(slot, 0, 0.0f);
+          const float incl = warp_incl_scan(tr, lane);
+          const float total = __shfl_sync(kFull, incl, 31);
+          const float thr = __fmul_rn(ufin, total);
+          const unsigned hit = __ballot_sync(kFull, lane < S && incl > thr);
+          const unsigned pos = __ballot_sync(kFull, lane < S && tr > 0.0f);
+          int owner = -1;
+          bool fb = false;
+          if (hit) {
+            owner = __ffs(hit) - 1;
+          } else if (pos) {
+            owner = 31 - __clz(pos);
+            fb = true;
+          }
+          const float excl = __shfl_up_sync(kFull, incl, 1);
+          const float ex_o = __shfl_sync(kFull, excl, owner > 0 ? owner : 0);
+          if (lane == 0) {
+            sm.bci[2] = (total > 0.0f) ? 1 : 0;
+            sm.bci[3] = owner;
+            sm.bcf[6] = fb ? INFINITY : __fadd_rn(thr, owner > 0 ? -ex_o : 0.0f);
+          }
+        }
+        __syncthreads();
+        if (!sm.bci[2]) {
+          if (attempt == 0 && resid) {  // rejection with no residual mass (rounding): draw from p
+            if (rank == 0 && tid == 0 && P.status) atomicOr(P.status, kEmptyResidual);
+            mode_c = 2;
+            continue;
+          }
+          break;  // nothing to draw: the token stays -1
+        }
+        if (sm.bci[3] == (int)rank) {
+          if (tid == 0) {
+            // the warp, then the round, holding the local threshold
+            const float th = sm.bcf[6];
+            int wsel = -1, wlast = -1;
+            for (int w = 0; w < kWarps; ++w) {
+              if (wsel < 0 && sm.woff[w + 1] > th) wsel = w;
+              if (sm.wtot[w] > 0.0f) wlast = w;
+            }
+            float thw = INFINITY;
+            if (wsel >= 0) {
+              thw = __fadd_rn(th, -sm.woff[wsel]);
+            } else {
+              wsel = wlast;
+            }
+            if (wsel < 0) wsel = 0;  // no positive weight in this CTA (rounding only)
+            const int lo = min(wsel * seg, nvec), hi = min(lo + seg, nvec);
+            const int nr = (hi - lo + 31) >> 5;
+            int rsel = -1, rlast = 0;
+            for (int r = 0; r < nr; ++r) {
+              if (rsel < 0 && sm.wrun[wsel][r + 1] > thw) rsel = r;
+              if (sm.wrun[wsel][r + 1] > sm.wrun[wsel][r]) rlast = r;
+            }
+            if (rsel < 0) {
+              rsel = rlast;
+              thw = INFINITY;
+            }
+            sm.bci[4] = wsel;
+            sm.bci[5] = rsel;
+            sm.bci[6] = -1;
+            sm.bcf[7] = thw;
+          }
+          __syncthreads();
+          if (warp == sm.bci[4]) {
+            const int r = sm.bci[5];
+            const float th = sm.bcf[7];
+            const float base = sm.wrun[warp][r];
+            const int j = v_lo + r * 32 + lane;
             float rs = 0.0f, w[PV], dummy = 0.0f;
 #pragma unroll
             for (int i = 0; i < PV; ++i) w[i] = 0.0f;
@@ -731,177 +992,42 @@ __global__ void __launch_bounds__(kThreads) sweep_kernel(const SweepParams P) {
               rs = resid ? draw_weights<E, true>(st[j], sd[j], s, c1t, c1d, ratio, w, dummy)
                          : draw_weights<E, false>(st[j], st[j], s, c1t, c1d, ratio, w, dummy);
             const float incl = warp_incl_scan(rs, lane);
-            const float rtot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-            // remember the last positive element seen, for the fallback
-            int my_last = -1;
+            const float excl = __shfl_up_sync(kFull, incl, 1);
+            const unsigned hit = __ballot_sync(kFull, __fadd_rn(base, incl) > th);
+            const unsigned pos = __ballot_sync(kFull, rs > 0.0f);
+            const int l = hit ? (__ffs(hit) - 1) : (pos ? 31 - __clz(pos) : -1);
+            if (lane == l) {
+              float accu = __fadd_rn(base, lane > 0 ? excl : 0.0f);
+              int pick = -1, lastp = -1;
 #pragma unroll
-            for (int i = 0; i < PV; ++i)
-              if (w[i] > 0.0f) my_last = e0 + j * PV + i;
-            const unsigned pos = __ballot_sync(0xFFFFFFFFu, my_last >= 0);
-            if (pos) last_el = __shfl_sync(0xFFFFFFFFu, my_last, 31 - __clz(pos));
-            if (__fadd_rn(rrun, rtot) > th) {
-              const unsigned hit = __ballot_sync(0xFFFFFFFFu, __fadd_rn(rrun, incl) > th);
-              const int l = __ffs(hit) - 1;
-              const float excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
-              if (lane == l) {
-                float accu = __fadd_rn(rrun, lane > 0 ? excl : 0.0f);
-                int pick = -1, lastp = -1;
-#pragma unroll
-                for (int i = 0; i < PV; ++i) {
-                  accu = __fadd_rn(accu, w[i]);
-                  if (w[i] > 0.0f) {
-                    lastp = i;
-                    if (pick < 0 && accu > th) pick = i;
-                  }
+              for (int i = 0; i < PV; ++i) {
+                accu = __fadd_rn(accu, w[i]);
+                if (w[i] > 0.0f) {
+                  lastp = i;
+                  if (pick < 0 && accu > th) pick = i;
                 }
-                if (pick < 0) pick = lastp;
-                found = e0 + j * PV + pick;
               }
-              found = __shfl_sync(0xFFFFFFFFu, found, l);
+              if (pick < 0) pick = lastp;
+              if (pick >= 0) sm.bci[6] = e0 + j * PV + pick;
             }
-            rrun = __fadd_rn(rrun, rtot);
           }
-          if (found < 0) found = last_el;
-          if (lane == 0) st_cluster_u32(map_rank(smem_addr(&mail_tok), 0), (uint32_t)found);
         }
-      }
-      break;
-    }
-    cluster_sync();  // ---- exchange 4: token in rank 0; peers done reading
-    if (rank != 0) return;
-    if (tid == 0) {
-      const float izt = 1.0f / Zt;
-      if (mode_c == 1 || mode_c == 2) token = (int)mail_tok;  // -1 if no draw completed
-      if constexpr (MODE == kVerify) {
-        VerifyRecord r;
-        r.acc = acc;
-        r.token = (mode_c == 3) ? -1 : token;
-        r.alpha = (mode_c == 3) ? __int_as_float(0x7FC00000) : __fmul_rn(a_sum, izt);
-        r.pad = 0;
-        P.rec[unit] = r;
-      } else if constexpr (MODE == kOverlap) {
-        const float al = (mode_c == 3) ? __int_as_float(0x7FC00000) : __fmul_rn(a_sum, izt);
-        P.alpha[b * K + k] = al;
-        if (P.tv) P.tv[b * K + k] = 1.0f - al;
-      } else {  // kE2E
-        E2EStats st2;
-        st2.c1t = c1t;
-        st2.cd = cd2;
-        st2.izt = izt;
-        st2.smass = __fmul_rn(s_sum, izt);
-        st2.alpha = (mode_c == 3) ? __int_as_float(0x7FC00000) : __fmul_rn(a_sum, izt);
-        st2.b1 = 0.0f;
-        st2.b0 = 0.0f;
-        st2.pad = 0.0f;
-        P.stats[unit] = st2;
-      }
-    }
-  }
-
-  // ================= per-row completion (rank 0 only) =================
-  __shared__ int s_last;
-  if (tid == 0) {
-    if (flags) atomicOr(P.status, flags);
-    bool need = true;
-    if constexpr (MODE == kOverlap || MODE == kOverlapGreedy) need = (P.surv != nullptr || P.exp_acc != nullptr);
-    int last = 0;
-    if (need) {
-      __threadfence();
-      const uint32_t per_row = kVerifyMode ? (uint32_t)(K + 1) : (uint32_t)K;
-      const uint32_t old = atomicAdd(&P.row_cnt[b], 1u);
-      last = (old == per_row - 1) ? 1 : 0;
-      if (last) __threadfence();
-    }
-    s_last = last;
-  }
-  __syncthreads();
-  if (!s_last) return;
-
-  if constexpr (kVerifyMode) {
-    // One warp decides the row: first rejection in prefix order.
-    if (warp != 0) return;
-    const VerifyRecord* rr = P.rec + (long long)b * (K + 1);
-    int nacc = K;
-    for (int base = 0; base < K; base += 32) {
-      const int kk = base + lane;
-      bool rej = false;
-      if (kk < K) rej = (__ldcg(&rr[kk].acc) == 0);
-      const unsigned m = __ballot_sync(0xFFFFFFFFu, rej);
-      if (m) {
-        nacc = base + __ffs(m) - 1;
         break;
       }
-    }
-    const int corr = __ldcg(&rr[nacc].token);
-    for (int kk = lane; kk <= K; kk += 32) {
-      int tokv = -1;
-      if (kk < nacc) tokv = P.draft_tokens[b * K + kk];
-      else if (kk == nacc) tokv = corr;
-      P.out_tokens[(long long)b * (K + 1) + kk] = tokv;
-      if (kk < K && P.alpha) P.alpha[b * K + kk] = __ldcg(&rr[kk].alpha);
-    }
-    __syncwarp();
-    // Leave the workspace zero-filled: the records of this row are consumed.
-    VerifyRecord* rw = P.rec + (long long)b * (K + 1);
-    for (int kk = lane; kk <= K; kk += 32) rw[kk] = VerifyRecord{0, 0, 0.0f, 0u};
-    if (lane == 0) {
-      P.n_accepted[b] = nacc;
-      P.row_cnt[b] = 0;
-    }
-  } else if constexpr (MODE == kOverlap || MODE == kOverlapGreedy) {
-    if (tid != 0) return;
-    float pr = 1.0f, sum = 0.0f;
-    for (int kk = 0; kk < K; ++kk) {
-      pr = __fmul_rn(pr, __ldcg(&P.alpha[b * K + kk]));
-      sum = __fadd_rn(sum, pr);
-      if (P.surv) P.surv[b * K + kk] = pr;
-    }
-    if (P.exp_acc) P.exp_acc[b] = sum;
-    P.row_cnt[b] = 0;
-  } else {  // kE2E
-    __shared__ int s_glast;
-    if (tid == 0) {
-      E2EStats* sr = P.stats + (long long)b * K;
-      // prefix products P_{k-1} and suffix sums G_k = 1 + alpha_{k+1} G_{k+1}
-      float g = 1.0f;
-      float suffix[64];
-      for (int kk = K - 1; kk >= 0; --kk) {
-        suffix[kk] = g;
-        g = fmaf(__ldcg(&sr[kk].alpha), g, 1.0f);
+      __syncthreads();  // the owner warp's token reaches thread 0
+      if (tid == 0) {
+        if (rank == 0) {
+          P.rec[u].acc = (MODE == kVerify && !x.bonus) ? acc : 0;
+          if (!sm.bci[2]) P.rec[u].token = -1;
+        }
+        if (sm.bci[2] && sm.bci[3] == (int)rank) P.rec[u].token = sm.bci[6];
+        queue_arrival(x.b);
       }
-      float pre = 1.0f, rowl = 0.0f;
-      const float scale = P.grad_scale / (float)P.B;
-      for (int kk = 0; kk < K; ++kk) {
-        const float al = __ldcg(&sr[kk].alpha);
-        const float coef = __fmul_rn(__fmul_rn(scale, pre), suffix[kk]);
-        const float A = __fmul_rn(__fmul_rn(coef, __ldcg(&sr[kk].izt)), P.inv_t);
-        const float S_ = __ldcg(&sr[kk].smass);
-        sr[kk].b1 = __fmul_rn(A, 1.0f - S_);
-        sr[kk].b0 = __fmul_rn(A, -S_);
-        pre = __fmul_rn(pre, al);
-        rowl = __fadd_rn(rowl, pre);
-        if (P.alpha) P.alpha[b * K + kk] = al;
-      }
-      P.row_loss[b] = rowl;
-      P.row_cnt[b] = 0;
-      __threadfence();
-      const uint32_t old = atomicAdd(P.glob_cnt, 1u);
-      s_glast = (old == (uint32_t)P.B - 1) ? 1 : 0;
-      if (s_glast) __threadfence();
-    }
-    __syncthreads();
-    if (!s_glast || warp != 0) return;
-    float acc_l = 0.0f;
-    for (int i = lane; i < P.B; i += 32) {
-      acc_l = __fadd_rn(acc_l, __ldcg(&P.row_loss[i]));
-      P.row_loss[i] = 0.0f;  // consumed: leave the workspace zero-filled
-    }
-    acc_l = warp_sum(acc_l);
-    if (lane == 0) {
-      *P.loss = acc_l / (float)P.B;
-      *P.glob_cnt = 0;
     }
   }
+  __syncthreads();
+  if (warp == 0) flush();
+  cluster_sync();  // no CTA leaves while a peer may still write to its mailbox
 }
 
 // ---- E2E-TV gradient: one streaming pass over both logit tensors ------------------

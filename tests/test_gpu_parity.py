@@ -116,15 +116,16 @@ def test_shapes_against_oracle(ssv, B, K, V, dtype, T):
         assert (tok[b, n[b] + 1:] == -1).all()
 
 
-@pytest.mark.parametrize("S", [1, 2, 3, 4, 8, 16])
-def test_cluster_sizes_agree(ssv, S):
+@pytest.mark.parametrize("S,nst", [(1, 2), (2, 1), (3, 2), (4, 1), (8, 2), (12, 1), (16, 2)])
+def test_launch_shapes_agree(ssv, S, nst):
     w = synth.gaussian(6, 3, 24000, sigma=2.0, noise=0.6, dtype=torch.bfloat16, temperature=1.0, seed=77)
-    ssv.set_cluster_override(S)
+    ssv.set_launch_override(S, nst)
     try:
+        assert ssv.launch_shape(torch.bfloat16, 6 * 4, 24000)[0] == S
         out = ssv.verify(*to_dev(w), w.temperature)
         torch.cuda.synchronize()
     finally:
-        ssv.set_cluster_override(0)
+        ssv.set_launch_override(0, 0)
     assert_verify(out, oracle_verify(w))
 
 
