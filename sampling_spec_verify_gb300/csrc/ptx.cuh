@@ -102,8 +102,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uin
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
+  uint32_t backoff = 32;
   for (;;) {
+    __nanosleep(backoff);  // a waiting warp issues (almost) nothing
     if (mbar_try_wait(bar, parity)) return true;
+    if (backoff < 256) backoff <<= 1;
     if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
