@@ -131,6 +131,12 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// Asks L2 to fetch [src, src + bytes) ahead of a later bulk copy of it.
+// `src` 16-byte aligned; `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ---- warp reductions in one instruction ---------------------------------------
 
 // Maximum of a float over the full warp (NaN inputs are ignored).
@@ -153,6 +159,37 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// ---- packed fp32 pairs: one instruction rounds two independent lanes ------------
+// Each lane of fma/add.rn.f32x2 is rounded exactly like its scalar fmaf /
+// __fadd_rn counterpart.
+
+using f32x2 = uint64_t;
+
+__device__ __forceinline__ f32x2 f2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(f32x2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// lo + hi of a pair
+__device__ __forceinline__ float f2_hsum(f32x2 v) {
+  float lo, hi;
+  f2_split(v, lo, hi);
+  return __fadd_rn(lo, hi);
 }
 
 }  // namespace ssv

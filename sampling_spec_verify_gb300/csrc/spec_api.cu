@@ -117,7 +117,7 @@ int max_active_clusters(Fn fn, int S, int smem) {
 // Picks the cluster size S and the stage count for a sweep over V: the
 // stages must fit in shared memory, and among the shapes that fit the one
 // with the lowest estimated time wins -- (units per cluster, rounded up) x
-// (rounds of 32 vectors per warp + a fixed per-unit allowance for the
+// (vectors per thread + a fixed per-unit allowance for the
 // exchanges, larger when the load of a unit is not prefetched).
 template <class Fn>
 bool pick_shape(Fn fn, int es, long long units, int V, int rows, Shape* out) {
@@ -136,13 +136,12 @@ bool pick_shape(Fn fn, int es, long long units, int V, int rows, Shape* out) {
       const long long smem = (long long)rows * nst * L * es;
       if (smem > smem_max) continue;
       const long long nvec = L / pv;
-      const long long per_warp = (nvec + ssv::kWarps - 1) / ssv::kWarps;
-      const long long rounds = (per_warp + 31) / 32;
-      if (rounds > ssv::kMaxRounds) continue;
+      long long cpt = (nvec + ssv::kThreads - 1) / ssv::kThreads;
+      if ((cpt & 1) == 0) ++cpt;
       const int G = max_active_clusters(fn, S, (int)smem);
       if (G <= 0) continue;
       const long long Ge = units < G ? units : G;
-      const double cost = (double)((units + Ge - 1) / Ge) * ((double)rounds + (nst == 2 ? 2.0 : 4.0));
+      const double cost = (double)((units + Ge - 1) / Ge) * ((double)cpt + (nst == 2 ? 2.0 : 4.0));
       if (best_cost < 0 || cost < best_cost) {
         best_cost = cost;
         out->S = S;
@@ -184,8 +183,13 @@ spec_status_t shape_for_dt(spec_dtype_t dt, long long units, int V, int rows, Sh
 }
 
 template <class E, int MODE>
-cudaError_t launch_sweep(const SweepParams& P, const Shape& sh, cudaStream_t stream) {
+cudaError_t launch_sweep(const SweepParams& P0, const Shape& sh, cudaStream_t stream) {
   auto fn = ssv::sweep_kernel<E, MODE>;
+  SweepParams P = P0;
+  // vectors per thread: enough for the slice, rounded up to an odd count
+  const int nvec = P.L / E::PV;
+  P.cpt = (nvec + ssv::kThreads - 1) / ssv::kThreads;
+  if ((P.cpt & 1) == 0) ++P.cpt;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(sh.G * sh.S), 1, 1);
   cfg.blockDim = dim3(ssv::kThreads, 1, 1);

@@ -40,7 +40,6 @@ namespace ssv {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxRounds = 16;     // rounds of 32 vectors per warp segment
 constexpr int kPartStride = 16;    // partial slots per unit (max cluster size)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s bound on any wait
 constexpr unsigned kFull = 0xFFFFFFFFu;
@@ -72,6 +71,7 @@ struct SweepParams {
   int units;
   int S;        // CTAs per cluster
   int L;        // slice length in elements (multiple of 8)
+  int cpt;      // 16-byte vectors per thread (odd, cpt * kThreads >= L / elements per vector)
   int aligned;  // rows start on 16-byte boundaries: bulk copies allowed
   int nst;      // shared-memory stages per CTA (1 or 2)
   int rows;     // logit rows staged per unit: 2 (target and draft) or 1 (target only)
@@ -115,6 +115,13 @@ struct Bf16 {
     x[6] = __uint_as_float(w.w << 16);
     x[7] = __uint_as_float(w.w & 0xFFFF0000u);
   }
+  // The 8 values as 4 packed pairs in element order (exact widening).
+  __device__ static __forceinline__ void pairs(const uint4& w, f32x2 (&p)[4]) {
+    p[0] = f2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
+    p[1] = f2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+    p[2] = f2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u));
+    p[3] = f2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u));
+  }
   __device__ static __forceinline__ float to_f32(Raw r) { return __uint_as_float(uint32_t(r) << 16); }
   // Maximum of the 8 values of a vector (packed compares; max needs no rounding).
   __device__ static __forceinline__ float vmax(const uint4& w) {
@@ -149,6 +156,10 @@ struct F32 {
     x[1] = __uint_as_float(w.y);
     x[2] = __uint_as_float(w.z);
     x[3] = __uint_as_float(w.w);
+  }
+  __device__ static __forceinline__ void pairs(const uint4& w, f32x2 (&p)[2]) {
+    p[0] = f2(__uint_as_float(w.x), __uint_as_float(w.y));
+    p[1] = f2(__uint_as_float(w.z), __uint_as_float(w.w));
   }
   __device__ static __forceinline__ float to_f32(Raw r) { return __uint_as_float(r); }
   __device__ static __forceinline__ float vmax(const uint4& w) {
@@ -217,32 +228,64 @@ __device__ __forceinline__ void warp_argmax_redux(float& v, int& i) {
   v = M;
 }
 
-// Per-element weights of the residual / target draws.  The first pass and the
-// owner's recomputation call this same function with every rounding pinned
-// (fmaf / __fadd_rn), so both see bit-identical values.
-template <class E, bool kResidual>
-__device__ __forceinline__ float draw_weights(const uint4& wt, const uint4& wd, float s, float c1t, float c1d,
-                                              float ratio, float (&w)[E::PV], float& min_mass) {
-  float t[E::PV];
-  E::unpack(wt, t);
-  if constexpr (kResidual) {
-    float d[E::PV], m[E::PV];
-    E::unpack(wd, d);
+// Sum of a vector's values held as pairs: ((v0 + v1) + (v2 + v3)) per lane.
+template <int NP>
+__device__ __forceinline__ f32x2 psum(const f32x2 (&v)[NP]) {
+  if constexpr (NP == 4) {
+    return f2_add(f2_add(v[0], v[1]), f2_add(v[2], v[3]));
+  } else {
+    return f2_add(v[0], v[1]);
+  }
+}
+
+// 2^(z s - c) of the values of one vector, as pairs in element order;
+// S2 = (s, s), C2 = (-c, -c).  Each lane is fmaf(z, s, -c) then ex2.
+template <class E>
+__device__ __forceinline__ void exp_pairs(const uint4& w, f32x2 S2, f32x2 C2, f32x2 (&ep)[E::PV / 2]) {
+  f32x2 p[E::PV / 2];
+  E::pairs(w, p);
 #pragma unroll
-    for (int i = 0; i < E::PV; ++i) {
-      const float et = ex2(fmaf(t[i], s, -c1t));
-      const float ed = ex2(fmaf(d[i], s, -c1d));
+  for (int h = 0; h < E::PV / 2; ++h) {
+    float x0, x1;
+    f2_split(f2_fma(p[h], S2, C2), x0, x1);
+    ep[h] = f2(ex2(x0), ex2(x1));
+  }
+}
+
+// Per-element weights of the residual / target draws and their vector total.
+// The sweep and the owner's walk call this same function, so both see
+// bit-identical weights and totals.  NR = (-Z_t/Z_d, -Z_t/Z_d).
+template <class E, bool kResidual>
+__device__ __forceinline__ float draw_weights(const uint4& wt, const uint4& wd, f32x2 S2, f32x2 CT, f32x2 CD,
+                                              f32x2 NR, float (&w)[E::PV], f32x2& min_mass) {
+  constexpr int NP = E::PV / 2;
+  f32x2 et[NP], wp[NP];
+  exp_pairs<E>(wt, S2, CT, et);
+  if constexpr (kResidual) {
+    f32x2 ed[NP], mp[NP];
+    exp_pairs<E>(wd, S2, CD, ed);
+    const f32x2 N1 = f2(-1.0f, -1.0f);
+#pragma unroll
+    for (int h = 0; h < NP; ++h) {
       // rho' = Z_t * max(0, p - q) = max(0, e_t - e_d * Z_t / Z_d)
-      const float r = fmaxf(fmaf(-ed, ratio, et), 0.0f);
-      w[i] = r;
-      m[i] = __fadd_rn(et, -r);  // Z_t * min(p, q)
+      float r0, r1;
+      f2_split(f2_fma(ed[h], NR, et[h]), r0, r1);
+      r0 = fmaxf(r0, 0.0f);
+      r1 = fmaxf(r1, 0.0f);
+      wp[h] = f2(r0, r1);
+      mp[h] = f2_fma(wp[h], N1, et[h]);  // Z_t * min(p, q) = e_t - rho'
+      w[2 * h] = r0;
+      w[2 * h + 1] = r1;
     }
-    min_mass = __fadd_rn(min_mass, tree_sum(m));
+    min_mass = f2_add(min_mass, psum(mp));
   } else {
 #pragma unroll
-    for (int i = 0; i < E::PV; ++i) w[i] = ex2(fmaf(t[i], s, -c1t));
+    for (int h = 0; h < NP; ++h) {
+      wp[h] = et[h];
+      f2_split(et[h], w[2 * h], w[2 * h + 1]);
+    }
   }
-  return tree_sum(w);
+  return f2_hsum(psum(wp));
 }
 
 // ---- the sweep kernel ----------------------------------------------------------
@@ -251,7 +294,6 @@ struct SweepSmem {
   uint64_t mbar[2][kWarps];
   float wred[kWarps][4];
   int wredi[kWarps][2];
-  float wrun[kWarps][kMaxRounds + 1];  // per-round prefix of a warp's draw weights
   float wtot[kWarps];
   float woff[kWarps + 1];
   alignas(16) float mbox[2][kPartStride][8];  // pushed by peers: [exchange slot][sender rank][field]
@@ -292,10 +334,15 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
   const int n = max(e1 - e0, 0);
   const int nvec = (n + PV - 1) / PV;
   const int nvec_alloc = P.L / PV;
-  const int seg = (nvec + kWarps - 1) / kWarps;
+  // thread t owns the contiguous chunk [t*cpt, (t+1)*cpt) of 16-byte vectors
+  // (cpt odd: the 8 lanes of a quarter warp hit distinct bank groups); a warp's
+  // segment is the union of its lanes' chunks
+  const int cpt = P.cpt;
+  const int seg = 32 * cpt;
   const int v_lo = min(warp * seg, nvec);
   const int v_hi = min(v_lo + seg, nvec);
-  const int nrounds = (v_hi - v_lo + 31) >> 5;
+  const int t_lo = min(v_lo + lane * cpt, v_hi);
+  const int t_hi = min(t_lo + cpt, v_hi);
   const bool bulk = P.aligned && v_hi > v_lo;
   const size_t stage_bytes = (size_t)P.rows * (size_t)nvec_alloc * 16u;
   auto stage_t = [&](int st) { return reinterpret_cast<uint4*>(dyn_smem + st * stage_bytes); };
@@ -343,6 +390,15 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
     uint4* dt = stage_t(st);
     bulk_load(smem_addr(dt + v_lo), x.tg + e0 + (long long)v_lo * PV, bytes, bar, pol);
     if (x.has_draft) bulk_load(smem_addr(dt + nvec_alloc + v_lo), x.dg + e0 + (long long)v_lo * PV, bytes, bar, pol);
+  };
+  // L2 prefetch of this warp's segment of unit u (lane 0), so that its bulk
+  // copy, issued once a stage is free, is served from L2.
+  auto prefetch = [&](int u) {
+    if (!bulk || lane != 0 || u >= P.units) return;
+    const Unit x = decode(u);
+    const uint32_t bytes = (uint32_t)(v_hi - v_lo) * 16u;
+    bulk_prefetch_l2(x.tg + e0 + (long long)v_lo * PV, bytes);
+    if (x.has_draft) bulk_prefetch_l2(x.dg + e0 + (long long)v_lo * PV, bytes);
   };
 
   // Warp 0 pushes eight values (held by every lane) into slot `slot` of every
@@ -561,8 +617,10 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
     const uint32_t par = (nst == 2) ? ((uint32_t)(it >> 1) & 1u) : ((uint32_t)it & 1u);
     if (nst == 2) {
       if (u + G < P.units) issue(u + G, stg ^ 1);
-    } else if (it > 0) {
-      issue(u, 0);  // this warp finished reading its segment of the previous unit
+      prefetch(u + 2 * G);
+    } else {
+      if (it > 0) issue(u, 0);  // this warp finished reading its segment of the previous unit
+      prefetch(u + G);
     }
     const Unit x = decode(u);
 
@@ -691,43 +749,47 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
       continue;
     } else {
       // ============ sampling path: T > 0 ============
-      // ---- pass A: one sweep, running max per thread, sums rescaled when it grows ----
+      const f32x2 S2 = f2(s, s);
+      // ---- pass A: per-thread sums of 2^(z s - c) over the thread's chunk ----
+      // c is fl(s * max of the chunk's first vector).  A chunk whose sum is not
+      // below 2^100 (a value far above that offset, an infinity or a NaN) is
+      // summed again with a running maximum.
       float mt = -INFINITY, md = -INFINITY, zt = 0.0f, zd = 0.0f;
-      if (ok && v_hi > v_lo) {
-        float ct = 0.0f, cd = 0.0f;  // fl(m * s) of the running maxima
-        for (int j = v_lo + lane; j < v_hi; j += 32) {
-          float xv[PV], e[PV];
-          const uint4 wt = st[j];
-          const float vt = E::vmax(wt);
-          if (vt > mt) {
-            const float cn = __fmul_rn(vt, s);
-            zt = (mt > -INFINITY) ? __fmul_rn(zt, ex2(__fadd_rn(ct, -cn))) : 0.0f;
-            ct = cn;
-            mt = vt;
+      if (ok && t_lo < t_hi) {
+        auto chunk_sum = [&](const uint4* base, float& m, float& z) {
+          m = E::vmax(base[t_lo]);
+          const float c = __fmul_rn(m, s);
+          const f32x2 C2 = f2(-c, -c);
+          f32x2 acc = f2(0.0f, 0.0f);
+          for (int i = t_lo; i < t_hi; ++i) {
+            f32x2 ep[PV / 2];
+            exp_pairs<E>(base[i], S2, C2, ep);
+            acc = f2_add(acc, psum(ep));
           }
-          if (mt > -INFINITY) {
-            E::unpack(wt, xv);
-#pragma unroll
-            for (int i = 0; i < PV; ++i) e[i] = ex2(fmaf(xv[i], s, -ct));
-            zt = __fadd_rn(zt, tree_sum(e));
-          }
-          if (x.has_draft) {
-            const uint4 wd = sd[j];
-            const float vd = E::vmax(wd);
-            if (vd > md) {
-              const float cn = __fmul_rn(vd, s);
-              zd = (md > -INFINITY) ? __fmul_rn(zd, ex2(__fadd_rn(cd, -cn))) : 0.0f;
-              cd = cn;
-              md = vd;
-            }
-            if (md > -INFINITY) {
-              E::unpack(wd, xv);
-#pragma unroll
-              for (int i = 0; i < PV; ++i) e[i] = ex2(fmaf(xv[i], s, -cd));
-              zd = __fadd_rn(zd, tree_sum(e));
+          z = f2_hsum(acc);
+          if (!(z < 0x1p100f) || !(c > -INFINITY)) {
+            m = -INFINITY;
+            z = 0.0f;
+            float cm = 0.0f;
+            for (int i = t_lo; i < t_hi; ++i) {
+              const uint4 w = base[i];
+              const float vm = E::vmax(w);
+              if (vm > m) {
+                const float cn = __fmul_rn(vm, s);
+                z = (m > -INFINITY) ? __fmul_rn(z, ex2(__fadd_rn(cm, -cn))) : 0.0f;
+                cm = cn;
+                m = vm;
+              }
+              if (m > -INFINITY) {
+                f32x2 ep[PV / 2];
+                exp_pairs<E>(w, S2, f2(-cm, -cm), ep);
+                z = __fadd_rn(z, f2_hsum(psum(ep)));
+              }
             }
           }
-        }
+        };
+        chunk_sum(st, mt, zt);
+        if (x.has_draft) chunk_sum(sd, md, zd);
       }
       warp_combine_mz2(mt, zt, md, zd, s);
       if (lane == 0) {
@@ -815,25 +877,32 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
       const float ufin = sm.bcf[5];
       int mode_c = sm.bci[0];
       const int acc = sm.bci[1];
+      const f32x2 CT = f2(-c1t, -c1t);
 
       if (mode_c == 0 || mode_c == 3) {
         // ---- pass C: overlap (and E2E S-mass) partials, no exchange ----
         float a = 0.0f, m2 = 0.0f;
         if (mode_c == 0 && ok && x.has_draft) {
-          for (int j = v_lo + lane; j < v_hi; j += 32) {
-            float t[PV], d[PV], e[PV], g[PV];
-            E::unpack(st[j], t);
-            E::unpack(sd[j], d);
+          const f32x2 CD = f2(-cd2, -cd2);
+          f32x2 a2 = f2(0.0f, 0.0f), g2 = f2(0.0f, 0.0f);
+          for (int i = t_lo; i < t_hi; ++i) {
+            f32x2 pt[PV / 2], pd[PV / 2], ep[PV / 2], gp[PV / 2];
+            E::pairs(st[i], pt);
+            E::pairs(sd[i], pd);
 #pragma unroll
-            for (int i = 0; i < PV; ++i) {
-              const float xt = fmaf(t[i], s, -c1t);
-              const float xd = fmaf(d[i], s, -cd2);
-              e[i] = ex2(fminf(xt, xd));
-              if constexpr (MODE == kE2E) g[i] = (xd < xt) ? e[i] : 0.0f;
+            for (int h = 0; h < PV / 2; ++h) {
+              float t0, t1, d0, d1;
+              f2_split(f2_fma(pt[h], S2, CT), t0, t1);
+              f2_split(f2_fma(pd[h], S2, CD), d0, d1);
+              const float e0 = ex2(fminf(t0, d0)), e1 = ex2(fminf(t1, d1));
+              ep[h] = f2(e0, e1);
+              if constexpr (MODE == kE2E) gp[h] = f2(d0 < t0 ? e0 : 0.0f, d1 < t1 ? e1 : 0.0f);
             }
-            a = __fadd_rn(a, tree_sum(e));
-            if constexpr (MODE == kE2E) m2 = __fadd_rn(m2, tree_sum(g));
+            a2 = f2_add(a2, psum(ep));
+            if constexpr (MODE == kE2E) g2 = f2_add(g2, psum(gp));
           }
+          a = f2_hsum(a2);
+          if constexpr (MODE == kE2E) m2 = f2_hsum(g2);
         }
         a = warp_sum(a);
         if constexpr (MODE == kE2E) m2 = warp_sum(m2);
@@ -877,50 +946,51 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
       }
 
       // ---- pass C': residual (mode 1) or target (mode 2) draw ----
+      // Prefix order is (CTA, warp, lane, vector, element): every thread sums
+      // its contiguous chunk in order, a warp scan orders the lanes, and one
+      // thread of the owning CTA walks its chunk again with the same arithmetic.
+      const f32x2 CDd = f2(-c1d, -c1d);
+      const f32x2 NR = f2(-ratio, -ratio);
       for (int attempt = 0; attempt < 2; ++attempt) {
         const bool resid = (mode_c == 1);
-        float run = 0.0f, mm = 0.0f;
+        float tot = 0.0f;
+        f32x2 mm2 = f2(0.0f, 0.0f);
         if (ok) {
-          for (int r = 0; r < nrounds; ++r) {
-            const int j = v_lo + r * 32 + lane;
-            float rs = 0.0f, w[PV];
-            if (j < v_hi)
-              rs = resid ? draw_weights<E, true>(st[j], sd[j], s, c1t, c1d, ratio, w, mm)
-                         : draw_weights<E, false>(st[j], st[j], s, c1t, c1d, ratio, w, mm);
-            const float incl = warp_incl_scan(rs, lane);
-            if (lane == 0) sm.wrun[warp][r] = run;
-            run = __fadd_rn(run, __shfl_sync(kFull, incl, 31));
+          for (int i = t_lo; i < t_hi; ++i) {
+            float w[PV];
+            const float rs = resid ? draw_weights<E, true>(st[i], sd[i], S2, CT, CDd, NR, w, mm2)
+                                   : draw_weights<E, false>(st[i], st[i], S2, CT, CDd, NR, w, mm2);
+            tot = __fadd_rn(tot, rs);
           }
         }
-        mm = warp_sum(mm);
-        if (lane == 0) {
-          sm.wrun[warp][ok ? nrounds : 0] = run;
-          sm.wtot[warp] = run;
-          sm.wred[warp][0] = mm;
-        }
+        const float incl = warp_incl_scan(tot, lane);
+        float excl = __shfl_up_sync(kFull, incl, 1);
+        if (lane == 0) excl = 0.0f;
+        const float mm = warp_sum(f2_hsum(mm2));
+        if (lane == 31) sm.wtot[warp] = incl;
+        if (lane == 0) sm.wred[warp][0] = mm;
         __syncthreads();
         slot = xc & 1;
         if (warp == 0) {
-          // warp offsets inside the CTA (one scan, so every later comparison
-          // uses the same numbers), the CTA total, and the overlap partial
+          // warp offsets inside the CTA, the CTA total and the overlap partial
           const float wt = lane < kWarps ? sm.wtot[lane] : 0.0f;
-          const float incl = warp_incl_scan(wt, lane);
-          if (lane < kWarps) sm.woff[lane + 1] = incl;
+          const float wincl = warp_incl_scan(wt, lane);
+          if (lane < kWarps) sm.woff[lane + 1] = wincl;
           if (lane == 0) sm.woff[0] = 0.0f;
-          const float tot = __shfl_sync(kFull, incl, kWarps - 1);
+          const float ctot = __shfl_sync(kFull, wincl, kWarps - 1);
           float A = lane < kWarps ? sm.wred[lane][0] : 0.0f;
           A = warp_sum(A);
           if (lane == 0 && attempt == 0 && resid) P.part[(long long)u * kPartStride + rank] = __fmul_rn(A, izt);
-          push8(slot, tot, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f);
+          push8(slot, ctot, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f);
         }
         cluster_sync();  // ---- exchange 2: CTA totals of the draw weights
         ++xc;
         if (warp == 0) {
           const float tr = mb(slot, 0, 0.0f);
-          const float incl = warp_incl_scan(tr, lane);
-          const float total = __shfl_sync(kFull, incl, 31);
+          const float cincl = warp_incl_scan(tr, lane);
+          const float total = __shfl_sync(kFull, cincl, 31);
           const float thr = __fmul_rn(ufin, total);
-          const unsigned hit = __ballot_sync(kFull, lane < S && incl > thr);
+          const unsigned hit = __ballot_sync(kFull, lane < S && tr > 0.0f && cincl > thr);
           const unsigned pos = __ballot_sync(kFull, lane < S && tr > 0.0f);
           int owner = -1;
           bool fb = false;
@@ -930,8 +1000,8 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
             owner = 31 - __clz(pos);
             fb = true;
           }
-          const float excl = __shfl_up_sync(kFull, incl, 1);
-          const float ex_o = __shfl_sync(kFull, excl, owner > 0 ? owner : 0);
+          const float cexcl = __shfl_up_sync(kFull, cincl, 1);
+          const float ex_o = __shfl_sync(kFull, cexcl, owner > 0 ? owner : 0);
           if (lane == 0) {
             sm.bci[2] = (total > 0.0f) ? 1 : 0;
             sm.bci[3] = owner;
@@ -949,12 +1019,13 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
         }
         if (sm.bci[3] == (int)rank) {
           if (tid == 0) {
-            // the warp, then the round, holding the local threshold
+            // the warp holding the local threshold (warps with positive mass only)
             const float th = sm.bcf[6];
             int wsel = -1, wlast = -1;
             for (int w = 0; w < kWarps; ++w) {
-              if (wsel < 0 && sm.woff[w + 1] > th) wsel = w;
-              if (sm.wtot[w] > 0.0f) wlast = w;
+              const bool posw = sm.wtot[w] > 0.0f;
+              if (posw && wsel < 0 && sm.woff[w + 1] > th) wsel = w;
+              if (posw) wlast = w;
             }
             float thw = INFINITY;
             if (wsel >= 0) {
@@ -962,59 +1033,61 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
             } else {
               wsel = wlast;
             }
-            if (wsel < 0) wsel = 0;  // no positive weight in this CTA (rounding only)
-            const int lo = min(wsel * seg, nvec), hi = min(lo + seg, nvec);
-            const int nr = (hi - lo + 31) >> 5;
-            int rsel = -1, rlast = 0;
-            for (int r = 0; r < nr; ++r) {
-              if (rsel < 0 && sm.wrun[wsel][r + 1] > thw) rsel = r;
-              if (sm.wrun[wsel][r + 1] > sm.wrun[wsel][r]) rlast = r;
-            }
-            if (rsel < 0) {
-              rsel = rlast;
-              thw = INFINITY;
-            }
             sm.bci[4] = wsel;
-            sm.bci[5] = rsel;
             sm.bci[6] = -1;
             sm.bcf[7] = thw;
           }
           __syncthreads();
           if (warp == sm.bci[4]) {
-            const int r = sm.bci[5];
-            const float th = sm.bcf[7];
-            const float base = sm.wrun[warp][r];
-            const int j = v_lo + r * 32 + lane;
-            float rs = 0.0f, w[PV], dummy = 0.0f;
-#pragma unroll
-            for (int i = 0; i < PV; ++i) w[i] = 0.0f;
-            if (j < v_hi)
-              rs = resid ? draw_weights<E, true>(st[j], sd[j], s, c1t, c1d, ratio, w, dummy)
-                         : draw_weights<E, false>(st[j], st[j], s, c1t, c1d, ratio, w, dummy);
-            const float incl = warp_incl_scan(rs, lane);
-            const float excl = __shfl_up_sync(kFull, incl, 1);
-            const unsigned hit = __ballot_sync(kFull, __fadd_rn(base, incl) > th);
-            const unsigned pos = __ballot_sync(kFull, rs > 0.0f);
+            const float thw = sm.bcf[7];
+            const unsigned hit = __ballot_sync(kFull, tot > 0.0f && incl > thw);
+            const unsigned pos = __ballot_sync(kFull, tot > 0.0f);
+            const bool fb = (hit == 0u);
             const int l = hit ? (__ffs(hit) - 1) : (pos ? 31 - __clz(pos) : -1);
             if (lane == l) {
-              float accu = __fadd_rn(base, lane > 0 ? excl : 0.0f);
-              int pick = -1, lastp = -1;
+              const float th = fb ? INFINITY : thw;
+              float run = excl;
+              int pick = -1, ilast = -1;
+              for (int i = t_lo; i < t_hi && pick < 0; ++i) {
+                float w[PV];
+                f32x2 dummy = f2(0.0f, 0.0f);
+                const float rs = resid ? draw_weights<E, true>(st[i], sd[i], S2, CT, CDd, NR, w, dummy)
+                                       : draw_weights<E, false>(st[i], st[i], S2, CT, CDd, NR, w, dummy);
+                if (rs > 0.0f) ilast = i;
+                const float nxt = __fadd_rn(run, rs);
+                if (nxt > th) {
+                  float a = run;
+                  int lastp = -1;
 #pragma unroll
-              for (int i = 0; i < PV; ++i) {
-                accu = __fadd_rn(accu, w[i]);
-                if (w[i] > 0.0f) {
-                  lastp = i;
-                  if (pick < 0 && accu > th) pick = i;
+                  for (int k = 0; k < PV; ++k) {
+                    a = __fadd_rn(a, w[k]);
+                    if (w[k] > 0.0f) {
+                      lastp = k;
+                      if (pick < 0 && a > th) pick = i * PV + k;
+                    }
+                  }
+                  if (pick < 0 && lastp >= 0) pick = i * PV + lastp;
                 }
+                run = nxt;
               }
-              if (pick < 0) pick = lastp;
-              if (pick >= 0) sm.bci[6] = e0 + j * PV + pick;
+              if (pick < 0 && ilast >= 0) {  // no crossing (rounding): the last positive weight
+                float w[PV];
+                f32x2 dummy = f2(0.0f, 0.0f);
+                if (resid)
+                  draw_weights<E, true>(st[ilast], sd[ilast], S2, CT, CDd, NR, w, dummy);
+                else
+                  draw_weights<E, false>(st[ilast], st[ilast], S2, CT, CDd, NR, w, dummy);
+#pragma unroll
+                for (int k = 0; k < PV; ++k)
+                  if (w[k] > 0.0f) pick = ilast * PV + k;
+              }
+              if (pick >= 0) sm.bci[6] = e0 + pick;
             }
           }
         }
         break;
       }
-      __syncthreads();  // the owner warp's token reaches thread 0
+      __syncthreads();  // the owner thread's token reaches thread 0
       if (tid == 0) {
         if (rank == 0) {
           P.rec[u].acc = (MODE == kVerify && !x.bonus) ? acc : 0;
