@@ -50,11 +50,17 @@ L2_NOTE = "inputs rotated over 8 resident copies of the batch (700 MB > 129 MB L
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--single", choices=["verify", "greedy", "overlap", "e2e"], default=None,
+                    help="run only `--calls` calls of one entry point (an L2 flush before each): the "
+                         "profiling target, prints no JSON")
+    ap.add_argument("--shape", default="32,4,151936", help="B,K,V of --single")
+    ap.add_argument("--temperature", type=float, default=1.0, help="T of --single verify")
+    ap.add_argument("--calls", type=int, default=3)
     return ap.parse_args()
 
 
@@ -444,8 +450,35 @@ def run_e2e(args, ssv, batches, dev, stream):
             "d2h_bytes_per_step": int(d2h), "steps": n, "ms_per_step": 1e3 * dt / n}
 
 
+def run_single(args):
+    """A few calls of one entry point on the entropy-mix workload at --shape,
+    each after a 512 MB L2 flush, for ncu captures of one launch."""
+    import sampling_spec_verify_gb300 as ssv
+    from sampling_spec_verify_gb300 import synth
+    Bs, Ks, Vs = (int(v) for v in args.shape.split(","))
+    dev = torch.device("cuda")
+    T = 0.0 if args.single == "greedy" else (1.0 if args.single in ("overlap", "e2e") else args.temperature)
+    w = synth.entropy_mix(seed=SEED, temperature=T, B=Bs, K=Ks, V=Vs)
+    t, d = w.target.to(dev), w.draft.to(dev)
+    y, ua, uf = w.draft_tokens.to(dev), w.u_accept.to(dev), w.u_final.to(dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.calls):
+        flush.zero_()
+        if args.single in ("verify", "greedy"):
+            ssv.verify(t, d if T > 0 else None, y, ua, uf, T)
+        elif args.single == "overlap":
+            ssv.overlap(t, d, 1.0, K=Ks)
+        else:
+            ssv.e2e_tv_fwd_bwd(t, d, 1.0, 1.0, K=Ks)
+    torch.cuda.synchronize()
+    print("ok", args.single, Bs, Ks, Vs, T)
+
+
 def main():
     args = parse()
+    if args.single:
+        run_single(args)
+        return
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, ws, rank)

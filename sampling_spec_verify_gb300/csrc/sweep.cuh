@@ -288,6 +288,148 @@ __device__ __forceinline__ float draw_weights(const uint4& wt, const uint4& wd, 
   return f2_hsum(psum(wp));
 }
 
+// ---- per-row completion (one warp of the CTA whose arrival completes the row) ----
+// Decides the prefix-order outcome, sums the CTA partials in rank order and
+// re-zeroes the workspace of row b.
+template <int MODE>
+__device__ __forceinline__ void complete_row(const SweepParams& P, int b, int S, int lane) {
+  constexpr bool kVerifyMode = (MODE == kVerify || MODE == kVerifyGreedy);
+  const int K = P.K;
+  const int per_row = kVerifyMode ? K + 1 : K;
+  const float* pp0 = P.part + (long long)b * per_row * kPartStride;
+  // overlap of position kk: partials summed in rank order
+  auto alpha_of = [&](int kk) {
+    const float* pp = pp0 + kk * kPartStride;
+    float a = 0.0f;
+    for (int r = 0; r < S; ++r) a = __fadd_rn(a, __ldcg(pp + r));
+    return a;
+  };
+  if constexpr (kVerifyMode) {
+    const VerifyRecord* rr = P.rec + (long long)b * (K + 1);
+    int nacc = K;
+    for (int base = 0; base < K; base += 32) {
+      const int kk = base + lane;
+      const bool rej = (kk < K) && (__ldcg(&rr[kk].acc) == 0);
+      const unsigned m = __ballot_sync(kFull, rej);
+      if (m) {
+        nacc = base + __ffs(m) - 1;
+        break;
+      }
+    }
+    const int corr = __ldcg(&rr[nacc].token);
+    for (int kk = lane; kk <= K; kk += 32) {
+      int tokv = -1;
+      if (kk < nacc) tokv = P.draft_tokens[b * K + kk];
+      else if (kk == nacc) tokv = corr;
+      P.out_tokens[(long long)b * (K + 1) + kk] = tokv;
+      if (kk < K && P.alpha) P.alpha[b * K + kk] = alpha_of(kk);
+    }
+    __syncwarp();
+    VerifyRecord* rw = P.rec + (long long)b * (K + 1);
+    float* pw = P.part + (long long)b * per_row * kPartStride;
+    for (int kk = lane; kk <= K; kk += 32) rw[kk] = VerifyRecord{0, 0, 0u, 0u};
+    for (int i = lane; i < per_row * kPartStride; i += 32) pw[i] = 0.0f;
+    if (lane == 0) {
+      P.n_accepted[b] = nacc;
+      P.row_cnt[b] = 0;
+    }
+  } else if constexpr (MODE == kOverlap || MODE == kOverlapGreedy) {
+    float al[2];
+    for (int h = 0; h < 2; ++h) {
+      const int kk = lane + 32 * h;
+      al[h] = (kk < K) ? alpha_of(kk) : 0.0f;
+      if (kk < K) {
+        P.alpha[b * K + kk] = al[h];
+        if (P.tv) P.tv[b * K + kk] = 1.0f - al[h];
+      }
+    }
+    // prefix products in position order
+    float pr = 1.0f, sum = 0.0f;
+    for (int kk = 0; kk < K; ++kk) {
+      const float a = __shfl_sync(kFull, al[kk >> 5], kk & 31);
+      pr = __fmul_rn(pr, a);
+      sum = __fadd_rn(sum, pr);
+      if (lane == 0 && P.surv) P.surv[b * K + kk] = pr;
+    }
+    __syncwarp();
+    float* pw = P.part + (long long)b * per_row * kPartStride;
+    for (int i = lane; i < per_row * kPartStride; i += 32) pw[i] = 0.0f;
+    if (lane == 0) {
+      if (P.exp_acc) P.exp_acc[b] = sum;
+      P.row_cnt[b] = 0;
+    }
+  } else {  // kE2E
+    E2EStats* sr = P.stats + (long long)b * K;
+    const float* qq0 = P.part2 + (long long)b * K * kPartStride;
+    float al[2], sm2[2];
+    for (int h = 0; h < 2; ++h) {
+      const int kk = lane + 32 * h;
+      al[h] = 0.0f;
+      sm2[h] = 0.0f;
+      if (kk < K) {
+        al[h] = alpha_of(kk);
+        const float* qq = qq0 + kk * kPartStride;
+        for (int r = 0; r < S; ++r) sm2[h] = __fadd_rn(sm2[h], __ldcg(qq + r));
+        if (P.alpha) P.alpha[b * K + kk] = al[h];
+      }
+    }
+    // prefix products P_{k-1}, suffix sums G_k = 1 + alpha_{k+1} G_{k+1}
+    float pre[2] = {1.0f, 1.0f}, suf[2] = {1.0f, 1.0f};
+    float pr = 1.0f, rowl = 0.0f;
+    for (int kk = 0; kk < K; ++kk) {
+      if ((kk & 31) == lane) pre[kk >> 5] = pr;
+      pr = __fmul_rn(pr, __shfl_sync(kFull, al[kk >> 5], kk & 31));
+      rowl = __fadd_rn(rowl, pr);
+    }
+    float g = 1.0f;
+    for (int kk = K - 1; kk >= 0; --kk) {
+      if ((kk & 31) == lane) suf[kk >> 5] = g;
+      g = fmaf(__shfl_sync(kFull, al[kk >> 5], kk & 31), g, 1.0f);
+    }
+    const float scale = P.grad_scale / (float)P.B;
+    for (int h = 0; h < 2; ++h) {
+      const int kk = lane + 32 * h;
+      if (kk < K) {
+        const float coef = __fmul_rn(__fmul_rn(scale, pre[h]), suf[h]);
+        const float A = __fmul_rn(__fmul_rn(coef, __ldcg(&sr[kk].izt)), P.inv_t);
+        sr[kk].smass = sm2[h];
+        sr[kk].alpha = al[h];
+        sr[kk].b1 = __fmul_rn(A, 1.0f - sm2[h]);
+        sr[kk].b0 = __fmul_rn(A, -sm2[h]);
+      }
+    }
+    __syncwarp();
+    float* pw = P.part + (long long)b * K * kPartStride;
+    float* pw2 = P.part2 + (long long)b * K * kPartStride;
+    for (int i = lane; i < K * kPartStride; i += 32) {
+      pw[i] = 0.0f;
+      pw2[i] = 0.0f;
+    }
+    int glast = 0;
+    if (lane == 0) {
+      P.row_loss[b] = rowl;
+      P.row_cnt[b] = 0;
+      __threadfence();
+      const uint32_t old = atomicAdd(P.glob_cnt, 1u);
+      glast = (old == (uint32_t)P.B - 1) ? 1 : 0;
+      if (glast) __threadfence();
+    }
+    glast = __shfl_sync(kFull, glast, 0);
+    if (glast) {
+      float acc_l = 0.0f;
+      for (int i = lane; i < P.B; i += 32) {
+        acc_l = __fadd_rn(acc_l, __ldcg(&P.row_loss[i]));
+        P.row_loss[i] = 0.0f;
+      }
+      acc_l = warp_sum(acc_l);
+      if (lane == 0) {
+        *P.loss = acc_l / (float)P.B;
+        *P.glob_cnt = 0;
+      }
+    }
+  }
+}
+
 // ---- the sweep kernel ----------------------------------------------------------
 
 struct SweepSmem {
@@ -412,142 +554,6 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
   };
   auto mb = [&](int slot, int f, float dflt) { return lane < S ? sm.mbox[slot][lane][f] : dflt; };
 
-  // ---- per-row completion (warp 0 of the CTA that arrives last) ----
-  auto complete_row = [&](int b) {
-    const float* pp0 = P.part + (long long)b * per_row * kPartStride;
-    // overlap of position kk: partials summed in rank order
-    auto alpha_of = [&](int kk) {
-      const float* pp = pp0 + kk * kPartStride;
-      float a = 0.0f;
-      for (int r = 0; r < S; ++r) a = __fadd_rn(a, __ldcg(pp + r));
-      return a;
-    };
-    if constexpr (kVerifyMode) {
-      const VerifyRecord* rr = P.rec + (long long)b * (K + 1);
-      int nacc = K;
-      for (int base = 0; base < K; base += 32) {
-        const int kk = base + lane;
-        const bool rej = (kk < K) && (__ldcg(&rr[kk].acc) == 0);
-        const unsigned m = __ballot_sync(kFull, rej);
-        if (m) {
-          nacc = base + __ffs(m) - 1;
-          break;
-        }
-      }
-      const int corr = __ldcg(&rr[nacc].token);
-      for (int kk = lane; kk <= K; kk += 32) {
-        int tokv = -1;
-        if (kk < nacc) tokv = P.draft_tokens[b * K + kk];
-        else if (kk == nacc) tokv = corr;
-        P.out_tokens[(long long)b * (K + 1) + kk] = tokv;
-        if (kk < K && P.alpha) P.alpha[b * K + kk] = alpha_of(kk);
-      }
-      __syncwarp();
-      VerifyRecord* rw = P.rec + (long long)b * (K + 1);
-      float* pw = P.part + (long long)b * per_row * kPartStride;
-      for (int kk = lane; kk <= K; kk += 32) rw[kk] = VerifyRecord{0, 0, 0u, 0u};
-      for (int i = lane; i < per_row * kPartStride; i += 32) pw[i] = 0.0f;
-      if (lane == 0) {
-        P.n_accepted[b] = nacc;
-        P.row_cnt[b] = 0;
-      }
-    } else if constexpr (MODE == kOverlap || MODE == kOverlapGreedy) {
-      float al[2];
-      for (int h = 0; h < 2; ++h) {
-        const int kk = lane + 32 * h;
-        al[h] = (kk < K) ? alpha_of(kk) : 0.0f;
-        if (kk < K) {
-          P.alpha[b * K + kk] = al[h];
-          if (P.tv) P.tv[b * K + kk] = 1.0f - al[h];
-        }
-      }
-      // prefix products in position order
-      float pr = 1.0f, sum = 0.0f;
-      for (int kk = 0; kk < K; ++kk) {
-        const float a = __shfl_sync(kFull, al[kk >> 5], kk & 31);
-        pr = __fmul_rn(pr, a);
-        sum = __fadd_rn(sum, pr);
-        if (lane == 0 && P.surv) P.surv[b * K + kk] = pr;
-      }
-      __syncwarp();
-      float* pw = P.part + (long long)b * per_row * kPartStride;
-      for (int i = lane; i < per_row * kPartStride; i += 32) pw[i] = 0.0f;
-      if (lane == 0) {
-        if (P.exp_acc) P.exp_acc[b] = sum;
-        P.row_cnt[b] = 0;
-      }
-    } else {  // kE2E
-      E2EStats* sr = P.stats + (long long)b * K;
-      const float* qq0 = P.part2 + (long long)b * K * kPartStride;
-      float al[2], sm2[2];
-      for (int h = 0; h < 2; ++h) {
-        const int kk = lane + 32 * h;
-        al[h] = 0.0f;
-        sm2[h] = 0.0f;
-        if (kk < K) {
-          al[h] = alpha_of(kk);
-          const float* qq = qq0 + kk * kPartStride;
-          for (int r = 0; r < S; ++r) sm2[h] = __fadd_rn(sm2[h], __ldcg(qq + r));
-          if (P.alpha) P.alpha[b * K + kk] = al[h];
-        }
-      }
-      // prefix products P_{k-1}, suffix sums G_k = 1 + alpha_{k+1} G_{k+1}
-      float pre[2] = {1.0f, 1.0f}, suf[2] = {1.0f, 1.0f};
-      float pr = 1.0f, rowl = 0.0f;
-      for (int kk = 0; kk < K; ++kk) {
-        if ((kk & 31) == lane) pre[kk >> 5] = pr;
-        pr = __fmul_rn(pr, __shfl_sync(kFull, al[kk >> 5], kk & 31));
-        rowl = __fadd_rn(rowl, pr);
-      }
-      float g = 1.0f;
-      for (int kk = K - 1; kk >= 0; --kk) {
-        if ((kk & 31) == lane) suf[kk >> 5] = g;
-        g = fmaf(__shfl_sync(kFull, al[kk >> 5], kk & 31), g, 1.0f);
-      }
-      const float scale = P.grad_scale / (float)P.B;
-      for (int h = 0; h < 2; ++h) {
-        const int kk = lane + 32 * h;
-        if (kk < K) {
-          const float coef = __fmul_rn(__fmul_rn(scale, pre[h]), suf[h]);
-          const float A = __fmul_rn(__fmul_rn(coef, __ldcg(&sr[kk].izt)), P.inv_t);
-          sr[kk].smass = sm2[h];
-          sr[kk].alpha = al[h];
-          sr[kk].b1 = __fmul_rn(A, 1.0f - sm2[h]);
-          sr[kk].b0 = __fmul_rn(A, -sm2[h]);
-        }
-      }
-      __syncwarp();
-      float* pw = P.part + (long long)b * K * kPartStride;
-      float* pw2 = P.part2 + (long long)b * K * kPartStride;
-      for (int i = lane; i < K * kPartStride; i += 32) {
-        pw[i] = 0.0f;
-        pw2[i] = 0.0f;
-      }
-      int glast = 0;
-      if (lane == 0) {
-        P.row_loss[b] = rowl;
-        P.row_cnt[b] = 0;
-        __threadfence();
-        const uint32_t old = atomicAdd(P.glob_cnt, 1u);
-        glast = (old == (uint32_t)P.B - 1) ? 1 : 0;
-        if (glast) __threadfence();
-      }
-      glast = __shfl_sync(kFull, glast, 0);
-      if (glast) {
-        float acc_l = 0.0f;
-        for (int i = lane; i < P.B; i += 32) {
-          acc_l = __fadd_rn(acc_l, __ldcg(&P.row_loss[i]));
-          P.row_loss[i] = 0.0f;
-        }
-        acc_l = warp_sum(acc_l);
-        if (lane == 0) {
-          *P.loss = acc_l / (float)P.B;
-          *P.glob_cnt = 0;
-        }
-      }
-    }
-  };
-
   // Publishes the queued arrivals (warp 0, converged): one release fence, one
   // counter update per queued row (lanes in parallel), then the rows whose
   // arrivals are complete are finished by the whole warp.
@@ -569,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
     while (m) {
       const int l = __ffs(m) - 1;
       m &= m - 1;
-      complete_row(__shfl_sync(kFull, row, l));
+      complete_row<MODE>(P, __shfl_sync(kFull, row, l), S, lane);
     }
     __syncwarp();
     if (lane == 0) sm.npend = 0;
