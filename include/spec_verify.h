@@ -211,7 +211,8 @@ spec_status_t spec_launch_shape(spec_dtype_t dtype, int V, int* chunk_elems, int
 
 /* Forces the largest vocabulary chunk (in logits, >= 256; smaller values
  * restore the automatic choice) and the shared-memory stages per CTA (2..16,
- * never above what fits; other values restore the automatic choice) of later
+ * raised to the pipeline's minimum of 6 for T > 0, never above what fits;
+ * other values restore the automatic choice) of later
  * launches in this process, for launch-shape sweeps in tests and benchmarks.
  * Workspace sizes queried afterwards account for the forced chunk.
  * Process-wide; not synchronised with launches in flight. */

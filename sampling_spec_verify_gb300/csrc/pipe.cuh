@@ -18,22 +18,26 @@
 //            position), the draw weights max(0, p - q) or p, summed per
 //            segment of 32 vectors.
 // Phase 2 of a unit needs the phase-1 partials of all of its C chunks, which
-// other CTAs compute.  The partials are published as self-validating 64-bit
-// words (each field is stored bitwise inverted, so an all-zero half means
-// "not written yet"; the workspace is zero between calls) and phase 2 of a
-// task runs kLag tasks after its phase 1, by which time the other chunks of
-// the unit are normally done: nothing on the data path waits for another CTA.
+// other CTAs compute.  All partials are published as self-validating words
+// (each 32-bit field is stored bitwise inverted, so an all-zero field means
+// "not written yet"; the workspace is zero between calls), which needs no
+// memory fence or atomic on the per-task path.  Phase 2 of a task runs kLag
+// tasks after its phase 1, by which time the other chunks of the unit are
+// normally done: nothing on the data path waits for another CTA.
 //
 // Warp roles (one CTA)
 // --------------------
-//   warps 0..7   compute: phase 1 of task i, then phase 2 of task i - kLag;
-//   warp 8       producer: bulk copies into a ring of D shared-memory stages;
-//   warp 9       control: combines the compute warps' partials, publishes a
-//                task's chunk partials, reads back the unit's partials,
-//                decides acceptance (identically in every CTA of the unit),
-//                publishes phase-2 partials and, for the last chunk of a
-//                unit to finish, hands the unit to the finaliser;
-//   warp 10      finaliser: sums the unit's phase-2 partials into alpha,
+//   warps 0..15  compute: phase 2 of task i - kLag, then phase 1 of task i;
+//   warp 16      producer: bulk copies into a ring of D shared-memory stages;
+//   warps 17..20 control: warp 17 + r serves the tasks i with i % 4 == r.  It
+//                combines the compute warps' partials, publishes the task's
+//                chunk partials, reads back the unit's partials, decides
+//                acceptance (identically in every CTA of the unit) and
+//                publishes phase-2 partials; the CTA holding a unit's
+//                finalising chunk (u mod C) reads back the unit's phase-2
+//                partials and hands the unit to the finaliser.  Four control warps keep four tasks'
+//                round trips to L2 in flight at once;
+//   warp 21      finaliser: sums the unit's phase-2 partials into alpha,
 //                locates the inverse-CDF token (chunk -> segment -> vector ->
 //                element, re-reading one 32-vector segment from L2), writes
 //                the unit's record and completes batch rows (prefix-order
@@ -53,15 +57,24 @@
 
 namespace ssv {
 
-constexpr int kCompWarps = 8;
+constexpr int kCompWarps = 16;
 constexpr int kCompThreads = kCompWarps * 32;
+constexpr int kP1Warps = 8;  // T > 0: warps 0..7 run phase 1, warps 8..15 phase 2
+constexpr int kP2Warps = kCompWarps - kP1Warps;
+constexpr int kP1Threads = kP1Warps * 32;
+constexpr int kP2Threads = kP2Warps * 32;
+constexpr int kCtlWarps = 4;  // control warp r serves the tasks i with i % 4 == r
 constexpr int kProducerWarp = kCompWarps;
-constexpr int kControlWarp = kCompWarps + 1;
-constexpr int kFinalWarp = kCompWarps + 2;
-constexpr int kThreads = (kCompWarps + 3) * 32;
+constexpr int kControlWarp0 = kCompWarps + 1;
+constexpr int kFinalWarp = kCompWarps + 1 + kCtlWarps;
+constexpr int kThreads = (kFinalWarp + 1) * 32;
 constexpr int kMaxStages = 16;
-constexpr int kLag = 3;       // phase 2 of task i runs after phase 1 of task i + kLag
+constexpr int kLag = 4;     // a control warp publishes task i - 4's phase-2 partials after task i's decision
+constexpr int kSlots = 4;   // phase-1 hand-off slots (task i uses slot i % 4)
+constexpr int kSlots2 = 8;  // decision / phase-2 hand-off slots (task i uses slot i % 8)
 constexpr int kJobSlots = 8;
+static_assert(kLag == kSlots && kCtlWarps == kSlots && kSlots2 == 2 * kSlots,
+              "task i's control warp is i % 4; its decision slot stays live until task i + 4 is decided");
 constexpr int kSegVecs = 32;  // 16-byte vectors per draw segment
 constexpr int kMaxSegs = 32;  // segments per chunk in sampling modes
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s bound on any wait
@@ -118,8 +131,8 @@ struct PipeParams {
   float* loss;
   // workspace
   uint64_t* part1;  // [units * C][4] tagged phase-1 words
-  uint64_t* part2;  // [units * C] phase-2 partials (alpha_c, R_c or S_c)
-  float* seg;       // [units * C][kMaxSegs] draw-weight segment totals (verify, T > 0)
+  uint64_t* part2;  // [units * C] tagged phase-2 partials (alpha_c, R_c or S_c)
+  uint32_t* seg;    // [units * C][kMaxSegs] tagged draw-weight segment totals (verify, T > 0)
   uint32_t* cnt;    // [units] chunks finished
   Rec* rec;         // [units] (verify, overlap)
   E2EStats* stats;  // [units] (E2E-TV)
@@ -179,11 +192,16 @@ struct TaskInfo {
   int u, c, e0, len, nv;
 };
 
+// The chunk whose CTA reads back a unit's partials and hands the unit to its
+// finaliser.  u mod C spreads units over the CTAs: the last chunk would
+// concentrate them on gcd(C, G) residues (8 CTAs when C = 19, G = 152).
+__device__ __forceinline__ int fin_chunk(const PipeParams& P, int u) { return u % P.C; }
+
 template <class E>
-__device__ __forceinline__ TaskInfo task_info(const PipeParams& P, long long t) {
-  TaskInfo x;
-  x.u = (int)(t / P.C);
-  x.c = (int)(t - (long long)x.u * P.C);
+__device__ __forceinline__ TaskInfo task_info(const PipeParams& P, int t) {
+  TaskInfo x;  // the host keeps units * C below 2^31
+  x.u = t / P.C;
+  x.c = t - x.u * P.C;
   x.e0 = x.c * P.Lc;
   x.len = min(P.Lc, P.V - x.e0);
   x.nv = (x.len + E::PV - 1) / E::PV;
@@ -199,6 +217,12 @@ struct Nrm {  // decision of one task's unit, written by the control warp
   int unit;
 };
 
+struct StageDesc {  // the task held by a shared-memory stage, written by the producer
+  int u, c, e0, nv;
+  int has_d;
+  int pad[3];
+};
+
 struct Job {  // a unit whose chunks are all finished, for the finaliser
   int unit, mode, acc, stop;
   float c1t, cd2, izt, uf;
@@ -206,13 +230,15 @@ struct Job {  // a unit whose chunks are all finished, for the finaliser
 
 struct PipeSmem {
   uint64_t full[kMaxStages], empty[kMaxStages];
-  uint64_t p1done[2], p2done[2], nrm_bar[2], p1free[2];
+  uint64_t p1done[kSlots], p1free[kSlots], p2done[kSlots2], nrm_bar[kSlots2];
   uint64_t job_full[kJobSlots], job_empty[kJobSlots];
-  float4 wp1[2][kCompWarps];
-  float wnan[2][kCompWarps];
-  float4 wp2[2][kCompWarps];
-  Nrm nrm[2];
+  float4 wp1[kSlots][kCompWarps];
+  float wnan[kSlots][kCompWarps];
+  float4 wp2[kSlots2][kP2Warps];
+  Nrm nrm[kSlots2];
+  StageDesc desc[kMaxStages];
   Job job[kJobSlots];
+  int job_tail;
   int dead;
   int wipe;
 };
@@ -230,16 +256,28 @@ __device__ __noinline__ void give_up(const PipeParams& P, PipeSmem& sm) {
 }
 
 // Waits for phase `parity` of an mbarrier; false after the time bound or once
-// any wait of the grid has given up.
+// any wait of the grid has given up.  After two probes the warp sleeps
+// between probes (64 ns, growing to 256 ns), and the abort flag (a global
+// load) and the clock are looked at only every 64 probes: a waiting warp
+// takes almost no issue slots from the warps of its SM that do work.
 __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, const PipeParams& P, PipeSmem& sm) {
-  if (mbar_try_wait(bar, parity, 0u)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (;;) {
-    if (mbar_try_wait(bar, parity, 20000u)) return true;
-    if (aborted(P, sm)) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      give_up(P, sm);
-      return false;
+  if (mbar_test(bar, parity)) return true;
+  uint64_t t0 = 0;
+  uint32_t back = 64;
+  for (uint32_t k = 1;; ++k) {
+    if (mbar_probe(bar, parity)) return true;
+    if (k >= 2) {
+      __nanosleep(back);
+      if (back < 256) back <<= 1;
+    }
+    if ((k & 63u) == 0u) {
+      if (aborted(P, sm)) return false;
+      const uint64_t now = global_timer_ns();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > kWaitLimitNs) {
+        give_up(P, sm);
+        return false;
+      }
     }
   }
 }
@@ -288,15 +326,16 @@ __device__ __forceinline__ float vec_weights(const uint4& wt, const uint4& wd, f
 }
 
 // Per-thread (max, sum) of one row with a running maximum: the slow path for
-// threads whose fast sum overflowed or met an infinity / NaN.
+// threads whose fast sum overflowed or met an infinity / NaN.  Returns
+// (max, sum) by value so that the callers' variables stay in registers.
 template <class E>
-__device__ __noinline__ void row_sum_slow(const uint4* base, int j, int nv, float s, float& m, float& z) {
+__device__ __noinline__ float2 row_sum_slow(const uint4* base, int j, int nv, float s, int stride) {
   constexpr int PV = E::PV;
   const f32x2 S2 = f2(s, s);
-  m = -INFINITY;
-  z = 0.0f;
+  float m = -INFINITY;
+  float z = 0.0f;
   float cm = 0.0f;
-  for (int v = j; v < nv; v += kCompThreads) {
+  for (int v = j; v < nv; v += stride) {
     const uint4 w = base[v];
     const float vm = E::vmax(w);
     if (vm > m) {
@@ -311,13 +350,14 @@ __device__ __noinline__ void row_sum_slow(const uint4* base, int j, int nv, floa
       z = __fadd_rn(z, f2_hsum(psum(ep)));
     }
   }
+  return make_float2(m, z);
 }
 
 // Phase 1 (T > 0): per-thread (max, sum) of the target and draft rows over
-// the vectors j, j + 256, ... of the chunk.  The sum is taken relative to
+// the vectors j, j + stride, ... of the chunk.  The sum is taken relative to
 // fl(s * max of the thread's first vector); a sum that is not below 2^100
 // (a much larger value later, an infinity or a NaN) is redone by the slow path.
-template <class E>
+template <class E, int kStride>
 __device__ __forceinline__ void phase1_sample(const uint4* st, const uint4* sd, bool has_d, int j, int nv, float s,
                                               float& mt, float& zt, float& md, float& zd) {
   constexpr int NP = E::PV / 2;
@@ -335,7 +375,7 @@ __device__ __forceinline__ void phase1_sample(const uint4* st, const uint4* sd, 
     const f32x2 CD = f2(-cd, -cd);
     f32x2 ad = f2(0.0f, 0.0f);
 #pragma unroll 2
-    for (int v = j; v < nv; v += kCompThreads) {
+    for (int v = j; v < nv; v += kStride) {
       f32x2 et[NP], ed[NP];
       exp_pairs<E>(st[v], S2, CT, et);
       exp_pairs<E>(sd[v], S2, CD, ed);
@@ -343,17 +383,25 @@ __device__ __forceinline__ void phase1_sample(const uint4* st, const uint4* sd, 
       ad = f2_add(ad, psum(ed));
     }
     zd = f2_hsum(ad);
-    if (!(zd < 0x1p100f) || !(cd > -INFINITY)) row_sum_slow<E>(sd, j, nv, s, md, zd);
+    if (!(zd < 0x1p100f) || !(cd > -INFINITY)) {
+      const float2 r = row_sum_slow<E>(sd, j, nv, s, kStride);
+      md = r.x;
+      zd = r.y;
+    }
   } else {
 #pragma unroll 4
-    for (int v = j; v < nv; v += kCompThreads) {
+    for (int v = j; v < nv; v += kStride) {
       f32x2 et[NP];
       exp_pairs<E>(st[v], S2, CT, et);
       at = f2_add(at, psum(et));
     }
   }
   zt = f2_hsum(at);
-  if (!(zt < 0x1p100f) || !(ct > -INFINITY)) row_sum_slow<E>(st, j, nv, s, mt, zt);
+  if (!(zt < 0x1p100f) || !(ct > -INFINITY)) {
+    const float2 r = row_sum_slow<E>(st, j, nv, s, kStride);
+    mt = r.x;
+    zt = r.y;
+  }
 }
 
 // Phase 1 (T == 0): per-thread arg-maximum of one row (smallest index on ties).
@@ -363,7 +411,7 @@ __device__ __forceinline__ void phase1_greedy_row(const uint4* base, int j, int 
   constexpr int PV = E::PV;
   best = -INFINITY;
   int jb = -1;
-  for (int v = j; v < nv; v += kCompThreads) {
+  for (int v = j; v < nv; v += kCompThreads) {  // greedy: all compute warps
     bool nn;
     const float vm = E::vmax_nan(base[v], nn);
     nan_seen |= nn;
@@ -389,7 +437,7 @@ __device__ __forceinline__ void phase1_greedy_row(const uint4* base, int j, int 
 // segment totals in order (lane 0), and A the min mass (mode 1).
 template <class E, int MODE>
 __device__ __forceinline__ void phase2_sample(const uint4* st, const uint4* sd, int j, int wi, int lane, int nv,
-                                              int mode, float s, float c1t, float cd2, float* seg, float& A,
+                                              int mode, float s, float c1t, float cd2, uint32_t* seg, float& A,
                                               float& R, float& Sm) {
   constexpr int NP = E::PV / 2;
   A = R = Sm = 0.0f;
@@ -398,7 +446,7 @@ __device__ __forceinline__ void phase2_sample(const uint4* st, const uint4* sd, 
   if (mode == 0) {
     f32x2 a2 = f2(0.0f, 0.0f), g2 = f2(0.0f, 0.0f);
 #pragma unroll 2
-    for (int v = j; v < nv; v += kCompThreads) {
+    for (int v = j; v < nv; v += kP2Threads) {
       f32x2 pt[NP], pd[NP], ep[NP], gp[NP];
       E::pairs(st[v], pt);
       E::pairs(sd[v], pd);
@@ -419,11 +467,11 @@ __device__ __forceinline__ void phase2_sample(const uint4* st, const uint4* sd, 
     return;
   }
   if constexpr (MODE == kVerify) {
-    const int rounds = (nv + kCompThreads - 1) / kCompThreads;
+    const int rounds = (nv + kP2Threads - 1) / kP2Threads;
     f32x2 mn = f2(0.0f, 0.0f);
     float racc = 0.0f;
     for (int r = 0; r < rounds; ++r) {
-      const int v = r * kCompThreads + j;
+      const int v = r * kP2Threads + j;
       float tot = 0.0f;
       if (v < nv) {
         float w[E::PV];
@@ -432,8 +480,8 @@ __device__ __forceinline__ void phase2_sample(const uint4* st, const uint4* sd, 
       }
       const float segt = warp_sum(tot);
       if (lane == 0) {
-        const int s0 = r * kCompThreads + wi * kSegVecs;
-        if (s0 < nv) seg[s0 / kSegVecs] = segt;
+        const int s0 = r * kP2Threads + wi * kSegVecs;
+        if (s0 < nv) st_relaxed_u32(seg + s0 / kSegVecs, tag_bits(__float_as_uint(segt)));
         racc = __fadd_rn(racc, segt);
       }
     }
@@ -471,6 +519,37 @@ __device__ __forceinline__ int scan_select(int n, float thr, float& rem, int lan
   }
   rem = INFINITY;
   return lastpos;
+}
+
+// Waits (bounded) until ok() holds in every lane, calling reload() in the
+// lanes where it does not; gives up after the time bound or once the grid has
+// aborted.  Used for the self-validating words written by other CTAs.
+__device__ __noinline__ void give_up_global(const PipeParams& P) {
+  if (P.status) atomicOr(P.status, kTimeout);
+  st_relaxed_u32(P.ctl + kCtlAbort, 1u);
+}
+
+template <class Ok, class Reload>
+__device__ __forceinline__ bool poll_words(const PipeParams& P, int lane, Ok ok, Reload reload) {
+  if (__all_sync(kFull, ok())) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t back = 32;
+  for (;;) {
+    __nanosleep(back);
+    if (back < 512) back <<= 1;
+    if (!ok()) reload();
+    if (__all_sync(kFull, ok())) return true;
+    int stop = 0;
+    if (lane == 0) {
+      if (ld_relaxed_u32(P.ctl + kCtlAbort) != 0u) {
+        stop = 1;
+      } else if (global_timer_ns() - t0 > kWaitLimitNs) {
+        give_up_global(P);
+        stop = 1;
+      }
+    }
+    if (__shfl_sync(kFull, stop, 0)) return false;
+  }
 }
 
 // One vector of a row read from global memory (L2): 16-byte load when rows
@@ -524,9 +603,14 @@ __device__ int draw_token(const PipeParams& P, const UnitInfo<E>& ui, int u, flo
   float rem2 = INFINITY;
   float w[PV];
   float tot = 0.0f;
-  const float* segs = (P.seg != nullptr) ? P.seg + ((long long)u * P.C + cs) * kMaxSegs : nullptr;
+  const uint32_t* segs = (P.seg != nullptr) ? P.seg + ((long long)u * P.C + cs) * kMaxSegs : nullptr;
   if (segs != nullptr) {
-    sel_seg = scan_select(nseg, rem, rem2, lane, [&](int i) { return __ldcg(segs + i); });
+    // the chunk's segment totals (nseg <= 32: one per lane), once all are written
+    uint32_t wv = ~0u;
+    if (lane < nseg) wv = ld_relaxed_u32(segs + lane);
+    poll_words(P, lane, [&]() { return wv != 0u; }, [&]() { wv = ld_relaxed_u32(segs + lane); });
+    const float sv = (lane < nseg) ? __uint_as_float(~wv) : 0.0f;
+    sel_seg = scan_select(nseg, rem, rem2, lane, [&](int) { return sv; });
     if (sel_seg < 0) return -1;
     tot = weights(sel_seg * kSegVecs + lane, w);
   } else {
@@ -677,8 +761,8 @@ __device__ __noinline__ void complete_row(const PipeParams& P, int b, int lane) 
   uint64_t* p2 = P.part2 + (long long)u0 * P.C;
   for (long long i = lane; i < nw; i += 32) p2[i] = 0ull;
   if (P.seg) {
-    float* sg = P.seg + (long long)u0 * P.C * kMaxSegs;
-    for (long long i = lane; i < nw * kMaxSegs; i += 32) sg[i] = 0.0f;
+    uint32_t* sg = P.seg + (long long)u0 * P.C * kMaxSegs;
+    for (long long i = lane; i < nw * kMaxSegs; i += 32) sg[i] = 0u;
   }
   for (int i = lane; i < per_row; i += 32) {
     P.cnt[u0 + i] = 0u;
@@ -770,17 +854,15 @@ __device__ __noinline__ void finalize_unit(const PipeParams& P, const Job& jb, i
     float a = 0.0f, r2 = 0.0f;
     for (int c = lane; c < C; c += 32) {
       const uint64_t w = __ldcg(P.part2 + (long long)u * C + c);
-      a = __fadd_rn(a, __uint_as_float((uint32_t)w));
-      r2 = __fadd_rn(r2, __uint_as_float((uint32_t)(w >> 32)));
+      a = __fadd_rn(a, tag_lo(w));
+      r2 = __fadd_rn(r2, tag_hi(w));
     }
     const float alpha = warp_sum(a);
     const float tot2 = warp_sum(r2);
     if constexpr (MODE == kVerify) {
       int token = -1;
       if (jb.mode == 1 || jb.mode == 2) {
-        auto get_r = [&](int c) {
-          return __uint_as_float((uint32_t)(__ldcg(P.part2 + (long long)u * C + c) >> 32));
-        };
+        auto get_r = [&](int c) { return tag_hi(__ldcg(P.part2 + (long long)u * C + c)); };
         if (tot2 > 0.0f) {
           const float thr = __fmul_rn(jb.uf, tot2);
           token = (jb.mode == 1) ? draw_token<E, 1>(P, ui, u, thr, jb.c1t, jb.cd2, lane, get_r)
@@ -842,7 +924,7 @@ __device__ __noinline__ void finalize_unit(const PipeParams& P, const Job& jb, i
 // ---- the kernel ------------------------------------------------------------------
 
 template <class E, int MODE>
-__global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const PipeParams P) {
+__global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const __grid_constant__ PipeParams P) {
   extern __shared__ __align__(128) uint8_t stage_mem[];
   __shared__ __align__(16) PipeSmem sm;
 
@@ -850,6 +932,8 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const PipeParams P) {
   using Raw = typename E::Raw;
   constexpr bool kGreedy = (MODE == kVerifyGreedy || MODE == kOverlapGreedy);
   constexpr bool kSample = !kGreedy;
+  constexpr int kP1Count = kGreedy ? kCompWarps : kP1Warps;     // warps running phase 1
+  constexpr int kRelease = kGreedy ? kCompWarps : kP2Warps;     // warps releasing a stage
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.x, G = gridDim.x;
@@ -861,18 +945,21 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const PipeParams P) {
   if (threadIdx.x == 0) {
     for (int d = 0; d < D; ++d) {
       mbar_init(smem_addr(&sm.full[d]), 1);
-      mbar_init(smem_addr(&sm.empty[d]), kCompWarps);
+      mbar_init(smem_addr(&sm.empty[d]), kRelease);
     }
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(smem_addr(&sm.p1done[h]), kCompWarps);
-      mbar_init(smem_addr(&sm.p2done[h]), kCompWarps);
-      mbar_init(smem_addr(&sm.nrm_bar[h]), 1);
+    for (int h = 0; h < kSlots; ++h) {
+      mbar_init(smem_addr(&sm.p1done[h]), kP1Count);
       mbar_init(smem_addr(&sm.p1free[h]), 1);
+    }
+    for (int h = 0; h < kSlots2; ++h) {
+      mbar_init(smem_addr(&sm.p2done[h]), kP2Warps);
+      mbar_init(smem_addr(&sm.nrm_bar[h]), 1);
     }
     for (int q = 0; q < kJobSlots; ++q) {
       mbar_init(smem_addr(&sm.job_full[q]), 1);
       mbar_init(smem_addr(&sm.job_empty[q]), 1);
     }
+    sm.job_tail = 0;
     sm.dead = 0;
     sm.wipe = 0;
     fence_mbar_init();
@@ -883,68 +970,68 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const PipeParams P) {
   auto stage_d = [&](int i) {
     return reinterpret_cast<const uint4*>(stage_mem + (size_t)(i % D) * P.stage + P.doff);
   };
-  auto task_of = [&](int i) { return task_info<E>(P, (long long)g + (long long)i * G); };
+  auto task_of = [&](int i) { return task_info<E>(P, g + i * G); };
+  // the k-th use of a slot (task i = slots * k + slot) completes phase k of its barriers
+  auto par = [](int i) { return (uint32_t)(i / kSlots) & 1u; };
+  auto par2 = [](int i) { return (uint32_t)(i / kSlots2) & 1u; };
 
-  if (warp < kCompWarps) {
-    // ================= compute warps =================
+  if (warp < kCompWarps && (kGreedy || warp < kP1Warps)) {
+    // ================= phase-1 warps =================
     const int j = warp * 32 + lane;
-    const int iters = n + (kSample ? kLag : 0);
-    for (int i = 0; i < iters; ++i) {
+    for (int i = 0; i < n; ++i) {
+      const int slot = i % kSlots;
+      pwait(smem_addr(&sm.full[i % D]), (uint32_t)(i / D) & 1u, P, sm);
+      const StageDesc dsc = sm.desc[i % D];
+      float4 part;
+      float nanw = 0.0f;
       if constexpr (kSample) {
-        const int jt = i - kLag;
-        if (jt >= 0) {
-          const int slot = jt & 1;
-          pwait(smem_addr(&sm.nrm_bar[slot]), (uint32_t)(jt >> 1) & 1u, P, sm);
-          const Nrm nr = sm.nrm[slot];
-          const TaskInfo tk = task_of(jt);
-          float A, R, Sm;
-          float* segp = (P.seg != nullptr) ? P.seg + ((long long)tk.u * P.C + tk.c) * kMaxSegs : nullptr;
-          phase2_sample<E, MODE>(stage_t(jt), stage_d(jt), j, warp, lane, tk.nv, nr.mode, s, nr.c1t, nr.cd2, segp,
-                                 A, R, Sm);
-          A = warp_sum(A);
-          if constexpr (MODE == kE2E) Sm = warp_sum(Sm);
-          if (lane == 0) {
-            sm.wp2[slot][warp] = make_float4(A, R, Sm, 0.0f);
-            if (nr.mode == 1 || nr.mode == 2) __threadfence();  // segment totals before the unit's arrival
-          }
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(smem_addr(&sm.p2done[slot]));
-            mbar_arrive(smem_addr(&sm.empty[jt % D]));
-          }
-        }
+        float mt, zt, md, zd;
+        phase1_sample<E, kP1Threads>(stage_t(i), stage_d(i), dsc.has_d != 0, j, dsc.nv, s, mt, zt, md, zd);
+        warp_combine_mz2(mt, zt, md, zd, s);
+        part = make_float4(mt, zt, md, zd);
+      } else {
+        float bt, bd = -INFINITY;
+        int it, id = 0x7FFFFFFF;
+        bool nn = false;
+        phase1_greedy_row<E>(stage_t(i), j, dsc.nv, dsc.e0, bt, it, nn);
+        if (dsc.has_d) phase1_greedy_row<E>(stage_d(i), j, dsc.nv, dsc.e0, bd, id, nn);
+        warp_argmax_redux(bt, it);
+        warp_argmax_redux(bd, id);
+        nanw = __any_sync(kFull, nn) ? 1.0f : 0.0f;
+        part = make_float4(bt, __int_as_float(it), bd, __int_as_float(id));
       }
-      if (i < n) {
-        const int slot = i & 1;
-        pwait(smem_addr(&sm.full[i % D]), (uint32_t)(i / D) & 1u, P, sm);
-        const TaskInfo tk = task_of(i);
-        const UnitInfo<E> ui = unit_info<E, MODE>(P, tk.u);
-        if constexpr (kSample) {
-          float mt, zt, md, zd;
-          phase1_sample<E>(stage_t(i), stage_d(i), ui.has_d, j, tk.nv, s, mt, zt, md, zd);
-          warp_combine_mz2(mt, zt, md, zd, s);
-          if (lane == 0) sm.wp1[slot][warp] = make_float4(mt, zt, md, zd);
-        } else {
-          float bt, bd = -INFINITY;
-          int it, id = 0x7FFFFFFF;
-          bool nn = false;
-          // the control warp has read this slot's previous partials (task i - 2)
-          if (i >= 2) pwait(smem_addr(&sm.p1free[slot]), (uint32_t)((i >> 1) + 1) & 1u, P, sm);
-          phase1_greedy_row<E>(stage_t(i), j, tk.nv, tk.e0, bt, it, nn);
-          if (ui.has_d) phase1_greedy_row<E>(stage_d(i), j, tk.nv, tk.e0, bd, id, nn);
-          warp_argmax_redux(bt, it);
-          warp_argmax_redux(bd, id);
-          const bool nw = __any_sync(kFull, nn);
-          if (lane == 0) {
-            sm.wp1[slot][warp] = make_float4(bt, __int_as_float(it), bd, __int_as_float(id));
-            sm.wnan[slot][warp] = nw ? 1.0f : 0.0f;
-          }
-        }
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_addr(&sm.p1done[slot]));
-          if constexpr (kGreedy) mbar_arrive(smem_addr(&sm.empty[i % D]));
-        }
+      // the control warp has read this slot's previous partials (task i - kSlots)
+      if (i >= kSlots) pwait(smem_addr(&sm.p1free[slot]), par(i) ^ 1u, P, sm);
+      if (lane == 0) {
+        sm.wp1[slot][warp] = part;
+        sm.wnan[slot][warp] = nanw;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_addr(&sm.p1done[slot]));
+        if constexpr (kGreedy) mbar_arrive(smem_addr(&sm.empty[i % D]));
+      }
+    }
+  } else if (warp < kCompWarps) {
+    // ================= phase-2 warps (T > 0) =================
+    const int w2 = warp - kP1Warps;
+    const int j = w2 * 32 + lane;
+    for (int jt = 0; jt < n; ++jt) {
+      const int slot = jt % kSlots2;
+      pwait(smem_addr(&sm.nrm_bar[slot]), par2(jt), P, sm);
+      const Nrm nr = sm.nrm[slot];
+      const StageDesc dsc = sm.desc[jt % D];  // the stage is held until these warps release it
+      float A, R, Sm;
+      uint32_t* segp = (P.seg != nullptr) ? P.seg + ((long long)dsc.u * P.C + dsc.c) * kMaxSegs : nullptr;
+      phase2_sample<E, MODE>(stage_t(jt), stage_d(jt), j, w2, lane, dsc.nv, nr.mode, s, nr.c1t, nr.cd2, segp, A, R,
+                             Sm);
+      A = warp_sum(A);
+      if constexpr (MODE == kE2E) Sm = warp_sum(Sm);
+      if (lane == 0) sm.wp2[slot][w2] = make_float4(A, R, Sm, 0.0f);
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_addr(&sm.p2done[slot]));
+        mbar_arrive(smem_addr(&sm.empty[jt % D]));
       }
     }
   } else if (warp == kProducerWarp) {
@@ -957,13 +1044,35 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const PipeParams P) {
       const UnitInfo<E> ui = unit_info<E, MODE>(P, tk.u);
       uint8_t* dst = stage_mem + (size_t)st * P.stage;
       const uint32_t bar = smem_addr(&sm.full[st]);
+      if (lane == 0) {
+        StageDesc dd;
+        dd.u = tk.u;
+        dd.c = tk.c;
+        dd.e0 = tk.e0;
+        dd.nv = tk.nv;
+        dd.has_d = ui.has_d ? 1 : 0;
+        dd.pad[0] = dd.pad[1] = dd.pad[2] = 0;
+        sm.desc[st] = dd;  // published by the arrival below (release), read after the full wait
+      }
       if (bulk) {
+        // 4 copies per stage (2 per row when both rows are loaded): a few
+        // copies of several KB each keep the memory pipe full, while copies
+        // of 1 KB or less cost more in per-copy overhead than they gain
+        const uint32_t bytes = (uint32_t)tk.len * (uint32_t)E::ES;
+        const int rows = ui.has_d ? 2 : 1;
+        const int per_row = 4 / rows;
+        const uint32_t piece = ((bytes + per_row - 1) / per_row + 15u) & ~15u;
         if (lane == 0) {
-          const uint32_t bytes = (uint32_t)tk.len * (uint32_t)E::ES;
           fence_proxy_async_smem();
-          mbar_arrive_expect_tx(bar, ui.has_d ? 2u * bytes : bytes);
-          bulk_load_plain(smem_addr(dst), ui.tg + tk.e0, bytes, bar);
-          if (ui.has_d) bulk_load_plain(smem_addr(dst + P.doff), ui.dg + tk.e0, bytes, bar);
+          mbar_arrive_expect_tx(bar, (uint32_t)rows * bytes);
+        }
+        __syncwarp();
+        const int row = lane / per_row;
+        const uint32_t off = (uint32_t)(lane % per_row) * piece;
+        if (row < rows && off < bytes) {
+          const uint32_t len = min(piece, bytes - off);
+          const char* src = reinterpret_cast<const char*>((row == 0 ? ui.tg : ui.dg) + tk.e0) + off;
+          bulk_load_plain(smem_addr(dst + (row ? P.doff : 0) + off), src, len, bar);
         }
       } else {
         // element-wise staging for rows off 16-byte boundaries (-inf padding)
@@ -983,167 +1092,119 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const PipeParams P) {
     if (bulk && lane == 0) {
       for (int i = (n > D ? n - D : 0); i < n; ++i) pwait(smem_addr(&sm.full[i % D]), (uint32_t)(i / D) & 1u, P, sm);
     }
-  } else if (warp == kControlWarp) {
-    // ================= control warp =================
-    int kc = 0;  // jobs pushed
+  } else if (warp < kFinalWarp) {
+    // ================= control warps =================
+    const int r = warp - kControlWarp0;
+    // one ticket per job; the finaliser takes them in ticket order
     auto push_job = [&](const Job& jb) {
+      int kc = 0;
+      if (lane == 0) kc = atomicAdd(&sm.job_tail, 1);
+      kc = __shfl_sync(kFull, kc, 0);
       const int q = kc % kJobSlots;
       if (kc >= kJobSlots) pwait(smem_addr(&sm.job_empty[q]), (uint32_t)((kc / kJobSlots) + 1) & 1u, P, sm);
       if (lane == 0) sm.job[q] = jb;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&sm.job_full[q]));
-      ++kc;
     };
-    auto job_of = [&](int u, const Nrm& nr) {
-      Job jb;
-      jb.unit = u;
-      jb.mode = nr.mode;
-      jb.acc = nr.acc;
-      jb.stop = 0;
-      jb.c1t = nr.c1t;
-      jb.cd2 = nr.cd2;
-      jb.izt = nr.izt;
-      jb.uf = nr.uf;
-      return jb;
+    // tagged words of every chunk of unit u, lanes over chunks in groups of 32,
+    // once all are written
+    auto read_unit = [&](int u, int nwords, uint64_t (&a)[3], const uint64_t* base_ptr, int stride, int base) {
+      const int c = base + lane;
+      const uint64_t* w = base_ptr + ((long long)u * P.C + c) * stride;
+      auto load = [&]() {
+#pragma unroll
+        for (int k = 0; k < 3; ++k) a[k] = (c < P.C && k < nwords) ? ld_relaxed_u64(w + k) : ~0ull;
+      };
+      auto ok = [&]() { return tag_ok(a[0]) && tag_ok(a[1]) && tag_ok(a[2]); };
+      load();
+      poll_words(P, lane, ok, load);
+    };
+    // phase-1 partials of task i from the compute warps' slot
+    auto read_wp1 = [&](int i, float& x, float& y, float& z, float& w, float& nn) {
+      const int slot = i % kSlots;
+      pwait(smem_addr(&sm.p1done[slot]), par(i), P, sm);
+      x = y = z = w = nn = 0.0f;
+      if (lane < kP1Count) {
+        const float4 q = sm.wp1[slot][lane];
+        x = q.x;
+        y = q.y;
+        z = q.z;
+        w = q.w;
+        nn = sm.wnan[slot][lane];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&sm.p1free[slot]));  // the slot may be reused
     };
 
     if constexpr (kGreedy) {
-      uint32_t old_prev = 0;
-      int u_prev = -1;
-      for (int i = 0; i <= n; ++i) {
-        uint32_t old_cur = 0;
-        int u_cur = -1;
-        if (i < n) {
-          const int slot = i & 1;
-          pwait(smem_addr(&sm.p1done[slot]), (uint32_t)(i >> 1) & 1u, P, sm);
-          float v1 = -INFINITY, v2 = -INFINITY, nn = 0.0f;
-          int i1 = 0x7FFFFFFF, i2 = 0x7FFFFFFF;
-          if (lane < kCompWarps) {
-            const float4 q = sm.wp1[slot][lane];
-            v1 = q.x;
-            i1 = __float_as_int(q.y);
-            v2 = q.z;
-            i2 = __float_as_int(q.w);
-            nn = sm.wnan[slot][lane];
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_addr(&sm.p1free[slot]));  // the slot may be reused
-          warp_argmax_redux(v1, i1);
-          warp_argmax_redux(v2, i2);
-          nn = redux_max_f32(nn);
-          const TaskInfo tk = task_of(i);
-          u_cur = tk.u;
-          if (lane == 0) {
-            uint64_t* w = P.part1 + ((long long)tk.u * P.C + tk.c) * 4;
-            st_relaxed_u64(w + 0, tag2i(v1, i1));
-            st_relaxed_u64(w + 1, tag2i(v2, i2));
-            st_relaxed_u64(w + 2, tag2(nn, 0.0f));
-            __threadfence();
-            old_cur = atomicAdd(P.cnt + tk.u, 1u);
-          }
+      for (int i = r; i < n; i += kCtlWarps) {
+        float v1, v2, fi1, fi2, nn;
+        read_wp1(i, v1, fi1, v2, fi2, nn);
+        int i1 = (lane < kP1Count) ? __float_as_int(fi1) : 0x7FFFFFFF;
+        int i2 = (lane < kP1Count) ? __float_as_int(fi2) : 0x7FFFFFFF;
+        if (lane >= kP1Count) v1 = v2 = -INFINITY;
+        warp_argmax_redux(v1, i1);
+        warp_argmax_redux(v2, i2);
+        nn = redux_max_f32(nn);
+        const TaskInfo tk = task_of(i);
+        if (lane == 0) {
+          uint64_t* w = P.part1 + ((long long)tk.u * P.C + tk.c) * 4;
+          st_relaxed_u64(w + 0, tag2i(v1, i1));
+          st_relaxed_u64(w + 1, tag2i(v2, i2));
+          st_relaxed_u64(w + 2, tag2(nn, 0.0f));
         }
-        if (i >= 1) {
-          const uint32_t o = __shfl_sync(kFull, old_prev, 0);
-          if (o == (uint32_t)P.C - 1) {
-            if (lane == 0) __threadfence();
-            Nrm nr{};
-            push_job(job_of(u_prev, nr));
+        // the CTA holding the unit's finalising chunk waits for the others' partials
+        if (tk.c == fin_chunk(P, tk.u)) {
+          for (int base = 0; base < P.C; base += 32) {
+            uint64_t a[3];
+            read_unit(tk.u, 3, a, P.part1, 4, base);
           }
+          Job jb{};
+          jb.unit = tk.u;
+          push_job(jb);
         }
-        old_prev = old_cur;
-        u_prev = u_cur;
       }
     } else {
-      // prefetched per-task scalars (lane 0): the drafted token of task i
-      int y_cur = -1;
-      auto token_of = [&](int i) {
-        if constexpr (MODE == kVerify) {
-          if (i < n) {
-            const TaskInfo tk = task_of(i);
-            const UnitInfo<E> ui = unit_info<E, MODE>(P, tk.u);
-            return ui.bonus ? -1 : __ldg(P.draft_tokens + ui.b * P.K + ui.k);
+      for (int i = r; i < n + kLag; i += kCtlWarps) {
+        // ---- task i: publish its phase-1 partials, read back the unit's, decide
+        if (i < n) {
+          float mt, zt, md, zd, nn;
+          read_wp1(i, mt, zt, md, zd, nn);
+          if (lane >= kP1Count) {
+            mt = md = -INFINITY;
+            zt = zd = 0.0f;
           }
-        }
-        return -1;
-      };
-      if (lane == 0) y_cur = token_of(0);
-      // loads in flight for the prepare of one task
-      uint64_t pw0 = 0, pw1 = 0, pw2 = 0;
-      int py = -1;
-      float pua = 0.0f, puf = 0.0f;
-      auto issue_loads = [&](int iq) {
-        const TaskInfo tq = task_of(iq);
-        const UnitInfo<E> uq = unit_info<E, MODE>(P, tq.u);
-        const bool need_g = (MODE == kVerify) && !uq.bonus;
-        if (lane < P.C) {
-          const uint64_t* w = P.part1 + ((long long)tq.u * P.C + lane) * 4;
-          pw0 = ld_relaxed_u64(w);
-          pw1 = uq.has_d ? ld_relaxed_u64(w + 1) : ~0ull;
-          pw2 = need_g ? ld_relaxed_u64(w + 2) : ~0ull;
-        } else {
-          pw0 = pw1 = pw2 = ~0ull;
-        }
-        if constexpr (MODE == kVerify) {
+          warp_combine_mz2(mt, zt, md, zd, s);
+          const TaskInfo tk = task_of(i);
+          const UnitInfo<E> ui = unit_info<E, MODE>(P, tk.u);
+          int y = -1;
+          float ua = 0.0f, uf = 0.0f;
+          if constexpr (MODE == kVerify) {
+            if (lane == 0) {
+              y = ui.bonus ? -1 : __ldg(P.draft_tokens + ui.b * P.K + ui.k);
+              ua = ui.bonus ? 0.0f : __ldg(P.u_accept + ui.b * P.K + ui.k);
+              uf = __ldg(P.u_final + ui.b);
+            }
+          }
           if (lane == 0) {
-            py = uq.bonus ? -1 : __ldg(P.draft_tokens + uq.b * P.K + uq.k);
-            pua = uq.bonus ? 0.0f : __ldg(P.u_accept + uq.b * P.K + uq.k);
-            puf = __ldg(P.u_final + uq.b);
+            float gt = 0.0f, gd = 0.0f;
+            if (MODE == kVerify && !ui.bonus && y >= tk.e0 && y < tk.e0 + tk.len) {
+              // the stage of task i is held until its phase 2, which needs this decision
+              gt = E::to_f32(reinterpret_cast<const Raw*>(stage_t(i))[y - tk.e0]);
+              gd = E::to_f32(reinterpret_cast<const Raw*>(stage_d(i))[y - tk.e0]);
+            }
+            uint64_t* w = P.part1 + ((long long)tk.u * P.C + tk.c) * 4;
+            st_relaxed_u64(w + 0, tag2(mt, zt));
+            if (ui.has_d) {
+              st_relaxed_u64(w + 1, tag2(md, zd));
+              st_relaxed_u64(w + 2, tag2(gt, gd));
+            }
           }
-        }
-      };
-
-      for (int i = 0; i < n + kLag; ++i) {
-        // ---- S2: decision for task i - 2 (its loads were issued last iteration)
-        if (i >= 2 && i - 2 < n) {
-          const int iq = i - 2;
-          const TaskInfo tq = task_of(iq);
-          const UnitInfo<E> uq = unit_info<E, MODE>(P, tq.u);
-          const bool need_g = (MODE == kVerify) && !uq.bonus;
-          auto words_ok = [&](uint64_t a0, uint64_t a1, uint64_t a2) {
-            return tag_ok(a0) && (!uq.has_d || tag_ok(a1)) && (!need_g || tag_ok(a2));
-          };
-          // wait until every chunk's words are there (bounded)
-          auto fetch_group = [&](int base, uint64_t& a0, uint64_t& a1, uint64_t& a2, bool preloaded) {
-            const int c = base + lane;
-            const uint64_t* w = P.part1 + ((long long)tq.u * P.C + c) * 4;
-            if (!preloaded) {
-              if (c < P.C) {
-                a0 = ld_relaxed_u64(w);
-                a1 = uq.has_d ? ld_relaxed_u64(w + 1) : ~0ull;
-                a2 = need_g ? ld_relaxed_u64(w + 2) : ~0ull;
-              } else {
-                a0 = a1 = a2 = ~0ull;
-              }
-            }
-            bool ok = (c >= P.C) || words_ok(a0, a1, a2);
-            if (__all_sync(kFull, ok)) return;
-            const uint64_t t0 = global_timer_ns();
-            uint32_t back = 32;
-            for (;;) {
-              __nanosleep(back);
-              if (back < 512) back <<= 1;
-              if (!ok) {
-                a0 = ld_relaxed_u64(w);
-                a1 = uq.has_d ? ld_relaxed_u64(w + 1) : ~0ull;
-                a2 = need_g ? ld_relaxed_u64(w + 2) : ~0ull;
-                ok = words_ok(a0, a1, a2);
-              }
-              if (__all_sync(kFull, ok)) return;
-              int stop = 0;
-              if (lane == 0) {
-                if (aborted(P, sm)) stop = 1;
-                else if (global_timer_ns() - t0 > kWaitLimitNs) {
-                  give_up(P, sm);
-                  stop = 1;
-                }
-              }
-              if (__shfl_sync(kFull, stop, 0)) return;
-            }
-          };
-          fetch_group(0, pw0, pw1, pw2, true);
-          const int pyb = __shfl_sync(kFull, py, 0);
-          const int cy = (need_g && pyb >= 0 && pyb < P.V) ? pyb / P.Lc : -1;
-          float mt = -INFINITY, zt = 0.0f, md = -INFINITY, zd = 0.0f, gt = 0.0f, gd = 0.0f;
+          const bool need_g = (MODE == kVerify) && !ui.bonus;
+          const int yb = __shfl_sync(kFull, y, 0);
+          const int cy = (need_g && yb >= 0 && yb < P.V) ? yb / P.Lc : -1;
+          const int nwords = need_g ? 3 : (ui.has_d ? 2 : 1);
+          float cm_t = -INFINITY, cz_t = 0.0f, cm_d = -INFINITY, cz_d = 0.0f, gt = 0.0f, gd = 0.0f;
           auto merge = [&](float& m, float& z, float m2, float z2) {
             if (!(m2 > -INFINITY)) {
               if (m2 != m2) m = m2;  // NaN propagates
@@ -1162,87 +1223,84 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const PipeParams P) {
                           __fmul_rn(z2, ex2(__fadd_rn(__fmul_rn(m2, s), -cM))));
             m = M;
           };
-          if (lane < P.C) {
-            mt = tag_lo(pw0);
-            zt = tag_hi(pw0);
-            if (uq.has_d) {
-              md = tag_lo(pw1);
-              zd = tag_hi(pw1);
-            }
-            if (lane == cy) {
-              gt = tag_lo(pw2);
-              gd = tag_hi(pw2);
-            }
-          }
-          for (int base = 32; base < P.C; base += 32) {
-            uint64_t a0, a1, a2;
-            fetch_group(base, a0, a1, a2, false);
+          for (int base = 0; base < P.C; base += 32) {
+            uint64_t a[3];
+            read_unit(tk.u, nwords, a, P.part1, 4, base);
             if (base + lane < P.C) {
-              merge(mt, zt, tag_lo(a0), tag_hi(a0));
-              if (uq.has_d) merge(md, zd, tag_lo(a1), tag_hi(a1));
+              if (base == 0) {
+                cm_t = tag_lo(a[0]);
+                cz_t = tag_hi(a[0]);
+                if (ui.has_d) {
+                  cm_d = tag_lo(a[1]);
+                  cz_d = tag_hi(a[1]);
+                }
+              } else {
+                merge(cm_t, cz_t, tag_lo(a[0]), tag_hi(a[0]));
+                if (ui.has_d) merge(cm_d, cz_d, tag_lo(a[1]), tag_hi(a[1]));
+              }
               if (base + lane == cy) {
-                gt = tag_lo(a2);
-                gd = tag_hi(a2);
+                gt = tag_lo(a[2]);
+                gd = tag_hi(a[2]);
               }
             }
           }
-          warp_combine_mz2(mt, zt, md, zd, s);
+          warp_combine_mz2(cm_t, cz_t, cm_d, cz_d, s);
           if (cy >= 0) {
             gt = __shfl_sync(kFull, gt, cy & 31);
             gd = __shfl_sync(kFull, gd, cy & 31);
           }
+          const int slot2 = i % kSlots2;
           if (lane == 0) {
-            const float Zt = zt, Zd = zd;
-            const float c1t = __fmul_rn(mt, s), c1d = __fmul_rn(md, s);
-            const bool valid = (Zt > 0.0f && Zt < INFINITY) && (!uq.has_d || (Zd > 0.0f && Zd < INFINITY));
+            const float Zt = cz_t, Zd = cz_d;
+            const float c1t = __fmul_rn(cm_t, s), c1d = __fmul_rn(cm_d, s);
+            const bool valid = (Zt > 0.0f && Zt < INFINITY) && (!ui.has_d || (Zd > 0.0f && Zd < INFINITY));
             const float izt = __frcp_rn(Zt), izd = __frcp_rn(Zd);
             uint32_t flags = 0;
             int mode = 0, acc = 1;
             if constexpr (MODE == kVerify) {
-              if (uq.bonus) {
+              if (ui.bonus) {
                 mode = 2;
                 acc = 0;
               } else {
-                const bool tok_ok = py >= 0 && py < P.V;
+                const bool tok_ok = y >= 0 && y < P.V;
                 // u * q(y) <= p(y), with p(y), q(y) formed like the per-element values
                 const float pyv = __fmul_rn(ex2(fmaf(gt, s, -c1t)), izt);
                 const float qyv = __fmul_rn(ex2(fmaf(gd, s, -c1d)), izd);
-                acc = (tok_ok && __fmul_rn(pua, qyv) <= pyv) ? 1 : 0;
+                acc = (tok_ok && __fmul_rn(ua, qyv) <= pyv) ? 1 : 0;
                 mode = acc ? 0 : 1;
-                if (!(pua >= 0.0f && pua < 1.0f)) flags |= kBadUniform;
+                if (!(ua >= 0.0f && ua < 1.0f)) flags |= kBadUniform;
                 if (!tok_ok) flags |= kBadToken;
               }
-              if (!(puf >= 0.0f && puf < 1.0f)) flags |= kBadUniform;
+              if (!(uf >= 0.0f && uf < 1.0f)) flags |= kBadUniform;
             }
             if (!valid) {
               flags |= kBadLogits;
               mode = 3;
               acc = 0;
             }
-            if (flags && tq.c == 0 && P.status) atomicOr(P.status, flags);
-            Nrm& nr = sm.nrm[iq & 1];
+            if (flags && tk.c == 0 && P.status) atomicOr(P.status, flags);
+            Nrm& nr = sm.nrm[slot2];  // its previous content (task i - 8) was consumed at task i - 4
             nr.c1t = c1t;
             nr.c1d = c1d;
-            nr.cd2 = (uq.has_d && valid) ? c1d + __log2f(__fmul_rn(Zd, izt)) : 0.0f;
+            nr.cd2 = (ui.has_d && valid) ? c1d + __log2f(__fmul_rn(Zd, izt)) : 0.0f;
             nr.izt = izt;
-            nr.uf = puf;
+            nr.uf = uf;
             nr.mode = mode;
             nr.acc = acc;
-            nr.unit = tq.u;
+            nr.unit = tk.u;
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_addr(&sm.nrm_bar[iq & 1]));
+          if (lane == 0) mbar_arrive(smem_addr(&sm.nrm_bar[slot2]));
         }
-        // ---- S1: phase-2 partials of task i - 3
-        uint32_t old = 0;
-        int u3 = -1;
+        // ---- task i - kLag: publish its phase-2 partials; the CTA holding the
+        // unit's finalising chunk waits for the others' and hands the unit on
         if (i >= kLag && i - kLag < n) {
-          const int i3 = i - kLag;
-          const int slot = i3 & 1;
-          pwait(smem_addr(&sm.p2done[slot]), (uint32_t)(i3 >> 1) & 1u, P, sm);
+          const int i4 = i - kLag;
+          const int slot2 = i4 % kSlots2;
+          pwait(smem_addr(&sm.p2done[slot2]), par2(i4), P, sm);
           float A = 0.0f, R = 0.0f, Sm = 0.0f;
-          if (lane < kCompWarps) {
-            const float4 q = sm.wp2[slot][lane];
+          if (lane < kP2Warps) {
+            const float4 q = sm.wp2[slot2][lane];
             A = q.x;
             R = q.y;
             Sm = q.z;
@@ -1250,75 +1308,49 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const PipeParams P) {
           A = warp_sum(A);
           R = warp_sum(R);
           Sm = warp_sum(Sm);
-          const TaskInfo t3 = task_of(i3);
-          u3 = t3.u;
+          const TaskInfo t4 = task_of(i4);
+          const Nrm nr = sm.nrm[slot2];
           if (lane == 0) {
-            const Nrm& nr = sm.nrm[slot];
             const float nanv = __int_as_float(0x7FC00000);
             const float ac = (nr.mode == 3) ? nanv : __fmul_rn(A, nr.izt);
             const float second = (MODE == kE2E) ? ((nr.mode == 3) ? nanv : __fmul_rn(Sm, nr.izt)) : R;
-            P.part2[(long long)t3.u * P.C + t3.c] =
-                (uint64_t)__float_as_uint(ac) | ((uint64_t)__float_as_uint(second) << 32);
-            __threadfence();
-            old = atomicAdd(P.cnt + t3.u, 1u);
+            st_relaxed_u64(P.part2 + (long long)t4.u * P.C + t4.c, tag2(ac, second));
           }
-        }
-        // ---- S3: phase-1 partials of task i
-        if (i < n) {
-          const int slot = i & 1;
-          pwait(smem_addr(&sm.p1done[slot]), (uint32_t)(i >> 1) & 1u, P, sm);
-          float mt = -INFINITY, zt = 0.0f, md = -INFINITY, zd = 0.0f;
-          if (lane < kCompWarps) {
-            const float4 q = sm.wp1[slot][lane];
-            mt = q.x;
-            zt = q.y;
-            md = q.z;
-            zd = q.w;
-          }
-          warp_combine_mz2(mt, zt, md, zd, s);
-          if (lane == 0) {
-            const TaskInfo tk = task_of(i);
-            const UnitInfo<E> ui = unit_info<E, MODE>(P, tk.u);
-            float gt = 0.0f, gd = 0.0f;
-            if (MODE == kVerify && !ui.bonus && y_cur >= tk.e0 && y_cur < tk.e0 + tk.len) {
-              const Raw* rt = reinterpret_cast<const Raw*>(stage_t(i));
-              const Raw* rd = reinterpret_cast<const Raw*>(stage_d(i));
-              gt = E::to_f32(rt[y_cur - tk.e0]);
-              gd = E::to_f32(rd[y_cur - tk.e0]);
+          if (t4.c == fin_chunk(P, t4.u)) {
+            for (int base = 0; base < P.C; base += 32) {
+              uint64_t a[3];
+              read_unit(t4.u, 1, a, P.part2, 1, base);
             }
-            uint64_t* w = P.part1 + ((long long)tk.u * P.C + tk.c) * 4;
-            st_relaxed_u64(w + 0, tag2(mt, zt));
-            if (ui.has_d) {
-              st_relaxed_u64(w + 1, tag2(md, zd));
-              st_relaxed_u64(w + 2, tag2(gt, gd));
-            }
+            Job jb{};
+            jb.unit = t4.u;
+            jb.mode = nr.mode;
+            jb.acc = nr.acc;
+            jb.c1t = nr.c1t;
+            jb.cd2 = nr.cd2;
+            jb.izt = nr.izt;
+            jb.uf = nr.uf;
+            push_job(jb);
           }
         }
-        // ---- S4: hand a finished unit to the finaliser
-        if (i >= kLag && i - kLag < n) {
-          const uint32_t o = __shfl_sync(kFull, old, 0);
-          if (o == (uint32_t)P.C - 1) {
-            if (lane == 0) __threadfence();
-            push_job(job_of(u3, sm.nrm[(i - kLag) & 1]));
-          }
-        }
-        // ---- S5: loads for the decision of task i - 1; token of task i + 1
-        if (i >= 1 && i - 1 < n) issue_loads(i - 1);
-        if (lane == 0) y_cur = token_of(i + 1);
       }
     }
+    // one stop job per control warp
     Job stop{};
     stop.stop = 1;
     push_job(stop);
   } else {
     // ================= finaliser warp =================
+    int stops = 0;
     for (int k = 0;; ++k) {
       const int q = k % kJobSlots;
       if (!pwait(smem_addr(&sm.job_full[q]), (uint32_t)(k / kJobSlots) & 1u, P, sm)) break;
       const Job jb = sm.job[q];
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&sm.job_empty[q]));
-      if (jb.stop) break;
+      if (jb.stop) {
+        if (++stops == kCtlWarps) break;
+        continue;
+      }
       finalize_unit<E, MODE>(P, jb, lane);
     }
   }

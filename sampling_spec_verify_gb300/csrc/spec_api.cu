@@ -7,7 +7,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "pipe.cuh"
 #include "spec_verify.h"
@@ -80,12 +82,22 @@ struct Chunking {
   int C = 0, Lc = 0;
 };
 
-Chunking chunking(int es, int V, int rows, bool draws) {
+// Chunk length for C chunks of V logits: a multiple of 128 bytes (so that
+// chunks of 128-byte-aligned rows start on cache-line boundaries) unless the
+// cap is smaller than that, and never above the cap.
+int chunk_len(int es, int V, int C, int cap) {
   const int pv = 16 / es;
+  const int line = 128 / es;
+  int Lc = (int)(ceil_div(ceil_div(V, C), line) * line);
+  if (Lc > cap) Lc = (int)(ceil_div(ceil_div(V, C), pv) * pv);
+  return Lc;
+}
+
+Chunking chunking(int es, int V, int rows, bool draws) {
   const int cap = chunk_cap(es, rows, draws);
   Chunking ch;
-  ch.C = (int)ceil_div(V, cap);
-  ch.Lc = (int)(ceil_div(ceil_div(V, ch.C), pv) * pv);
+  ch.Lc = chunk_len(es, V, (int)ceil_div(V, cap), cap);
+  ch.C = (int)ceil_div(V, ch.Lc);  // every chunk starts below V
   return ch;
 }
 
@@ -146,7 +158,7 @@ void bind_workspace(PipeParams& P, const WsLayout& w, void* ws, size_t bytes) {
   char* base = static_cast<char*>(ws);
   P.part1 = reinterpret_cast<uint64_t*>(base + w.part1);
   P.part2 = reinterpret_cast<uint64_t*>(base + w.part2);
-  P.seg = w.has_seg ? reinterpret_cast<float*>(base + w.seg) : nullptr;
+  P.seg = w.has_seg ? reinterpret_cast<uint32_t*>(base + w.seg) : nullptr;
   P.cnt = reinterpret_cast<uint32_t*>(base + w.cnt);
   P.rec = w.stats ? nullptr : reinterpret_cast<Rec*>(base + w.rec);
   P.stats = w.stats ? reinterpret_cast<E2EStats*>(base + w.stats) : nullptr;
@@ -182,8 +194,33 @@ int static_smem() {
   return x;
 }
 
+std::mutex g_occ_mu;
+std::map<std::tuple<const void*, int, int>, int> g_occ;  // (kernel, smem, device) -> CTAs per SM
+
+// Resident CTAs per SM of `fn` with `smem` dynamic bytes (queried once per
+// kernel, size and device: the query costs tens of microseconds).
+template <class Fn>
+int occupancy(Fn fn, int smem, int dev) {
+  const auto key = std::make_tuple((const void*)fn, smem, dev);
+  {
+    std::lock_guard<std::mutex> lk(g_occ_mu);
+    const auto it = g_occ.find(key);
+    if (it != g_occ.end()) return it->second;
+  }
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, ssv::kThreads, (size_t)smem) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  std::lock_guard<std::mutex> lk(g_occ_mu);
+  g_occ[key] = nb;
+  return nb;
+}
+
 // Sets the kernel's shared-memory limit (once per device) and computes the
-// plan: chunking, stages that fit, and the persistent grid.
+// plan: chunking, stages that fit, and the persistent grid.  In the sampling
+// modes the chunk is shrunk until kLag + 4 stages fit (the kLag + 1 stages a
+// CTA holds for its two passes, and three in flight).
 template <class E, int MODE>
 spec_status_t make_plan(int V, int rows, Plan* pl) {
   constexpr bool kSample = !(MODE == ssv::kVerifyGreedy || MODE == ssv::kOverlapGreedy);
@@ -201,25 +238,35 @@ spec_status_t make_plan(int V, int rows, Plan* pl) {
       return SPEC_ERR_CUDA;
     prepared_mask<E, MODE>().fetch_or(bit);
   }
-  const Chunking ch = chunking(E::ES, V, rows, MODE == ssv::kVerify);
+  Chunking ch = chunking(E::ES, V, rows, MODE == ssv::kVerify);
+  const int cap = chunk_cap(E::ES, rows, MODE == ssv::kVerify);
+  const int want = kSample ? ssv::kLag + 4 : 4;
+  int c_try = ch.C;
   Plan p;
-  p.C = ch.C;
-  p.Lc = ch.Lc;
-  p.doff = (int)((ch.Lc * E::ES + 127) / 128 * 128);
-  p.stage = rows == 2 ? (int)((p.doff + ch.Lc * E::ES + 127) / 128 * 128) : p.doff;
+  for (;;) {
+    p.C = ch.C;
+    p.Lc = ch.Lc;
+    p.doff = (int)((ch.Lc * E::ES + 127) / 128 * 128);
+    p.stage = rows == 2 ? (int)((p.doff + ch.Lc * E::ES + 127) / 128 * 128) : p.doff;
+    if (avail / p.stage >= want || g_chunk_override.load() > 0) break;
+    // smaller chunks, more stages, as long as the workspace holds the chunks
+    const int nLc = chunk_len(E::ES, V, c_try + 1, cap);
+    const int nC = (int)ceil_div(V, nLc);
+    if (nC > ws_chunks(V)) break;
+    ++c_try;
+    ch.Lc = nLc;
+    ch.C = nC;
+  }
   int D = avail / p.stage;
   if (D > ssv::kMaxStages) D = ssv::kMaxStages;
-  const int ovs = g_stage_override.load();
-  if (ovs > 0 && ovs < D) D = ovs;
   const int dmin = kSample ? ssv::kLag + 2 : 2;
   if (D < dmin) return SPEC_ERR_UNSUPPORTED;
+  const int ovs = g_stage_override.load();
+  if (ovs > 0 && ovs < D) D = ovs < dmin ? dmin : ovs;
   p.D = D;
   p.smem = D * p.stage;
-  int nb = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, ssv::kThreads, (size_t)p.smem) != cudaSuccess) {
-    cudaGetLastError();
-    return SPEC_ERR_CUDA;
-  }
+  const int nb = occupancy(fn, p.smem, dev);
+  if (nb < 0) return SPEC_ERR_CUDA;
   if (nb < 1) return SPEC_ERR_UNSUPPORTED;
   p.G = nb * di.sms;
   // a unit's chunks must sit in different CTAs for the phase-2 exchange
