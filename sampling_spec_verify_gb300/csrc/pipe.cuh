@@ -285,10 +285,12 @@ __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, const PipeP
 // ---- per-element arithmetic ------------------------------------------------------
 
 // Draw weights of one vector and their total (fixed association).  KIND 1:
-// Z_t * max(0, p - q) = max(0, e_t - e_d) with e_t = 2^(z_t s - c1t),
-// e_d = 2^(z_d s - cd2) (cd2 folds log2(Z_d / Z_t) in), and Z_t * min(p, q)
-// added to `mn`.  KIND 2: Z_t * p = e_t.  Phase 2 and the finaliser's walk call
-// this same function, so both see bit-identical weights.
+// Z_t * max(0, p - q) = e_t - e_m with e_t = 2^(z_t s - c1t) and
+// e_m = 2^min(z_t s - c1t, z_d s - cd2) = Z_t * min(p, q) (cd2 folds
+// log2(Z_d / Z_t) in); e_m is added to `mn`.  Where p <= q the two exponents
+// are the same value, so the weight is exactly 0.  KIND 2: Z_t * p = e_t.
+// Phase 2 and the finaliser's walk call this same function, so both see
+// bit-identical weights.
 template <class E, int KIND>
 __device__ __forceinline__ float vec_weights(const uint4& wt, const uint4& wd, f32x2 S2, f32x2 CT, f32x2 CD,
                                              float (&w)[E::PV], f32x2& mn) {
@@ -303,10 +305,11 @@ __device__ __forceinline__ float vec_weights(const uint4& wt, const uint4& wd, f
       float t0, t1, d0, d1;
       f2_split(f2_fma(pt[h], S2, CT), t0, t1);
       f2_split(f2_fma(pd[h], S2, CD), d0, d1);
-      const float et0 = ex2(t0), et1 = ex2(t1), ed0 = ex2(d0), ed1 = ex2(d1);
-      const float r0 = fmaxf(__fsub_rn(et0, ed0), 0.0f), r1 = fmaxf(__fsub_rn(et1, ed1), 0.0f);
+      const float et0 = ex2(t0), et1 = ex2(t1);
+      const float em0 = ex2(fminf(t0, d0)), em1 = ex2(fminf(t1, d1));
+      const float r0 = __fsub_rn(et0, em0), r1 = __fsub_rn(et1, em1);
       wp[h] = f2(r0, r1);
-      mp[h] = f2(fminf(et0, ed0), fminf(et1, ed1));
+      mp[h] = f2(em0, em1);
       w[2 * h] = r0;
       w[2 * h + 1] = r1;
     }
@@ -806,6 +809,22 @@ __device__ __noinline__ void finalize_unit(const PipeParams& P, const Job& jb, i
   const UnitInfo<E> ui = unit_info<E, MODE>(P, u);
   const int C = P.C;
   uint32_t flags = 0;
+  // wait until every chunk of the unit has published its words (phase-1
+  // arg-maxima at T == 0, phase-2 partials otherwise)
+  for (int base = 0; base < C; base += 32) {
+    const int c = base + lane;
+    const uint64_t* w = kGreedy ? P.part1 + ((long long)u * C + c) * 4 : P.part2 + (long long)u * C + c;
+    uint64_t a0 = ~0ull, a1 = ~0ull, a2 = ~0ull;  // each word is validated on its own
+    auto load = [&]() {
+      a0 = (c < C) ? ld_relaxed_u64(w) : ~0ull;
+      if (kGreedy) {
+        a1 = (c < C) ? ld_relaxed_u64(w + 1) : ~0ull;
+        a2 = (c < C) ? ld_relaxed_u64(w + 2) : ~0ull;
+      }
+    };
+    load();
+    poll_words(P, lane, [&]() { return tag_ok(a0) && tag_ok(a1) && tag_ok(a2); }, load);
+  }
   if constexpr (kGreedy) {
     // arg-maxima of the chunks, in chunk order
     float bt = -INFINITY, bd = -INFINITY, nn = 0.0f;
@@ -1153,12 +1172,9 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const __grid_constant
           st_relaxed_u64(w + 1, tag2i(v2, i2));
           st_relaxed_u64(w + 2, tag2(nn, 0.0f));
         }
-        // the CTA holding the unit's finalising chunk waits for the others' partials
+        // the CTA holding the unit's finalising chunk hands the unit to its
+        // finaliser, which waits for the other chunks' partials
         if (tk.c == fin_chunk(P, tk.u)) {
-          for (int base = 0; base < P.C; base += 32) {
-            uint64_t a[3];
-            read_unit(tk.u, 3, a, P.part1, 4, base);
-          }
           Job jb{};
           jb.unit = tk.u;
           push_job(jb);
@@ -1317,10 +1333,6 @@ __global__ void __launch_bounds__(kThreads, 1) pipe_kernel(const __grid_constant
             st_relaxed_u64(P.part2 + (long long)t4.u * P.C + t4.c, tag2(ac, second));
           }
           if (t4.c == fin_chunk(P, t4.u)) {
-            for (int base = 0; base < P.C; base += 32) {
-              uint64_t a[3];
-              read_unit(t4.u, 1, a, P.part2, 1, base);
-            }
             Job jb{};
             jb.unit = t4.u;
             jb.mode = nr.mode;
