@@ -33,12 +33,8 @@
  *    Two calls that may run at the same time on the GPU must not share a
  *    workspace.
  *  - Temperatures are float32; T == 0 selects greedy decoding where allowed.
- *  - Limits: B >= 0, 0 <= K <= 64, 1 <= V; the number of (row, position,
- *    vocabulary chunk) tasks, about B * (K + 1) * V / 4096, must stay below
- *    2^31.
- *  - Kernels are launched cooperatively (every CTA of the grid resident at
- *    once, one per SM): a launch fails with SPEC_ERR_CUDA rather than
- *    waiting when the device cannot hold the whole grid.
+ *  - Limits: B >= 0, 0 <= K <= 64, 1 <= V, and 2 * V * elem_size may not
+ *    exceed 16 CTAs' worth of shared memory (V up to about 900k for bf16).
  */
 #ifndef SPEC_VERIFY_H_
 #define SPEC_VERIFY_H_
@@ -122,16 +118,16 @@ spec_status_t spec_verify(const void* target_logits, const void* draft_logits,
  * scratch is a fixed device array of SPEC_NOALLOC_SCRATCH_BYTES inside the
  * library, held by every GPU that loads the library until the process exits.
  * Sizes whose spec_verify_workspace_bytes(B, K, V) exceeds it are rejected with
- * SPEC_ERR_UNSUPPORTED (at K = 4 and V = 151,936 that is about 500 rows).
- * No call allocates or frees memory; each clears the part of the array it
- * uses with cudaMemsetAsync on `stream`.
+ * SPEC_ERR_UNSUPPORTED (at K = 4 that is about 12,000 rows).  No call
+ * allocates or frees memory; each clears the part of the array it uses with
+ * cudaMemsetAsync on `stream`.
  *  - The first call on a device looks up the array's device address (once per
  *    device, with that device current); make that first call before any
  *    stream capture.
  *  - Every call on a device shares the one array: calls that may overlap on
  *    the GPU (different streams without ordering between them) race and give
  *    wrong results.  Serialise them. */
-#define SPEC_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define SPEC_NOALLOC_SCRATCH_BYTES (1u << 20)
 
 spec_status_t spec_verify_noalloc(const void* target_logits,
                                   const void* draft_logits, spec_dtype_t dtype,
@@ -201,22 +197,20 @@ spec_status_t spec_e2e_tv_fwd_bwd(const void* target_logits,
                                   size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
-/* Launch plan the library picks for a sampling verify (T > 0) over rows of V
- * logits (for benchmarks and diagnostics): logits per vocabulary chunk, chunks
- * per row, threads per CTA, dynamic shared memory per CTA, CTAs of the
- * persistent grid and shared-memory stages per CTA.  Needs a current CUDA
- * device.  Any output pointer may be NULL. */
-spec_status_t spec_launch_shape(spec_dtype_t dtype, int V, int* chunk_elems, int* chunks, int* threads,
-                                int* smem_bytes, int* ctas, int* stages);
+/* Launch shape the library picks for a verify sweep over `units` (row,
+ * position) pairs of V logits (for benchmarks and diagnostics): CTAs per
+ * cluster, threads per CTA, dynamic shared memory per CTA, the number of
+ * persistent clusters launched and the shared-memory stages per CTA.  Needs a current CUDA device.  Returns
+ * SPEC_ERR_UNSUPPORTED if V does not fit.  Any output pointer may be NULL. */
+spec_status_t spec_launch_shape(spec_dtype_t dtype, int units, int V,
+                                int* cluster_ctas, int* threads,
+                                int* smem_bytes, int* clusters, int* stages);
 
-/* Forces the largest vocabulary chunk (in logits, >= 256; smaller values
- * restore the automatic choice) and the shared-memory stages per CTA (2..16,
- * raised to the pipeline's minimum of 6 for T > 0, never above what fits;
- * other values restore the automatic choice) of later
- * launches in this process, for launch-shape sweeps in tests and benchmarks.
- * Workspace sizes queried afterwards account for the forced chunk.
- * Process-wide; not synchronised with launches in flight. */
-void spec_set_launch_override(int chunk_elems, int stages);
+/* Forces the CTAs per cluster (1..16) and the shared-memory stages per CTA
+ * (1 or 2) of later launches in this process, for launch-shape sweeps in
+ * benchmarks; 0 restores the automatic choice of either.  Process-wide; not
+ * synchronised with launches in flight. */
+void spec_set_launch_override(int cluster_ctas, int stages);
 
 #ifdef __cplusplus
 }

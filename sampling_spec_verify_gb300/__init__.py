@@ -74,7 +74,7 @@ def lib():
     L.spec_e2e_tv_fwd_bwd.restype = i32
     L.spec_e2e_tv_fwd_bwd.argtypes = [vp, vp, i32, i32, i32, i32, i32, f32, f32, vp, vp, vp, vp, vp, sz, vp]
     L.spec_launch_shape.restype = i32
-    L.spec_launch_shape.argtypes = [i32, i32] + [ctypes.POINTER(i32)] * 6
+    L.spec_launch_shape.argtypes = [i32, i32, i32] + [ctypes.POINTER(i32)] * 5
     L.spec_set_launch_override.restype = None
     L.spec_set_launch_override.argtypes = [i32, i32]
     _lib = L
@@ -136,18 +136,18 @@ def _check(status: int, what: str):
         raise SpecError(status, what)
 
 
-def set_launch_override(chunk_elems: int = 0, stages: int = 0) -> None:
-    """Force the largest vocabulary chunk (logits, >= 256) and the shared-memory
-    stages per CTA (2..16) of later launches; 0 = automatic."""
-    lib().spec_set_launch_override(int(chunk_elems), int(stages))
+def set_launch_override(cluster_ctas: int = 0, stages: int = 0) -> None:
+    """Force the CTAs per cluster (1..16) and shared-memory stages (1 or 2)
+    of later launches; 0 = automatic."""
+    lib().spec_set_launch_override(int(cluster_ctas), int(stages))
 
 
-def launch_shape(dtype: torch.dtype, V: int):
-    """(chunk logits, chunks per row, threads per CTA, dynamic shared bytes,
-    CTAs, stages) of a sampling verify over rows of V logits."""
-    v = [ctypes.c_int() for _ in range(6)]
+def launch_shape(dtype: torch.dtype, units: int, V: int):
+    """(cluster CTAs, threads per CTA, dynamic shared bytes, clusters, stages)
+    of a verify sweep over `units` (row, position) pairs."""
+    v = [ctypes.c_int() for _ in range(5)]
     code = SPEC_BF16 if dtype == torch.bfloat16 else SPEC_F32
-    _check(lib().spec_launch_shape(code, V, *[ctypes.byref(x) for x in v]), "spec_launch_shape")
+    _check(lib().spec_launch_shape(code, units, V, *[ctypes.byref(x) for x in v]), "spec_launch_shape")
     return tuple(x.value for x in v)
 
 

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings_and_version(L):
-    assert L.spec_abi_version() == 3
+    assert L.spec_abi_version() == 2
     assert L.spec_status_string(0) == b"ok"
     assert L.spec_status_string(1) == b"invalid argument"
     assert L.spec_status_string(99) == b"unknown status"
