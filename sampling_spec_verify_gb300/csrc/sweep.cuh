@@ -953,8 +953,9 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
 
       // ---- pass C': residual (mode 1) or target (mode 2) draw ----
       // Prefix order is (CTA, warp, lane, vector, element): every thread sums
-      // its contiguous chunk in order, a warp scan orders the lanes, and one
-      // thread of the owning CTA walks its chunk again with the same arithmetic.
+      // its contiguous chunk in order, a warp scan orders the lanes, and the
+      // warp of the owning thread walks that thread's chunk again with the
+      // same per-element arithmetic, one vector per lane.
       const f32x2 CDd = f2(-c1d, -c1d);
       const f32x2 NR = f2(-ratio, -ratio);
       for (int attempt = 0; attempt < 2; ++attempt) {
@@ -1050,44 +1051,67 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
             const unsigned pos = __ballot_sync(kFull, tot > 0.0f);
             const bool fb = (hit == 0u);
             const int l = hit ? (__ffs(hit) - 1) : (pos ? 31 - __clz(pos) : -1);
-            if (lane == l) {
+            if (l >= 0) {
+              // The whole warp walks thread l's chunk: lane k takes its k-th
+              // vector, a warp scan orders the vector totals, and the lane
+              // whose vector crosses the threshold walks its 8 weights.
               const float th = fb ? INFINITY : thw;
-              float run = excl;
+              const int o_lo = min(v_lo + l * cpt, v_hi);
+              const int o_hi = min(o_lo + cpt, v_hi);
+              float carry = __shfl_sync(kFull, excl, l);
               int pick = -1, ilast = -1;
-              for (int i = t_lo; i < t_hi && pick < 0; ++i) {
+              for (int base = o_lo; base < o_hi; base += 32) {
+                const int i = base + lane;
                 float w[PV];
-                f32x2 dummy = f2(0.0f, 0.0f);
-                const float rs = resid ? draw_weights<E, true>(st[i], sd[i], S2, CT, CDd, NR, w, dummy)
-                                       : draw_weights<E, false>(st[i], st[i], S2, CT, CDd, NR, w, dummy);
-                if (rs > 0.0f) ilast = i;
-                const float nxt = __fadd_rn(run, rs);
-                if (nxt > th) {
-                  float a = run;
-                  int lastp = -1;
-#pragma unroll
-                  for (int k = 0; k < PV; ++k) {
-                    a = __fadd_rn(a, w[k]);
-                    if (w[k] > 0.0f) {
-                      lastp = k;
-                      if (pick < 0 && a > th) pick = i * PV + k;
-                    }
-                  }
-                  if (pick < 0 && lastp >= 0) pick = i * PV + lastp;
+                float rs = 0.0f;
+                if (i < o_hi) {
+                  f32x2 dummy = f2(0.0f, 0.0f);
+                  rs = resid ? draw_weights<E, true>(st[i], sd[i], S2, CT, CDd, NR, w, dummy)
+                             : draw_weights<E, false>(st[i], st[i], S2, CT, CDd, NR, w, dummy);
                 }
-                run = nxt;
+                const float run = __fadd_rn(carry, warp_incl_scan(rs, lane));
+                const float up = __shfl_up_sync(kFull, run, 1);
+                const float before = (lane == 0) ? carry : up;
+                const unsigned pos2 = __ballot_sync(kFull, rs > 0.0f);
+                if (pos2) ilast = base + 31 - __clz(pos2);
+                const unsigned h2 = __ballot_sync(kFull, rs > 0.0f && run > th);
+                if (h2) {
+                  const int k = __ffs(h2) - 1;
+                  int pk = -1;
+                  if (lane == k) {
+                    float a = before;
+                    int lastp = -1;
+#pragma unroll
+                    for (int j = 0; j < PV; ++j) {
+                      a = __fadd_rn(a, w[j]);
+                      if (w[j] > 0.0f) {
+                        lastp = j;
+                        if (pk < 0 && a > th) pk = j;
+                      }
+                    }
+                    if (pk < 0) pk = lastp;  // the vector crosses but no element does (rounding)
+                    pk = i * PV + pk;
+                  }
+                  pick = __shfl_sync(kFull, pk, k);
+                  break;
+                }
+                carry = __shfl_sync(kFull, run, 31);
               }
               if (pick < 0 && ilast >= 0) {  // no crossing (rounding): the last positive weight
-                float w[PV];
-                f32x2 dummy = f2(0.0f, 0.0f);
-                if (resid)
-                  draw_weights<E, true>(st[ilast], sd[ilast], S2, CT, CDd, NR, w, dummy);
-                else
-                  draw_weights<E, false>(st[ilast], st[ilast], S2, CT, CDd, NR, w, dummy);
+                if (lane == 0) {
+                  float w[PV];
+                  f32x2 dummy = f2(0.0f, 0.0f);
+                  if (resid)
+                    draw_weights<E, true>(st[ilast], sd[ilast], S2, CT, CDd, NR, w, dummy);
+                  else
+                    draw_weights<E, false>(st[ilast], st[ilast], S2, CT, CDd, NR, w, dummy);
 #pragma unroll
-                for (int k = 0; k < PV; ++k)
-                  if (w[k] > 0.0f) pick = ilast * PV + k;
+                  for (int k = 0; k < PV; ++k)
+                    if (w[k] > 0.0f) pick = ilast * PV + k;
+                }
+                pick = __shfl_sync(kFull, pick, 0);
               }
-              if (pick >= 0) sm.bci[6] = e0 + pick;
+              if (lane == 0 && pick >= 0) sm.bci[6] = e0 + pick;
             }
           }
         }
