@@ -372,6 +372,78 @@ def overlap_stats(target_logits, draft_logits, temperature, rows=None):
 
 
 # ---------------------------------------------------------------------------
+# Entropy and acceptance diagnostics
+# ---------------------------------------------------------------------------
+
+def entropy(p):
+    """H(p) = -sum_y p(y) log p(y) in nats, with 0 log 0 = 0.
+
+    Bebop/DSpark blog, section "Qwen Bebop：RL 里的瓶颈不是 MTP 不会猜，而是
+    策略熵在变" (the target policy's entropy that drives acceptance)."""
+    p = np.asarray(p, dtype=np.float64)
+    nz = p > 0
+    return float(-np.sum(p[nz] * np.log(p[nz])))
+
+
+def cross_entropy(p, q):
+    """L_CE = -sum_y p(y) log q(y) in nats (terms with p(y) = 0 vanish).
+
+    Bebop/DSpark blog, section "Bebop 的解法", equation for L_CE."""
+    p = np.asarray(p, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    nz = p > 0
+    return float(-np.sum(p[nz] * np.log(q[nz])))
+
+
+def kl_divergence(p, q):
+    """D_KL(p || q) = sum_y p(y) log(p(y) / q(y)) in nats (terms with p(y) = 0
+    vanish) -- Bebop/DSpark blog, section "Bebop 的解法", equation for D_KL."""
+    p = np.asarray(p, dtype=np.float64)
+    q = np.asarray(q, dtype=np.float64)
+    nz = p > 0
+    return float(np.sum(p[nz] * np.log(p[nz] / q[nz])))
+
+
+def alpha_target_only(p, q):
+    """Single-step acceptance of target-only verification of a greedy draft:
+    alpha_TO = p(y_hat) with y_hat = argmax_y q(y) (smallest index on ties).
+
+    Bebop/DSpark blog, section "Qwen Bebop：RL 里的瓶颈...", equation for
+    alpha_TO."""
+    return float(np.asarray(p, dtype=np.float64)[argmax_first(q)])
+
+
+@dataclass
+class DiagResult:
+    alpha: np.ndarray          # [B, K] sum min(p, q)
+    entropy: np.ndarray        # [B, K] H(p), nats
+    cross_entropy: np.ndarray  # [B, K] -sum p log q, nats
+    kl: np.ndarray             # [B, K] D_KL(p || q), nats
+    alpha_to: np.ndarray       # [B, K] p(argmax q)
+
+
+def diagnostics(target_logits, draft_logits, temperature, rows=None):
+    """Per-position overlap, target entropy, cross-entropy, KL divergence and
+    target-only acceptance for logits [B, K, V] (both sides) at temperature
+    T > 0; p and q are the temperature softmaxes of the two logit rows."""
+    zt = np.asarray(target_logits)
+    zd = np.asarray(draft_logits)
+    B, K, V = zt.shape
+    rows = range(B) if rows is None else list(rows)
+    R = len(rows)
+    out = [np.zeros((R, K)) for _ in range(5)]
+    for i, b in enumerate(rows):
+        for k in range(K):
+            p = softmax_t(zt[b, k], temperature)
+            q = softmax_t(zd[b, k], temperature)
+            vals = (overlap(p, q), entropy(p), cross_entropy(p, q), kl_divergence(p, q),
+                    alpha_target_only(p, q))
+            for o, v in zip(out, vals):
+                o[i, k] = v
+    return DiagResult(*out)
+
+
+# ---------------------------------------------------------------------------
 # E2E-TV loss and its gradient with respect to the draft logits
 # ---------------------------------------------------------------------------
 

@@ -467,3 +467,80 @@ def test_inverse_cdf_strict_boundary_reading():
     assert so.inverse_cdf(np.array([1.0, 1.0]), 0.5)[0] == 1
     assert so.inverse_cdf(np.array([1.0, 1.0]), 0.0)[0] == 0
     assert so.inverse_cdf(np.array([0.0, 1.0, 1.0]), 0.0)[0] == 1
+
+
+# ---------------------------------------------------------------------------
+# entropy, cross-entropy, KL and target-only acceptance
+# ---------------------------------------------------------------------------
+
+def test_entropy_closed_forms():
+    # uniform over V tokens: ln V; a point mass: 0
+    for V in (1, 2, 7, 1024):
+        assert abs(so.entropy(np.full(V, 1.0 / V)) - math.log(V)) < 1e-12
+    assert so.entropy(np.array([0.0, 1.0, 0.0])) == 0.0
+    # infinite temperature flattens any logits to the uniform distribution
+    z = np.random.default_rng(3).normal(size=50) * 3
+    assert abs(so.entropy(so.softmax_t(z, 1e9)) - math.log(50)) < 1e-6
+
+
+def test_two_token_worked_example():
+    # p = (1/2, 1/2), q = (1/4, 3/4), worked by hand:
+    #   H = ln 2 = 0.6931471805599453
+    #   KL = 1/2 ln 2 + 1/2 ln(2/3) = 1/2 ln(4/3) = 0.14384103622589045
+    #   CE = -1/2 ln(1/4) - 1/2 ln(3/4) = 0.8369882167858358
+    #   alpha_TO = p(argmax q) = p(1) = 1/2
+    p, q = np.array([0.5, 0.5]), np.array([0.25, 0.75])
+    assert abs(so.entropy(p) - 0.6931471805599453) < 1e-15
+    assert abs(so.kl_divergence(p, q) - 0.14384103622589045) < 1e-15
+    assert abs(so.cross_entropy(p, q) - 0.8369882167858358) < 1e-15
+    assert so.alpha_target_only(p, q) == 0.5
+
+
+def test_entropy_and_kl_match_scipy():
+    from scipy.stats import entropy as sp_entropy
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        V = int(rng.integers(2, 300))
+        p = so.softmax_t(rng.normal(size=V) * 2, 1.0)
+        q = so.softmax_t(rng.normal(size=V) * 2, 0.7)
+        assert abs(so.entropy(p) - sp_entropy(p)) < 1e-12
+        assert abs(so.kl_divergence(p, q) - sp_entropy(p, q)) < 1e-12
+
+
+def test_cross_entropy_is_entropy_plus_kl_and_inequalities():
+    rng = np.random.default_rng(6)
+    for _ in range(50):
+        V = int(rng.integers(2, 200))
+        p = so.softmax_t(rng.normal(size=V) * 3, 1.0)
+        q = so.softmax_t(rng.normal(size=V) * 3, 1.0)
+        h, ce, kl = so.entropy(p), so.cross_entropy(p, q), so.kl_divergence(p, q)
+        assert abs(ce - (h + kl)) < 1e-10
+        assert kl >= 0.0 and 0.0 <= h <= math.log(V) + 1e-12
+        # Pinsker: d_TV <= sqrt(KL / 2)
+        assert so.tv_distance(p, q) <= math.sqrt(kl / 2) + 1e-12
+        assert abs(so.kl_divergence(p, p)) < 1e-15
+
+
+def test_point_mass_drafter_acceptance_is_target_only():
+    # a greedy drafter is a point mass at y_hat: the rejection-sampling
+    # acceptance sum min(p, q) then equals the target-only p(y_hat)
+    rng = np.random.default_rng(7)
+    p = so.softmax_t(rng.normal(size=40) * 2, 1.0)
+    for y in (0, 13, 39):
+        q = np.zeros(40)
+        q[y] = 1.0
+        assert so.overlap(p, q) == so.alpha_target_only(p, q) == p[y]
+
+
+def test_diagnostics_shift_invariant_and_batched():
+    rng = np.random.default_rng(8)
+    zt = rng.normal(size=(2, 3, 64)) * 2
+    zd = zt + rng.normal(size=(2, 3, 64)) * 0.5
+    a = so.diagnostics(zt, zd, 0.8)
+    b = so.diagnostics(zt + 7.0, zd - 3.0, 0.8)
+    for f in ("alpha", "entropy", "cross_entropy", "kl", "alpha_to"):
+        np.testing.assert_allclose(getattr(a, f), getattr(b, f), rtol=0, atol=1e-12)
+    p = so.softmax_t(zt[1, 2], 0.8)
+    q = so.softmax_t(zd[1, 2], 0.8)
+    assert a.alpha_to[1, 2] == p[np.argmax(q)]
+    np.testing.assert_allclose(a.cross_entropy, a.entropy + a.kl, rtol=1e-12, atol=1e-12)
