@@ -197,6 +197,40 @@ spec_status_t spec_e2e_tv_fwd_bwd(const void* target_logits,
                                   size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Per-position distribution diagnostics of K drafted positions.
+ *
+ * "读 Qwen Bebop 与 DeepSeek DSpark", section "Qwen Bebop：RL 里的瓶颈不是 MTP
+ * 不会猜，而是策略熵在变" (acceptance falls as the target's entropy rises; a
+ * point-mass drafter is accepted with probability p(argmax q)) and section
+ * "Bebop 的解法" (cross-entropy or KL training of the drafter against
+ * training for the acceptance itself).  With p = softmax(target / T) and
+ * q = softmax(draft / T), natural logarithms, 0 log 0 = 0:
+ *   alpha   = sum_v min(p_v, q_v)
+ *   entropy = -sum_v p_v log p_v
+ *   kl      = sum_v p_v (log p_v - log q_v)   (+inf if some q_v = 0 < p_v)
+ *   cross_entropy = entropy + kl = -sum_v p_v log q_v
+ *   alpha_target_only = p(y_hat), y_hat = argmax_v q_v (smallest index on ties)
+ *
+ * target_logits  [B, KT, V] dtype, KT >= K (first K positions used).
+ * draft_logits   [B, K, V] dtype.
+ * temperature    T > 0.
+ * alpha, entropy, cross_entropy, kl, alpha_target_only
+ *                [B, K] float32 each, or NULL (not written).
+ * A row with NaN or +inf logits, or no finite logit, gets NaN in every output
+ * and SPEC_DEV_BAD_LOGITS.
+ */
+size_t spec_diagnostics_workspace_bytes(int B, int K, int V);
+
+spec_status_t spec_diagnostics(const void* target_logits,
+                               const void* draft_logits, spec_dtype_t dtype,
+                               int B, int K, int KT, int V, float temperature,
+                               float* alpha, float* entropy,
+                               float* cross_entropy, float* kl,
+                               float* alpha_target_only, uint32_t* dev_status,
+                               void* workspace, size_t workspace_bytes,
+                               void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Launch shape the library picks for a verify sweep over `units` (row,
  * position) pairs of V logits (for benchmarks and diagnostics): CTAs per
  * cluster, threads per CTA, dynamic shared memory per CTA, the number of

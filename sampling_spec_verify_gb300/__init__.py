@@ -10,7 +10,9 @@ Entry points (same names as the C ABI, see include/spec_verify.h):
 * ``verify``          -- batched draft/verify step (acceptance, residual
                          correction, bonus token, greedy at T == 0);
 * ``overlap``         -- alpha = sum min(p, q), TV, prefix survival, E[tau];
-* ``e2e_tv_fwd_bwd``  -- E2E-TV loss and its draft-logit gradient.
+* ``e2e_tv_fwd_bwd``  -- E2E-TV loss and its draft-logit gradient;
+* ``diagnostics``     -- alpha, target entropy, cross-entropy, KL and the
+                         target-only acceptance p(argmax q) per position.
 """
 
 from __future__ import annotations
@@ -23,8 +25,8 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "SpecError", "lib", "verify", "overlap", "e2e_tv_fwd_bwd", "launch_shape",
-    "set_launch_override", "VerifyOutput", "OverlapOutput", "E2EOutput", "HostVerifier",
+    "SpecError", "lib", "verify", "overlap", "e2e_tv_fwd_bwd", "diagnostics", "launch_shape",
+    "set_launch_override", "VerifyOutput", "OverlapOutput", "E2EOutput", "DiagOutput", "HostVerifier",
     "DEV_BAD_TOKEN", "DEV_BAD_LOGITS", "DEV_BAD_UNIFORM", "DEV_TIMEOUT", "DEV_EMPTY_RESIDUAL",
     "SPEC_OK", "SPEC_ERR_INVALID_ARG", "SPEC_ERR_UNSUPPORTED", "SPEC_ERR_CUDA",
 ]
@@ -73,6 +75,10 @@ def lib():
     L.spec_e2e_tv_workspace_bytes.argtypes = [i32, i32, i32]
     L.spec_e2e_tv_fwd_bwd.restype = i32
     L.spec_e2e_tv_fwd_bwd.argtypes = [vp, vp, i32, i32, i32, i32, i32, f32, f32, vp, vp, vp, vp, vp, sz, vp]
+    L.spec_diagnostics_workspace_bytes.restype = sz
+    L.spec_diagnostics_workspace_bytes.argtypes = [i32, i32, i32]
+    L.spec_diagnostics.restype = i32
+    L.spec_diagnostics.argtypes = [vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.spec_launch_shape.restype = i32
     L.spec_launch_shape.argtypes = [i32, i32, i32] + [ctypes.POINTER(i32)] * 5
     L.spec_set_launch_override.restype = None
@@ -281,6 +287,49 @@ def e2e_tv_fwd_bwd(target: torch.Tensor, draft: torch.Tensor, temperature: float
                                float(grad_scale), _ptr(out.loss), _ptr(out.alpha), _ptr(out.grad),
                                _ptr(out.status), _ptr(ws), ws.numel() * ws.element_size(), sh)
     _check(st, "spec_e2e_tv_fwd_bwd")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# diagnostics
+# ---------------------------------------------------------------------------
+
+@dataclass
+class DiagOutput:
+    alpha: Optional[torch.Tensor]              # float32 [B, K]: sum_v min(p, q)
+    entropy: Optional[torch.Tensor]            # H(p), nats
+    cross_entropy: Optional[torch.Tensor]      # -sum_v p log q
+    kl: Optional[torch.Tensor]                 # KL(p || q)
+    alpha_target_only: Optional[torch.Tensor]  # p(argmax q)
+    status: torch.Tensor
+
+
+def diagnostics(target: torch.Tensor, draft: torch.Tensor, temperature: float, *, K: Optional[int] = None,
+                out: Optional[DiagOutput] = None, workspace: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> DiagOutput:
+    """Per-position alpha, entropy of p, cross-entropy and KL of q against p,
+    and the acceptance p(argmax q) of a point-mass drafter, p and q at
+    temperature T > 0.  target [B, KT, V] with KT >= K, draft [B, K, V].
+    Fields of ``out`` left as None are not computed."""
+    L = lib()
+    _need(target, "target")
+    _need(draft, "draft", dtype=target.dtype)
+    B, KT, V = target.shape
+    K = draft.shape[1] if K is None else K
+    if tuple(draft.shape) != (B, K, V) or KT < K:
+        raise ValueError("draft must be [B, K, V] with K <= target.shape[1]")
+    dev = target.device
+    if out is None:
+        f = lambda: torch.empty((B, K), dtype=torch.float32, device=dev)  # noqa: E731
+        out = DiagOutput(f(), f(), f(), f(), f(), torch.zeros((1,), dtype=torch.int32, device=dev))
+    sh, s = _stream_handle(stream, dev)
+    need = L.spec_diagnostics_workspace_bytes(B, K, V)
+    ws = workspace if workspace is not None else _workspace(need, dev, s)
+    st = L.spec_diagnostics(_ptr(target), _ptr(draft), _dtype_code(target), B, K, KT, V, float(temperature),
+                            _ptr(out.alpha), _ptr(out.entropy), _ptr(out.cross_entropy), _ptr(out.kl),
+                            _ptr(out.alpha_target_only), _ptr(out.status), _ptr(ws),
+                            ws.numel() * ws.element_size(), sh)
+    _check(st, "spec_diagnostics")
     return out
 
 

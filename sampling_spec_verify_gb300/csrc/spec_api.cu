@@ -261,6 +261,20 @@ E2EWs e2e_ws(int B, int K) {
   return w;
 }
 
+struct DiagWs {
+  size_t part = 0, part2 = 0, part3 = 0, cnt = 0, total = 0;
+};
+DiagWs diag_ws(int B, int K) {
+  const long long units = (long long)B * K;
+  DiagWs w;
+  w.part = 0;
+  w.part2 = part_bytes(units);
+  w.part3 = w.part2 + part_bytes(units);
+  w.cnt = w.part3 + part_bytes(units);
+  w.total = w.cnt + align256((size_t)B * sizeof(uint32_t));
+  return w;
+}
+
 bool dims_ok(int B, int K, int V) { return B >= 0 && K >= 0 && K <= kMaxK && V >= 1; }
 
 bool dtype_ok(spec_dtype_t dt) { return dt == SPEC_F32 || dt == SPEC_BF16; }
@@ -493,6 +507,59 @@ spec_status_t spec_e2e_tv_fwd_bwd(const void* target_logits, const void* draft_l
   // The per-position statistics are consumed by the gradient kernel; clear
   // them so the workspace is zero-filled again when the call completes.
   return from_cuda(cudaMemsetAsync(w + ws.stats, 0, (size_t)B * K * sizeof(E2EStats), st));
+}
+
+size_t spec_diagnostics_workspace_bytes(int B, int K, int V) {
+  if (!dims_ok(B, K, V)) return 0;
+  return diag_ws(B, K).total;
+}
+
+spec_status_t spec_diagnostics(const void* target_logits, const void* draft_logits, spec_dtype_t dtype, int B, int K,
+                               int KT, int V, float temperature, float* alpha, float* entropy, float* cross_entropy,
+                               float* kl, float* alpha_target_only, uint32_t* dev_status, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  if (!dims_ok(B, K, V) || !dtype_ok(dtype) || KT < K) return SPEC_ERR_INVALID_ARG;
+  if (!(temperature > 0.0f) || !std::isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
+  if (B == 0 || K == 0) return SPEC_OK;
+  if (!target_logits || !draft_logits) return SPEC_ERR_INVALID_ARG;
+  const DiagWs ws = diag_ws(B, K);
+  if (!workspace || workspace_bytes < ws.total || !aligned16(workspace)) return SPEC_ERR_INVALID_ARG;
+  const long long units = (long long)B * K;
+  if (units > 0x7FFFFFFFLL) return SPEC_ERR_UNSUPPORTED;
+  const int es = elem_size(dtype);
+  Shape sh;
+  {
+    const spec_status_t r = shape_for_dt<ssv::kDiag>(dtype, units, V, 2, &sh);
+    if (r != SPEC_OK) return r;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  SweepParams P = {};
+  P.target = target_logits;
+  P.draft = draft_logits;
+  P.B = B;
+  P.K = K;
+  P.KT = KT;
+  P.V = V;
+  P.units = (int)units;
+  P.S = sh.S;
+  P.L = sh.L;
+  P.nst = sh.nst;
+  P.rows = 2;
+  P.aligned = aligned16(target_logits) && aligned16(draft_logits) && ((long long)V * es) % 16 == 0;
+  P.s = (float)(1.4426950408889634 / (double)temperature);
+  P.inv_t = (float)(1.0 / (double)temperature);
+  P.alpha = alpha;
+  P.ent = entropy;
+  P.ce = cross_entropy;
+  P.kl = kl;
+  P.ato = alpha_target_only;
+  char* w = static_cast<char*>(workspace);
+  P.part = reinterpret_cast<float*>(w + ws.part);
+  P.part2 = reinterpret_cast<float*>(w + ws.part2);
+  P.part3 = reinterpret_cast<float*>(w + ws.part3);
+  P.row_cnt = reinterpret_cast<uint32_t*>(w + ws.cnt);
+  P.status = dev_status;
+  return from_cuda(launch_sweep_dt<ssv::kDiag>(dtype, P, sh, st));
 }
 
 }  // extern "C"

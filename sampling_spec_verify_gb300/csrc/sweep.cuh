@@ -46,7 +46,7 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 
 constexpr uint32_t kBadToken = 1u, kBadLogits = 2u, kBadUniform = 4u, kTimeout = 8u, kEmptyResidual = 16u;
 
-enum Mode : int { kVerify = 0, kVerifyGreedy = 1, kOverlap = 2, kOverlapGreedy = 3, kE2E = 4 };
+enum Mode : int { kVerify = 0, kVerifyGreedy = 1, kOverlap = 2, kOverlapGreedy = 3, kE2E = 4, kDiag = 5 };
 
 struct VerifyRecord {  // one per (b, k), k = 0..K
   int32_t acc;         // 1 accepted, 0 rejected (draft positions)
@@ -91,7 +91,12 @@ struct SweepParams {
   VerifyRecord* rec;
   E2EStats* stats;
   float* part;   // [units][kPartStride] overlap partials
-  float* part2;  // [units][kPartStride] E2E S-mass partials
+  float* part2;  // [units][kPartStride] E2E S-mass partials; diagnostics: entropy partials
+  float* part3;  // [units][kPartStride] diagnostics: KL partials
+  float* ent;    // [B, K] diagnostics outputs (each may be null)
+  float* ce;
+  float* kl;
+  float* ato;
   float* row_loss;
   uint32_t* row_cnt;
   uint32_t* glob_cnt;
@@ -358,6 +363,34 @@ __device__ __forceinline__ void complete_row(const SweepParams& P, int b, int S,
       if (P.exp_acc) P.exp_acc[b] = sum;
       P.row_cnt[b] = 0;
     }
+  } else if constexpr (MODE == kDiag) {
+    const float* hh0 = P.part2 + (long long)b * K * kPartStride;
+    const float* kk0 = P.part3 + (long long)b * K * kPartStride;
+    const float ln2 = 0.69314718055994531f;
+    for (int kk = lane; kk < K; kk += 32) {
+      const float* hh = hh0 + kk * kPartStride;
+      const float* kq = kk0 + kk * kPartStride;
+      float hs = 0.0f, ks = 0.0f;
+      for (int r = 0; r < S; ++r) {
+        hs = __fadd_rn(hs, __ldcg(hh + r));
+        ks = __fadd_rn(ks, __ldcg(kq + r));
+      }
+      const float H = __fmul_rn(-ln2, hs), KL = __fmul_rn(ln2, ks);
+      if (P.alpha) P.alpha[b * K + kk] = alpha_of(kk);
+      if (P.ent) P.ent[b * K + kk] = H;
+      if (P.kl) P.kl[b * K + kk] = KL;
+      if (P.ce) P.ce[b * K + kk] = __fadd_rn(H, KL);
+    }
+    __syncwarp();
+    float* pw = P.part + (long long)b * K * kPartStride;
+    float* pw2 = P.part2 + (long long)b * K * kPartStride;
+    float* pw3 = P.part3 + (long long)b * K * kPartStride;
+    for (int i = lane; i < K * kPartStride; i += 32) {
+      pw[i] = 0.0f;
+      pw2[i] = 0.0f;
+      pw3[i] = 0.0f;
+    }
+    if (lane == 0) P.row_cnt[b] = 0;
   } else {  // kE2E
     E2EStats* sr = P.stats + (long long)b * K;
     const float* qq0 = P.part2 + (long long)b * K * kPartStride;
@@ -437,6 +470,8 @@ struct SweepSmem {
   float wred[kWarps][4];
   int wredi[kWarps][2];
   float wtot[kWarps];
+  float wamax[kWarps];  // diagnostics: per-warp draft arg-maximum
+  int wamaxi[kWarps];
   float woff[kWarps + 1];
   alignas(16) float mbox[2][kPartStride][8];  // pushed by peers: [exchange slot][sender rank][field]
   float bcf[8];
@@ -797,6 +832,31 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
         chunk_sum(st, mt, zt);
         if (x.has_draft) chunk_sum(sd, md, zd);
       }
+      if constexpr (MODE == kDiag) {
+        // arg-maximum of the draft logits (smallest index on ties): y_hat
+        float bv = -INFINITY;
+        int bi = 0x7FFFFFFF, jb = -1;
+        if (ok) {
+          for (int i = t_lo; i < t_hi; ++i) {
+            const float vm = E::vmax(sd[i]);
+            if (vm > bv) {
+              bv = vm;
+              jb = i;
+            }
+          }
+        }
+        if (jb >= 0) {
+          float xv[PV];
+          E::unpack(sd[jb], xv);
+          for (int k = PV - 1; k >= 0; --k)
+            if (xv[k] == bv) bi = e0 + jb * PV + k;
+        }
+        warp_argmax_redux(bv, bi);
+        if (lane == 0) {
+          sm.wamax[warp] = bv;
+          sm.wamaxi[warp] = bi;
+        }
+      }
       warp_combine_mz2(mt, zt, md, zd, s);
       if (lane == 0) {
         sm.wred[warp][0] = mt;
@@ -825,7 +885,16 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
           gt = __shfl_sync(kFull, gt, 0);
           gd = __shfl_sync(kFull, gd, 0);
         }
-        push8(slot, a, za, d, zda, gt, gd, 0.0f, 0.0f);
+        float av = -INFINITY;
+        int ai = 0x7FFFFFFF;
+        if constexpr (MODE == kDiag) {
+          if (lane < kWarps) {
+            av = sm.wamax[lane];
+            ai = sm.wamaxi[lane];
+          }
+          warp_argmax_redux(av, ai);
+        }
+        push8(slot, a, za, d, zda, gt, gd, av, __int_as_float(ai));
       }
       cluster_sync();  // ---- exchange 1: (max, sum) of both rows
       ++xc;
@@ -841,6 +910,12 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
           zdy = sm.mbox[slot][own][5];
         }
         warp_combine_mz2(a, za, d, zda, s);
+        if constexpr (MODE == kDiag) {
+          float av = mb(slot, 6, -INFINITY);
+          int ai = lane < S ? __float_as_int(sm.mbox[slot][lane][7]) : 0x7FFFFFFF;
+          warp_argmax_redux(av, ai);
+          if (lane == 0) sm.bci[5] = ai;  // y_hat, identical in every CTA
+        }
         if (lane == 0) {
           const float Zt = za, Zd = zda;
           const float c1t = __fmul_rn(a, s), c1d = __fmul_rn(d, s);
@@ -874,6 +949,7 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
           sm.bcf[3] = izt;
           sm.bcf[4] = __fmul_rn(Zt, izd);
           sm.bcf[5] = uf;
+          if constexpr (MODE == kDiag) sm.bcf[6] = __log2f(Zt);
           sm.bci[0] = mode_c;
           sm.bci[1] = acc;
         }
@@ -887,12 +963,12 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
 
       if (mode_c == 0 || mode_c == 3) {
         // ---- pass C: overlap (and E2E S-mass) partials, no exchange ----
-        float a = 0.0f, m2 = 0.0f;
+        float a = 0.0f, m2 = 0.0f, m3 = 0.0f;
         if (mode_c == 0 && ok && x.has_draft) {
           const f32x2 CD = f2(-cd2, -cd2);
-          f32x2 a2 = f2(0.0f, 0.0f), g2 = f2(0.0f, 0.0f);
+          f32x2 a2 = f2(0.0f, 0.0f), g2 = f2(0.0f, 0.0f), k2 = f2(0.0f, 0.0f);
           for (int i = t_lo; i < t_hi; ++i) {
-            f32x2 pt[PV / 2], pd[PV / 2], ep[PV / 2], gp[PV / 2];
+            f32x2 pt[PV / 2], pd[PV / 2], ep[PV / 2], gp[PV / 2], kp[PV / 2];
             E::pairs(st[i], pt);
             E::pairs(sd[i], pd);
 #pragma unroll
@@ -903,28 +979,63 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
               const float e0 = ex2(fminf(t0, d0)), e1 = ex2(fminf(t1, d1));
               ep[h] = f2(e0, e1);
               if constexpr (MODE == kE2E) gp[h] = f2(d0 < t0 ? e0 : 0.0f, d1 < t1 ? e1 : 0.0f);
+              if constexpr (MODE == kDiag) {
+                // Z_t p log2-terms, x_t = log2(Z_t p), x_d = log2(Z_t q):
+                // e_t x_t (entropy) and e_t (x_t - x_d) (KL); a token with
+                // p = 0 adds nothing (0 log 0 = 0)
+                const float et0 = ex2(t0), et1 = ex2(t1);
+                gp[h] = f2(et0 > 0.0f ? __fmul_rn(et0, t0) : 0.0f, et1 > 0.0f ? __fmul_rn(et1, t1) : 0.0f);
+                kp[h] = f2(et0 > 0.0f ? __fmul_rn(et0, __fsub_rn(t0, d0)) : 0.0f,
+                           et1 > 0.0f ? __fmul_rn(et1, __fsub_rn(t1, d1)) : 0.0f);
+              }
             }
             a2 = f2_add(a2, psum(ep));
-            if constexpr (MODE == kE2E) g2 = f2_add(g2, psum(gp));
+            if constexpr (MODE == kE2E || MODE == kDiag) g2 = f2_add(g2, psum(gp));
+            if constexpr (MODE == kDiag) k2 = f2_add(k2, psum(kp));
           }
           a = f2_hsum(a2);
-          if constexpr (MODE == kE2E) m2 = f2_hsum(g2);
+          if constexpr (MODE == kE2E || MODE == kDiag) m2 = f2_hsum(g2);
+          if constexpr (MODE == kDiag) m3 = f2_hsum(k2);
         }
         a = warp_sum(a);
-        if constexpr (MODE == kE2E) m2 = warp_sum(m2);
+        if constexpr (MODE == kE2E || MODE == kDiag) m2 = warp_sum(m2);
+        if constexpr (MODE == kDiag) m3 = warp_sum(m3);
         if (lane == 0) {
           sm.wred[warp][0] = a;
           sm.wred[warp][1] = m2;
+          sm.wred[warp][2] = m3;
+        }
+        // p(y_hat) from the CTA whose slice holds y_hat, read before the
+        // barrier: past it the other warps refill their segments
+        float py_hat = -1.0f;
+        if constexpr (MODE == kDiag) {
+          const int yh = sm.bci[5];
+          if (tid == 0 && mode_c == 0 && yh >= e0 && yh < e1) {
+            const float zy = E::to_f32(reinterpret_cast<const Raw*>(st)[yh - e0]);
+            py_hat = __fmul_rn(ex2(fmaf(zy, s, -c1t)), izt);
+          }
         }
         __syncthreads();
         if (warp == 0) {
           float A = lane < kWarps ? sm.wred[lane][0] : 0.0f;
           float M2 = lane < kWarps ? sm.wred[lane][1] : 0.0f;
+          float M3 = lane < kWarps ? sm.wred[lane][2] : 0.0f;
           A = warp_sum(A);
-          if constexpr (MODE == kE2E) M2 = warp_sum(M2);
+          if constexpr (MODE == kE2E || MODE == kDiag) M2 = warp_sum(M2);
+          if constexpr (MODE == kDiag) M3 = warp_sum(M3);
           if (lane == 0) {
             const float nanv = __int_as_float(0x7FC00000);
             P.part[(long long)u * kPartStride + rank] = (mode_c == 3) ? nanv : __fmul_rn(A, izt);
+            if constexpr (MODE == kDiag) {
+              // entropy partial sum_v p x_t; rank 0 folds in -log2 Z_t, so
+              // that the rank-ordered sum is -H / ln 2
+              float h2 = __fmul_rn(M2, izt);
+              if (rank == 0) h2 = __fsub_rn(h2, sm.bcf[6]);
+              P.part2[(long long)u * kPartStride + rank] = (mode_c == 3) ? nanv : h2;
+              P.part3[(long long)u * kPartStride + rank] = (mode_c == 3) ? nanv : __fmul_rn(M3, izt);
+              if (P.ato && py_hat >= 0.0f) P.ato[u] = py_hat;
+              if (P.ato && mode_c == 3 && rank == 0) P.ato[u] = nanv;
+            }
             if constexpr (MODE == kE2E) {
               P.part2[(long long)u * kPartStride + rank] = (mode_c == 3) ? nanv : __fmul_rn(M2, izt);
               if (rank == 0) {

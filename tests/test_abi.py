@@ -31,7 +31,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("spec_verify", "spec_overlap", "spec_e2e_tv_fwd_bwd", "spec_status_string",
-                 "spec_verify_workspace_bytes", "spec_overlap_workspace_bytes", "spec_e2e_tv_workspace_bytes"):
+                 "spec_verify_workspace_bytes", "spec_overlap_workspace_bytes", "spec_e2e_tv_workspace_bytes",
+                 "spec_diagnostics", "spec_diagnostics_workspace_bytes"):
         assert want in names
 
 
@@ -57,6 +58,8 @@ def test_workspace_sizes(L):
     assert L.spec_verify_workspace_bytes(1, 65, 10) == 0
     assert L.spec_e2e_tv_workspace_bytes(256, 7, 151936) >= 256 * 7 * 32
     assert L.spec_overlap_workspace_bytes(8, 4, 100) >= 32
+    assert L.spec_diagnostics_workspace_bytes(8, 4, 100) >= 3 * 32 * 16 * 4
+    assert L.spec_diagnostics_workspace_bytes(8, 65, 100) == 0
 
 
 def test_argument_validation_without_gpu(L):
@@ -86,3 +89,10 @@ def test_argument_validation_without_gpu(L):
     # overlap: KT < K, missing alpha
     assert L.spec_overlap(fake, fake, 1, 2, 3, 2, 10, 1.0, fake, None, None, None, None, ws, 1 << 20, None) == 1
     assert L.spec_overlap(fake, fake, 1, 2, 3, 3, 10, 1.0, None, None, None, None, None, ws, 1 << 20, None) == 1
+    # diagnostics: T > 0, KT >= K, workspace large enough; empty batch is a no-op
+    assert L.spec_diagnostics(fake, fake, 1, 2, 2, 2, 10, 0.0, fake, None, None, None, None, None, ws, 1 << 20,
+                              None) == 1
+    assert L.spec_diagnostics(fake, fake, 1, 2, 3, 2, 10, 1.0, fake, None, None, None, None, None, ws, 1 << 20,
+                              None) == 1
+    assert L.spec_diagnostics(fake, fake, 1, 2, 2, 2, 10, 1.0, fake, None, None, None, None, None, ws, 8, None) == 1
+    assert L.spec_diagnostics(None, None, 1, 0, 2, 2, 10, 1.0, None, None, None, None, None, None, None, 0, None) == 0
