@@ -118,7 +118,7 @@ spec_status_t spec_verify(const void* target_logits, const void* draft_logits,
  * scratch is a fixed device array of SPEC_NOALLOC_SCRATCH_BYTES inside the
  * library, held by every GPU that loads the library until the process exits.
  * Sizes whose spec_verify_workspace_bytes(B, K, V) exceeds it are rejected with
- * SPEC_ERR_UNSUPPORTED (at K = 4 that is about 12,000 rows).  No call
+ * SPEC_ERR_UNSUPPORTED (at K = 4 that is about 2,500 rows).  No call
  * allocates or frees memory; each clears the part of the array it uses with
  * cudaMemsetAsync on `stream`.
  *  - The first call on a device looks up the array's device address (once per

@@ -133,6 +133,17 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 
 // Asks L2 to fetch [src, src + bytes) ahead of a later bulk copy of it.
 // `src` 16-byte aligned; `bytes` a multiple of 16.
+// 16-byte asynchronous copy global -> shared through L2 (not L1); the issuing
+// thread waits for it with cp_async_wait_all.  Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async_16_cg(uint32_t dst, const void* src) {
+  asm volatile(
+      "cp.async.cg.shared.global [%0], [%1], 16;\n\t"
+      "cp.async.commit_group;" ::"r"(dst),
+      "l"(src)
+      : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }

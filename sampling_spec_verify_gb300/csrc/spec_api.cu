@@ -182,6 +182,14 @@ spec_status_t shape_for_dt(spec_dtype_t dt, long long units, int V, int rows, Sh
   return dt == SPEC_BF16 ? shape_for<Bf16, MODE>(units, V, rows, sh) : shape_for<F32, MODE>(units, V, rows, sh);
 }
 
+// Sets the attributes of the dtype's instantiation of a mode whose launch
+// shape was picked with another mode's (same code size and shared memory).
+template <int MODE>
+cudaError_t prepare_dt(spec_dtype_t dt) {
+  return dt == SPEC_BF16 ? prepare_kernel(ssv::sweep_kernel<Bf16, MODE>, prepared_mask<Bf16, MODE>())
+                         : prepare_kernel(ssv::sweep_kernel<F32, MODE>, prepared_mask<F32, MODE>());
+}
+
 template <class E, int MODE>
 cudaError_t launch_sweep(const SweepParams& P0, const Shape& sh, cudaStream_t stream) {
   auto fn = ssv::sweep_kernel<E, MODE>;
@@ -224,7 +232,7 @@ cudaError_t launch_grad(const ssv::GradParams& G, cudaStream_t stream) {
 size_t part_bytes(long long units) { return align256((size_t)units * ssv::kPartStride * sizeof(float)); }
 
 struct VerifyWs {
-  size_t rec = 0, part = 0, cnt = 0, total = 0;
+  size_t rec = 0, part = 0, cnt = 0, rej = 0, total = 0;
 };
 VerifyWs verify_ws(int B, int K) {
   const long long units = (long long)B * (K + 1);
@@ -232,7 +240,8 @@ VerifyWs verify_ws(int B, int K) {
   w.rec = 0;
   w.part = align256((size_t)units * sizeof(VerifyRecord));
   w.cnt = w.part + part_bytes(units);
-  w.total = w.cnt + align256((size_t)B * sizeof(uint32_t));
+  w.rej = w.cnt + align256((size_t)B * sizeof(uint32_t));
+  w.total = w.rej + align256((size_t)B * sizeof(uint32_t));
   return w;
 }
 struct OverlapWs {
@@ -343,6 +352,7 @@ spec_status_t spec_verify(const void* target_logits, const void* draft_logits, s
   const int rows = (greedy && !alpha_out) ? 1 : 2;  // greedy without overlap reads no draft row
   Shape sh;
   {
+    // both sampling orders share one launch shape
     const spec_status_t r = greedy ? shape_for_dt<ssv::kVerifyGreedy>(dtype, units, V, rows, &sh)
                                    : shape_for_dt<ssv::kVerify>(dtype, units, V, rows, &sh);
     if (r != SPEC_OK) return r;
@@ -373,10 +383,21 @@ spec_status_t spec_verify(const void* target_logits, const void* draft_logits, s
   P.rec = reinterpret_cast<VerifyRecord*>(static_cast<char*>(workspace) + ws.rec);
   P.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.part);
   P.row_cnt = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + ws.cnt);
+  P.rej = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + ws.rej);
   P.status = dev_status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = greedy ? launch_sweep_dt<ssv::kVerifyGreedy>(dtype, P, sh, st)
-                         : launch_sweep_dt<ssv::kVerify>(dtype, P, sh, st);
+  // At least one row per cluster: rows in groups, position-major (later
+  // positions can skip draws that an earlier rejection makes unused).
+  // Fewer rows: row-major order, which measured faster there.
+  cudaError_t e;
+  if (greedy) {
+    e = launch_sweep_dt<ssv::kVerifyGreedy>(dtype, P, sh, st);
+  } else if (B >= sh.G) {
+    e = prepare_dt<ssv::kVerifyGrouped>(dtype);
+    if (e == cudaSuccess) e = launch_sweep_dt<ssv::kVerifyGrouped>(dtype, P, sh, st);
+  } else {
+    e = launch_sweep_dt<ssv::kVerify>(dtype, P, sh, st);
+  }
   return from_cuda(e);
 }
 

@@ -46,10 +46,17 @@ constexpr unsigned kFull = 0xFFFFFFFFu;
 
 constexpr uint32_t kBadToken = 1u, kBadLogits = 2u, kBadUniform = 4u, kTimeout = 8u, kEmptyResidual = 16u;
 
-enum Mode : int { kVerify = 0, kVerifyGreedy = 1, kOverlap = 2, kOverlapGreedy = 3, kE2E = 4, kDiag = 5 };
+// Earliest-rejection word of a row: kRejBase - j for a rejection at position j
+// (larger = earlier; 0 = none seen yet).
+constexpr uint32_t kRejBase = 128u;
+
+// kVerifyGrouped is kVerify with rows in groups of one row per cluster,
+// position-major inside a group (for at least as many rows as clusters).
+enum Mode : int { kVerify = 0, kVerifyGreedy = 1, kOverlap = 2, kOverlapGreedy = 3, kE2E = 4, kDiag = 5,
+                  kVerifyGrouped = 6 };
 
 struct VerifyRecord {  // one per (b, k), k = 0..K
-  int32_t acc;         // 1 accepted, 0 rejected (draft positions)
+  int32_t acc;         // 1 accepted, 0 rejected, 2 rejected with an empty residual (draft positions)
   int32_t token;       // correction / bonus / greedy choice; -1 if none
   uint32_t pad0, pad1;
 };
@@ -99,6 +106,7 @@ struct SweepParams {
   float* ato;
   float* row_loss;
   uint32_t* row_cnt;
+  uint32_t* rej;  // [B] sampling verify: kRejBase - (earliest rejected position seen), 0 if none
   uint32_t* glob_cnt;
   uint32_t* status;
 };
@@ -298,7 +306,7 @@ __device__ __forceinline__ float draw_weights(const uint4& wt, const uint4& wd, 
 // re-zeroes the workspace of row b.
 template <int MODE>
 __device__ __forceinline__ void complete_row(const SweepParams& P, int b, int S, int lane) {
-  constexpr bool kVerifyMode = (MODE == kVerify || MODE == kVerifyGreedy);
+  constexpr bool kVerifyMode = (MODE == kVerify || MODE == kVerifyGreedy || MODE == kVerifyGrouped);
   const int K = P.K;
   const int per_row = kVerifyMode ? K + 1 : K;
   const float* pp0 = P.part + (long long)b * per_row * kPartStride;
@@ -311,17 +319,21 @@ __device__ __forceinline__ void complete_row(const SweepParams& P, int b, int S,
   };
   if constexpr (kVerifyMode) {
     const VerifyRecord* rr = P.rec + (long long)b * (K + 1);
-    int nacc = K;
+    // acc: 1 accepted, 0 rejected, 2 rejected with an empty residual
+    int nacc = K, acc_first = 1;
     for (int base = 0; base < K; base += 32) {
       const int kk = base + lane;
-      const bool rej = (kk < K) && (__ldcg(&rr[kk].acc) == 0);
-      const unsigned m = __ballot_sync(kFull, rej);
+      const int a = (kk < K) ? __ldcg(&rr[kk].acc) : 1;
+      const unsigned m = __ballot_sync(kFull, (a & 1) == 0);
       if (m) {
-        nacc = base + __ffs(m) - 1;
+        const int l = __ffs(m) - 1;
+        nacc = base + l;
+        acc_first = __shfl_sync(kFull, a, l);
         break;
       }
     }
     const int corr = __ldcg(&rr[nacc].token);
+    if (lane == 0 && acc_first == 2 && P.status) atomicOr(P.status, kEmptyResidual);
     for (int kk = lane; kk <= K; kk += 32) {
       int tokv = -1;
       if (kk < nacc) tokv = P.draft_tokens[b * K + kk];
@@ -337,6 +349,7 @@ __device__ __forceinline__ void complete_row(const SweepParams& P, int b, int S,
     if (lane == 0) {
       P.n_accepted[b] = nacc;
       P.row_cnt[b] = 0;
+      if (P.rej) P.rej[b] = 0;
     }
   } else if constexpr (MODE == kOverlap || MODE == kOverlapGreedy) {
     float al[2];
@@ -473,6 +486,7 @@ struct SweepSmem {
   float wamax[kWarps];  // diagnostics: per-warp draft arg-maximum
   int wamaxi[kWarps];
   float woff[kWarps + 1];
+  alignas(16) uint32_t rejw[4];  // sampling verify: the 16-byte group of row words holding this unit's row
   alignas(16) float mbox[2][kPartStride][8];  // pushed by peers: [exchange slot][sender rank][field]
   float bcf[8];
   int bci[8];
@@ -493,7 +507,8 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
   constexpr int PV = E::PV;
   using Raw = typename E::Raw;
   constexpr bool kGreedy = (MODE == kVerifyGreedy || MODE == kOverlapGreedy);
-  constexpr bool kVerifyMode = (MODE == kVerify || MODE == kVerifyGreedy);
+  constexpr bool kVerifyMode = (MODE == kVerify || MODE == kVerifyGreedy || MODE == kVerifyGrouped);
+  constexpr bool kSample = (MODE == kVerify || MODE == kVerifyGrouped);  // sampling verify
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int S = P.S;
@@ -540,7 +555,20 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
   };
   auto decode = [&](int u) {
     Unit x;
-    if constexpr (kVerifyMode) {
+    if constexpr (MODE == kVerifyGrouped) {
+      // Rows in groups of G, position-major inside a group: a unit starts
+      // about one unit-time after the earlier positions of its row have
+      // decided, so that it can skip a draw that cannot be emitted, and rows
+      // keep completing all through the launch.
+      const int gsz = G * (K + 1);
+      const int g = u / gsz;
+      const int j = u - g * gsz;
+      const int r0 = g * G;
+      const int rg = min(G, P.B - r0);
+      x.k = j / rg;
+      x.b = r0 + (j - x.k * rg);
+      x.bonus = (x.k == K);
+    } else if constexpr (kVerifyMode) {
       x.b = u / (K + 1);
       x.k = u - x.b * (K + 1);
       x.bonus = (x.k == K);
@@ -555,6 +583,9 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
     x.dg = x.has_draft ? reinterpret_cast<const Raw*>(P.draft) + ((long long)x.b * K + x.k) * V : nullptr;
     return x;
   };
+
+  // index of a unit's record and partials: b * per_row + k
+  auto rec_idx = [&](const Unit& x) { return x.b * per_row + x.k; };
 
   // Bulk copies of this warp's segment of unit u into stage st (lane 0).
   auto issue = [&](int u, int st) {
@@ -641,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
     if constexpr (kVerifyMode) {
       const Unit x = decode(u);
       if (!x.bonus) y_ = P.draft_tokens[x.b * K + x.k];
-      if constexpr (MODE == kVerify) {
+      if constexpr (kSample) {
         if (!x.bonus) ua_ = P.u_accept[x.b * K + x.k];
         uf_ = P.u_final[x.b];
       }
@@ -670,6 +701,11 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
     const float ua = ua_next, uf = uf_next;
     if (tid == 0 && u + G < P.units) fetch_scalars(u + G, y_next, ua_next, uf_next);
     const bool tok_ok = x.bonus || (y >= 0 && y < V);
+    // earliest rejection of this row seen so far: copied to shared memory
+    // (thread 0) while pass A runs, read before the first exchange
+    if constexpr (kSample) {
+      if (tid == 0) cp_async_16_cg(smem_addr(sm.rejw), P.rej + (x.b & ~3));
+    }
 
     // queued arrivals are published when the queue is full
     if (warp == 0 && __shfl_sync(kFull, sm.npend, 0) == 32) flush();
@@ -780,9 +816,9 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
             r.acc = (!x.bonus && tok_ok && y == am_t) ? 1 : 0;
             r.token = am_t;
             r.pad0 = r.pad1 = 0;
-            P.rec[u] = r;
+            P.rec[rec_idx(x)] = r;
           }
-          P.part[(long long)u * kPartStride] = al;
+          P.part[(long long)rec_idx(x) * kPartStride] = al;
           if (flags && P.status) atomicOr(P.status, flags);
         }
         if (lane == 0) queue_arrival(x.b);
@@ -877,7 +913,7 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
         warp_combine_mz2(a, za, d, zda, s);
         // the CTA holding the drafted token publishes its two logits
         float gt = 0.0f, gd = 0.0f;
-        if constexpr (MODE == kVerify) {
+        if constexpr (kSample) {
           if (lane == 0 && !x.bonus && tok_ok && y >= e0 && y < e1) {
             gt = E::to_f32(reinterpret_cast<const Raw*>(st)[y - e0]);
             gd = E::to_f32(reinterpret_cast<const Raw*>(sd)[y - e0]);
@@ -887,6 +923,14 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
         }
         float av = -INFINITY;
         int ai = 0x7FFFFFFF;
+        if constexpr (kSample) {
+          uint32_t seen = 0;
+          if (lane == 0) {
+            cp_async_wait_all();
+            seen = sm.rejw[x.b & 3];
+          }
+          av = __uint_as_float(__shfl_sync(kFull, seen, 0));
+        }
         if constexpr (MODE == kDiag) {
           if (lane < kWarps) {
             av = sm.wamax[lane];
@@ -902,7 +946,7 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
         float a = mb(slot, 0, -INFINITY), za = mb(slot, 1, 0.0f);
         float d = mb(slot, 2, -INFINITY), zda = mb(slot, 3, 0.0f);
         float zty = 0.0f, zdy = 0.0f;
-        if constexpr (MODE == kVerify) {
+        if constexpr (kSample) {
           const int yy = __shfl_sync(kFull, y, 0);
           const bool ok_y = __shfl_sync(kFull, (int)tok_ok, 0) != 0;
           const int own = (ok_y && !x.bonus) ? yy / P.L : 0;
@@ -924,7 +968,7 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
           uint32_t flags = 0;
           int mode_c = 0;  // 0: overlap only, 1: residual draw, 2: draw from p, 3: invalid
           int acc = 1;
-          if constexpr (MODE == kVerify) {
+          if constexpr (kSample) {
             if (x.bonus) {
               mode_c = 2;
             } else {
@@ -942,6 +986,21 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
             flags |= kBadLogits;
             mode_c = 3;
           }
+          int skip = 0;
+          if constexpr (kSample) {
+            // publish a rejection (the record will hold acc = 0), then skip a
+            // draw that cannot be emitted: rank 0's reading of the row's word
+            // decides for the whole cluster
+            if (rank == 0 && !x.bonus && (mode_c == 1 || mode_c == 3))
+              atomicMax(&P.rej[x.b], kRejBase - (uint32_t)x.k);
+            const uint32_t seen = __float_as_uint(sm.mbox[slot][0][6]);
+            if (seen > kRejBase - (uint32_t)x.k) {
+              if (mode_c == 2) mode_c = 0;     // bonus of a row with a rejection
+              else if (mode_c == 1) skip = 1;  // a later rejection: overlap partial only
+            }
+          }
+          sm.bci[7] = skip;
+          if (skip) sm.bci[2] = 0;
           if (flags && rank == 0 && P.status) atomicOr(P.status, flags);
           sm.bcf[0] = c1t;
           sm.bcf[1] = c1d;
@@ -1025,35 +1084,35 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
           if constexpr (MODE == kDiag) M3 = warp_sum(M3);
           if (lane == 0) {
             const float nanv = __int_as_float(0x7FC00000);
-            P.part[(long long)u * kPartStride + rank] = (mode_c == 3) ? nanv : __fmul_rn(A, izt);
+            P.part[(long long)rec_idx(x) * kPartStride + rank] = (mode_c == 3) ? nanv : __fmul_rn(A, izt);
             if constexpr (MODE == kDiag) {
               // entropy partial sum_v p x_t; rank 0 folds in -log2 Z_t, so
               // that the rank-ordered sum is -H / ln 2
               float h2 = __fmul_rn(M2, izt);
               if (rank == 0) h2 = __fsub_rn(h2, sm.bcf[6]);
-              P.part2[(long long)u * kPartStride + rank] = (mode_c == 3) ? nanv : h2;
-              P.part3[(long long)u * kPartStride + rank] = (mode_c == 3) ? nanv : __fmul_rn(M3, izt);
-              if (P.ato && py_hat >= 0.0f) P.ato[u] = py_hat;
-              if (P.ato && mode_c == 3 && rank == 0) P.ato[u] = nanv;
+              P.part2[(long long)rec_idx(x) * kPartStride + rank] = (mode_c == 3) ? nanv : h2;
+              P.part3[(long long)rec_idx(x) * kPartStride + rank] = (mode_c == 3) ? nanv : __fmul_rn(M3, izt);
+              if (P.ato && py_hat >= 0.0f) P.ato[rec_idx(x)] = py_hat;
+              if (P.ato && mode_c == 3 && rank == 0) P.ato[rec_idx(x)] = nanv;
             }
             if constexpr (MODE == kE2E) {
-              P.part2[(long long)u * kPartStride + rank] = (mode_c == 3) ? nanv : __fmul_rn(M2, izt);
+              P.part2[(long long)rec_idx(x) * kPartStride + rank] = (mode_c == 3) ? nanv : __fmul_rn(M2, izt);
               if (rank == 0) {
                 E2EStats e2;
                 e2.c1t = c1t;
                 e2.cd = cd2;
                 e2.izt = izt;
                 e2.smass = e2.alpha = e2.b1 = e2.b0 = e2.pad = 0.0f;
-                P.stats[u] = e2;
+                P.stats[rec_idx(x)] = e2;
               }
             }
-            if constexpr (MODE == kVerify) {
+            if constexpr (kSample) {
               if (rank == 0) {
                 VerifyRecord r;
                 r.acc = (mode_c == 3) ? 0 : acc;
                 r.token = -1;
                 r.pad0 = r.pad1 = 0;
-                P.rec[u] = r;
+                P.rec[rec_idx(x)] = r;
               }
             }
             queue_arrival(x.b);
@@ -1069,6 +1128,8 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
       // same per-element arithmetic, one vector per lane.
       const f32x2 CDd = f2(-c1d, -c1d);
       const f32x2 NR = f2(-ratio, -ratio);
+      const bool skip = sm.bci[7] != 0;
+      bool emptied = false;
       for (int attempt = 0; attempt < 2; ++attempt) {
         const bool resid = (mode_c == 1);
         float tot = 0.0f;
@@ -1098,9 +1159,12 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
           const float ctot = __shfl_sync(kFull, wincl, kWarps - 1);
           float A = lane < kWarps ? sm.wred[lane][0] : 0.0f;
           A = warp_sum(A);
-          if (lane == 0 && attempt == 0 && resid) P.part[(long long)u * kPartStride + rank] = __fmul_rn(A, izt);
-          push8(slot, ctot, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f);
+          if (lane == 0 && attempt == 0 && resid) P.part[(long long)rec_idx(x) * kPartStride + rank] = __fmul_rn(A, izt);
+          if (!skip) push8(slot, ctot, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f);
         }
+        // a later rejection keeps the overlap partial, computed with the
+        // draw's arithmetic (bits independent of the skip), and draws nothing
+        if (skip) break;
         cluster_sync();  // ---- exchange 2: CTA totals of the draw weights
         ++xc;
         if (warp == 0) {
@@ -1129,7 +1193,8 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
         __syncthreads();
         if (!sm.bci[2]) {
           if (attempt == 0 && resid) {  // rejection with no residual mass (rounding): draw from p
-            if (rank == 0 && tid == 0 && P.status) atomicOr(P.status, kEmptyResidual);
+            // reported by the row's completion if this position is the one emitted
+            emptied = true;
             mode_c = 2;
             continue;
           }
@@ -1231,10 +1296,10 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
       __syncthreads();  // the owner thread's token reaches thread 0
       if (tid == 0) {
         if (rank == 0) {
-          P.rec[u].acc = (MODE == kVerify && !x.bonus) ? acc : 0;
-          if (!sm.bci[2]) P.rec[u].token = -1;
+          P.rec[rec_idx(x)].acc = (kSample && !x.bonus) ? (emptied ? 2 : acc) : 0;
+          if (!sm.bci[2]) P.rec[rec_idx(x)].token = -1;
         }
-        if (sm.bci[2] && sm.bci[3] == (int)rank) P.rec[u].token = sm.bci[6];
+        if (sm.bci[2] && sm.bci[3] == (int)rank) P.rec[rec_idx(x)].token = sm.bci[6];
         queue_arrival(x.b);
       }
     }

@@ -129,6 +129,26 @@ def test_launch_shapes_agree(ssv, S, nst):
     assert_verify(out, oracle_verify(w))
 
 
+def test_row_groups_with_draw_skip_against_oracle(ssv):
+    """More rows than clusters: rows run in groups, position-major inside a
+    group, and units skip draws that an earlier rejection makes unused.  Every
+    row against the oracle (tokens, counts and alpha of skipped rejections),
+    with a partial last group."""
+    B, K, V = 230, 3, 6000
+    w = synth.gaussian(B, K, V, sigma=2.0, noise=1.0, dtype=torch.float32, temperature=1.0, seed=4545)
+    ssv.set_launch_override(16, 1)
+    try:
+        G = ssv.launch_shape(torch.float32, B * (K + 1), V)[3]
+        assert B > G and B % G != 0, G
+        out = ssv.verify(*to_dev(w), w.temperature)
+        torch.cuda.synchronize()
+    finally:
+        ssv.set_launch_override(0, 0)
+    ref = oracle_verify(w)
+    assert_verify(out, ref)
+    assert (ref.n_accepted < K - 1).sum() > 20  # many rows with positions after the first rejection
+
+
 def test_greedy_ties_take_smallest_index(ssv):
     B, K, V = 4, 3, 2048
     zt = torch.zeros((B, K + 1, V), dtype=torch.bfloat16)
@@ -352,6 +372,37 @@ def test_status_bits(ssv):
     out = ssv.verify(t, d, y, ua2, uf, 1.0)
     torch.cuda.synchronize()
     assert int(out.status.item()) & ssv.DEV_BAD_UNIFORM
+
+
+def test_empty_residual_reported_for_the_emitted_position(ssv):
+    """EMPTY_RESIDUAL is raised only by the rejection a row emits (the
+    oracle's ``residual_empty``), whatever later positions hold."""
+    B, K, V = 2, 3, 1000
+    w = synth.gaussian(B, K, V, sigma=1.0, noise=0.5, dtype=torch.float32, temperature=1.0, seed=8)
+    t, d, y, ua, uf = to_dev(w)
+    d2 = d.clone()
+    d2[:, 2] = t[:, 2]   # position 2: q = p
+    d2[0, 1] = t[0, 1]   # row 0, position 1: q = p
+    y2 = y.clone()
+    ua2 = ua.clone()
+    ua2[0, 0] = 0.0      # row 0: position 0 accepted
+    y2[0, 1] = V + 1     # row 0: rejected at 1 with an empty residual: drawn from p_1
+    y2[1, 0] = V + 1     # row 1: rejected at 0, residual not empty
+    y2[1, 2] = V + 1     # row 1: position 2 empty but never emitted
+    both = ssv.verify(t, d2, y2, ua2, uf, 1.0)
+    row1 = ssv.verify(t[1:].contiguous(), d2[1:].contiguous(), y2[1:].contiguous(), ua2[1:].contiguous(),
+                      uf[1:].contiguous(), 1.0)
+    torch.cuda.synchronize()
+    assert int(both.status.item()) == ssv.DEV_BAD_TOKEN | ssv.DEV_EMPTY_RESIDUAL
+    assert int(row1.status.item()) == ssv.DEV_BAD_TOKEN
+    assert both.n_accepted.cpu().tolist() == [1, 0]
+    p01 = oracle.softmax_t(synth.f64(w.target[0, 1]), 1.0)
+    v, _ = oracle.inverse_cdf(p01, float(w.u_final[0]))
+    assert int(both.tokens[0, 1]) == v
+    zt, zd = synth.f64(w.target[1, 0]), synth.f64(w.draft[1, 0])
+    rho = oracle.residual(oracle.softmax_t(zt, 1.0), oracle.softmax_t(zd, 1.0))
+    v1, _ = oracle.inverse_cdf(rho, float(w.u_final[1]))
+    assert int(both.tokens[1, 0]) == v1 == int(row1.tokens[0, 0])
 
 
 def test_empty_batch_and_invalid_args(ssv):
