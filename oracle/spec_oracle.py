@@ -40,6 +40,10 @@ reason, in the design notes of the repository):
   maximised) and its gradient is taken with respect to the draft logits only,
   the target being a constant; the sub-gradient of ``min`` uses the strict
   indicator ``1[q_v < p_v]``.
+* top-k / top-p truncation ranks tokens by logit (ties by smaller index),
+  applies top-k first, then keeps the shortest ranked prefix whose
+  renormalised mass at temperature T reaches top_p; dropped logits become
+  -inf, on the target and the draft alike.
 
 Parity pins: every function here is checked in ``tests/test_oracle_pins.py``
 against closed forms, worked examples printed on the pages, exact rational
@@ -76,6 +80,54 @@ def softmax_t(z, temperature):
     a = (z - np.max(z)) / t
     e = np.exp(a)
     return e / np.sum(e)
+
+
+# ---------------------------------------------------------------------------
+# Top-k / top-p truncation, applied the same way to target and draft logits
+# ---------------------------------------------------------------------------
+
+# Distance (in probability mass) below which a top-p cut is reported as a
+# near tie: another implementation's rounding may move the cut by one token.
+NEAR_TRUNC = 1e-5
+
+
+def truncate_logits(z, temperature, top_k=0, top_p=1.0):
+    """Top-k, then top-p truncation of one logit row, as sampling applies it.
+
+    Speculative Decoding 与 MTP, section 4: p and q must both be computed after
+    the agreed temperature and top-k / top-p transforms; section 23: a mask
+    applied to one side only breaks correctness.  The pages give no formula;
+    the transform taken is the common one:
+
+    * tokens are ranked by logit, larger first, ties by smaller index;
+    * top-k (0 < top_k < V) keeps the first top_k tokens of that ranking;
+    * top-p (top_p < 1) renormalises softmax(z / T) over the kept tokens and
+      keeps, in ranking order, every token whose preceding mass is below
+      top_p (the shortest prefix reaching top_p);
+    * dropped tokens get logit -inf; kept tokens keep their logit.
+
+    Returns ``(z_out, near)``; ``near`` reports a top-p cut whose preceding
+    mass lies within NEAR_TRUNC of top_p on either side of the boundary.
+    """
+    z = np.asarray(z, dtype=np.float64)
+    V = z.shape[0]
+    order = np.lexsort((np.arange(V), -z))  # logit descending, then index ascending
+    keep = np.ones(V, dtype=bool)
+    if 0 < top_k < V:
+        keep[:] = False
+        keep[order[:top_k]] = True
+    near = False
+    if top_p < 1.0:
+        ranked = order[keep[order]]  # kept tokens in ranking order
+        p = softmax_t(z[ranked], temperature)
+        before = np.concatenate(([0.0], np.cumsum(p)[:-1]))
+        sel = before < top_p
+        n = int(sel.sum())
+        near = bool(abs(before[n - 1] - top_p) < NEAR_TRUNC or
+                    (n < before.size and abs(before[n] - top_p) < NEAR_TRUNC))
+        keep[:] = False
+        keep[ranked[:n]] = True
+    return np.where(keep, z, -np.inf), near
 
 
 def overlap(p, q):

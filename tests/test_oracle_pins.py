@@ -544,3 +544,108 @@ def test_diagnostics_shift_invariant_and_batched():
     q = so.softmax_t(zd[1, 2], 0.8)
     assert a.alpha_to[1, 2] == p[np.argmax(q)]
     np.testing.assert_allclose(a.cross_entropy, a.entropy + a.kl, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# top-k / top-p truncation
+# ---------------------------------------------------------------------------
+
+def _kept(z_out):
+    return [int(v) for v in np.nonzero(np.isfinite(z_out))[0]]
+
+
+def test_truncation_worked_example():
+    # z = (2, 1, 0, 1) at T = 1: p = (e^2, e, 1, e) / (e^2 + 2e + 1)
+    #   = (0.534447, 0.196612, 0.072329, 0.196612); ranking 0, 1, 3, 2
+    #   (tokens 1 and 3 tie: smaller index first); preceding masses in that
+    #   order 0, 0.534447, 0.731059, 0.927671.
+    z = np.array([2.0, 1.0, 0.0, 1.0])
+    cases = [
+        (2, 1.0, 1.0, [0, 1]),     # top-k: the tie at 1 keeps the smaller index
+        (0, 0.6, 1.0, [0, 1]),     # 0.534 < 0.6 <= 0.731
+        (0, 0.5, 1.0, [0]),        # 0.534 >= 0.5
+        (0, 0.8, 1.0, [0, 1, 3]),  # 0.731 < 0.8 <= 0.928
+        (3, 0.9, 1.0, [0, 1, 3]),  # top-3 renormalised: preceding 0, 0.576, 0.788
+        (1, 1.0, 1.0, [0]),
+        # T = 0.5: p = (e^4, e^2, 1, e^2) / (e^4 + 2e^2 + 1) = (0.7758, 0.1050, 0.0142, 0.1050)
+        (0, 0.8, 0.5, [0, 1]),     # 0.776 < 0.8 <= 0.881
+    ]
+    for k, tp, T, want in cases:
+        out, near = so.truncate_logits(z, T, k, tp)
+        assert _kept(out) == want, (k, tp, T)
+        assert not near
+        assert (out[want] == z[want]).all() and np.isneginf(np.delete(out, want)).all()
+    # a cut exactly at a preceding mass is a near tie, and the token is dropped
+    p0 = math.exp(2) / (math.exp(2) + 2 * math.e + 1)
+    out, near = so.truncate_logits(z, 1.0, 0, p0)
+    assert near and _kept(out) in ([0], [0, 1])
+
+
+def test_truncation_closed_forms():
+    z = np.zeros(10)  # uniform: the preceding mass of rank i is i / 10
+    for tp, n in ((0.35, 4), (0.05, 1), (0.5, 5), (0.95, 10)):
+        out, _ = so.truncate_logits(z, 1.3, 0, tp)
+        assert _kept(out) == list(range(n))  # ties rank by index
+    out, _ = so.truncate_logits(z, 1.0, 3, 1.0)
+    assert _kept(out) == [0, 1, 2]
+    rng = np.random.default_rng(11)
+    z = rng.normal(size=50) * 2
+    assert _kept(so.truncate_logits(z, 1.0, 1, 1.0)[0]) == [so.argmax_first(z)]
+    assert _kept(so.truncate_logits(z, 1.0, 0, 1e-9)[0]) == [so.argmax_first(z)]
+    for k in (0, 50, 80):
+        out, _ = so.truncate_logits(z, 0.7, k, 1.0)
+        assert (out == z).all()
+
+
+def test_truncation_brute_force_tiny():
+    """The kept set is the smallest subset of the top-k set whose
+    renormalised mass reaches top_p, with the largest mass among subsets of
+    that size (unique here: no equal masses)."""
+    rng = np.random.default_rng(12)
+    for trial in range(300):
+        V = int(rng.integers(1, 7))
+        z = rng.normal(size=V) * 1.5
+        T = float(rng.choice([0.5, 1.0, 2.0]))
+        k = int(rng.integers(0, V + 2))
+        tp = float(rng.uniform(0.05, 1.0))
+        out, near = so.truncate_logits(z, T, k, tp)
+        if near:
+            continue
+        kept = set(_kept(out))
+        cand = list(range(V)) if not (0 < k < V) else sorted(np.argsort(-z, kind="stable")[:k].tolist())
+        p = so.softmax_t(z[cand], T)
+        mass = dict(zip(cand, p))
+        best = None
+        for size in range(1, len(cand) + 1):
+            sets = [s for s in itertools.combinations(cand, size) if sum(mass[v] for v in s) >= tp]
+            if sets:
+                best = max(sets, key=lambda s: sum(mass[v] for v in s))
+                break
+        if tp >= 1.0:
+            best = tuple(cand)
+        assert kept == set(best), (trial, z, T, k, tp)
+
+
+def test_truncation_invariants_random_rows():
+    rng = np.random.default_rng(13)
+    for trial in range(40):
+        V = 500
+        z = np.round(rng.normal(size=V) * 3, 1)  # rounded: many ties
+        T = float(rng.uniform(0.3, 2.0))
+        k = int(rng.integers(0, 600))
+        tp = float(rng.uniform(0.1, 1.0))
+        out, near = so.truncate_logits(z, T, k, tp)
+        kept = np.isfinite(out)
+        n = int(kept.sum())
+        assert n >= 1 and (n <= k or not 0 < k < V)
+        # upward closed in the ranking (logit descending, index ascending)
+        rank = sorted(range(V), key=lambda v: (-z[v], v))
+        flags = [bool(kept[v]) for v in rank]
+        assert flags == sorted(flags, reverse=True)
+        if tp < 1.0 and not near:
+            top = rank[: (k if 0 < k < V else V)]
+            p = so.softmax_t(z[top], T)
+            m = dict(zip(top, p))
+            ranked_kept = [v for v in rank if kept[v]]
+            assert sum(m[v] for v in ranked_kept) >= tp
+            assert sum(m[v] for v in ranked_kept[:-1]) < tp
