@@ -55,7 +55,7 @@ def parse():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=100)
-    ap.add_argument("--single", choices=["verify", "greedy", "overlap", "e2e", "diag"], default=None,
+    ap.add_argument("--single", choices=["verify", "greedy", "overlap", "e2e", "diag", "truncate"], default=None,
                     help="run only `--calls` calls of one entry point (an L2 flush before each): the "
                          "profiling target, prints no JSON")
     ap.add_argument("--shape", default="32,4,151936", help="B,K,V of --single")
@@ -457,7 +457,8 @@ def run_single(args):
     from sampling_spec_verify_gb300 import synth
     Bs, Ks, Vs = (int(v) for v in args.shape.split(","))
     dev = torch.device("cuda")
-    T = 0.0 if args.single == "greedy" else (1.0 if args.single in ("overlap", "e2e", "diag") else args.temperature)
+    T = 0.0 if args.single == "greedy" else (1.0 if args.single in ("overlap", "e2e", "diag", "truncate")
+                                             else args.temperature)
     w = synth.entropy_mix(seed=SEED, temperature=T, B=Bs, K=Ks, V=Vs)
     t, d = w.target.to(dev), w.draft.to(dev)
     y, ua, uf = w.draft_tokens.to(dev), w.u_accept.to(dev), w.u_final.to(dev)
@@ -470,6 +471,8 @@ def run_single(args):
             ssv.overlap(t, d, 1.0, K=Ks)
         elif args.single == "diag":
             ssv.diagnostics(t, d, 1.0, K=Ks)
+        elif args.single == "truncate":  # top-k 50, top-p 0.9 on the target tensor
+            ssv.truncate_logits(t, 1.0, 50, 0.9)
         else:
             ssv.e2e_tv_fwd_bwd(t, d, 1.0, 1.0, K=Ks)
     torch.cuda.synchronize()

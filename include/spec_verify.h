@@ -231,6 +231,34 @@ spec_status_t spec_diagnostics(const void* target_logits,
                                void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Top-k / top-p truncation of logit rows, to be applied with the same
+ * arguments to the target and the draft logits before a verify step.
+ *
+ * "Speculative Decoding 与 MTP", section 4 (p and q are both computed after the
+ * agreed temperature and top-k / top-p transforms) and section 23 (a mask that
+ * only one side applies breaks correctness).  Tokens are ranked by logit,
+ * larger first, ties to the smaller index.  Top-k (0 < top_k < V) keeps the
+ * first top_k.  Top-p (top_p < 1) then renormalises softmax(z / T) over the
+ * kept tokens and keeps the shortest ranked prefix whose mass reaches top_p.
+ * Dropped logits become -inf; kept logits are copied unchanged.
+ *
+ * logits       [rows, V] dtype, device.
+ * out          [rows, V] dtype, device; may be `logits` itself (in place) but
+ *              may not overlap it otherwise.
+ * temperature  T > 0 when top_p < 1 (unused otherwise).
+ * top_k        >= 0; 0 or >= V disables top-k.
+ * top_p        in (0, 1]; 1 disables top-p.
+ * A row holding a NaN or +inf logit, or no finite logit, is copied unchanged
+ * and sets SPEC_DEV_BAD_LOGITS.  Top-p masses are fixed point with 2^-44 of
+ * the row maximum's mass as unit; a cut whose preceding mass lies within
+ * about 1e-6 of top_p may move by one token against exact arithmetic.
+ */
+spec_status_t spec_truncate_logits(const void* logits, void* out,
+                                   spec_dtype_t dtype, int rows, int V,
+                                   float temperature, int top_k, float top_p,
+                                   uint32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Launch shape the library picks for a verify sweep over `units` (row,
  * position) pairs of V logits (for benchmarks and diagnostics): CTAs per
  * cluster, threads per CTA, dynamic shared memory per CTA, the number of

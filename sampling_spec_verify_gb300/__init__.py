@@ -12,7 +12,9 @@ Entry points (same names as the C ABI, see include/spec_verify.h):
 * ``overlap``         -- alpha = sum min(p, q), TV, prefix survival, E[tau];
 * ``e2e_tv_fwd_bwd``  -- E2E-TV loss and its draft-logit gradient;
 * ``diagnostics``     -- alpha, target entropy, cross-entropy, KL and the
-                         target-only acceptance p(argmax q) per position.
+                         target-only acceptance p(argmax q) per position;
+* ``truncate_logits`` -- top-k / top-p truncation, to apply identically to
+                         target and draft logits before ``verify``.
 """
 
 from __future__ import annotations
@@ -25,7 +27,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "SpecError", "lib", "verify", "overlap", "e2e_tv_fwd_bwd", "diagnostics", "launch_shape",
+    "SpecError", "lib", "verify", "overlap", "e2e_tv_fwd_bwd", "diagnostics", "truncate_logits", "launch_shape",
     "set_launch_override", "VerifyOutput", "OverlapOutput", "E2EOutput", "DiagOutput", "HostVerifier",
     "DEV_BAD_TOKEN", "DEV_BAD_LOGITS", "DEV_BAD_UNIFORM", "DEV_TIMEOUT", "DEV_EMPTY_RESIDUAL",
     "SPEC_OK", "SPEC_ERR_INVALID_ARG", "SPEC_ERR_UNSUPPORTED", "SPEC_ERR_CUDA",
@@ -79,6 +81,8 @@ def lib():
     L.spec_diagnostics_workspace_bytes.argtypes = [i32, i32, i32]
     L.spec_diagnostics.restype = i32
     L.spec_diagnostics.argtypes = [vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.spec_truncate_logits.restype = i32
+    L.spec_truncate_logits.argtypes = [vp, vp, i32, i32, i32, f32, i32, f32, vp, vp]
     L.spec_launch_shape.restype = i32
     L.spec_launch_shape.argtypes = [i32, i32, i32] + [ctypes.POINTER(i32)] * 5
     L.spec_set_launch_override.restype = None
@@ -330,6 +334,32 @@ def diagnostics(target: torch.Tensor, draft: torch.Tensor, temperature: float, *
                             _ptr(out.alpha_target_only), _ptr(out.status), _ptr(ws),
                             ws.numel() * ws.element_size(), sh)
     _check(st, "spec_diagnostics")
+    return out
+
+
+# ---------------------------------------------------------------------------
+# top-k / top-p truncation
+# ---------------------------------------------------------------------------
+
+def truncate_logits(logits: torch.Tensor, temperature: float, top_k: int = 0, top_p: float = 1.0, *,
+                    out: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Top-k then top-p truncation of every row of ``logits`` [..., V]
+    (dropped logits become -inf).  Apply it with the same arguments to the
+    target and the draft logits of a verify step.  ``out`` may be ``logits``
+    (in place); ``status`` is an optional int32 [1] device word."""
+    L = lib()
+    _need(logits, "logits")
+    V = logits.shape[-1]
+    rows = logits.numel() // V if V else 0
+    if out is None:
+        out = torch.empty_like(logits)
+    elif out.shape != logits.shape or out.dtype != logits.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of the shape and dtype of logits")
+    sh, _ = _stream_handle(stream, logits.device)
+    st = L.spec_truncate_logits(_ptr(logits), _ptr(out), _dtype_code(logits), rows, V, float(temperature),
+                                int(top_k), float(top_p), _ptr(status), sh)
+    _check(st, "spec_truncate_logits")
     return out
 
 

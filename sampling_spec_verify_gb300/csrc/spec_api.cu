@@ -13,6 +13,7 @@
 
 #include "spec_verify.h"
 #include "sweep.cuh"
+#include "truncate.cuh"
 
 namespace {
 
@@ -581,6 +582,38 @@ spec_status_t spec_diagnostics(const void* target_logits, const void* draft_logi
   P.row_cnt = reinterpret_cast<uint32_t*>(w + ws.cnt);
   P.status = dev_status;
   return from_cuda(launch_sweep_dt<ssv::kDiag>(dtype, P, sh, st));
+}
+
+spec_status_t spec_truncate_logits(const void* logits, void* out, spec_dtype_t dtype, int rows, int V,
+                                   float temperature, int top_k, float top_p, uint32_t* dev_status, void* stream) {
+  if (rows < 0 || V < 1 || !dtype_ok(dtype) || top_k < 0) return SPEC_ERR_INVALID_ARG;
+  if (!(top_p > 0.0f && top_p <= 1.0f)) return SPEC_ERR_INVALID_ARG;
+  if (top_p < 1.0f && (!(temperature > 0.0f) || !std::isfinite(temperature))) return SPEC_ERR_INVALID_ARG;
+  if (rows == 0) return SPEC_OK;
+  if (!logits || !out) return SPEC_ERR_INVALID_ARG;
+  const int es = elem_size(dtype);
+  const size_t bytes = (size_t)rows * (size_t)V * (size_t)es;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(logits), b = reinterpret_cast<uintptr_t>(out);
+  if (a != b && a < b + bytes && b < a + bytes) return SPEC_ERR_INVALID_ARG;  // partial overlap
+  DevInfo di;
+  if (!device_info(&di)) return SPEC_ERR_CUDA;
+  ssv::TruncParams P = {};
+  P.in = logits;
+  P.out = out;
+  P.rows = rows;
+  P.V = V;
+  P.aligned = aligned16(logits) && aligned16(out) && ((long long)V * es) % 16 == 0;
+  P.s = top_p < 1.0f ? (float)(1.4426950408889634 / (double)temperature) : 0.0f;
+  P.top_k = top_k;
+  P.top_p = top_p;
+  P.status = dev_status;
+  const int grid = rows < 2 * di.sms ? rows : 2 * di.sms;  // two resident CTAs per SM
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == SPEC_BF16)
+    ssv::truncate_kernel<Bf16><<<grid, ssv::kTThreads, 0, st>>>(P);
+  else
+    ssv::truncate_kernel<F32><<<grid, ssv::kTThreads, 0, st>>>(P);
+  return from_cuda(cudaGetLastError());
 }
 
 }  // extern "C"

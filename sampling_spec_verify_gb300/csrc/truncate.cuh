@@ -1,0 +1,459 @@
+// Top-k / top-p truncation of logit rows, applied the same way to target and
+// draft logits before a verify step.
+//
+// "Speculative Decoding 与 MTP", section 4: p and q must both be computed after
+// the agreed temperature and top-k / top-p transforms; section 23: a mask that
+// only one side applies breaks correctness.  The transform: rank tokens by
+// logit (larger first, ties to the smaller index); top-k keeps the first
+// top_k; top-p renormalises softmax(z / T) over what is left and keeps the
+// shortest ranked prefix whose mass reaches top_p; dropped logits become -inf.
+//
+// One CTA per row.  Every pass streams the row through L2 (the first one from
+// HBM): a maximum pass, radix-select passes over order-preserving keys (8 bits
+// per pass, 2 passes for bf16, 4 for fp32), a tie pass in index order for the
+// threshold key, and the write pass.  A radix pass builds one histogram per
+// warp (logits crowd into a few exponent digits, and shared atomics that many
+// warps aim at one counter serialise); for counts, the lanes holding the same
+// digit are grouped and one of them adds the group's size.  Top-p masses are
+// fixed point (2^44 for the row maximum) and summed as integers, so every cut
+// is independent of the order of the additions.
+#pragma once
+
+#include <cstdint>
+
+namespace ssv {
+
+constexpr int kTThreads = 512;
+constexpr int kTWarps = kTThreads / 32;
+constexpr float kMassScale = 0x1p44f;  // fixed-point unit of the top-p masses
+
+struct TruncParams {
+  const void* in;
+  void* out;  // may equal in
+  int rows, V;
+  int aligned;  // in and out rows on 16-byte boundaries and V * elem a multiple of 16
+  float s;      // log2(e) / T
+  int top_k;    // active when 0 < top_k < V
+  float top_p;  // active when top_p < 1
+  uint32_t* status;
+};
+
+struct TruncSmem {
+  unsigned long long ph[kTWarps][256];  // per-warp histograms of one radix pass
+  unsigned long long hist[256];
+  unsigned long long wtot[kTWarps];
+  float wmax[kTWarps];
+  int wnan[kTWarps];
+  unsigned long long bc;
+  int bin;
+  int tie;
+};
+
+// Order-preserving key of a logit (larger value, larger key), -0 folded onto
+// +0, keeping the top KB bits (16 for bf16 values, whose low bits are zero).
+template <int KB>
+__device__ __forceinline__ uint32_t order_key(float x) {
+  uint32_t u = __float_as_uint(x);
+  if (u == 0x80000000u) u = 0u;
+  const uint32_t k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return k >> (32 - KB);
+}
+
+// The value whose key is k (inverse of order_key).
+template <int KB>
+__device__ __forceinline__ float key_value(uint32_t k) {
+  uint32_t k32 = k << (32 - KB);
+  if (KB < 32 && !(k32 & 0x80000000u)) k32 |= (1u << (32 - KB)) - 1u;  // negative: low bits were ones
+  const uint32_t u = (k32 & 0x80000000u) ? (k32 & 0x7FFFFFFFu) : ~k32;
+  return __uint_as_float(u);
+}
+
+// Fixed-point mass of a logit x against the row maximum M: round(2^((x - M) s) * 2^44).
+__device__ __forceinline__ unsigned long long fixed_mass(float x, float M, float s) {
+  return __float2ull_rn(__fmul_rn(ex2(__fmul_rn(__fsub_rn(x, M), s)), kMassScale));
+}
+
+// Calls f(v, x) for every element of the row: coalesced 16-byte loads when the
+// row is aligned, element loads otherwise.
+constexpr int kTUnroll = 4;  // independent 16-byte loads in flight per thread
+
+template <class E, class F>
+__device__ __forceinline__ void for_each_elem(const typename E::Raw* row, int V, bool aligned, F&& f) {
+  if (aligned) {
+    const uint4* r4 = reinterpret_cast<const uint4*>(row);
+    const int nvec = V / E::PV;
+    for (int i0 = threadIdx.x; i0 < nvec; i0 += kTThreads * kTUnroll) {
+      uint4 w[kTUnroll];
+#pragma unroll
+      for (int u = 0; u < kTUnroll; ++u) {
+        const int i = i0 + u * kTThreads;
+        w[u] = i < nvec ? __ldcg(r4 + i) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kTUnroll; ++u) {
+        const int i = i0 + u * kTThreads;
+        if (i >= nvec) break;
+        float x[E::PV];
+        E::unpack(w[u], x);
+#pragma unroll
+        for (int k = 0; k < E::PV; ++k) f(i * E::PV + k, x[k]);
+      }
+    }
+  } else {
+    for (int v = threadIdx.x; v < V; v += kTThreads) f(v, E::to_f32(__ldcg(row + v)));
+  }
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long warp_incl_scan_u64(unsigned long long v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// Block sum of a 64-bit value, returned to every thread.
+__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, TruncSmem& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum_u64(v);
+  __syncthreads();  // earlier readers of wtot / bc are done
+  if (lane == 0) sm.wtot[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long t = lane < kTWarps ? sm.wtot[lane] : 0ull;
+    t = warp_sum_u64(t);
+    if (lane == 0) sm.bc = t;
+  }
+  __syncthreads();
+  return sm.bc;
+}
+
+// Block inclusive scan of a 64-bit value in thread order; *total gets the sum.
+__device__ __forceinline__ unsigned long long block_incl_scan_u64(unsigned long long v, TruncSmem& sm,
+                                                                  unsigned long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long incl = warp_incl_scan_u64(v, lane);
+  __syncthreads();
+  if (lane == 31) sm.wtot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const unsigned long long t = lane < kTWarps ? sm.wtot[lane] : 0ull;
+    const unsigned long long ti = warp_incl_scan_u64(t, lane);
+    if (lane < kTWarps) sm.wtot[lane] = ti - t;  // exclusive offsets of the warps
+    if (lane == kTWarps - 1) sm.bc = ti;
+  }
+  __syncthreads();
+  *total = sm.bc;
+  return incl + sm.wtot[warp];
+}
+
+// One radix pass: sm.hist[d] = total weight of the eligible elements whose key
+// matches `prefix` under `pmask` and whose digit (key >> shift) & 255 is d.
+// kCount: every weight is 1.
+template <class E, bool kCount, class Elig, class Wt>
+__device__ void hist_pass(const typename E::Raw* row, int V, bool aligned, uint32_t prefix, uint32_t pmask,
+                          int shift, Elig elig, Wt wt, TruncSmem& sm) {
+  constexpr int KB = 8 * E::ES;
+  constexpr int PV = E::PV;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long* ph = sm.ph[warp];
+  __syncthreads();  // readers of the previous pass's histograms are done
+  for (int b = lane; b < 256; b += 32) ph[b] = 0ull;
+  __syncwarp();
+  const int nitem = aligned ? V / PV : V;
+  const int per = aligned ? PV : 1;
+  for (int base = warp * 32; base < nitem; base += kTThreads * kTUnroll) {
+    uint4 raw[kTUnroll];
+#pragma unroll
+    for (int u = 0; u < kTUnroll; ++u) {
+      const int i = base + u * kTThreads + lane;
+      raw[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (i < nitem) {
+        if (aligned)
+          raw[u] = __ldcg(reinterpret_cast<const uint4*>(row) + i);
+        else
+          raw[u].x = (uint32_t)__ldcg(row + i);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kTUnroll; ++u) {
+      const int i = base + u * kTThreads + lane;
+      if (base + u * kTThreads >= nitem) break;  // warp-uniform
+      const bool valid = i < nitem;
+      float x[PV];
+#pragma unroll
+      for (int j = 0; j < PV; ++j) x[j] = -INFINITY;
+      if (valid) {
+        if (aligned)
+          E::unpack(raw[u], x);
+        else
+          x[0] = E::to_f32((typename E::Raw)raw[u].x);
+      }
+#pragma unroll
+      for (int j = 0; j < PV; ++j) {
+        if (j >= per) break;  // warp-uniform
+        const int v = aligned ? i * PV + j : i;
+        const uint32_t key = order_key<KB>(x[j]);
+        const bool on = valid && (key & pmask) == prefix && elig(v, key);
+        const unsigned long long w = on ? (kCount ? 1ull : wt(x[j])) : 0ull;
+        const uint32_t digit = (key >> shift) & 255u;
+        if constexpr (kCount) {
+          // lanes with equal digits: the lowest adds the group's count
+          const unsigned grp = __match_any_sync(kFull, on ? digit : 0x100u);
+          if (on && lane == __ffs(grp) - 1) atomicAdd(&ph[digit], (unsigned long long)__popc(grp));
+        } else if (w) {
+          atomicAdd(&ph[digit], w);  // the warp's own histogram: conflicts only within the warp
+        }
+      }
+    }
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < 256; b += kTThreads) {
+    unsigned long long t = 0;
+#pragma unroll
+    for (int w = 0; w < kTWarps; ++w) t += sm.ph[w][b];
+    sm.hist[b] = t;
+  }
+  __syncthreads();
+}
+
+// Radix select, descending: the key thr of the element at which the running
+// weight, in ranking order over the eligible elements, first reaches `need`
+// (need >= 1).  *above gets the weight of eligible elements with larger keys
+// (< need); the rest, need - *above, is still needed inside the key thr.
+// Returns false if the eligible weight is below need.
+template <class E, bool kCount, class Elig, class Wt>
+__device__ bool radix_select(const typename E::Raw* row, int V, bool aligned, unsigned long long need, Elig elig,
+                             Wt wt, TruncSmem& sm, uint32_t* thr, unsigned long long* above) {
+  constexpr int KB = 8 * E::ES;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t prefix = 0, pmask = 0;
+  unsigned long long abv = 0;
+  for (int shift = KB - 8; shift >= 0; shift -= 8) {
+    hist_pass<E, kCount>(row, V, aligned, prefix, pmask, shift, elig, wt, sm);
+    if (warp == 0) {
+      // lane l scans bins 255 - 8l down to 248 - 8l: lanes in descending key order
+      unsigned long long c[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = sm.hist[255 - 8 * lane - j];
+        tot += c[j];
+      }
+      const unsigned long long rem = need - abv;
+      const unsigned long long incl = warp_incl_scan_u64(tot, lane);
+      const unsigned long long excl = incl - tot;
+      const bool mine = excl < rem && rem <= incl;
+      if (mine) {
+        unsigned long long run = excl;
+        int b = 255 - 8 * lane - 7;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (run + c[j] >= rem) {
+            b = 255 - 8 * lane - j;
+            break;
+          }
+          run += c[j];
+        }
+        sm.bin = b;
+        sm.bc = run;
+      }
+      if (__ballot_sync(kFull, mine) == 0u && lane == 0) sm.bin = -1;
+    }
+    __syncthreads();
+    const int b = sm.bin;
+    const unsigned long long run = sm.bc;
+    if (b < 0) return false;
+    abv += run;
+    prefix |= (uint32_t)b << shift;
+    pmask |= 0xFFu << shift;
+  }
+  *thr = prefix;
+  *above = abv;
+  return true;
+}
+
+// Index of the need-th (1-based) eligible element with key thr, in index
+// order; V if there are fewer.
+template <class E, class Elig>
+__device__ int tie_index(const typename E::Raw* row, int V, bool aligned, uint32_t thr, unsigned long long need,
+                         Elig elig, TruncSmem& sm) {
+  constexpr int KB = 8 * E::ES;
+  constexpr int PV = E::PV;
+  const int per = aligned ? PV : 1;
+  const int tile = kTThreads * per;
+  unsigned long long running = 0;
+  for (int base = 0; base < V; base += tile) {
+    const int v0 = base + threadIdx.x * per;
+    float x[PV];
+#pragma unroll
+    for (int j = 0; j < PV; ++j) x[j] = -INFINITY;
+    if (aligned) {
+      if (v0 < V) E::unpack(__ldcg(reinterpret_cast<const uint4*>(row + v0)), x);
+    } else if (v0 < V) {
+      x[0] = E::to_f32(__ldcg(row + v0));
+    }
+    unsigned long long c = 0;
+#pragma unroll
+    for (int j = 0; j < PV; ++j)
+      if (j < per && v0 + j < V) {
+        const uint32_t key = order_key<KB>(x[j]);
+        if (key == thr && elig(v0 + j, key)) ++c;
+      }
+    unsigned long long total;
+    const unsigned long long incl = block_incl_scan_u64(c, sm, &total);
+    if (running + total >= need) {
+      const unsigned long long before = running + incl - c;
+      if (c > 0 && before < need && running + incl >= need) {
+        unsigned long long k = need - before;
+#pragma unroll
+        for (int j = 0; j < PV; ++j)
+          if (j < per && v0 + j < V) {
+            const uint32_t key = order_key<KB>(x[j]);
+            if (key == thr && elig(v0 + j, key) && --k == 0) sm.tie = v0 + j;
+          }
+      }
+      __syncthreads();
+      const int t = sm.tie;
+      __syncthreads();
+      return t;
+    }
+    running += total;
+  }
+  return V;
+}
+
+template <class E>
+__global__ void __launch_bounds__(kTThreads, 2) truncate_kernel(const __grid_constant__ TruncParams P) {
+  __shared__ TruncSmem sm;
+  using Raw = typename E::Raw;
+  constexpr int KB = 8 * E::ES;
+  constexpr int PV = E::PV;
+  const int V = P.V;
+  const bool al = P.aligned != 0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool do_k = P.top_k > 0 && P.top_k < V;
+  const bool do_p = P.top_p < 1.0f;
+  const float s = P.s;
+  for (int row = blockIdx.x; row < P.rows; row += gridDim.x) {
+    const Raw* zin = reinterpret_cast<const Raw*>(P.in) + (long long)row * V;
+    Raw* zout = reinterpret_cast<Raw*>(P.out) + (long long)row * V;
+
+    // ---- row maximum and NaN check (brings the row into L2) ----
+    float mx = -INFINITY;
+    int nan = 0;
+    for_each_elem<E>(zin, V, al, [&](int, float x) {
+      mx = fmaxf(mx, x);
+      nan |= (x != x);
+    });
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    nan = __any_sync(kFull, nan);
+    __syncthreads();
+    if (lane == 0) {
+      sm.wmax[warp] = mx;
+      sm.wnan[warp] = nan;
+    }
+    __syncthreads();
+    float M = -INFINITY;
+    int bad = 0;
+    for (int w = 0; w < kTWarps; ++w) {
+      M = fmaxf(M, sm.wmax[w]);
+      bad |= sm.wnan[w];
+    }
+    bad |= !(M > -INFINITY && M < INFINITY);
+
+    // ---- top-k: key thr1, ties kept up to index tie1 ----
+    uint32_t thr1 = 0;
+    int tie1 = V;
+    bool ok = !bad;
+    if (ok && do_k) {
+      unsigned long long above = 0;
+      ok = radix_select<E, true>(
+          zin, V, al, (unsigned long long)P.top_k, [](int, uint32_t) { return true; },
+          [](float) { return 1ull; }, sm, &thr1, &above);
+      if (ok) tie1 = tie_index<E>(zin, V, al, thr1, (unsigned long long)P.top_k - above,
+                                  [](int, uint32_t) { return true; }, sm);
+    }
+    auto kept1 = [&](int v, uint32_t key) { return key > thr1 || (key == thr1 && v <= tie1); };
+
+    // ---- top-p over the top-k set: key thr2, ties kept up to index tie2 ----
+    uint32_t thr2 = 0;
+    int tie2 = V;
+    if (ok && do_p) {
+      unsigned long long z = 0;
+      for_each_elem<E>(zin, V, al, [&](int v, float x) {
+        if (kept1(v, order_key<KB>(x))) z += fixed_mass(x, M, s);
+      });
+      z = block_sum_u64(z, sm);
+      unsigned long long tau = (unsigned long long)ceil((double)P.top_p * (double)z);
+      if (tau == 0ull) tau = 1ull;
+      unsigned long long above = 0;
+      ok = radix_select<E, false>(zin, V, al, tau, kept1, [&](float x) { return fixed_mass(x, M, s); }, sm,
+                                  &thr2, &above);
+      if (ok) {
+        // tied tokens share one mass: keep the first ceil(rest / w) of them
+        const unsigned long long w = fixed_mass(key_value<KB>(thr2), M, s);
+        const unsigned long long rest = tau - above;
+        const unsigned long long n = w ? (rest + w - 1) / w : 1ull;
+        tie2 = tie_index<E>(zin, V, al, thr2, n, kept1, sm);
+      }
+    }
+    // a row with NaN or infinite logits (or none finite) is copied unchanged
+    if ((bad || !ok) && threadIdx.x == 0 && P.status) atomicOr(P.status, kBadLogits);
+    const bool cut = ok && (do_k || do_p);
+    auto keep = [&](int v, float x) {
+      if (!cut) return true;
+      const uint32_t key = order_key<KB>(x);
+      return kept1(v, key) && (!do_p || key > thr2 || (key == thr2 && v <= tie2));
+    };
+
+    // ---- write pass ----
+    if (al) {
+      const uint4* r4 = reinterpret_cast<const uint4*>(zin);
+      uint4* o4 = reinterpret_cast<uint4*>(zout);
+      const int nvec = V / PV;
+      for (int i0 = threadIdx.x; i0 < nvec; i0 += kTThreads * kTUnroll) {
+        uint4 raw[kTUnroll];
+#pragma unroll
+        for (int u = 0; u < kTUnroll; ++u) {
+          const int i = i0 + u * kTThreads;
+          raw[u] = i < nvec ? __ldcg(r4 + i) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < kTUnroll; ++u) {
+          const int i = i0 + u * kTThreads;
+          if (i >= nvec) break;
+          const uint4 w = raw[u];
+          float x[PV];
+          E::unpack(w, x);
+          uint32_t wd[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int k = 0; k < PV; ++k) {
+            if (keep(i * PV + k, x[k])) continue;
+            if constexpr (PV == 8) {  // bf16: element 2j in the low half of word j
+              wd[k >> 1] = (k & 1) ? ((wd[k >> 1] & 0x0000FFFFu) | 0xFF800000u) : ((wd[k >> 1] & 0xFFFF0000u) | 0xFF80u);
+            } else {
+              wd[k] = 0xFF800000u;
+            }
+          }
+          __stcs(o4 + i, make_uint4(wd[0], wd[1], wd[2], wd[3]));
+        }
+      }
+    } else {
+      for (int v = threadIdx.x; v < V; v += kTThreads) {
+        const Raw r = __ldcg(zin + v);
+        zout[v] = keep(v, E::to_f32(r)) ? r : E::kNegInf;
+      }
+    }
+    __syncthreads();  // shared state is reused by the next row
+  }
+}
+
+}  // namespace ssv

@@ -32,7 +32,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("spec_verify", "spec_overlap", "spec_e2e_tv_fwd_bwd", "spec_status_string",
                  "spec_verify_workspace_bytes", "spec_overlap_workspace_bytes", "spec_e2e_tv_workspace_bytes",
-                 "spec_diagnostics", "spec_diagnostics_workspace_bytes"):
+                 "spec_diagnostics", "spec_diagnostics_workspace_bytes", "spec_truncate_logits"):
         assert want in names
 
 
@@ -96,3 +96,10 @@ def test_argument_validation_without_gpu(L):
                               None) == 1
     assert L.spec_diagnostics(fake, fake, 1, 2, 2, 2, 10, 1.0, fake, None, None, None, None, None, ws, 8, None) == 1
     assert L.spec_diagnostics(None, None, 1, 0, 2, 2, 10, 1.0, None, None, None, None, None, None, None, 0, None) == 0
+    # truncation: top_k >= 0, top_p in (0, 1], T > 0 when top-p is on; no rows is a no-op
+    assert L.spec_truncate_logits(fake, fake, 1, 2, 10, 1.0, -1, 1.0, None, None) == 1
+    assert L.spec_truncate_logits(fake, fake, 1, 2, 10, 1.0, 3, 0.0, None, None) == 1
+    assert L.spec_truncate_logits(fake, fake, 1, 2, 10, 1.0, 3, 1.5, None, None) == 1
+    assert L.spec_truncate_logits(fake, fake, 1, 2, 10, 0.0, 3, 0.5, None, None) == 1
+    assert L.spec_truncate_logits(fake, ctypes.c_void_p(0x1004), 1, 2, 10, 1.0, 3, 1.0, None, None) == 1
+    assert L.spec_truncate_logits(None, None, 1, 0, 10, 1.0, 3, 0.5, None, None) == 0
