@@ -572,3 +572,71 @@ def speedup_estimate(alpha, t_ar, t_draft, t_verify, t_overhead):
     on Speculative Decoding 与 MTP, section 7; this reading reproduces both of
     its printed examples."""
     return expected_emitted(alpha) * t_ar / (t_draft + t_verify + t_overhead)
+
+
+# ---------------------------------------------------------------------------
+# Verify-length scheduling over prefix survivals and a throughput table
+# ---------------------------------------------------------------------------
+
+# Relative gap below which two candidate throughputs count as a tie: another
+# implementation's summation order may then pick the other one.
+NEAR_SCHED = 1e-9
+
+
+@dataclass
+class ScheduleResult:
+    lengths: np.ndarray  # int [R]: verify length l_r of every request
+    theta: float         # tau * SPS(B) at the choice
+    tau: float           # expected produced tokens
+    batch: int           # B = sum_r (1 + l_r)
+    near: bool           # another total length is within NEAR_SCHED of theta
+
+
+def schedule_lengths(survival, sps):
+    """Verify lengths that maximise the expected throughput.
+
+    Bebop/DSpark blog, section "DSpark 的第二块拼图" and the equations after it:
+    request r verifying l_r drafted tokens adds 1 + l_r tokens to the target
+    batch, B = sum_r (1 + l_r); it produces tau_r = 1 + sum_{j<=l_r} a_{r,j}
+    tokens in expectation, a_{r,j} the prefix survival; the throughput is
+    Theta = (sum_r tau_r) * SPS(B), SPS(B) the decode steps per second at
+    batch B (a measured table with steps and cliffs); the scheduler takes the
+    argmax over l_1..l_R.
+
+    survival: [R, L] a_{r,j} for j = 1..L (non-increasing in j as a product of
+    per-position acceptances; the running minimum along j is used, which
+    changes nothing for such input); sps: SPS(B) for B = 0, 1, ...,
+    at least R * (1 + L).
+
+    For a fixed B the best tau takes the B - R largest survivals (a row's
+    survivals are non-increasing, so the chosen ones form a prefix of every
+    row); the search is then over B.  Ties: equal survivals are taken in
+    (row, position) order and equal throughputs keep the smaller B.
+    """
+    a = np.asarray(survival, dtype=np.float64)
+    R, L = a.shape
+    s = np.asarray(sps, dtype=np.float64)
+    if s.shape[0] < R * (1 + L) + 1:
+        raise ValueError("sps must cover B = 0 .. R * (1 + L)")
+    a = np.minimum.accumulate(np.maximum(a, 0.0), axis=1)
+    flat = a.reshape(-1)
+    order = np.lexsort((np.arange(R * L), -flat))  # survival descending, then (row, position)
+    vals = flat[order]
+    best_m, best = 0, None
+    thetas = []
+    run = 0.0
+    for m in range(R * L + 1):
+        if m > 0:
+            run += vals[m - 1]
+        th = (R + run) * s[R + m]
+        thetas.append(th)
+        if best is None or th > best:
+            best, best_m = th, m
+    lengths = np.zeros(R, dtype=np.int64)
+    for idx in order[:best_m]:
+        lengths[idx // L] += 1
+    tau = R + float(np.sum(vals[:best_m]))
+    th = np.asarray(thetas)
+    others = np.delete(th, best_m)
+    near = bool(others.size and np.any(np.abs(others - best) <= NEAR_SCHED * max(abs(best), 1e-300)))
+    return ScheduleResult(lengths, float(best), tau, int(R + best_m), near)

@@ -649,3 +649,74 @@ def test_truncation_invariants_random_rows():
             ranked_kept = [v for v in rank if kept[v]]
             assert sum(m[v] for v in ranked_kept) >= tp
             assert sum(m[v] for v in ranked_kept[:-1]) < tp
+
+
+# ---------------------------------------------------------------------------
+# verify-length scheduling
+# ---------------------------------------------------------------------------
+
+def test_schedule_hand_example():
+    # R = 2, L = 2, a = [[0.9, 0.5], [0.6, 0.1]], SPS(2..6) = 100, 95, 80, 78, 60.
+    # Taking the largest survivals first: B = 2 -> 2 * 100 = 200; B = 3 -> 2.9 * 95 = 275.5;
+    # B = 4 -> 3.5 * 80 = 280; B = 5 -> 4.0 * 78 = 312; B = 6 -> 4.1 * 60 = 246.
+    r = so.schedule_lengths([[0.9, 0.5], [0.6, 0.1]], [0, 0, 100, 95, 80, 78, 60])
+    assert r.lengths.tolist() == [2, 1]
+    assert r.theta == pytest.approx(312.0, rel=1e-15) and r.tau == pytest.approx(4.0) and r.batch == 5
+    assert not r.near
+
+
+def _survivals(rng, R, L):
+    c = rng.uniform(0.3, 1.0, size=(R, L))
+    return np.cumprod(c, axis=1)
+
+
+def _step_sps(rng, n):
+    # a decreasing throughput curve with cliffs at random batch sizes
+    base = 1000.0 / (1.0 + np.arange(n) / rng.uniform(2.0, 8.0))
+    cliffs = rng.choice(np.arange(1, n), size=min(3, n - 1), replace=False)
+    for c in cliffs:
+        base[c:] *= rng.uniform(0.6, 0.95)
+    return base
+
+
+def test_schedule_brute_force_tiny():
+    rng = np.random.default_rng(21)
+    for trial in range(200):
+        R = int(rng.integers(1, 4))
+        L = int(rng.integers(1, 4))
+        a = _survivals(rng, R, L)
+        sps = _step_sps(rng, R * (1 + L) + 1)
+        r = so.schedule_lengths(a, sps)
+        best, best_b = -1.0, None
+        for ls in itertools.product(range(L + 1), repeat=R):
+            B = sum(1 + l for l in ls)
+            tau = sum(1 + a[i, :l].sum() for i, l in enumerate(ls))
+            th = tau * sps[B]
+            if th > best * (1 + 1e-12):
+                best, best_b = th, B
+            elif abs(th - best) <= 1e-12 * best and B < best_b:
+                best_b = B
+        assert r.theta == pytest.approx(best, rel=1e-12)
+        ls = r.lengths
+        B = int(sum(1 + l for l in ls))
+        tau = sum(1 + a[i, :l].sum() for i, l in enumerate(ls))
+        assert B == r.batch and tau * sps[B] == pytest.approx(best, rel=1e-12)
+        if not r.near:
+            assert B == best_b
+
+
+def test_schedule_closed_forms():
+    rng = np.random.default_rng(22)
+    a = _survivals(rng, 5, 4)
+    flat = np.full(5 * 5 + 1, 7.0)  # constant SPS: every positive survival pays
+    r = so.schedule_lengths(a, flat)
+    assert r.lengths.tolist() == [4] * 5 and r.batch == 25
+    assert r.tau == pytest.approx(5 + a.sum())
+    cliff = np.zeros(26)
+    cliff[: 5 + 1] = 10.0  # nothing beyond one token per request runs
+    r = so.schedule_lengths(a, cliff)
+    assert r.lengths.tolist() == [0] * 5 and r.batch == 5 and r.theta == 50.0
+    # non-monotone input: the running minimum is what counts
+    r1 = so.schedule_lengths([[0.5, 0.9]], [0, 10, 9, 8])
+    r2 = so.schedule_lengths([[0.5, 0.5]], [0, 10, 9, 8])
+    assert r1.lengths.tolist() == r2.lengths.tolist() and r1.theta == r2.theta
