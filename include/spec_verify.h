@@ -259,6 +259,34 @@ spec_status_t spec_truncate_logits(const void* logits, void* out,
                                    uint32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Verify-length scheduling.
+ *
+ * "读 Qwen Bebop 与 DeepSeek DSpark", section "DSpark 的第二块拼图：置信度调度验证
+ * 长度": request r verifying l_r drafted tokens adds 1 + l_r tokens to the
+ * target batch, B = sum_r (1 + l_r), and produces tau_r = 1 +
+ * sum_{j<=l_r} a_{r,j} tokens in expectation; the lengths maximise
+ * Theta = (sum_r tau_r) * SPS(B), SPS(B) the engine's decode steps per second
+ * at batch B.  For a fixed B the best choice takes the B - R largest
+ * survivals; equal survivals are taken in (row, position) order and equal
+ * Theta keeps the smaller B.
+ *
+ * survival   [R, L] float32: a_{r,j}, j = 1..L, non-increasing in j (the
+ *            prefix_survival output of spec_overlap is such a table); the
+ *            running minimum along j is used; NaN counts as 0 and sets
+ *            SPEC_DEV_BAD_LOGITS.
+ * sps        [sps_len] float32 >= 0: SPS(B) for B = 0 .. sps_len - 1,
+ *            sps_len >= R * (1 + L) + 1.
+ * lengths    [R] int32 (written): l_r in [0, L].
+ * objective  [2] float32 or NULL: {Theta, tau} at the choice.
+ * Limits: 1 <= L <= 64 and R * L <= 16384 (SPEC_ERR_UNSUPPORTED beyond).
+ * One CTA; sums in fp64.
+ */
+spec_status_t spec_schedule_lengths(const float* survival, int R, int L,
+                                    const float* sps, int sps_len,
+                                    int32_t* lengths, float* objective,
+                                    uint32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Launch shape the library picks for a verify sweep over `units` (row,
  * position) pairs of V logits (for benchmarks and diagnostics): CTAs per
  * cluster, threads per CTA, dynamic shared memory per CTA, the number of

@@ -14,7 +14,9 @@ Entry points (same names as the C ABI, see include/spec_verify.h):
 * ``diagnostics``     -- alpha, target entropy, cross-entropy, KL and the
                          target-only acceptance p(argmax q) per position;
 * ``truncate_logits`` -- top-k / top-p truncation, to apply identically to
-                         target and draft logits before ``verify``.
+                         target and draft logits before ``verify``;
+* ``schedule_lengths`` -- verify lengths maximising tau * SPS(B) over prefix
+                         survivals and a throughput table.
 """
 
 from __future__ import annotations
@@ -27,7 +29,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "SpecError", "lib", "verify", "overlap", "e2e_tv_fwd_bwd", "diagnostics", "truncate_logits", "launch_shape",
+    "SpecError", "lib", "verify", "overlap", "e2e_tv_fwd_bwd", "diagnostics", "truncate_logits", "schedule_lengths", "launch_shape",
     "set_launch_override", "VerifyOutput", "OverlapOutput", "E2EOutput", "DiagOutput", "HostVerifier",
     "DEV_BAD_TOKEN", "DEV_BAD_LOGITS", "DEV_BAD_UNIFORM", "DEV_TIMEOUT", "DEV_EMPTY_RESIDUAL",
     "SPEC_OK", "SPEC_ERR_INVALID_ARG", "SPEC_ERR_UNSUPPORTED", "SPEC_ERR_CUDA",
@@ -83,6 +85,8 @@ def lib():
     L.spec_diagnostics.argtypes = [vp, vp, i32, i32, i32, i32, i32, f32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.spec_truncate_logits.restype = i32
     L.spec_truncate_logits.argtypes = [vp, vp, i32, i32, i32, f32, i32, f32, vp, vp]
+    L.spec_schedule_lengths.restype = i32
+    L.spec_schedule_lengths.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp]
     L.spec_launch_shape.restype = i32
     L.spec_launch_shape.argtypes = [i32, i32, i32] + [ctypes.POINTER(i32)] * 5
     L.spec_set_launch_override.restype = None
@@ -361,6 +365,30 @@ def truncate_logits(logits: torch.Tensor, temperature: float, top_k: int = 0, to
                                 int(top_k), float(top_p), _ptr(status), sh)
     _check(st, "spec_truncate_logits")
     return out
+
+
+# ---------------------------------------------------------------------------
+# verify-length scheduling
+# ---------------------------------------------------------------------------
+
+def schedule_lengths(survival: torch.Tensor, sps: torch.Tensor, *, status: Optional[torch.Tensor] = None,
+                     stream: Optional[torch.cuda.Stream] = None):
+    """Verify lengths l_r maximising tau * SPS(B) for prefix survivals
+    ``survival`` [R, L] (float32, e.g. ``overlap(...).prefix_survival``) and
+    a throughput table ``sps`` [>= R * (1 + L) + 1] (float32, SPS(B) at index
+    B).  Returns (lengths int32 [R], objective float32 [2] = {Theta, tau})."""
+    L_ = lib()
+    _need(survival, "survival", dtype=torch.float32)
+    _need(sps, "sps", dtype=torch.float32, device=survival.device)
+    R, L = survival.shape
+    dev = survival.device
+    lengths = torch.empty((R,), dtype=torch.int32, device=dev)
+    objective = torch.empty((2,), dtype=torch.float32, device=dev)
+    sh, _ = _stream_handle(stream, dev)
+    st = L_.spec_schedule_lengths(_ptr(survival), R, L, _ptr(sps), sps.numel(), _ptr(lengths), _ptr(objective),
+                                  _ptr(status), sh)
+    _check(st, "spec_schedule_lengths")
+    return lengths, objective
 
 
 # ---------------------------------------------------------------------------

@@ -14,6 +14,7 @@
 #include "spec_verify.h"
 #include "sweep.cuh"
 #include "truncate.cuh"
+#include "schedule.cuh"
 
 namespace {
 
@@ -613,6 +614,40 @@ spec_status_t spec_truncate_logits(const void* logits, void* out, spec_dtype_t d
     ssv::truncate_kernel<Bf16><<<grid, ssv::kTThreads, 0, st>>>(P);
   else
     ssv::truncate_kernel<F32><<<grid, ssv::kTThreads, 0, st>>>(P);
+  return from_cuda(cudaGetLastError());
+}
+
+spec_status_t spec_schedule_lengths(const float* survival, int R, int L, const float* sps, int sps_len,
+                                    int32_t* lengths, float* objective, uint32_t* dev_status, void* stream) {
+  if (R < 0 || L < 1 || L > kMaxK || sps_len < 0) return SPEC_ERR_INVALID_ARG;
+  if (R == 0) return SPEC_OK;
+  if ((long long)sps_len < (long long)R * (1 + L) + 1) return SPEC_ERR_INVALID_ARG;
+  if (!survival || !sps || !lengths) return SPEC_ERR_INVALID_ARG;
+  if ((long long)R * L > ssv::kSchedMaxItems) return SPEC_ERR_UNSUPPORTED;
+  int N = 1;
+  while (N < R * L) N <<= 1;
+  const size_t smem = (size_t)N * sizeof(unsigned long long) + (((size_t)R * sizeof(int) + 15) & ~size_t(15));
+  static std::atomic<uint64_t> prepared{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(prepared.load(std::memory_order_acquire) & bit)) {
+    const size_t most = (size_t)ssv::kSchedMaxItems * (sizeof(unsigned long long) + sizeof(int));
+    e = cudaFuncSetAttribute(ssv::schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
+    if (e != cudaSuccess) return SPEC_ERR_CUDA;
+    prepared.fetch_or(bit, std::memory_order_release);
+  }
+  ssv::SchedParams P = {};
+  P.surv = survival;
+  P.R = R;
+  P.L = L;
+  P.sps = sps;
+  P.nsps = sps_len;
+  P.lengths = lengths;
+  P.objective = objective;
+  P.status = dev_status;
+  ssv::schedule_kernel<<<1, ssv::kSThreads, smem, static_cast<cudaStream_t>(stream)>>>(P);
   return from_cuda(cudaGetLastError());
 }
 

@@ -32,7 +32,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for want in ("spec_verify", "spec_overlap", "spec_e2e_tv_fwd_bwd", "spec_status_string",
                  "spec_verify_workspace_bytes", "spec_overlap_workspace_bytes", "spec_e2e_tv_workspace_bytes",
-                 "spec_diagnostics", "spec_diagnostics_workspace_bytes", "spec_truncate_logits"):
+                 "spec_diagnostics", "spec_diagnostics_workspace_bytes", "spec_truncate_logits",
+                 "spec_schedule_lengths"):
         assert want in names
 
 
@@ -103,3 +104,9 @@ def test_argument_validation_without_gpu(L):
     assert L.spec_truncate_logits(fake, fake, 1, 2, 10, 0.0, 3, 0.5, None, None) == 1
     assert L.spec_truncate_logits(fake, ctypes.c_void_p(0x1004), 1, 2, 10, 1.0, 3, 1.0, None, None) == 1
     assert L.spec_truncate_logits(None, None, 1, 0, 10, 1.0, 3, 0.5, None, None) == 0
+    # scheduling: 1 <= L <= 64, a table covering B = 0 .. R(1 + L), R * L <= 16384
+    assert L.spec_schedule_lengths(fake, 2, 0, fake, 100, fake, None, None, None) == 1
+    assert L.spec_schedule_lengths(fake, 2, 65, fake, 1000, fake, None, None, None) == 1
+    assert L.spec_schedule_lengths(fake, 2, 3, fake, 8, fake, None, None, None) == 1
+    assert L.spec_schedule_lengths(fake, 16385, 1, fake, 40000, fake, None, None, None) == 2
+    assert L.spec_schedule_lengths(None, 0, 3, None, 0, None, None, None, None) == 0
