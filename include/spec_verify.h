@@ -61,6 +61,7 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
 #define SPEC_DEV_BAD_UNIFORM 4u    /* a uniform outside [0, 1) */
 #define SPEC_DEV_TIMEOUT 8u        /* a bounded wait inside a kernel gave up */
 #define SPEC_DEV_EMPTY_RESIDUAL 16u /* rejection with zero residual mass: drawn from p */
+#define SPEC_DEV_BAD_OFFSETS 32u   /* ragged verify: row offsets rejected, nothing computed */
 
 /* Version of this ABI (bumped on any signature change). */
 int spec_abi_version(void);
@@ -106,6 +107,46 @@ spec_status_t spec_verify(const void* target_logits, const void* draft_logits,
                           float* alpha_out, uint32_t* dev_status,
                           void* workspace, size_t workspace_bytes,
                           void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Ragged verify: every row verifies its own number of drafted tokens, in
+ * flattened tensors.
+ *
+ * "读 Qwen Bebop 与 DeepSeek DSpark", section "DSpark 真正厉害的地方：它为生产系统
+ * 做了让步" (variable-length verification tokens of all requests are
+ * flattened, and a marker tensor carries which request each belongs to) and
+ * section "DSpark 的第二块拼图" (per-request verify lengths l_r); the
+ * acceptance, correction and bonus rules are those of spec_verify.
+ *
+ * row_offsets  [B + 1] int32, device: row r owns flattened target rows
+ *              [row_offsets[r], row_offsets[r+1]) = its l_r drafted positions
+ *              then its bonus position; row_offsets[0] = 0,
+ *              row_offsets[B] = units, 0 <= l_r <= 64.  Offsets that break
+ *              this set SPEC_DEV_BAD_OFFSETS and nothing is computed.
+ * units        the number of flattened target rows (host value).
+ * target_logits [units, V] dtype; draft_logits [units - B, V] dtype, drafted
+ *              row of (r, j) at row_offsets[r] - r + j (NULL if units == B).
+ * draft_tokens, u_accept [units - B]: same flattened order as the drafts.
+ * u_final      [B].  temperature T > 0.
+ * out_tokens   [units] int32: row r's n accepted drafts, then the correction
+ *              or bonus token, then -1, at row_offsets[r] ...
+ * n_accepted   [B]; alpha_out [units - B] float32 or NULL.
+ * The workspace follows the common rules (zero before first use, zero
+ * after every call).  The per-unit marker (row, position, bonus) is built in
+ * the workspace by the call.
+ */
+size_t spec_verify_ragged_workspace_bytes(int B, int units, int V);
+
+spec_status_t spec_verify_ragged(const void* target_logits,
+                                 const void* draft_logits, spec_dtype_t dtype,
+                                 int B, const int32_t* row_offsets, int units,
+                                 int V, float temperature,
+                                 const int32_t* draft_tokens,
+                                 const float* u_accept, const float* u_final,
+                                 int32_t* out_tokens, int32_t* n_accepted,
+                                 float* alpha_out, uint32_t* dev_status,
+                                 void* workspace, size_t workspace_bytes,
+                                 void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Allocation-free verify.  The pages have no counterpart: this entry point

@@ -9,6 +9,8 @@ Entry points (same names as the C ABI, see include/spec_verify.h):
 
 * ``verify``          -- batched draft/verify step (acceptance, residual
                          correction, bonus token, greedy at T == 0);
+* ``verify_ragged``   -- the same with a length of its own per row, over
+                         flattened tensors and row offsets;
 * ``overlap``         -- alpha = sum min(p, q), TV, prefix survival, E[tau];
 * ``e2e_tv_fwd_bwd``  -- E2E-TV loss and its draft-logit gradient;
 * ``diagnostics``     -- alpha, target entropy, cross-entropy, KL and the
@@ -29,9 +31,9 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "SpecError", "lib", "verify", "overlap", "e2e_tv_fwd_bwd", "diagnostics", "truncate_logits", "schedule_lengths", "launch_shape",
+    "SpecError", "lib", "verify", "verify_ragged", "overlap", "e2e_tv_fwd_bwd", "diagnostics", "truncate_logits", "schedule_lengths", "launch_shape",
     "set_launch_override", "VerifyOutput", "OverlapOutput", "E2EOutput", "DiagOutput", "HostVerifier",
-    "DEV_BAD_TOKEN", "DEV_BAD_LOGITS", "DEV_BAD_UNIFORM", "DEV_TIMEOUT", "DEV_EMPTY_RESIDUAL",
+    "DEV_BAD_TOKEN", "DEV_BAD_LOGITS", "DEV_BAD_UNIFORM", "DEV_TIMEOUT", "DEV_EMPTY_RESIDUAL", "DEV_BAD_OFFSETS",
     "SPEC_OK", "SPEC_ERR_INVALID_ARG", "SPEC_ERR_UNSUPPORTED", "SPEC_ERR_CUDA",
 ]
 
@@ -41,6 +43,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libspec_verify.so")
 SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED, SPEC_ERR_CUDA = 0, 1, 2, 3
 SPEC_F32, SPEC_BF16 = 0, 1
 DEV_BAD_TOKEN, DEV_BAD_LOGITS, DEV_BAD_UNIFORM, DEV_TIMEOUT, DEV_EMPTY_RESIDUAL = 1, 2, 4, 8, 16
+DEV_BAD_OFFSETS = 32
 
 _lib = None
 
@@ -87,6 +90,10 @@ def lib():
     L.spec_truncate_logits.argtypes = [vp, vp, i32, i32, i32, f32, i32, f32, vp, vp]
     L.spec_schedule_lengths.restype = i32
     L.spec_schedule_lengths.argtypes = [vp, i32, i32, vp, i32, vp, vp, vp, vp]
+    L.spec_verify_ragged_workspace_bytes.restype = sz
+    L.spec_verify_ragged_workspace_bytes.argtypes = [i32, i32, i32]
+    L.spec_verify_ragged.restype = i32
+    L.spec_verify_ragged.argtypes = [vp, vp, i32, i32, vp, i32, i32, f32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.spec_launch_shape.restype = i32
     L.spec_launch_shape.argtypes = [i32, i32, i32] + [ctypes.POINTER(i32)] * 5
     L.spec_set_launch_override.restype = None
@@ -212,6 +219,43 @@ def verify(target: torch.Tensor, draft: Optional[torch.Tensor], draft_tokens: to
                        _ptr(out.n_accepted), _ptr(out.alpha), _ptr(out.status), _ptr(ws),
                        ws.numel() * ws.element_size(), sh)
     _check(st, "spec_verify")
+    return out
+
+
+def verify_ragged(target: torch.Tensor, draft: Optional[torch.Tensor], row_offsets: torch.Tensor,
+                  draft_tokens: Optional[torch.Tensor], u_accept: Optional[torch.Tensor], u_final: torch.Tensor,
+                  temperature: float, *, want_alpha: bool = True, workspace: Optional[torch.Tensor] = None,
+                  stream: Optional[torch.cuda.Stream] = None) -> VerifyOutput:
+    """Verify with a length of its own per row (see spec_verify_ragged in
+    the C header).  target [units, V]: row r's drafted positions then its
+    bonus position at rows row_offsets[r] .. row_offsets[r+1]-1; draft
+    [units - B, V], draft_tokens and u_accept [units - B] in the same
+    flattened order; row_offsets int32 [B + 1]; u_final [B].  Returns tokens
+    [units] (flattened like target), n_accepted [B], alpha [units - B]."""
+    L = lib()
+    _need(target, "target")
+    units, V = target.shape
+    dev = target.device
+    _need(row_offsets, "row_offsets", dtype=torch.int32, device=dev)
+    B = row_offsets.numel() - 1
+    nd = units - B
+    _need(u_final, "u_final", dtype=torch.float32, shape=(B,), device=dev)
+    if nd > 0:
+        _need(draft, "draft", dtype=target.dtype, shape=(nd, V), device=dev)
+        _need(draft_tokens, "draft_tokens", dtype=torch.int32, shape=(nd,), device=dev)
+        _need(u_accept, "u_accept", dtype=torch.float32, shape=(nd,), device=dev)
+    out = VerifyOutput(torch.empty((units,), dtype=torch.int32, device=dev),
+                       torch.empty((B,), dtype=torch.int32, device=dev),
+                       torch.empty((nd,), dtype=torch.float32, device=dev) if want_alpha and nd > 0 else None,
+                       torch.zeros((1,), dtype=torch.int32, device=dev))
+    sh, s = _stream_handle(stream, dev)
+    need = L.spec_verify_ragged_workspace_bytes(B, units, V)
+    ws = workspace if workspace is not None else _workspace(need, dev, s)
+    st = L.spec_verify_ragged(_ptr(target), _ptr(draft), _dtype_code(target), B, _ptr(row_offsets), units, V,
+                              float(temperature), _ptr(draft_tokens), _ptr(u_accept), _ptr(u_final),
+                              _ptr(out.tokens), _ptr(out.n_accepted), _ptr(out.alpha), _ptr(out.status), _ptr(ws),
+                              ws.numel() * ws.element_size(), sh)
+    _check(st, "spec_verify_ragged")
     return out
 
 

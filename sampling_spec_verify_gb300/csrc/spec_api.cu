@@ -286,6 +286,40 @@ DiagWs diag_ws(int B, int K) {
   return w;
 }
 
+// Ragged verify workspace: records and partials per unit, row counters and
+// row words, then the packed unit words and the offsets-rejected flag.
+struct RaggedWs {
+  size_t rec = 0, part = 0, cnt = 0, rej = 0, uinfo = 0, bad = 0, total = 0;
+};
+RaggedWs ragged_ws(int B, long long units) {
+  RaggedWs w;
+  w.rec = 0;
+  w.part = align256((size_t)units * sizeof(VerifyRecord));
+  w.cnt = w.part + part_bytes(units);
+  w.rej = w.cnt + align256((size_t)B * sizeof(uint32_t));
+  w.uinfo = w.rej + align256((size_t)B * sizeof(uint32_t));
+  w.bad = w.uinfo + align256((size_t)units * sizeof(uint32_t));
+  w.total = w.bad + 256;
+  return w;
+}
+
+// One thread per row: checks the row's offsets and writes its packed unit
+// words; any bad row sets the flag that makes the sweep return at once.
+__global__ void ragged_units_kernel(const int32_t* roff, int B, int units, uint32_t* uinfo, uint32_t* bad,
+                                    uint32_t* status) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int s0 = roff[b], s1 = roff[b + 1];
+  const int l = s1 - s0 - 1;
+  const bool ok = s0 >= 0 && s1 > s0 && l <= kMaxK && s1 <= units && (b > 0 || s0 == 0) && (b < B - 1 || s1 == units);
+  if (!ok) {
+    atomicOr(bad, 1u);
+    if (status) atomicOr(status, SPEC_DEV_BAD_OFFSETS);
+    return;
+  }
+  for (int k = 0; k <= l; ++k) uinfo[s0 + k] = ssv::pack_unit((uint32_t)b, (uint32_t)k, k == l);
+}
+
 bool dims_ok(int B, int K, int V) { return B >= 0 && K >= 0 && K <= kMaxK && V >= 1; }
 
 bool dtype_ok(spec_dtype_t dt) { return dt == SPEC_F32 || dt == SPEC_BF16; }
@@ -649,6 +683,76 @@ spec_status_t spec_schedule_lengths(const float* survival, int R, int L, const f
   P.status = dev_status;
   ssv::schedule_kernel<<<1, ssv::kSThreads, smem, static_cast<cudaStream_t>(stream)>>>(P);
   return from_cuda(cudaGetLastError());
+}
+
+size_t spec_verify_ragged_workspace_bytes(int B, int units, int V) {
+  if (B < 0 || units < B || V < 1) return 0;
+  return ragged_ws(B, units).total;
+}
+
+spec_status_t spec_verify_ragged(const void* target_logits, const void* draft_logits, spec_dtype_t dtype, int B,
+                                 const int32_t* row_offsets, int units, int V, float temperature,
+                                 const int32_t* draft_tokens, const float* u_accept, const float* u_final,
+                                 int32_t* out_tokens, int32_t* n_accepted, float* alpha_out, uint32_t* dev_status,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || units < B || V < 1 || !dtype_ok(dtype)) return SPEC_ERR_INVALID_ARG;
+  if ((long long)units > (long long)B * (kMaxK + 1)) return SPEC_ERR_INVALID_ARG;
+  if (!(temperature > 0.0f) || !std::isfinite(temperature)) return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  if (!target_logits || !row_offsets || !u_final || !out_tokens || !n_accepted || !workspace)
+    return SPEC_ERR_INVALID_ARG;
+  const bool drafted = units > B;
+  if (drafted && (!draft_logits || !draft_tokens || !u_accept)) return SPEC_ERR_INVALID_ARG;
+  const RaggedWs ws = ragged_ws(B, units);
+  if (workspace_bytes < ws.total || !aligned16(workspace)) return SPEC_ERR_INVALID_ARG;
+  const int es = elem_size(dtype);
+  Shape sh;
+  {
+    const spec_status_t r = shape_for_dt<ssv::kVerify>(dtype, units, V, 2, &sh);
+    if (r != SPEC_OK) return r;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(workspace);
+  uint32_t* uinfo = reinterpret_cast<uint32_t*>(w + ws.uinfo);
+  uint32_t* bad = reinterpret_cast<uint32_t*>(w + ws.bad);
+  ragged_units_kernel<<<(B + 255) / 256, 256, 0, st>>>(row_offsets, B, units, uinfo, bad, dev_status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  SweepParams P = {};
+  P.target = target_logits;
+  P.draft = draft_logits;
+  P.B = B;
+  P.K = kMaxK;
+  P.KT = kMaxK + 1;
+  P.V = V;
+  P.units = units;
+  P.S = sh.S;
+  P.L = sh.L;
+  P.nst = sh.nst;
+  P.rows = 2;
+  P.aligned = aligned16(target_logits) && (!draft_logits || aligned16(draft_logits)) && ((long long)V * es) % 16 == 0;
+  P.s = (float)(1.4426950408889634 / (double)temperature);
+  P.inv_t = (float)(1.0 / (double)temperature);
+  P.draft_tokens = draft_tokens;
+  P.u_accept = u_accept;
+  P.u_final = u_final;
+  P.out_tokens = out_tokens;
+  P.n_accepted = n_accepted;
+  P.alpha = alpha_out;
+  P.rec = reinterpret_cast<VerifyRecord*>(w + ws.rec);
+  P.part = reinterpret_cast<float*>(w + ws.part);
+  P.row_cnt = reinterpret_cast<uint32_t*>(w + ws.cnt);
+  P.rej = reinterpret_cast<uint32_t*>(w + ws.rej);
+  P.uinfo = uinfo;
+  P.roff = row_offsets;
+  P.ragbad = bad;
+  P.status = dev_status;
+  e = prepare_dt<ssv::kVerifyRagged>(dtype);
+  if (e == cudaSuccess) e = launch_sweep_dt<ssv::kVerifyRagged>(dtype, P, sh, st);
+  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  // the unit words and the flag are the only parts not left zero by the sweep
+  e = cudaMemsetAsync(w + ws.uinfo, 0, ws.total - ws.uinfo, st);
+  return from_cuda(e);
 }
 
 }  // extern "C"

@@ -52,8 +52,15 @@ constexpr uint32_t kRejBase = 128u;
 
 // kVerifyGrouped is kVerify with rows in groups of one row per cluster,
 // position-major inside a group (for at least as many rows as clusters).
+// kVerifyRagged is kVerify over flattened rows of their own lengths: unit u is
+// flattened target row u, described by a packed word (row, position, bonus).
 enum Mode : int { kVerify = 0, kVerifyGreedy = 1, kOverlap = 2, kOverlapGreedy = 3, kE2E = 4, kDiag = 5,
-                  kVerifyGrouped = 6 };
+                  kVerifyGrouped = 6, kVerifyRagged = 7 };
+
+// Packed unit word of the ragged verify: row << 8 | bonus << 7 | position.
+__host__ __device__ constexpr uint32_t pack_unit(uint32_t row, uint32_t pos, bool bonus) {
+  return (row << 8) | (bonus ? 0x80u : 0u) | pos;
+}
 
 struct VerifyRecord {  // one per (b, k), k = 0..K
   int32_t acc;         // 1 accepted, 0 rejected, 2 rejected with an empty residual (draft positions)
@@ -107,6 +114,9 @@ struct SweepParams {
   float* row_loss;
   uint32_t* row_cnt;
   uint32_t* rej;  // [B] sampling verify: kRejBase - (earliest rejected position seen), 0 if none
+  const uint32_t* uinfo;   // ragged: [units] packed unit words
+  const int32_t* roff;     // ragged: [B + 1] first flattened target row of every row
+  const uint32_t* ragbad;  // ragged: nonzero when the offsets were rejected (nothing runs)
   uint32_t* glob_cnt;
   uint32_t* status;
 };
@@ -306,10 +316,20 @@ __device__ __forceinline__ float draw_weights(const uint4& wt, const uint4& wd, 
 // re-zeroes the workspace of row b.
 template <int MODE>
 __device__ __forceinline__ void complete_row(const SweepParams& P, int b, int S, int lane) {
-  constexpr bool kVerifyMode = (MODE == kVerify || MODE == kVerifyGreedy || MODE == kVerifyGrouped);
-  const int K = P.K;
-  const int per_row = kVerifyMode ? K + 1 : K;
-  const float* pp0 = P.part + (long long)b * per_row * kPartStride;
+  constexpr bool kVerifyMode =
+      (MODE == kVerify || MODE == kVerifyGreedy || MODE == kVerifyGrouped || MODE == kVerifyRagged);
+  // units of row b: [base, base + per_row); drafted positions K of them,
+  // the first at dbase
+  int K = P.K;
+  int per_row = kVerifyMode ? K + 1 : K;
+  int base = b * per_row;
+  if constexpr (MODE == kVerifyRagged) {
+    base = __ldg(P.roff + b);
+    per_row = __ldg(P.roff + b + 1) - base;
+    K = per_row - 1;
+  }
+  const int dbase = (MODE == kVerifyRagged) ? base - b : b * K;
+  const float* pp0 = P.part + (long long)base * kPartStride;
   // overlap of position kk: partials summed in rank order
   auto alpha_of = [&](int kk) {
     const float* pp = pp0 + kk * kPartStride;
@@ -318,7 +338,7 @@ __device__ __forceinline__ void complete_row(const SweepParams& P, int b, int S,
     return a;
   };
   if constexpr (kVerifyMode) {
-    const VerifyRecord* rr = P.rec + (long long)b * (K + 1);
+    const VerifyRecord* rr = P.rec + base;
     // acc: 1 accepted, 0 rejected, 2 rejected with an empty residual
     int nacc = K, acc_first = 1;
     for (int base = 0; base < K; base += 32) {
@@ -336,14 +356,14 @@ __device__ __forceinline__ void complete_row(const SweepParams& P, int b, int S,
     if (lane == 0 && acc_first == 2 && P.status) atomicOr(P.status, kEmptyResidual);
     for (int kk = lane; kk <= K; kk += 32) {
       int tokv = -1;
-      if (kk < nacc) tokv = P.draft_tokens[b * K + kk];
+      if (kk < nacc) tokv = P.draft_tokens[dbase + kk];
       else if (kk == nacc) tokv = corr;
-      P.out_tokens[(long long)b * (K + 1) + kk] = tokv;
-      if (kk < K && P.alpha) P.alpha[b * K + kk] = alpha_of(kk);
+      P.out_tokens[base + kk] = tokv;
+      if (kk < K && P.alpha) P.alpha[dbase + kk] = alpha_of(kk);
     }
     __syncwarp();
-    VerifyRecord* rw = P.rec + (long long)b * (K + 1);
-    float* pw = P.part + (long long)b * per_row * kPartStride;
+    VerifyRecord* rw = P.rec + base;
+    float* pw = P.part + (long long)base * kPartStride;
     for (int kk = lane; kk <= K; kk += 32) rw[kk] = VerifyRecord{0, 0, 0u, 0u};
     for (int i = lane; i < per_row * kPartStride; i += 32) pw[i] = 0.0f;
     if (lane == 0) {
@@ -507,8 +527,13 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
   constexpr int PV = E::PV;
   using Raw = typename E::Raw;
   constexpr bool kGreedy = (MODE == kVerifyGreedy || MODE == kOverlapGreedy);
-  constexpr bool kVerifyMode = (MODE == kVerify || MODE == kVerifyGreedy || MODE == kVerifyGrouped);
-  constexpr bool kSample = (MODE == kVerify || MODE == kVerifyGrouped);  // sampling verify
+  constexpr bool kVerifyMode =
+      (MODE == kVerify || MODE == kVerifyGreedy || MODE == kVerifyGrouped || MODE == kVerifyRagged);
+  constexpr bool kSample = (MODE == kVerify || MODE == kVerifyGrouped || MODE == kVerifyRagged);  // sampling verify
+  constexpr bool kRagged = (MODE == kVerifyRagged);
+  if constexpr (kRagged) {
+    if (__ldg(P.ragbad)) return;  // the same word for every CTA: the whole grid returns
+  }
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int S = P.S;
@@ -549,13 +574,20 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
 
   struct Unit {
     int b, k;
+    int u;  // ragged: the unit (its flattened target row and record index)
     bool bonus, has_draft;
     const Raw* tg;
     const Raw* dg;
   };
   auto decode = [&](int u) {
     Unit x;
-    if constexpr (MODE == kVerifyGrouped) {
+    if constexpr (kRagged) {
+      x.u = u;
+      const uint32_t w = __ldg(P.uinfo + u);
+      x.b = (int)(w >> 8);
+      x.k = (int)(w & 0x7Fu);
+      x.bonus = (w & 0x80u) != 0u;
+    } else if constexpr (MODE == kVerifyGrouped) {
       // Rows in groups of G, position-major inside a group: a unit starts
       // about one unit-time after the earlier positions of its row have
       // decided, so that it can skip a draw that cannot be emitted, and rows
@@ -579,13 +611,21 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
     }
     x.has_draft = !x.bonus;
     if constexpr (MODE == kVerifyGreedy) x.has_draft = !x.bonus && P.alpha != nullptr;
-    x.tg = reinterpret_cast<const Raw*>(P.target) + ((long long)x.b * P.KT + x.k) * V;
-    x.dg = x.has_draft ? reinterpret_cast<const Raw*>(P.draft) + ((long long)x.b * K + x.k) * V : nullptr;
+    if constexpr (kRagged) {
+      x.tg = reinterpret_cast<const Raw*>(P.target) + (long long)u * V;
+      x.dg = x.has_draft ? reinterpret_cast<const Raw*>(P.draft) + (long long)(u - x.b) * V : nullptr;
+    } else {
+      x.tg = reinterpret_cast<const Raw*>(P.target) + ((long long)x.b * P.KT + x.k) * V;
+      x.dg = x.has_draft ? reinterpret_cast<const Raw*>(P.draft) + ((long long)x.b * K + x.k) * V : nullptr;
+    }
     return x;
   };
 
   // index of a unit's record and partials: b * per_row + k
-  auto rec_idx = [&](const Unit& x) { return x.b * per_row + x.k; };
+  auto rec_idx = [&](const Unit& x) {
+    if constexpr (kRagged) return x.u;
+    return x.b * per_row + x.k;
+  };
 
   // Bulk copies of this warp's segment of unit u into stage st (lane 0).
   auto issue = [&](int u, int st) {
@@ -633,8 +673,10 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
     if (lane < np) {
       row = sm.pend_row[lane];
       const uint32_t c = (uint32_t)sm.pend_cnt[lane];
+      int units_of_row = per_row;
+      if constexpr (kRagged) units_of_row = __ldg(P.roff + row + 1) - __ldg(P.roff + row);
       const uint32_t old = atomicAdd(&P.row_cnt[row], c);
-      last = (old + c == (uint32_t)(per_row * S)) ? 1 : 0;
+      last = (old + c == (uint32_t)(units_of_row * S)) ? 1 : 0;
     }
     unsigned m = __ballot_sync(kFull, last);
     if (m) __threadfence();
@@ -671,9 +713,10 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
     uf_ = 0.0f;
     if constexpr (kVerifyMode) {
       const Unit x = decode(u);
-      if (!x.bonus) y_ = P.draft_tokens[x.b * K + x.k];
+      const long long di = kRagged ? (long long)(u - x.b) : (long long)x.b * K + x.k;  // drafted position
+      if (!x.bonus) y_ = P.draft_tokens[di];
       if constexpr (kSample) {
-        if (!x.bonus) ua_ = P.u_accept[x.b * K + x.k];
+        if (!x.bonus) ua_ = P.u_accept[di];
         uf_ = P.u_final[x.b];
       }
     }

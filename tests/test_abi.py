@@ -33,7 +33,7 @@ def test_header_declares_the_boundary():
     for want in ("spec_verify", "spec_overlap", "spec_e2e_tv_fwd_bwd", "spec_status_string",
                  "spec_verify_workspace_bytes", "spec_overlap_workspace_bytes", "spec_e2e_tv_workspace_bytes",
                  "spec_diagnostics", "spec_diagnostics_workspace_bytes", "spec_truncate_logits",
-                 "spec_schedule_lengths"):
+                 "spec_schedule_lengths", "spec_verify_ragged", "spec_verify_ragged_workspace_bytes"):
         assert want in names
 
 
@@ -110,3 +110,15 @@ def test_argument_validation_without_gpu(L):
     assert L.spec_schedule_lengths(fake, 2, 3, fake, 8, fake, None, None, None) == 1
     assert L.spec_schedule_lengths(fake, 16385, 1, fake, 40000, fake, None, None, None) == 2
     assert L.spec_schedule_lengths(None, 0, 3, None, 0, None, None, None, None) == 0
+    # ragged verify: T > 0, B <= units <= 65 B, a large enough workspace; no rows is a no-op
+    assert L.spec_verify_ragged(fake, fake, 1, 2, fake, 5, 10, 0.0, fake, fake, fake, fake, fake, None, None, ws,
+                                1 << 20, None) == 1
+    assert L.spec_verify_ragged(fake, fake, 1, 2, fake, 1, 10, 1.0, fake, fake, fake, fake, fake, None, None, ws,
+                                1 << 20, None) == 1
+    assert L.spec_verify_ragged(fake, fake, 1, 2, fake, 200, 10, 1.0, fake, fake, fake, fake, fake, None, None, ws,
+                                1 << 20, None) == 1
+    assert L.spec_verify_ragged(fake, fake, 1, 2, fake, 5, 10, 1.0, fake, fake, fake, fake, fake, None, None, ws,
+                                8, None) == 1
+    assert L.spec_verify_ragged(None, None, 1, 0, None, 0, 10, 1.0, None, None, None, None, None, None, None, None,
+                                0, None) == 0
+    assert L.spec_verify_ragged_workspace_bytes(4, 3, 10) == 0
