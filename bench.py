@@ -55,7 +55,8 @@ def parse():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=100)
-    ap.add_argument("--single", choices=["verify", "greedy", "overlap", "e2e", "diag", "truncate"], default=None,
+    ap.add_argument("--single", choices=["verify", "greedy", "overlap", "e2e", "diag", "truncate", "ragged",
+                                         "schedule"], default=None,
                     help="run only `--calls` calls of one entry point (an L2 flush before each): the "
                          "profiling target, prints no JSON")
     ap.add_argument("--shape", default="32,4,151936", help="B,K,V of --single")
@@ -162,11 +163,12 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 def kernel_source_hash():
+    """Hash of the sweep kernel's device code (the kernel the ncu traffic
+    record describes); other kernels' sources do not change it."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "sampling_spec_verify_gb300", "csrc")
-    for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(d, name), "rb").read())
+    for name in ("ptx.cuh", "sweep.cuh"):
+        h.update(open(os.path.join(d, name), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -457,8 +459,8 @@ def run_single(args):
     from sampling_spec_verify_gb300 import synth
     Bs, Ks, Vs = (int(v) for v in args.shape.split(","))
     dev = torch.device("cuda")
-    T = 0.0 if args.single == "greedy" else (1.0 if args.single in ("overlap", "e2e", "diag", "truncate")
-                                             else args.temperature)
+    T = 0.0 if args.single == "greedy" else (
+        1.0 if args.single in ("overlap", "e2e", "diag", "truncate", "ragged", "schedule") else args.temperature)
     w = synth.entropy_mix(seed=SEED, temperature=T, B=Bs, K=Ks, V=Vs)
     t, d = w.target.to(dev), w.draft.to(dev)
     y, ua, uf = w.draft_tokens.to(dev), w.u_accept.to(dev), w.u_final.to(dev)
@@ -473,6 +475,14 @@ def run_single(args):
             ssv.diagnostics(t, d, 1.0, K=Ks)
         elif args.single == "truncate":  # top-k 50, top-p 0.9 on the target tensor
             ssv.truncate_logits(t, 1.0, 50, 0.9)
+        elif args.single == "ragged":  # every row verifies all of its positions, flattened
+            offs = torch.arange(0, (Bs + 1) * (Ks + 1), Ks + 1, dtype=torch.int32, device=dev)
+            ssv.verify_ragged(t.reshape(-1, Vs), d.reshape(-1, Vs), offs, y.reshape(-1), ua.reshape(-1), uf, 1.0)
+        elif args.single == "schedule":  # 1024 requests x 16 positions of prefix survivals
+            g = torch.Generator(device=dev).manual_seed(SEED)
+            a = torch.cumprod(torch.rand((1024, 16), generator=g, device=dev) * 0.7 + 0.3, dim=1)
+            sps = 2000.0 / (1.0 + torch.arange(1024 * 17 + 1, device=dev, dtype=torch.float32) / 256.0)
+            ssv.schedule_lengths(a, sps)
         else:
             ssv.e2e_tv_fwd_bwd(t, d, 1.0, 1.0, K=Ks)
     torch.cuda.synchronize()
