@@ -8,15 +8,22 @@
 // top_k; top-p renormalises softmax(z / T) over what is left and keeps the
 // shortest ranked prefix whose mass reaches top_p; dropped logits become -inf.
 //
-// One CTA per row.  Every pass streams the row through L2 (the first one from
-// HBM): a maximum pass, radix-select passes over order-preserving keys (8 bits
-// per pass, 2 passes for bf16, 4 for fp32), a tie pass in index order for the
-// threshold key, and the write pass.  A radix pass builds one histogram per
-// warp (logits crowd into a few exponent digits, and shared atomics that many
-// warps aim at one counter serialise); for counts, the lanes holding the same
-// digit are grouped and one of them adds the group's size.  Top-p masses are
-// fixed point (2^44 for the row maximum) and summed as integers, so every cut
-// is independent of the order of the additions.
+// One CTA per row; every pass streams the row through L2 (the first one from
+// HBM).  Keys are order-preserving 16-bit (bf16) or 32-bit (fp32) images of
+// the logits, selected 8 bits at a time.  Warp w always walks the same
+// contiguous chunk of the row, so per-warp counts give ordered compaction.
+//  1. maximum, NaN check and, for top-k, per-warp counts of the first digit;
+//  2. top-k: the digit where the count reaches top_k; its elements (usually a
+//     few hundred) are compacted, in index order, into shared memory, and the
+//     remaining digits and the index-order tie are resolved on that list;
+//  3. top-p: per-warp fixed-point masses (2^44 for the row maximum, summed as
+//     integers, so every cut is independent of the order of the additions)
+//     and counts of the first digit over the top-k set; the same compaction
+//     and list selection by mass;
+//  4. the write pass.
+// A digit holding more than kTCap elements falls back to radix passes over
+// the whole row.  Histograms are per warp, so atomics conflict only between
+// the lanes of one warp.
 #pragma once
 
 #include <cstdint>
@@ -26,6 +33,7 @@ namespace ssv {
 constexpr int kTThreads = 512;
 constexpr int kTWarps = kTThreads / 32;
 constexpr float kMassScale = 0x1p44f;  // fixed-point unit of the top-p masses
+constexpr int kTCap = 6144;            // candidates held in shared memory after the first digit
 
 struct TruncParams {
   const void* in;
@@ -40,6 +48,9 @@ struct TruncParams {
 
 struct TruncSmem {
   unsigned long long ph[kTWarps][256];  // per-warp histograms of one radix pass
+  uint32_t pc[kTWarps][256];            // per-warp counts of the first digit (compaction offsets)
+  int cand_idx[kTCap];                  // candidates of the crossing first digit, in index order
+  float cand_x[kTCap];
   unsigned long long hist[256];
   unsigned long long wtot[kTWarps];
   float wmax[kTWarps];
@@ -228,15 +239,24 @@ __device__ void hist_pass(const typename E::Raw* row, int V, bool aligned, uint3
 // weight, in ranking order over the eligible elements, first reaches `need`
 // (need >= 1).  *above gets the weight of eligible elements with larger keys
 // (< need); the rest, need - *above, is still needed inside the key thr.
-// Returns false if the eligible weight is below need.
+// Returns false if the eligible weight is below need.  first >= 0: the first
+// digit is already known to be `first`, with weight `above0` above it.
 template <class E, bool kCount, class Elig, class Wt>
 __device__ bool radix_select(const typename E::Raw* row, int V, bool aligned, unsigned long long need, Elig elig,
-                             Wt wt, TruncSmem& sm, uint32_t* thr, unsigned long long* above) {
+                             Wt wt, TruncSmem& sm, uint32_t* thr, unsigned long long* above, int first = -1,
+                             unsigned long long above0 = 0) {
   constexpr int KB = 8 * E::ES;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t prefix = 0, pmask = 0;
   unsigned long long abv = 0;
-  for (int shift = KB - 8; shift >= 0; shift -= 8) {
+  int shift = KB - 8;
+  if (first >= 0) {
+    prefix = (uint32_t)first << shift;
+    pmask = 0xFFu << shift;
+    abv = above0;
+    shift -= 8;
+  }
+  for (; shift >= 0; shift -= 8) {
     hist_pass<E, kCount>(row, V, aligned, prefix, pmask, shift, elig, wt, sm);
     if (warp == 0) {
       // lane l scans bins 255 - 8l down to 248 - 8l: lanes in descending key order
@@ -329,14 +349,250 @@ __device__ int tie_index(const typename E::Raw* row, int V, bool aligned, uint32
   return V;
 }
 
+// Warp w walks its own contiguous chunk of the row, 32 consecutive vectors
+// (elements, for unaligned rows) per step, kTUnroll steps of loads in flight;
+// f(i, valid, x) runs warp-converged for every lane: vector i (element i if
+// unaligned), x its PV values (-inf past the end; x[0] only if unaligned).
+template <class E, class F>
+__device__ __forceinline__ void chunk_walk(const typename E::Raw* row, int V, bool aligned, F&& f) {
+  constexpr int PV = E::PV;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nitem = aligned ? V / PV : V;
+  const int cw = (nitem + kTWarps - 1) / kTWarps;
+  const int lo = min(warp * cw, nitem), hi = min(lo + cw, nitem);
+  for (int base = lo; base < hi; base += 32 * kTUnroll) {
+    uint4 raw[kTUnroll];
+#pragma unroll
+    for (int u = 0; u < kTUnroll; ++u) {
+      const int i = base + u * 32 + lane;
+      raw[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (i < hi) {
+        if (aligned)
+          raw[u] = __ldcg(reinterpret_cast<const uint4*>(row) + i);
+        else
+          raw[u].x = (uint32_t)__ldcg(row + i);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kTUnroll; ++u) {
+      if (base + u * 32 >= hi) break;  // warp-uniform
+      const int i = base + u * 32 + lane;
+      const bool valid = i < hi;
+      float x[PV];
+#pragma unroll
+      for (int j = 0; j < PV; ++j) x[j] = -INFINITY;
+      if (valid) {
+        if (aligned)
+          E::unpack(raw[u], x);
+        else
+          x[0] = E::to_f32((typename E::Raw)raw[u].x);
+      }
+      f(i, valid, x);
+    }
+  }
+}
+
+// Ordered compaction: every element (index v, value x) with pick(v, x) goes
+// to the candidate list in index order.  pc[w][digit] must hold, for warp
+// w's chunk, the number of picked elements (they all have first digit d1).
+template <class E, class Pick>
+__device__ int compact(const typename E::Raw* row, int V, bool aligned, uint32_t d1, Pick pick, TruncSmem& sm) {
+  constexpr int PV = E::PV;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = aligned ? PV : 1;
+  int off = 0, total = 0;
+  for (int w = 0; w < kTWarps; ++w) {
+    const int c = (int)sm.pc[w][d1];
+    if (w < warp) off += c;
+    total += c;
+  }
+  chunk_walk<E>(row, V, aligned, [&](int i, bool valid, const float (&x)[PV]) {
+    unsigned m = 0;  // picked elements of this lane, bit j
+#pragma unroll
+    for (int j = 0; j < PV; ++j)
+      if (j < per && valid && pick(aligned ? i * PV + j : i, x[j])) m |= 1u << j;
+    const int c = __popc(m);
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += t;
+    }
+    int at = off + incl - c;
+#pragma unroll
+    for (int j = 0; j < PV; ++j)
+      if ((m >> j) & 1u) {
+        sm.cand_idx[at] = aligned ? i * PV + j : i;
+        sm.cand_x[at] = x[j];
+        ++at;
+      }
+    off += __shfl_sync(kFull, incl, 31);
+  });
+  __syncthreads();
+  return total;
+}
+
+// Radix select over the candidate list for the digits below the first:
+// prefix holds the first digit; need is the weight still needed inside it.
+// Returns the full threshold key; *above gets the weight of candidates with
+// larger keys.
+template <class E, bool kCount, class Wt>
+__device__ uint32_t list_select(int n, uint32_t prefix, unsigned long long need, Wt wt, TruncSmem& sm,
+                                unsigned long long* above) {
+  constexpr int KB = 8 * E::ES;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t pmask = 0xFFu << (KB - 8);
+  unsigned long long abv = 0;
+  for (int shift = KB - 16; shift >= 0; shift -= 8) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < 256; i += kTThreads) sm.hist[i] = 0ull;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += kTThreads) {
+      const float x = sm.cand_x[i];
+      const uint32_t key = order_key<KB>(x);
+      if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & 255u], kCount ? 1ull : wt(x));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      unsigned long long c[8], tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = sm.hist[255 - 8 * lane - j];
+        tot += c[j];
+      }
+      const unsigned long long rem = need - abv;
+      const unsigned long long incl = warp_incl_scan_u64(tot, lane);
+      const unsigned long long excl = incl - tot;
+      const bool mine = excl < rem && rem <= incl;
+      if (mine) {
+        unsigned long long run = excl;
+        int b = 255 - 8 * lane - 7;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (run + c[j] >= rem) {
+            b = 255 - 8 * lane - j;
+            break;
+          }
+          run += c[j];
+        }
+        sm.bin = b;
+        sm.bc = run;
+      }
+      if (__ballot_sync(kFull, mine) == 0u && lane == 0) {  // cannot happen for consistent weights
+        sm.bin = 0;
+        sm.bc = 0;
+      }
+    }
+    __syncthreads();
+    abv += sm.bc;
+    prefix |= (uint32_t)sm.bin << shift;
+    pmask |= 0xFFu << shift;
+  }
+  *above = abv;
+  return prefix;
+}
+
+// Index of the need-th candidate (list order = index order) with key thr;
+// V if there are fewer.
+template <int KB>
+__device__ int list_tie(int n, uint32_t thr, unsigned long long need, int V, TruncSmem& sm) {
+  const int per = (n + kTThreads - 1) / kTThreads;
+  const int lo = min((int)threadIdx.x * per, n), hi = min(lo + per, n);
+  unsigned long long c = 0;
+  for (int i = lo; i < hi; ++i) c += order_key<KB>(sm.cand_x[i]) == thr;
+  unsigned long long total;
+  const unsigned long long incl = block_incl_scan_u64(c, sm, &total);
+  if (threadIdx.x == 0) sm.tie = V;
+  __syncthreads();
+  const unsigned long long before = incl - c;
+  if (c > 0 && before < need && incl >= need) {
+    unsigned long long k = need - before;
+    for (int i = lo; i < hi; ++i)
+      if (order_key<KB>(sm.cand_x[i]) == thr && --k == 0) {
+        sm.tie = sm.cand_idx[i];
+        break;
+      }
+  }
+  __syncthreads();
+  const int t = sm.tie;
+  __syncthreads();
+  return t;
+}
+
+// Reduces the per-warp first-digit histograms (counts pc or weights ph) into
+// sm.hist; returns the total weight.
+template <bool kFromCounts>
+__device__ unsigned long long reduce_first(TruncSmem& sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  for (int b = threadIdx.x; b < 256; b += kTThreads) {
+    unsigned long long t = 0;
+#pragma unroll
+    for (int w = 0; w < kTWarps; ++w) t += kFromCounts ? (unsigned long long)sm.pc[w][b] : sm.ph[w][b];
+    sm.hist[b] = t;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    unsigned long long t = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t += sm.hist[8 * lane + j];
+    t = warp_sum_u64(t);
+    if (lane == 0) sm.bc = t;
+  }
+  __syncthreads();
+  const unsigned long long total = sm.bc;
+  __syncthreads();
+  return total;
+}
+
+// The first-digit bin, scanning sm.hist from the top, at which the running
+// weight reaches need (>= 1); *above gets the weight of the bins above it.
+// -1 if the total is below need.
+__device__ int crossing_bin(unsigned long long need, TruncSmem& sm, unsigned long long* above) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp == 0) {
+    unsigned long long c[8], tot = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      c[j] = sm.hist[255 - 8 * lane - j];
+      tot += c[j];
+    }
+    const unsigned long long incl = warp_incl_scan_u64(tot, lane);
+    const unsigned long long excl = incl - tot;
+    const bool mine = excl < need && need <= incl;
+    if (mine) {
+      unsigned long long run = excl;
+      int b = 255 - 8 * lane - 7;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (run + c[j] >= need) {
+          b = 255 - 8 * lane - j;
+          break;
+        }
+        run += c[j];
+      }
+      sm.bin = b;
+      sm.bc = run;
+    }
+    if (__ballot_sync(kFull, mine) == 0u && lane == 0) sm.bin = -1;
+  }
+  __syncthreads();
+  *above = sm.bc;
+  const int bin = sm.bin;
+  __syncthreads();
+  return bin;
+}
+
 template <class E>
 __global__ void __launch_bounds__(kTThreads, 2) truncate_kernel(const __grid_constant__ TruncParams P) {
-  __shared__ TruncSmem sm;
+  extern __shared__ __align__(16) unsigned char tsm_raw[];
+  TruncSmem& sm = *reinterpret_cast<TruncSmem*>(tsm_raw);
   using Raw = typename E::Raw;
   constexpr int KB = 8 * E::ES;
   constexpr int PV = E::PV;
   const int V = P.V;
   const bool al = P.aligned != 0;
+  const int per = al ? PV : 1;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool do_k = P.top_k > 0 && P.top_k < V;
   const bool do_p = P.top_p < 1.0f;
@@ -345,17 +601,27 @@ __global__ void __launch_bounds__(kTThreads, 2) truncate_kernel(const __grid_con
     const Raw* zin = reinterpret_cast<const Raw*>(P.in) + (long long)row * V;
     Raw* zout = reinterpret_cast<Raw*>(P.out) + (long long)row * V;
 
-    // ---- row maximum and NaN check (brings the row into L2) ----
+    // ---- pass 1: maximum, NaN check and (top-k) first-digit counts ----
+    __syncthreads();  // the previous row is done with the shared state
+    for (int b = lane; b < 256; b += 32) sm.pc[warp][b] = 0u;
+    __syncwarp();
     float mx = -INFINITY;
     int nan = 0;
-    for_each_elem<E>(zin, V, al, [&](int, float x) {
-      mx = fmaxf(mx, x);
-      nan |= (x != x);
+    chunk_walk<E>(zin, V, al, [&](int, bool valid, const float (&x)[PV]) {
+#pragma unroll
+      for (int j = 0; j < PV; ++j) {
+        if (j >= per) break;
+        mx = fmaxf(mx, x[j]);
+        nan |= (x[j] != x[j]);
+        if (do_k) {
+          const uint32_t d = order_key<KB>(x[j]) >> (KB - 8);
+          if (valid) atomicAdd(&sm.pc[warp][d], 1u);  // the warp's own counters
+        }
+      }
     });
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
     nan = __any_sync(kFull, nan);
-    __syncthreads();
     if (lane == 0) {
       sm.wmax[warp] = mx;
       sm.wnan[warp] = nan;
@@ -374,12 +640,27 @@ __global__ void __launch_bounds__(kTThreads, 2) truncate_kernel(const __grid_con
     int tie1 = V;
     bool ok = !bad;
     if (ok && do_k) {
+      reduce_first<true>(sm);
       unsigned long long above = 0;
-      ok = radix_select<E, true>(
-          zin, V, al, (unsigned long long)P.top_k, [](int, uint32_t) { return true; },
-          [](float) { return 1ull; }, sm, &thr1, &above);
-      if (ok) tie1 = tie_index<E>(zin, V, al, thr1, (unsigned long long)P.top_k - above,
-                                  [](int, uint32_t) { return true; }, sm);
+      const int b1 = crossing_bin((unsigned long long)P.top_k, sm, &above);
+      const unsigned long long n1 = b1 >= 0 ? sm.hist[b1] : 0ull;
+      if (b1 < 0) {
+        ok = false;
+      } else if (n1 <= (unsigned long long)kTCap) {
+        // the candidates of the crossing digit, in index order; the rest of the key on them
+        const int n = compact<E>(zin, V, al, (uint32_t)b1,
+                                 [&](int, float x) { return (order_key<KB>(x) >> (KB - 8)) == (uint32_t)b1; }, sm);
+        unsigned long long above2 = 0;
+        thr1 = list_select<E, true>(n, (uint32_t)b1 << (KB - 8), (unsigned long long)P.top_k - above,
+                                    [](float) { return 1ull; }, sm, &above2);
+        tie1 = list_tie<KB>(n, thr1, (unsigned long long)P.top_k - above - above2, V, sm);
+      } else {  // a crowded digit: select its lower digits over the whole row
+        ok = radix_select<E, true>(
+            zin, V, al, (unsigned long long)P.top_k, [](int, uint32_t) { return true; },
+            [](float) { return 1ull; }, sm, &thr1, &above, b1, above);
+        if (ok) tie1 = tie_index<E>(zin, V, al, thr1, (unsigned long long)P.top_k - above,
+                                    [](int, uint32_t) { return true; }, sm);
+      }
     }
     auto kept1 = [&](int v, uint32_t key) { return key > thr1 || (key == thr1 && v <= tie1); };
 
@@ -387,22 +668,62 @@ __global__ void __launch_bounds__(kTThreads, 2) truncate_kernel(const __grid_con
     uint32_t thr2 = 0;
     int tie2 = V;
     if (ok && do_p) {
-      unsigned long long z = 0;
-      for_each_elem<E>(zin, V, al, [&](int v, float x) {
-        if (kept1(v, order_key<KB>(x))) z += fixed_mass(x, M, s);
+      // pass: fixed-point masses and counts of the first digit over the top-k set
+      __syncthreads();
+      for (int b = lane; b < 256; b += 32) {
+        sm.ph[warp][b] = 0ull;
+        sm.pc[warp][b] = 0u;
+      }
+      __syncwarp();
+      unsigned long long* ph = sm.ph[warp];
+      chunk_walk<E>(zin, V, al, [&](int i, bool valid, const float (&x)[PV]) {
+#pragma unroll
+        for (int j = 0; j < PV; ++j) {
+          if (j >= per) break;
+          const uint32_t key = order_key<KB>(x[j]);
+          const bool on = valid && kept1(al ? i * PV + j : i, key);
+          const uint32_t d = key >> (KB - 8);
+          if (on) {
+            atomicAdd(&sm.pc[warp][d], 1u);
+            const unsigned long long w = fixed_mass(x[j], M, s);
+            if (w) atomicAdd(&ph[d], w);
+          }
+        }
       });
-      z = block_sum_u64(z, sm);
+      const unsigned long long z = reduce_first<false>(sm);
       unsigned long long tau = (unsigned long long)ceil((double)P.top_p * (double)z);
       if (tau == 0ull) tau = 1ull;
       unsigned long long above = 0;
-      ok = radix_select<E, false>(zin, V, al, tau, kept1, [&](float x) { return fixed_mass(x, M, s); }, sm,
-                                  &thr2, &above);
-      if (ok) {
+      const int c1 = crossing_bin(tau, sm, &above);
+      unsigned long long n2 = 0;
+      if (c1 >= 0)
+        for (int w = 0; w < kTWarps; ++w) n2 += sm.pc[w][c1];
+      if (c1 < 0) {
+        ok = false;
+      } else if (n2 <= (unsigned long long)kTCap) {
+        const int n = compact<E>(zin, V, al, (uint32_t)c1,
+                                 [&](int v, float x) {
+                                   const uint32_t key = order_key<KB>(x);
+                                   return (key >> (KB - 8)) == (uint32_t)c1 && kept1(v, key);
+                                 },
+                                 sm);
+        unsigned long long above2 = 0;
+        thr2 = list_select<E, false>(n, (uint32_t)c1 << (KB - 8), tau - above,
+                                     [&](float x) { return fixed_mass(x, M, s); }, sm, &above2);
         // tied tokens share one mass: keep the first ceil(rest / w) of them
         const unsigned long long w = fixed_mass(key_value<KB>(thr2), M, s);
-        const unsigned long long rest = tau - above;
-        const unsigned long long n = w ? (rest + w - 1) / w : 1ull;
-        tie2 = tie_index<E>(zin, V, al, thr2, n, kept1, sm);
+        const unsigned long long rest = tau - above - above2;
+        const unsigned long long nk = w ? (rest + w - 1) / w : 1ull;
+        tie2 = list_tie<KB>(n, thr2, nk, V, sm);
+      } else {  // a crowded digit: select its lower digits over the whole row
+        ok = radix_select<E, false>(zin, V, al, tau, kept1, [&](float x) { return fixed_mass(x, M, s); }, sm,
+                                    &thr2, &above, c1, above);
+        if (ok) {
+          const unsigned long long w = fixed_mass(key_value<KB>(thr2), M, s);
+          const unsigned long long rest = tau - above;
+          const unsigned long long nk = w ? (rest + w - 1) / w : 1ull;
+          tie2 = tie_index<E>(zin, V, al, thr2, nk, kept1, sm);
+        }
       }
     }
     // a row with NaN or infinite logits (or none finite) is copied unchanged
