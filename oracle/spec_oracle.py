@@ -40,6 +40,11 @@ reason, in the design notes of the repository):
   maximised) and its gradient is taken with respect to the draft logits only,
   the target being a constant; the sub-gradient of ``min`` uses the strict
   indicator ``1[q_v < p_v]``.
+* relaxed (lossy) acceptance: a draft is accepted when it ranks in the
+  target's top-k (ties by smaller index) and its target log-probability lies
+  within delta of the largest; the first rejection emits a draw from the
+  full target distribution (no residual), the bonus stays as in the exact
+  verify;
 * top-k / top-p truncation ranks tokens by logit (ties by smaller index),
   applies top-k first, then keeps the shortest ranked prefix whose
   renormalised mass at temperature T reaches top_p; dropped logits become
@@ -382,6 +387,84 @@ def verify(target_logits, draft_logits, draft_tokens, u_accept, u_final,
         c_near[i] = res.cdf_near
         r_empty[i] = res.residual_empty
     return VerifyResult(tokens, n_acc, alpha, tv, surv, a_near, c_near, r_empty)
+
+
+# ---------------------------------------------------------------------------
+# Relaxed (lossy) acceptance
+# ---------------------------------------------------------------------------
+
+def relaxed_accept(z, y, temperature, top_k, delta):
+    """Relaxed acceptance of drafted token y against target logits z: y must
+    rank among the target's top_k tokens (by logit, ties to the smaller
+    index; top_k <= 0: no such condition) and its target log-probability may
+    fall at most delta below the target's largest (delta = inf: no such
+    condition).  Speculative Decoding 与 MTP, section 4: accepting a candidate
+    that lies in the target's top-k, or whose logprob is close, raises the
+    acceptance rate but no longer preserves the target distribution (the
+    relaxed_topk / relaxed_delta switches it cites); such runs are lossy.
+
+    Returns (accepted, near): near reports |gap + delta| < NEAR_TIE, gap the
+    log-probability difference."""
+    z = np.asarray(z, dtype=np.float64)
+    V = z.shape[0]
+    if not 0 <= y < V:
+        return False, False
+    zy = z[y]
+    rank = int(np.sum(z > zy) + np.sum(z[:y] == zy))
+    gap = (zy - np.max(z)) / float(temperature)
+    ok_k = top_k <= 0 or rank < top_k
+    ok_d = not np.isfinite(delta) or gap >= -delta
+    near = bool(np.isfinite(delta) and abs(gap + delta) < NEAR_TIE)
+    return bool(ok_k and ok_d), near
+
+
+def verify_relaxed(target_logits, draft_logits, draft_tokens, u_final, temperature, top_k, delta,
+                   rows=None):
+    """Verify with relaxed acceptance (LOSSY): drafted tokens are accepted in
+    prefix order while ``relaxed_accept`` holds; the first rejected position
+    emits a draw from the full target distribution p_k with u' (a residual has
+    no meaning once acceptance no longer follows min(1, p/q)), and a block with
+    every draft accepted emits the bonus draw from p_{K+1}, as in the exact
+    verify.  Overlaps are reported as for the exact verify when draft logits
+    are given."""
+    zt = np.asarray(target_logits)
+    zd = None if draft_logits is None else np.asarray(draft_logits)
+    B, K1, V = zt.shape
+    K = K1 - 1
+    rows = range(B) if rows is None else list(rows)
+    R = len(rows)
+    tokens = np.full((R, K + 1), -1, dtype=np.int64)
+    n_acc = np.zeros(R, dtype=np.int64)
+    alpha = np.zeros((R, K))
+    tv = np.zeros((R, K))
+    surv = np.zeros((R, K))
+    a_near = np.zeros(R, dtype=bool)
+    c_near = np.zeros(R, dtype=bool)
+    t = float(temperature)
+    for i, b in enumerate(rows):
+        p = [softmax_t(zt[b, k], t) for k in range(K + 1)]
+        if zd is not None:
+            q = [softmax_t(zd[b, k], t) for k in range(K)]
+            alpha[i] = [overlap(p[k], q[k]) for k in range(K)]
+            tv[i] = [tv_distance(p[k], q[k]) for k in range(K)]
+            surv[i] = prefix_survival(alpha[i]) if K else []
+        n = K
+        for k in range(K):
+            y = int(draft_tokens[b][k])
+            acc, near = relaxed_accept(zt[b, k], y, t, top_k, delta)
+            a_near[i] |= near
+            if acc:
+                tokens[i, k] = y
+                continue
+            v, c_near[i] = inverse_cdf(p[k], float(u_final[b]))
+            tokens[i, k] = v
+            n = k
+            break
+        else:
+            v, c_near[i] = inverse_cdf(p[K], float(u_final[b]))
+            tokens[i, K] = v
+        n_acc[i] = n
+    return VerifyResult(tokens, n_acc, alpha, tv, surv, a_near, c_near, np.zeros(R, dtype=bool))
 
 
 # ---------------------------------------------------------------------------

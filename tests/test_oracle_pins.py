@@ -720,3 +720,60 @@ def test_schedule_closed_forms():
     r1 = so.schedule_lengths([[0.5, 0.9]], [0, 10, 9, 8])
     r2 = so.schedule_lengths([[0.5, 0.5]], [0, 10, 9, 8])
     assert r1.lengths.tolist() == r2.lengths.tolist() and r1.theta == r2.theta
+
+
+# ---------------------------------------------------------------------------
+# relaxed (lossy) acceptance
+# ---------------------------------------------------------------------------
+
+def test_relaxed_accept_hand_example():
+    # z = (2, 1, 0, 1), T = 1, y = 3: two logits rank above or tie before it
+    # (2, and the tied 1 at index 1), so its rank is 2; log p(3) - log p_max = -1.
+    z = [2.0, 1.0, 0.0, 1.0]
+    inf = float("inf")
+    assert so.relaxed_accept(z, 3, 1.0, 2, inf) == (False, False)
+    assert so.relaxed_accept(z, 3, 1.0, 3, inf) == (True, False)
+    assert so.relaxed_accept(z, 3, 1.0, 0, 0.5) == (False, False)
+    assert so.relaxed_accept(z, 3, 1.0, 0, 1.5) == (True, False)
+    assert so.relaxed_accept(z, 3, 2.0, 0, 0.6) == (True, False)  # gap -1/2 at T = 2
+    acc, near = so.relaxed_accept(z, 3, 1.0, 0, 1.0)  # gap exactly -delta
+    assert acc and near
+    assert so.relaxed_accept(z, 1, 1.0, 2, inf) == (True, False)  # the tie at index 1 ranks first
+    assert so.relaxed_accept(z, 7, 1.0, 0, inf)[0] is False        # a token outside the vocabulary
+
+
+def test_relaxed_limits():
+    rng = np.random.default_rng(31)
+    B, K, V = 6, 4, 40
+    zt = rng.normal(size=(B, K + 1, V)) * 2
+    y = rng.integers(0, V, size=(B, K))
+    uf = rng.uniform(size=B)
+    r = so.verify_relaxed(zt, None, y, uf, 1.0, 0, float("inf"))  # no condition: everything accepted
+    assert (r.n_accepted == K).all()
+    for b in range(B):
+        assert r.tokens[b, :K].tolist() == y[b].tolist()
+        assert r.tokens[b, K] == so.inverse_cdf(so.softmax_t(zt[b, K], 1.0), uf[b])[0]
+    r = so.verify_relaxed(zt, None, y, uf, 1.0, 1, float("inf"))  # top-1: the greedy test
+    for b in range(B):
+        n = next((k for k in range(K) if y[b, k] != so.argmax_first(zt[b, k])), K)
+        assert r.n_accepted[b] == n
+
+
+def test_relaxed_is_lossy_exact_enumeration():
+    """With the draft drawn from q, the first emitted token of the exact
+    verify has distribution p; the relaxed rule does not."""
+    z = np.array([1.0, 0.8, -1.0])
+    p = so.softmax_t(z, 1.0)
+    q = np.array([0.05, 0.9, 0.05])
+    # relaxed, top-2: a rejected draft (token 2) emits a draw from p
+    dist = np.zeros(3)
+    for y in range(3):
+        if so.relaxed_accept(z, y, 1.0, 2, float("inf"))[0]:
+            dist[y] += q[y]
+        else:
+            dist += q[y] * p
+    assert abs(dist.sum() - 1.0) < 1e-12
+    assert np.max(np.abs(dist - p)) > 0.2
+    # the exact rule on the same pair: accepted mass min(p, q), residual the rest
+    exact = np.minimum(p, q) + (1 - so.overlap(p, q)) * so.residual(p, q) / so.residual(p, q).sum()
+    np.testing.assert_allclose(exact, p, atol=1e-12)
