@@ -109,6 +109,34 @@ spec_status_t spec_verify(const void* target_logits, const void* draft_logits,
                           void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Relaxed verify -- LOSSY: the output no longer follows the target
+ * distribution.
+ *
+ * "Speculative Decoding 与 MTP", section 4: accepting a candidate because it
+ * lies in the target's top-k, or because its logprob is close, raises the
+ * acceptance rate but gives up the lossless guarantee; results must be
+ * labelled lossy.  Draft k is accepted, in prefix order, when its drafted
+ * token ranks among the target's top_k tokens (by logit, ties to the smaller
+ * index; top_k <= 0: no rank condition) and
+ * log p_k(y) >= max_v log p_k(v) - delta (delta = +inf: no gap condition).
+ * The first rejected position emits a draw from the full p_k with u_final
+ * (no residual); a block with every draft accepted emits the bonus from
+ * p_{K+1}, as spec_verify does.  alpha_out reports the exact overlap.
+ *
+ * Arguments as spec_verify (same workspace size), without u_accept;
+ * temperature T > 0; delta >= 0.
+ */
+spec_status_t spec_verify_relaxed(const void* target_logits,
+                                  const void* draft_logits, spec_dtype_t dtype,
+                                  int B, int K, int V, float temperature,
+                                  int top_k, float delta,
+                                  const int32_t* draft_tokens,
+                                  const float* u_final, int32_t* out_tokens,
+                                  int32_t* n_accepted, float* alpha_out,
+                                  uint32_t* dev_status, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Ragged verify: every row verifies its own number of drafted tokens, in
  * flattened tensors.
  *

@@ -11,6 +11,8 @@ Entry points (same names as the C ABI, see include/spec_verify.h):
                          correction, bonus token, greedy at T == 0);
 * ``verify_ragged``   -- the same with a length of its own per row, over
                          flattened tensors and row offsets;
+* ``verify_relaxed``  -- LOSSY relaxed acceptance (target top-k rank and
+                         log-probability gap);
 * ``overlap``         -- alpha = sum min(p, q), TV, prefix survival, E[tau];
 * ``e2e_tv_fwd_bwd``  -- E2E-TV loss and its draft-logit gradient;
 * ``diagnostics``     -- alpha, target entropy, cross-entropy, KL and the
@@ -31,7 +33,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "SpecError", "lib", "verify", "verify_ragged", "overlap", "e2e_tv_fwd_bwd", "diagnostics", "truncate_logits", "schedule_lengths", "launch_shape",
+    "SpecError", "lib", "verify", "verify_ragged", "verify_relaxed", "overlap", "e2e_tv_fwd_bwd", "diagnostics", "truncate_logits", "schedule_lengths", "launch_shape",
     "set_launch_override", "VerifyOutput", "OverlapOutput", "E2EOutput", "DiagOutput", "HostVerifier",
     "DEV_BAD_TOKEN", "DEV_BAD_LOGITS", "DEV_BAD_UNIFORM", "DEV_TIMEOUT", "DEV_EMPTY_RESIDUAL", "DEV_BAD_OFFSETS",
     "SPEC_OK", "SPEC_ERR_INVALID_ARG", "SPEC_ERR_UNSUPPORTED", "SPEC_ERR_CUDA",
@@ -94,6 +96,8 @@ def lib():
     L.spec_verify_ragged_workspace_bytes.argtypes = [i32, i32, i32]
     L.spec_verify_ragged.restype = i32
     L.spec_verify_ragged.argtypes = [vp, vp, i32, i32, vp, i32, i32, f32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.spec_verify_relaxed.restype = i32
+    L.spec_verify_relaxed.argtypes = [vp, vp, i32, i32, i32, i32, f32, i32, f32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.spec_launch_shape.restype = i32
     L.spec_launch_shape.argtypes = [i32, i32, i32] + [ctypes.POINTER(i32)] * 5
     L.spec_set_launch_override.restype = None
@@ -256,6 +260,37 @@ def verify_ragged(target: torch.Tensor, draft: Optional[torch.Tensor], row_offse
                               _ptr(out.tokens), _ptr(out.n_accepted), _ptr(out.alpha), _ptr(out.status), _ptr(ws),
                               ws.numel() * ws.element_size(), sh)
     _check(st, "spec_verify_ragged")
+    return out
+
+
+def verify_relaxed(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.Tensor, u_final: torch.Tensor,
+                   temperature: float, top_k: int = 0, delta: float = float("inf"), *, want_alpha: bool = True,
+                   workspace: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None) -> VerifyOutput:
+    """LOSSY verify: a draft is accepted while it ranks in the target's
+    top_k (0: no rank condition) and its log-probability lies within delta
+    of the target's largest (inf: no gap condition); the first rejection
+    draws from the full target.  Shapes as ``verify``, without u_accept."""
+    L = lib()
+    _need(target, "target")
+    B, K1, V = target.shape
+    K = K1 - 1
+    dev = target.device
+    _need(draft, "draft", dtype=target.dtype, shape=(B, K, V), device=dev)
+    _need(draft_tokens, "draft_tokens", dtype=torch.int32, shape=(B, K), device=dev)
+    _need(u_final, "u_final", dtype=torch.float32, shape=(B,), device=dev)
+    out = VerifyOutput(torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+                       torch.empty((B,), dtype=torch.int32, device=dev),
+                       torch.empty((B, K), dtype=torch.float32, device=dev) if want_alpha else None,
+                       torch.zeros((1,), dtype=torch.int32, device=dev))
+    sh, s = _stream_handle(stream, dev)
+    need = L.spec_verify_workspace_bytes(B, K, V)
+    ws = workspace if workspace is not None else _workspace(need, dev, s)
+    st = L.spec_verify_relaxed(_ptr(target), _ptr(draft), _dtype_code(target), B, K, V, float(temperature),
+                               int(top_k), float(delta), _ptr(draft_tokens), _ptr(u_final), _ptr(out.tokens),
+                               _ptr(out.n_accepted), _ptr(out.alpha), _ptr(out.status), _ptr(ws),
+                               ws.numel() * ws.element_size(), sh)
+    _check(st, "spec_verify_relaxed")
     return out
 
 

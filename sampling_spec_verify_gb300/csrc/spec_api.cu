@@ -770,4 +770,59 @@ spec_status_t spec_verify_ragged(const void* target_logits, const void* draft_lo
   return from_cuda(e);
 }
 
+spec_status_t spec_verify_relaxed(const void* target_logits, const void* draft_logits, spec_dtype_t dtype, int B,
+                                  int K, int V, float temperature, int top_k, float delta,
+                                  const int32_t* draft_tokens, const float* u_final, int32_t* out_tokens,
+                                  int32_t* n_accepted, float* alpha_out, uint32_t* dev_status, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (!dims_ok(B, K, V) || !dtype_ok(dtype)) return SPEC_ERR_INVALID_ARG;
+  if (!(temperature > 0.0f) || !std::isfinite(temperature) || !(delta >= 0.0f)) return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  if (!target_logits || !draft_logits || !u_final || !out_tokens || !n_accepted || !workspace)
+    return SPEC_ERR_INVALID_ARG;
+  if (K > 0 && !draft_tokens) return SPEC_ERR_INVALID_ARG;
+  const VerifyWs ws = verify_ws(B, K);
+  if (workspace_bytes < ws.total || !aligned16(workspace)) return SPEC_ERR_INVALID_ARG;
+  const long long units = (long long)B * (K + 1);
+  if (units > 0x7FFFFFFFLL) return SPEC_ERR_UNSUPPORTED;
+  const int es = elem_size(dtype);
+  Shape sh;
+  {
+    const spec_status_t r = shape_for_dt<ssv::kVerify>(dtype, units, V, 2, &sh);
+    if (r != SPEC_OK) return r;
+  }
+  SweepParams P = {};
+  P.target = target_logits;
+  P.draft = draft_logits;
+  P.B = B;
+  P.K = K;
+  P.KT = K + 1;
+  P.V = V;
+  P.units = (int)units;
+  P.S = sh.S;
+  P.L = sh.L;
+  P.nst = sh.nst;
+  P.rows = 2;
+  P.aligned = aligned16(target_logits) && aligned16(draft_logits) && ((long long)V * es) % 16 == 0;
+  P.s = (float)(1.4426950408889634 / (double)temperature);
+  P.inv_t = (float)(1.0 / (double)temperature);
+  P.relax_k = top_k;
+  P.relax_delta = delta;
+  P.draft_tokens = draft_tokens;
+  P.u_final = u_final;
+  P.out_tokens = out_tokens;
+  P.n_accepted = n_accepted;
+  P.alpha = alpha_out;
+  char* w = static_cast<char*>(workspace);
+  P.rec = reinterpret_cast<VerifyRecord*>(w + ws.rec);
+  P.part = reinterpret_cast<float*>(w + ws.part);
+  P.row_cnt = reinterpret_cast<uint32_t*>(w + ws.cnt);
+  P.rej = reinterpret_cast<uint32_t*>(w + ws.rej);
+  P.status = dev_status;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = prepare_dt<ssv::kVerifyRelaxed>(dtype);
+  if (e == cudaSuccess) e = launch_sweep_dt<ssv::kVerifyRelaxed>(dtype, P, sh, st);
+  return from_cuda(e);
+}
+
 }  // extern "C"

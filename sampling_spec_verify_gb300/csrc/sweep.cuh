@@ -54,8 +54,10 @@ constexpr uint32_t kRejBase = 128u;
 // position-major inside a group (for at least as many rows as clusters).
 // kVerifyRagged is kVerify over flattened rows of their own lengths: unit u is
 // flattened target row u, described by a packed word (row, position, bonus).
+// kVerifyRelaxed is kVerify with the relaxed (lossy) acceptance: target top-k
+// rank and log-probability gap; a rejection draws from the full target.
 enum Mode : int { kVerify = 0, kVerifyGreedy = 1, kOverlap = 2, kOverlapGreedy = 3, kE2E = 4, kDiag = 5,
-                  kVerifyGrouped = 6, kVerifyRagged = 7 };
+                  kVerifyGrouped = 6, kVerifyRagged = 7, kVerifyRelaxed = 8 };
 
 // Packed unit word of the ragged verify: row << 8 | bonus << 7 | position.
 __host__ __device__ constexpr uint32_t pack_unit(uint32_t row, uint32_t pos, bool bonus) {
@@ -117,6 +119,8 @@ struct SweepParams {
   const uint32_t* uinfo;   // ragged: [units] packed unit words
   const int32_t* roff;     // ragged: [B + 1] first flattened target row of every row
   const uint32_t* ragbad;  // ragged: nonzero when the offsets were rejected (nothing runs)
+  int relax_k;             // relaxed: top-k rank bound (<= 0: none)
+  float relax_delta;       // relaxed: log-probability gap bound (+inf: none)
   uint32_t* glob_cnt;
   uint32_t* status;
 };
@@ -316,8 +320,8 @@ __device__ __forceinline__ float draw_weights(const uint4& wt, const uint4& wd, 
 // re-zeroes the workspace of row b.
 template <int MODE>
 __device__ __forceinline__ void complete_row(const SweepParams& P, int b, int S, int lane) {
-  constexpr bool kVerifyMode =
-      (MODE == kVerify || MODE == kVerifyGreedy || MODE == kVerifyGrouped || MODE == kVerifyRagged);
+  constexpr bool kVerifyMode = (MODE == kVerify || MODE == kVerifyGreedy || MODE == kVerifyGrouped ||
+                                 MODE == kVerifyRagged || MODE == kVerifyRelaxed);
   // units of row b: [base, base + per_row); drafted positions K of them,
   // the first at dbase
   int K = P.K;
@@ -505,6 +509,7 @@ struct SweepSmem {
   float wtot[kWarps];
   float wamax[kWarps];  // diagnostics: per-warp draft arg-maximum
   int wamaxi[kWarps];
+  uint32_t wcnt[kWarps];  // relaxed: per-warp count of tokens ranked above the drafted one
   float woff[kWarps + 1];
   alignas(16) uint32_t rejw[4];  // sampling verify: the 16-byte group of row words holding this unit's row
   alignas(16) float mbox[2][kPartStride][8];  // pushed by peers: [exchange slot][sender rank][field]
@@ -527,10 +532,12 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
   constexpr int PV = E::PV;
   using Raw = typename E::Raw;
   constexpr bool kGreedy = (MODE == kVerifyGreedy || MODE == kOverlapGreedy);
-  constexpr bool kVerifyMode =
-      (MODE == kVerify || MODE == kVerifyGreedy || MODE == kVerifyGrouped || MODE == kVerifyRagged);
-  constexpr bool kSample = (MODE == kVerify || MODE == kVerifyGrouped || MODE == kVerifyRagged);  // sampling verify
+  constexpr bool kVerifyMode = (MODE == kVerify || MODE == kVerifyGreedy || MODE == kVerifyGrouped ||
+                                 MODE == kVerifyRagged || MODE == kVerifyRelaxed);
+  constexpr bool kSample =
+      (MODE == kVerify || MODE == kVerifyGrouped || MODE == kVerifyRagged || MODE == kVerifyRelaxed);
   constexpr bool kRagged = (MODE == kVerifyRagged);
+  constexpr bool kRelaxed = (MODE == kVerifyRelaxed);
   if constexpr (kRagged) {
     if (__ldg(P.ragbad)) return;  // the same word for every CTA: the whole grid returns
   }
@@ -749,6 +756,16 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
     if constexpr (kSample) {
       if (tid == 0) cp_async_16_cg(smem_addr(sm.rejw), P.rej + (x.b & ~3));
     }
+    // relaxed: the drafted token and its target logit (lane 0 of every warp,
+    // in flight during pass A)
+    int ry = -1;
+    float rzy = -INFINITY;
+    if constexpr (kRelaxed) {
+      if (lane == 0 && !x.bonus) {
+        ry = P.draft_tokens[(long long)x.b * K + x.k];
+        if (ry >= 0 && ry < V) rzy = E::to_f32(x.tg[ry]);
+      }
+    }
 
     // queued arrivals are published when the queue is full
     if (warp == 0 && __shfl_sync(kFull, sm.npend, 0) == 32) flush();
@@ -911,6 +928,22 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
         chunk_sum(st, mt, zt);
         if (x.has_draft) chunk_sum(sd, md, zd);
       }
+      if constexpr (kRelaxed) {
+        // tokens ranked above the drafted one: larger logit, or equal at a smaller index
+        const int yy = __shfl_sync(kFull, ry, 0);
+        const float zy = __shfl_sync(kFull, rzy, 0);
+        uint32_t cnt = 0;
+        if (ok && yy >= 0 && yy < V) {
+          for (int i = t_lo; i < t_hi; ++i) {
+            float xv[PV];
+            E::unpack(st[i], xv);
+#pragma unroll
+            for (int k = 0; k < PV; ++k) cnt += (xv[k] > zy || (xv[k] == zy && e0 + i * PV + k < yy)) ? 1u : 0u;
+          }
+        }
+        cnt = __reduce_add_sync(kFull, cnt);
+        if (lane == 0) sm.wcnt[warp] = cnt;
+      }
       if constexpr (MODE == kDiag) {
         // arg-maximum of the draft logits (smallest index on ties): y_hat
         float bv = -INFINITY;
@@ -974,6 +1007,11 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
           }
           av = __uint_as_float(__shfl_sync(kFull, seen, 0));
         }
+        if constexpr (kRelaxed) {
+          uint32_t c = lane < kWarps ? sm.wcnt[lane] : 0u;
+          c = __reduce_add_sync(kFull, c);
+          ai = (int)c;
+        }
         if constexpr (MODE == kDiag) {
           if (lane < kWarps) {
             av = sm.wamax[lane];
@@ -997,6 +1035,11 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
           zdy = sm.mbox[slot][own][5];
         }
         warp_combine_mz2(a, za, d, zda, s);
+        uint32_t rrank = 0;
+        if constexpr (kRelaxed) {
+          uint32_t c = lane < S ? __float_as_uint(sm.mbox[slot][lane][7]) : 0u;
+          rrank = __reduce_add_sync(kFull, c);  // rank of the drafted token in the whole row
+        }
         if constexpr (MODE == kDiag) {
           float av = mb(slot, 6, -INFINITY);
           int ai = lane < S ? __float_as_int(sm.mbox[slot][lane][7]) : 0x7FFFFFFF;
@@ -1014,6 +1057,14 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
           if constexpr (kSample) {
             if (x.bonus) {
               mode_c = 2;
+            } else if constexpr (kRelaxed) {
+              // in the target's top-k and within delta of its largest log-probability
+              const bool in_k = P.relax_k <= 0 || rrank < (uint32_t)P.relax_k;
+              const float gap = __fmul_rn(__fsub_rn(rzy, a), P.inv_t);
+              const bool in_d = !(P.relax_delta < INFINITY) || gap >= -P.relax_delta;
+              acc = (tok_ok && in_k && in_d) ? 1 : 0;
+              mode_c = acc ? 0 : 2;  // a rejection draws from the full target
+              if (!tok_ok) flags |= kBadToken;
             } else {
               // u * q(y) <= p(y), with p(y), q(y) formed like the per-element values
               const float py = __fmul_rn(ex2(fmaf(zty, s, -c1t)), izt);
@@ -1034,7 +1085,7 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
             // publish a rejection (the record will hold acc = 0), then skip a
             // draw that cannot be emitted: rank 0's reading of the row's word
             // decides for the whole cluster
-            if (rank == 0 && !x.bonus && (mode_c == 1 || mode_c == 3))
+            if (rank == 0 && !x.bonus && (mode_c == 1 || mode_c == 3 || (kRelaxed && mode_c == 2)))
               atomicMax(&P.rej[x.b], kRejBase - (uint32_t)x.k);
             const uint32_t seen = __float_as_uint(sm.mbox[slot][0][6]);
             if (seen > kRejBase - (uint32_t)x.k) {
@@ -1177,12 +1228,28 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
         const bool resid = (mode_c == 1);
         float tot = 0.0f;
         f32x2 mm2 = f2(0.0f, 0.0f);
+        // relaxed rejection: the overlap partial, element by element as pass C forms it
+        const bool ralpha = kRelaxed && attempt == 0 && x.has_draft;
+        const f32x2 CD = f2(-cd2, -cd2);
         if (ok) {
           for (int i = t_lo; i < t_hi; ++i) {
             float w[PV];
             const float rs = resid ? draw_weights<E, true>(st[i], sd[i], S2, CT, CDd, NR, w, mm2)
                                    : draw_weights<E, false>(st[i], st[i], S2, CT, CDd, NR, w, mm2);
             tot = __fadd_rn(tot, rs);
+            if (ralpha) {
+              f32x2 pt[PV / 2], pd[PV / 2], ep[PV / 2];
+              E::pairs(st[i], pt);
+              E::pairs(sd[i], pd);
+#pragma unroll
+              for (int h = 0; h < PV / 2; ++h) {
+                float t0, t1, d0, d1;
+                f2_split(f2_fma(pt[h], S2, CT), t0, t1);
+                f2_split(f2_fma(pd[h], S2, CD), d0, d1);
+                ep[h] = f2(ex2(fminf(t0, d0)), ex2(fminf(t1, d1)));
+              }
+              mm2 = f2_add(mm2, psum(ep));
+            }
           }
         }
         const float incl = warp_incl_scan(tot, lane);
@@ -1202,7 +1269,8 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
           const float ctot = __shfl_sync(kFull, wincl, kWarps - 1);
           float A = lane < kWarps ? sm.wred[lane][0] : 0.0f;
           A = warp_sum(A);
-          if (lane == 0 && attempt == 0 && resid) P.part[(long long)rec_idx(x) * kPartStride + rank] = __fmul_rn(A, izt);
+          if (lane == 0 && attempt == 0 && (resid || ralpha))
+            P.part[(long long)rec_idx(x) * kPartStride + rank] = __fmul_rn(A, izt);
           if (!skip) push8(slot, ctot, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f);
         }
         // a later rejection keeps the overlap partial, computed with the

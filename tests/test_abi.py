@@ -33,7 +33,8 @@ def test_header_declares_the_boundary():
     for want in ("spec_verify", "spec_overlap", "spec_e2e_tv_fwd_bwd", "spec_status_string",
                  "spec_verify_workspace_bytes", "spec_overlap_workspace_bytes", "spec_e2e_tv_workspace_bytes",
                  "spec_diagnostics", "spec_diagnostics_workspace_bytes", "spec_truncate_logits",
-                 "spec_schedule_lengths", "spec_verify_ragged", "spec_verify_ragged_workspace_bytes"):
+                 "spec_schedule_lengths", "spec_verify_ragged", "spec_verify_ragged_workspace_bytes",
+                 "spec_verify_relaxed"):
         assert want in names
 
 
@@ -122,3 +123,10 @@ def test_argument_validation_without_gpu(L):
     assert L.spec_verify_ragged(None, None, 1, 0, None, 0, 10, 1.0, None, None, None, None, None, None, None, None,
                                 0, None) == 0
     assert L.spec_verify_ragged_workspace_bytes(4, 3, 10) == 0
+    # relaxed verify: T > 0, delta >= 0; no rows is a no-op
+    assert L.spec_verify_relaxed(fake, fake, 1, 2, 2, 10, 0.0, 3, 1.0, fake, fake, fake, fake, None, None, ws,
+                                 1 << 20, None) == 1
+    assert L.spec_verify_relaxed(fake, fake, 1, 2, 2, 10, 1.0, 3, -1.0, fake, fake, fake, fake, None, None, ws,
+                                 1 << 20, None) == 1
+    assert L.spec_verify_relaxed(None, None, 1, 0, 2, 10, 1.0, 3, 1.0, None, None, None, None, None, None, None,
+                                 0, None) == 0
