@@ -12,9 +12,13 @@
 // HBM).  Keys are order-preserving 16-bit (bf16) or 32-bit (fp32) images of
 // the logits, selected 8 bits at a time.  Warp w always walks the same
 // contiguous chunk of the row, so per-warp counts give ordered compaction.
-//  1. maximum, NaN check and, for top-k, per-warp counts of the first digit;
-//  2. top-k: the digit where the count reaches top_k; its elements (usually a
-//     few hundred) are compacted, in index order, into shared memory, and the
+//  1. maximum and NaN check;
+//  2. top-k: for bf16, per-warp counts of the 256 keys just below the
+//     maximum's (one bin per key), which hold the top_k-th key in the usual
+//     case; the tied tokens of the threshold key are compacted, in index
+//     order, only when some of them are cut.  Otherwise (fp32, or a threshold
+//     further down) per-warp counts of the first digit; the crossing digit's
+//     elements are compacted, in index order, into shared memory, and the
 //     remaining digits and the index-order tie are resolved on that list;
 //  3. top-p: per-warp fixed-point masses (2^44 for the row maximum, summed as
 //     integers, so every cut is independent of the order of the additions)
@@ -601,22 +605,16 @@ __global__ void __launch_bounds__(kTThreads, 2) truncate_kernel(const __grid_con
     const Raw* zin = reinterpret_cast<const Raw*>(P.in) + (long long)row * V;
     Raw* zout = reinterpret_cast<Raw*>(P.out) + (long long)row * V;
 
-    // ---- pass 1: maximum, NaN check and (top-k) first-digit counts ----
+    // ---- pass 1: maximum and NaN check ----
     __syncthreads();  // the previous row is done with the shared state
-    for (int b = lane; b < 256; b += 32) sm.pc[warp][b] = 0u;
-    __syncwarp();
     float mx = -INFINITY;
     int nan = 0;
-    chunk_walk<E>(zin, V, al, [&](int, bool valid, const float (&x)[PV]) {
+    chunk_walk<E>(zin, V, al, [&](int, bool, const float (&x)[PV]) {
 #pragma unroll
       for (int j = 0; j < PV; ++j) {
         if (j >= per) break;
         mx = fmaxf(mx, x[j]);
         nan |= (x[j] != x[j]);
-        if (do_k) {
-          const uint32_t d = order_key<KB>(x[j]) >> (KB - 8);
-          if (valid) atomicAdd(&sm.pc[warp][d], 1u);  // the warp's own counters
-        }
       }
     });
 #pragma unroll
@@ -639,7 +637,56 @@ __global__ void __launch_bounds__(kTThreads, 2) truncate_kernel(const __grid_con
     uint32_t thr1 = 0;
     int tie1 = V;
     bool ok = !bad;
-    if (ok && do_k) {
+    bool done_k = !do_k;
+    if (ok && do_k && KB == 16) {
+      // bf16: per-warp counts of the 256 keys just below the maximum's, one
+      // bin per key (bin 255 - d for key kM - d); the top_k-th key usually
+      // lies among them, and elements further down cost no atomic
+      const uint32_t kM = order_key<KB>(M);
+      __syncthreads();
+      for (int b = lane; b < 256; b += 32) sm.pc[warp][b] = 0u;
+      __syncwarp();
+      chunk_walk<E>(zin, V, al, [&](int, bool valid, const float (&x)[PV]) {
+#pragma unroll
+        for (int j = 0; j < PV; ++j) {
+          if (j >= per) break;
+          const uint32_t dk = kM - order_key<KB>(x[j]);
+          if (valid && dk < 256u) atomicAdd(&sm.pc[warp][255u - dk], 1u);
+        }
+      });
+      const unsigned long long inwin = reduce_first<true>(sm);
+      if (inwin >= (unsigned long long)P.top_k) {
+        unsigned long long above = 0;
+        const int b = crossing_bin((unsigned long long)P.top_k, sm, &above);
+        thr1 = kM - (255u - (uint32_t)b);
+        const unsigned long long rem = (unsigned long long)P.top_k - above;
+        const unsigned long long nt = sm.hist[b];
+        if (rem >= nt) {
+          tie1 = V;  // every token of the threshold key is kept
+        } else if (nt <= (unsigned long long)kTCap) {
+          const uint32_t t1 = thr1;
+          const int n = compact<E>(zin, V, al, (uint32_t)b, [&](int, float x) { return order_key<KB>(x) == t1; },
+                                   sm);
+          tie1 = list_tie<KB>(n, thr1, rem, V, sm);
+        } else {
+          tie1 = tie_index<E>(zin, V, al, thr1, rem, [](int, uint32_t) { return true; }, sm);
+        }
+        done_k = true;
+      }
+    }
+    if (ok && !done_k) {
+      // first-digit counts, then the crossing digit's candidates
+      __syncthreads();
+      for (int b = lane; b < 256; b += 32) sm.pc[warp][b] = 0u;
+      __syncwarp();
+      chunk_walk<E>(zin, V, al, [&](int, bool valid, const float (&x)[PV]) {
+#pragma unroll
+        for (int j = 0; j < PV; ++j) {
+          if (j >= per) break;
+          const uint32_t d = order_key<KB>(x[j]) >> (KB - 8);
+          if (valid) atomicAdd(&sm.pc[warp][d], 1u);  // the warp's own counters
+        }
+      });
       reduce_first<true>(sm);
       unsigned long long above = 0;
       const int b1 = crossing_bin((unsigned long long)P.top_k, sm, &above);
