@@ -88,6 +88,12 @@ def barrier(ws):
         dist.barrier()
 
 
+def job_rate(ms_total_max, steps, ws, rows_per_step):
+    """Whole-job rows/s: every rank verifies rows_per_step rows per step, and
+    the job takes the slowest rank's time (weak scaling)."""
+    return ws * rows_per_step / (ms_total_max / steps * 1e-3)
+
+
 def max_over_ranks(x, ws, device):
     if ws == 1:
         return x
@@ -360,7 +366,7 @@ def run_native(args, ws, rank, local):
             per_kind[kinds_per_step[j]].append(evs[i][j][0].elapsed_time(evs[i][j][1]))
     ms_step = ms_total / args.steps
     rows_per_step = len(TEMPS) * B * K
-    value = ws * rows_per_step / (ms_step * 1e-3)
+    value = job_rate(ms_total, args.steps, ws, rows_per_step)
 
     # ---- end to end through the public API, host buffers ----
     e2e = run_e2e(args, ssv, batches, dev, stream)
