@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--single", choices=["verify", "greedy", "overlap", "e2e", "diag", "truncate", "ragged",
-                                         "schedule"], default=None,
+                                         "schedule", "relaxed"], default=None,
                     help="run only `--calls` calls of one entry point (an L2 flush before each): the "
                          "profiling target, prints no JSON")
     ap.add_argument("--shape", default="32,4,151936", help="B,K,V of --single")
@@ -466,7 +466,8 @@ def run_single(args):
     Bs, Ks, Vs = (int(v) for v in args.shape.split(","))
     dev = torch.device("cuda")
     T = 0.0 if args.single == "greedy" else (
-        1.0 if args.single in ("overlap", "e2e", "diag", "truncate", "ragged", "schedule") else args.temperature)
+        1.0 if args.single in ("overlap", "e2e", "diag", "truncate", "ragged", "schedule", "relaxed")
+        else args.temperature)
     w = synth.entropy_mix(seed=SEED, temperature=T, B=Bs, K=Ks, V=Vs)
     t, d = w.target.to(dev), w.draft.to(dev)
     y, ua, uf = w.draft_tokens.to(dev), w.u_accept.to(dev), w.u_final.to(dev)
@@ -484,6 +485,8 @@ def run_single(args):
         elif args.single == "ragged":  # every row verifies all of its positions, flattened
             offs = torch.arange(0, (Bs + 1) * (Ks + 1), Ks + 1, dtype=torch.int32, device=dev)
             ssv.verify_ragged(t.reshape(-1, Vs), d.reshape(-1, Vs), offs, y.reshape(-1), ua.reshape(-1), uf, 1.0)
+        elif args.single == "relaxed":  # top-k 8, log-probability gap 3
+            ssv.verify_relaxed(t, d, y, uf, 1.0, 8, 3.0)
         elif args.single == "schedule":  # 1024 requests x 16 positions of prefix survivals
             g = torch.Generator(device=dev).manual_seed(SEED)
             a = torch.cumprod(torch.rand((1024, 16), generator=g, device=dev) * 0.7 + 0.3, dim=1)

@@ -63,18 +63,17 @@ __global__ void __launch_bounds__(kSThreads, 1) schedule_kernel(const __grid_con
   for (int i = n + tid; i < N; i += kSThreads) keys[i] = 0ull;  // below every real key
   __syncthreads();
 
-  // ---- bitonic sort, descending ----
+  // ---- bitonic sort, descending; thread work is over pairs (i, i + j), i's bit j clear ----
   for (int k = 2; k <= N; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < N; i += kSThreads) {
-        const int p = i ^ j;
-        if (p > i) {
-          const unsigned long long a = keys[i], b = keys[p];
-          const bool desc = (i & k) == 0;
-          if (desc ? (a < b) : (a > b)) {
-            keys[i] = b;
-            keys[p] = a;
-          }
+      for (int q = tid; q < (N >> 1); q += kSThreads) {
+        const int i = ((q & ~(j - 1)) << 1) | (q & (j - 1));
+        const int p = i + j;
+        const unsigned long long a = keys[i], b = keys[p];
+        const bool desc = (i & k) == 0;
+        if (desc ? (a < b) : (a > b)) {
+          keys[i] = b;
+          keys[p] = a;
         }
       }
       __syncthreads();
