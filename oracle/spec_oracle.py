@@ -45,6 +45,9 @@ reason, in the design notes of the repository):
   within delta of the largest; the first rejection emits a draw from the
   full target distribution (no residual), the bonus stays as in the exact
   verify;
+* a candidate tree's greedy verify walks from the prefix to the first child
+  (in node order) whose token is the target argmax of the current slot, and
+  emits that argmax where no child matches;
 * top-k / top-p truncation ranks tokens by logit (ties by smaller index),
   applies top-k first, then keeps the shortest ranked prefix whose
   renormalised mass at temperature T reaches top_p; dropped logits become
@@ -387,6 +390,76 @@ def verify(target_logits, draft_logits, draft_tokens, u_accept, u_final,
         c_near[i] = res.cdf_near
         r_empty[i] = res.residual_empty
     return VerifyResult(tokens, n_acc, alpha, tv, surv, a_near, c_near, r_empty)
+
+
+# ---------------------------------------------------------------------------
+# Tree-shaped candidates: the tree attention mask and the greedy verify
+# ---------------------------------------------------------------------------
+
+def tree_mask(parent):
+    """Tree attention mask of a candidate tree given by its parent map
+    (parent[i] < i, -1 for a node hung on the committed prefix): M[u, v] = 1
+    iff v is u or a strict ancestor of u.  SpecOPD summary, section "树注意力
+    (Tree Attention)": each node sees only its ancestors and itself, so one
+    batched pass scores every node without leaking sibling branches.  Also
+    returns each node's depth (0 for a node hung on the prefix), its position
+    in the sequence it belongs to."""
+    parent = [int(x) for x in parent]
+    N = len(parent)
+    M = np.zeros((N, N), dtype=bool)
+    depth = np.zeros(N, dtype=np.int64)
+    for u in range(N):
+        v = u
+        while v >= 0:
+            M[u, v] = True
+            v = parent[v]
+        depth[u] = int(M[u].sum()) - 1
+    return M, depth
+
+
+@dataclass
+class TreeResult:
+    path: np.ndarray        # int64 [B, N]: accepted nodes, root side first, -1 after
+    tokens: np.ndarray      # int64 [B, N + 1]: their tokens, then the target's token, -1 after
+    n_accepted: np.ndarray  # int64 [B]
+
+
+def tree_verify_greedy(target_logits, parent, node_tokens):
+    """Greedy (T == 0) verify of a candidate tree, committing one path.
+
+    Speculative Decoding 与 MTP, section 4 (greedy: a candidate is kept when
+    it equals the target argmax; at the first mismatch the target's token is
+    used) and section 11 (a tree of candidates commits a single path).
+
+    target_logits [B, N + 1, V]: slot 0 holds the target's logits after the
+    committed prefix, slot i + 1 those after candidate node i (one batched
+    target pass over the tree with ``tree_mask``).  parent [B, N] with
+    parent[b, i] < i (-1: hung on the prefix); node_tokens [B, N].  From the
+    prefix, the walk moves to the first child (in node order) whose token is
+    the argmax (smallest index on ties) of the current slot; where no child
+    matches it emits that argmax and stops."""
+    zt = np.asarray(target_logits)
+    B, N1, V = zt.shape
+    N = N1 - 1
+    parent = np.asarray(parent)
+    toks = np.asarray(node_tokens)
+    path = np.full((B, N), -1, dtype=np.int64)
+    out = np.full((B, N + 1), -1, dtype=np.int64)
+    n_acc = np.zeros(B, dtype=np.int64)
+    for b in range(B):
+        cur, n = -1, 0
+        while True:
+            a = argmax_first(zt[b, cur + 1])
+            nxt = next((c for c in range(N) if int(parent[b, c]) == cur and int(toks[b, c]) == a), None)
+            if nxt is None:
+                out[b, n] = a
+                break
+            path[b, n] = nxt
+            out[b, n] = a
+            n += 1
+            cur = nxt
+        n_acc[b] = n
+    return TreeResult(path, out, n_acc)
 
 
 # ---------------------------------------------------------------------------

@@ -777,3 +777,63 @@ def test_relaxed_is_lossy_exact_enumeration():
     # the exact rule on the same pair: accepted mass min(p, q), residual the rest
     exact = np.minimum(p, q) + (1 - so.overlap(p, q)) * so.residual(p, q) / so.residual(p, q).sum()
     np.testing.assert_allclose(exact, p, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# candidate trees
+# ---------------------------------------------------------------------------
+
+def test_tree_mask_closed_forms_and_brute_force():
+    M, depth = so.tree_mask([-1, 0, 1, 2])  # a chain: lower-triangular, depth = index
+    assert (M == np.tril(np.ones((4, 4), dtype=bool))).all() and depth.tolist() == [0, 1, 2, 3]
+    M, depth = so.tree_mask([-1, -1, -1])   # siblings on the prefix: each sees itself
+    assert (M == np.eye(3, dtype=bool)).all() and depth.tolist() == [0, 0, 0]
+    # the example tree of two branches: 0 -> {1, 2}, 1 -> {3}, 2 -> {4, 5}
+    M, depth = so.tree_mask([-1, 0, 0, 1, 2, 2])
+    assert M[3].nonzero()[0].tolist() == [0, 1, 3] and M[5].nonzero()[0].tolist() == [0, 2, 5]
+    assert not M[4, 5] and not M[3, 2] and depth.tolist() == [0, 1, 1, 2, 2, 2]
+    rng = np.random.default_rng(41)
+    for _ in range(50):
+        N = int(rng.integers(1, 12))
+        par = [-1] + [int(rng.integers(-1, i)) for i in range(1, N)]
+        M, depth = so.tree_mask(par)
+        for u in range(N):
+            anc = set()
+            v = par[u]
+            while v >= 0:
+                anc.add(v)
+                v = par[v]
+            assert set(M[u].nonzero()[0].tolist()) == anc | {u}
+            assert depth[u] == len(anc)
+
+
+def test_tree_greedy_chain_is_the_linear_greedy_verify():
+    rng = np.random.default_rng(42)
+    B, K, V = 8, 5, 30
+    zt = rng.normal(size=(B, K + 1, V))
+    zt = np.round(zt * 2) / 2  # ties
+    y = np.array([[so.argmax_first(zt[b, k]) if rng.uniform() < 0.7 else int(rng.integers(0, V))
+                   for k in range(K)] for b in range(B)])
+    lin = so.verify(zt, None, y, np.zeros((B, K)), np.zeros(B), 0.0)
+    tr = so.tree_verify_greedy(zt, np.tile(np.arange(-1, K - 1), (B, 1)), y)
+    assert tr.n_accepted.tolist() == lin.n_accepted.tolist()
+    assert tr.tokens.tolist() == lin.tokens.tolist()
+    for b in range(B):
+        assert tr.path[b, : tr.n_accepted[b]].tolist() == list(range(tr.n_accepted[b]))
+
+
+def test_tree_greedy_branches_by_hand():
+    # two branches on the prefix: node 0 (token 3) and node 1 (token 5); node 1 has a child,
+    # node 2 (token 7).  The prefix slot's argmax is 5, node 1's slot argmax is 7, node 2's is 9.
+    V = 10
+    zt = np.zeros((1, 4, V))
+    zt[0, 0, 5] = 2.0   # after the prefix
+    zt[0, 1, 0] = 2.0   # after node 0 (not taken)
+    zt[0, 2, 7] = 2.0   # after node 1
+    zt[0, 3, 9] = 2.0   # after node 2
+    r = so.tree_verify_greedy(zt, [[-1, -1, 1]], [[3, 5, 7]])
+    assert r.path.tolist() == [[1, 2, -1]] and r.n_accepted.tolist() == [2]
+    assert r.tokens.tolist() == [[5, 7, 9, -1]]
+    # duplicate sibling tokens: the first in node order is taken
+    r = so.tree_verify_greedy(zt, [[-1, -1, 0]], [[5, 5, 7]])
+    assert r.path[0, 0] == 0 and r.n_accepted[0] == 1 and r.tokens[0].tolist() == [5, 0, -1, -1]
