@@ -61,7 +61,7 @@ typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
 #define SPEC_DEV_BAD_UNIFORM 4u    /* a uniform outside [0, 1) */
 #define SPEC_DEV_TIMEOUT 8u        /* a bounded wait inside a kernel gave up */
 #define SPEC_DEV_EMPTY_RESIDUAL 16u /* rejection with zero residual mass: drawn from p */
-#define SPEC_DEV_BAD_OFFSETS 32u   /* ragged verify: row offsets rejected, nothing computed */
+#define SPEC_DEV_BAD_OFFSETS 32u   /* ragged row offsets rejected (nothing computed), or a tree parent outside [-1, i) */
 
 /* Version of this ABI (bumped on any signature change). */
 int spec_abi_version(void);
@@ -135,6 +135,53 @@ spec_status_t spec_verify_relaxed(const void* target_logits,
                                   int32_t* n_accepted, float* alpha_out,
                                   uint32_t* dev_status, void* workspace,
                                   size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Candidate trees.
+ *
+ * A tree of N candidate nodes per row is given by parent[b][i] < i (-1: the
+ * node hangs on the committed prefix).  "SpecOPD", section "树注意力(Tree
+ * Attention)": node u may attend to v iff v is u or an ancestor of u, so one
+ * batched target pass scores every node without leaking sibling branches.
+ *
+ * spec_tree_mask: mask [B, N, N] uint8 (written): 1 iff v is u or an
+ * ancestor of u; depth [B, N] int32 or NULL: the number of strict ancestors
+ * (the node's offset past the prefix).  A parent outside [-1, i) sets
+ * SPEC_DEV_BAD_OFFSETS and stops that node's walk.
+ */
+spec_status_t spec_tree_mask(const int32_t* parent, int B, int N,
+                             uint8_t* mask, int32_t* depth,
+                             uint32_t* dev_status, void* stream);
+
+/* Greedy (T = 0) verify of a candidate tree, committing one path per row:
+ * "Speculative Decoding 与 MTP", section 4 (keep a candidate equal to the
+ * target argmax; the first mismatch emits the target's token) and section 11
+ * (a tree commits a single path).
+ *
+ * target_logits [B, N + 1, V] dtype: slot 0 after the committed prefix, slot
+ *               i + 1 after node i (one target pass over the tree, masked as
+ *               spec_tree_mask gives).
+ * parent, node_tokens [B, N] int32.
+ * From the prefix, the walk moves to the first child (node order) whose token
+ * is the current slot's argmax (smallest index on ties), and emits that argmax
+ * where no child matches.
+ * path        [B, N] int32 (written): accepted nodes, prefix side first, -1 after.
+ * out_tokens  [B, N + 1] int32 (written): their tokens, then the emitted
+ *             target token, then -1.
+ * n_accepted  [B] int32 (written): accepted nodes (-1 for a bad parent map).
+ * Sampling (T > 0) over trees needs a multi-candidate acceptance rule that
+ * the cited pages do not give; it is not provided.
+ */
+size_t spec_tree_verify_workspace_bytes(int B, int N, int V);
+
+spec_status_t spec_tree_verify_greedy(const void* target_logits,
+                                      spec_dtype_t dtype, int B, int N, int V,
+                                      const int32_t* parent,
+                                      const int32_t* node_tokens,
+                                      int32_t* path, int32_t* out_tokens,
+                                      int32_t* n_accepted,
+                                      uint32_t* dev_status, void* workspace,
+                                      size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Ragged verify: every row verifies its own number of drafted tokens, in

@@ -13,6 +13,9 @@ Entry points (same names as the C ABI, see include/spec_verify.h):
                          flattened tensors and row offsets;
 * ``verify_relaxed``  -- LOSSY relaxed acceptance (target top-k rank and
                          log-probability gap);
+* ``tree_mask``, ``tree_verify_greedy`` -- candidate trees: the attention
+                         mask of a parent map, and the greedy verify that
+                         commits one path;
 * ``overlap``         -- alpha = sum min(p, q), TV, prefix survival, E[tau];
 * ``e2e_tv_fwd_bwd``  -- E2E-TV loss and its draft-logit gradient;
 * ``diagnostics``     -- alpha, target entropy, cross-entropy, KL and the
@@ -33,8 +36,8 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "SpecError", "lib", "verify", "verify_ragged", "verify_relaxed", "overlap", "e2e_tv_fwd_bwd", "diagnostics", "truncate_logits", "schedule_lengths", "launch_shape",
-    "set_launch_override", "VerifyOutput", "OverlapOutput", "E2EOutput", "DiagOutput", "HostVerifier",
+    "SpecError", "lib", "verify", "verify_ragged", "verify_relaxed", "tree_mask", "tree_verify_greedy", "overlap", "e2e_tv_fwd_bwd", "diagnostics", "truncate_logits", "schedule_lengths", "launch_shape",
+    "set_launch_override", "VerifyOutput", "OverlapOutput", "E2EOutput", "DiagOutput", "TreeOutput", "HostVerifier",
     "DEV_BAD_TOKEN", "DEV_BAD_LOGITS", "DEV_BAD_UNIFORM", "DEV_TIMEOUT", "DEV_EMPTY_RESIDUAL", "DEV_BAD_OFFSETS",
     "SPEC_OK", "SPEC_ERR_INVALID_ARG", "SPEC_ERR_UNSUPPORTED", "SPEC_ERR_CUDA",
 ]
@@ -98,6 +101,12 @@ def lib():
     L.spec_verify_ragged.argtypes = [vp, vp, i32, i32, vp, i32, i32, f32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.spec_verify_relaxed.restype = i32
     L.spec_verify_relaxed.argtypes = [vp, vp, i32, i32, i32, i32, f32, i32, f32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.spec_tree_mask.restype = i32
+    L.spec_tree_mask.argtypes = [vp, i32, i32, vp, vp, vp, vp]
+    L.spec_tree_verify_workspace_bytes.restype = sz
+    L.spec_tree_verify_workspace_bytes.argtypes = [i32, i32, i32]
+    L.spec_tree_verify_greedy.restype = i32
+    L.spec_tree_verify_greedy.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.spec_launch_shape.restype = i32
     L.spec_launch_shape.argtypes = [i32, i32, i32] + [ctypes.POINTER(i32)] * 5
     L.spec_set_launch_override.restype = None
@@ -291,6 +300,55 @@ def verify_relaxed(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torc
                                _ptr(out.n_accepted), _ptr(out.alpha), _ptr(out.status), _ptr(ws),
                                ws.numel() * ws.element_size(), sh)
     _check(st, "spec_verify_relaxed")
+    return out
+
+
+def tree_mask(parent: torch.Tensor, *, status: Optional[torch.Tensor] = None,
+              stream: Optional[torch.cuda.Stream] = None):
+    """Tree attention mask of parent maps [B, N] (int32, parent[i] < i, -1
+    on the prefix): (mask uint8 [B, N, N], depth int32 [B, N])."""
+    L = lib()
+    _need(parent, "parent", dtype=torch.int32)
+    B, N = parent.shape
+    dev = parent.device
+    mask = torch.empty((B, N, N), dtype=torch.uint8, device=dev)
+    depth = torch.empty((B, N), dtype=torch.int32, device=dev)
+    sh, _ = _stream_handle(stream, dev)
+    _check(L.spec_tree_mask(_ptr(parent), B, N, _ptr(mask), _ptr(depth), _ptr(status), sh), "spec_tree_mask")
+    return mask, depth
+
+
+@dataclass
+class TreeOutput:
+    path: torch.Tensor        # int32 [B, N]
+    tokens: torch.Tensor      # int32 [B, N + 1]
+    n_accepted: torch.Tensor  # int32 [B]
+    status: torch.Tensor
+
+
+def tree_verify_greedy(target: torch.Tensor, parent: torch.Tensor, node_tokens: torch.Tensor, *,
+                       workspace: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None) -> TreeOutput:
+    """Greedy verify of candidate trees: target [B, N + 1, V] (slot 0 after
+    the prefix, slot i + 1 after node i), parent and node_tokens [B, N]."""
+    L = lib()
+    _need(target, "target")
+    B, N1, V = target.shape
+    N = N1 - 1
+    dev = target.device
+    _need(parent, "parent", dtype=torch.int32, shape=(B, N), device=dev)
+    _need(node_tokens, "node_tokens", dtype=torch.int32, shape=(B, N), device=dev)
+    out = TreeOutput(torch.empty((B, N), dtype=torch.int32, device=dev),
+                     torch.empty((B, N + 1), dtype=torch.int32, device=dev),
+                     torch.empty((B,), dtype=torch.int32, device=dev),
+                     torch.zeros((1,), dtype=torch.int32, device=dev))
+    sh, s = _stream_handle(stream, dev)
+    need = L.spec_tree_verify_workspace_bytes(B, N, V)
+    ws = workspace if workspace is not None else _workspace(need, dev, s)
+    st = L.spec_tree_verify_greedy(_ptr(target), _dtype_code(target), B, N, V, _ptr(parent), _ptr(node_tokens),
+                                   _ptr(out.path), _ptr(out.tokens), _ptr(out.n_accepted), _ptr(out.status),
+                                   _ptr(ws), ws.numel() * ws.element_size(), sh)
+    _check(st, "spec_tree_verify_greedy")
     return out
 
 

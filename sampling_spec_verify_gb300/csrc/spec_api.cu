@@ -15,6 +15,7 @@
 #include "sweep.cuh"
 #include "truncate.cuh"
 #include "schedule.cuh"
+#include "tree.cuh"
 
 namespace {
 
@@ -823,6 +824,69 @@ spec_status_t spec_verify_relaxed(const void* target_logits, const void* draft_l
   cudaError_t e = prepare_dt<ssv::kVerifyRelaxed>(dtype);
   if (e == cudaSuccess) e = launch_sweep_dt<ssv::kVerifyRelaxed>(dtype, P, sh, st);
   return from_cuda(e);
+}
+
+spec_status_t spec_tree_mask(const int32_t* parent, int B, int N, uint8_t* mask, int32_t* depth,
+                             uint32_t* dev_status, void* stream) {
+  if (B < 0 || N < 0) return SPEC_ERR_INVALID_ARG;
+  if (B == 0 || N == 0) return SPEC_OK;
+  if (!parent || !mask) return SPEC_ERR_INVALID_ARG;
+  const long long n = (long long)B * N;
+  if (n * N > (1ll << 40)) return SPEC_ERR_UNSUPPORTED;
+  const unsigned grid = (unsigned)((n + 255) / 256);
+  ssv::tree_mask_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(parent, B, N, mask, depth,
+                                                                             dev_status);
+  return from_cuda(cudaGetLastError());
+}
+
+size_t spec_tree_verify_workspace_bytes(int B, int N, int V) {
+  if (B < 0 || N < 0 || V < 1) return 0;
+  return align256((size_t)B * (N + 1) * sizeof(int32_t));
+}
+
+spec_status_t spec_tree_verify_greedy(const void* target_logits, spec_dtype_t dtype, int B, int N, int V,
+                                      const int32_t* parent, const int32_t* node_tokens, int32_t* path,
+                                      int32_t* out_tokens, int32_t* n_accepted, uint32_t* dev_status,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 0 || N < 0 || V < 1 || !dtype_ok(dtype)) return SPEC_ERR_INVALID_ARG;
+  if (B == 0) return SPEC_OK;
+  if (!target_logits || !out_tokens || !n_accepted || !workspace) return SPEC_ERR_INVALID_ARG;
+  if (N > 0 && (!parent || !node_tokens || !path)) return SPEC_ERR_INVALID_ARG;
+  if (workspace_bytes < spec_tree_verify_workspace_bytes(B, N, V) || !aligned16(workspace))
+    return SPEC_ERR_INVALID_ARG;
+  const long long units = (long long)B * (N + 1);
+  if (units > 0x7FFFFFFFLL) return SPEC_ERR_UNSUPPORTED;
+  const int es = elem_size(dtype);
+  Shape sh;
+  {
+    const spec_status_t r = shape_for_dt<ssv::kVerifyGreedy>(dtype, units, V, 1, &sh);
+    if (r != SPEC_OK) return r;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t* am = static_cast<int32_t*>(workspace);  // target argmax of every slot
+  SweepParams P = {};
+  P.target = target_logits;
+  P.B = B;
+  P.K = N + 1;
+  P.KT = N + 1;
+  P.V = V;
+  P.units = (int)units;
+  P.S = sh.S;
+  P.L = sh.L;
+  P.nst = sh.nst;
+  P.rows = 1;
+  P.aligned = aligned16(target_logits) && ((long long)V * es) % 16 == 0;
+  P.out_tokens = am;
+  P.status = dev_status;
+  cudaError_t e = prepare_dt<ssv::kArgmax>(dtype);
+  if (e == cudaSuccess) e = launch_sweep_dt<ssv::kArgmax>(dtype, P, sh, st);
+  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  ssv::tree_walk_kernel<<<(B + 127) / 128, 128, 0, st>>>(am, parent, node_tokens, B, N, path, out_tokens,
+                                                          n_accepted, dev_status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  // the argmax array is the only workspace written: leave it zero
+  return from_cuda(cudaMemsetAsync(am, 0, (size_t)units * sizeof(int32_t), st));
 }
 
 }  // extern "C"

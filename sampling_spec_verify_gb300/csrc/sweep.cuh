@@ -56,8 +56,10 @@ constexpr uint32_t kRejBase = 128u;
 // flattened target row u, described by a packed word (row, position, bonus).
 // kVerifyRelaxed is kVerify with the relaxed (lossy) acceptance: target top-k
 // rank and log-probability gap; a rejection draws from the full target.
+// kArgmax writes the target argmax of every unit (a candidate tree's slots)
+// to out_tokens, with no row completion.
 enum Mode : int { kVerify = 0, kVerifyGreedy = 1, kOverlap = 2, kOverlapGreedy = 3, kE2E = 4, kDiag = 5,
-                  kVerifyGrouped = 6, kVerifyRagged = 7, kVerifyRelaxed = 8 };
+                  kVerifyGrouped = 6, kVerifyRagged = 7, kVerifyRelaxed = 8, kArgmax = 9 };
 
 // Packed unit word of the ragged verify: row << 8 | bonus << 7 | position.
 __host__ __device__ constexpr uint32_t pack_unit(uint32_t row, uint32_t pos, bool bonus) {
@@ -531,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
 
   constexpr int PV = E::PV;
   using Raw = typename E::Raw;
-  constexpr bool kGreedy = (MODE == kVerifyGreedy || MODE == kOverlapGreedy);
+  constexpr bool kGreedy = (MODE == kVerifyGreedy || MODE == kOverlapGreedy || MODE == kArgmax);
   constexpr bool kVerifyMode = (MODE == kVerify || MODE == kVerifyGreedy || MODE == kVerifyGrouped ||
                                  MODE == kVerifyRagged || MODE == kVerifyRelaxed);
   constexpr bool kSample =
@@ -618,6 +620,7 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
     }
     x.has_draft = !x.bonus;
     if constexpr (MODE == kVerifyGreedy) x.has_draft = !x.bonus && P.alpha != nullptr;
+    if constexpr (MODE == kArgmax) x.has_draft = false;
     if constexpr (kRagged) {
       x.tg = reinterpret_cast<const Raw*>(P.target) + (long long)u * V;
       x.dg = x.has_draft ? reinterpret_cast<const Raw*>(P.draft) + (long long)(u - x.b) * V : nullptr;
@@ -878,10 +881,14 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
             r.pad0 = r.pad1 = 0;
             P.rec[rec_idx(x)] = r;
           }
-          P.part[(long long)rec_idx(x) * kPartStride] = al;
+          if constexpr (MODE == kArgmax) {
+            P.out_tokens[rec_idx(x)] = am_t;
+          } else {
+            P.part[(long long)rec_idx(x) * kPartStride] = al;
+          }
           if (flags && P.status) atomicOr(P.status, flags);
         }
-        if (lane == 0) queue_arrival(x.b);
+        if (MODE != kArgmax && lane == 0) queue_arrival(x.b);
       }
       continue;
     } else {

@@ -34,7 +34,8 @@ def test_header_declares_the_boundary():
                  "spec_verify_workspace_bytes", "spec_overlap_workspace_bytes", "spec_e2e_tv_workspace_bytes",
                  "spec_diagnostics", "spec_diagnostics_workspace_bytes", "spec_truncate_logits",
                  "spec_schedule_lengths", "spec_verify_ragged", "spec_verify_ragged_workspace_bytes",
-                 "spec_verify_relaxed"):
+                 "spec_verify_relaxed", "spec_tree_mask", "spec_tree_verify_greedy",
+                 "spec_tree_verify_workspace_bytes"):
         assert want in names
 
 
@@ -130,3 +131,9 @@ def test_argument_validation_without_gpu(L):
                                  1 << 20, None) == 1
     assert L.spec_verify_relaxed(None, None, 1, 0, 2, 10, 1.0, 3, 1.0, None, None, None, None, None, None, None,
                                  0, None) == 0
+    # trees: sizes >= 0, a workspace for the argmax of every slot; empty is a no-op
+    assert L.spec_tree_mask(fake, -1, 3, fake, None, None, None) == 1
+    assert L.spec_tree_mask(None, 0, 3, None, None, None, None) == 0
+    assert L.spec_tree_verify_greedy(fake, 1, 2, 3, 10, fake, fake, fake, fake, fake, None, ws, 8, None) == 1
+    assert L.spec_tree_verify_greedy(None, 1, 0, 3, 10, None, None, None, None, None, None, None, 0, None) == 0
+    assert L.spec_tree_verify_workspace_bytes(2, 3, 10) >= 2 * 4 * 4
