@@ -609,6 +609,20 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
       x.k = j / rg;
       x.b = r0 + (j - x.k * rg);
       x.bonus = (x.k == K);
+    } else if constexpr (MODE == kVerify) {
+      // drafted positions row-major, then every row's bonus: the last units
+      // read the target only and usually skip their draw (a rejection in
+      // the row is known by then)
+      const int nd = P.B * K;
+      if (u < nd) {
+        x.b = u / K;
+        x.k = u - x.b * K;
+        x.bonus = false;
+      } else {
+        x.b = u - nd;
+        x.k = K;
+        x.bonus = true;
+      }
     } else if constexpr (kVerifyMode) {
       x.b = u / (K + 1);
       x.k = u - x.b * (K + 1);
