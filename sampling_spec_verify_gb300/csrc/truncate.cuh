@@ -64,6 +64,58 @@ struct TruncSmem {
   int tie;
 };
 
+// Per-warp 32-bit limb counters, kept in the candidate arrays' storage while a
+// histogram pass runs (the list is not in use then): a weight w <= 2^44 adds
+// its low 22 bits to lo[d] and the rest to hi[d] with native 32-bit shared
+// atomics, and every 3 steps of 256 elements the limbs are folded into the
+// warp's 64-bit histogram, before either could overflow.
+struct Limbs {
+  uint32_t* lo;
+  uint32_t* hi;
+  unsigned long long* ph;
+  int steps;
+  bool dirty;  // limbs may be nonzero
+  __device__ __forceinline__ Limbs(TruncSmem& sm, int warp)
+      : lo(reinterpret_cast<uint32_t*>(sm.cand_idx) + warp * 256),
+        hi(reinterpret_cast<uint32_t*>(sm.cand_x) + warp * 256),
+        ph(sm.ph[warp]),
+        steps(0),
+        dirty(false) {}
+  __device__ __forceinline__ void zero(int lane) {
+    for (int b = lane; b < 256; b += 32) {
+      lo[b] = 0u;
+      hi[b] = 0u;
+      ph[b] = 0ull;
+    }
+    __syncwarp();
+  }
+  __device__ __forceinline__ void add(uint32_t d, unsigned long long w) {
+    atomicAdd(lo + d, (uint32_t)(w & 0x3FFFFFull));
+    const uint32_t h = (uint32_t)(w >> 22);
+    if (h) atomicAdd(hi + d, h);
+  }
+  __device__ __forceinline__ void flush(int lane) {
+    if (!dirty) return;
+    dirty = false;
+    __syncwarp();
+    for (int b = lane; b < 256; b += 32) {
+      ph[b] += (unsigned long long)lo[b] + ((unsigned long long)hi[b] << 22);
+      lo[b] = 0u;
+      hi[b] = 0u;
+    }
+    __syncwarp();
+  }
+  // once per 32 lanes x PV elements, warp-converged; added: this lane added a weight
+  __device__ __forceinline__ void step(int lane, bool added) {
+    dirty |= __any_sync(kFull, added);
+    if (++steps == 3) {
+      flush(lane);
+      steps = 0;
+    }
+  }
+};
+static_assert(sizeof(int) * kTCap >= kTWarps * 256 * sizeof(uint32_t), "limbs fit in the candidate storage");
+
 // Order-preserving key of a logit (larger value, larger key), -0 folded onto
 // +0, keeping the top KB bits (16 for bf16 values, whose low bits are zero).
 template <int KB>
@@ -178,10 +230,9 @@ __device__ void hist_pass(const typename E::Raw* row, int V, bool aligned, uint3
   constexpr int KB = 8 * E::ES;
   constexpr int PV = E::PV;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  unsigned long long* ph = sm.ph[warp];
   __syncthreads();  // readers of the previous pass's histograms are done
-  for (int b = lane; b < 256; b += 32) ph[b] = 0ull;
-  __syncwarp();
+  Limbs lb(sm, warp);
+  lb.zero(lane);
   const int nitem = aligned ? V / PV : V;
   const int per = aligned ? PV : 1;
   for (int base = warp * 32; base < nitem; base += kTThreads * kTUnroll) {
@@ -202,6 +253,7 @@ __device__ void hist_pass(const typename E::Raw* row, int V, bool aligned, uint3
       const int i = base + u * kTThreads + lane;
       if (base + u * kTThreads >= nitem) break;  // warp-uniform
       const bool valid = i < nitem;
+      bool added = false;
       float x[PV];
 #pragma unroll
       for (int j = 0; j < PV; ++j) x[j] = -INFINITY;
@@ -219,16 +271,13 @@ __device__ void hist_pass(const typename E::Raw* row, int V, bool aligned, uint3
         const bool on = valid && (key & pmask) == prefix && elig(v, key);
         const unsigned long long w = on ? (kCount ? 1ull : wt(x[j])) : 0ull;
         const uint32_t digit = (key >> shift) & 255u;
-        if constexpr (kCount) {
-          // lanes with equal digits: the lowest adds the group's count
-          const unsigned grp = __match_any_sync(kFull, on ? digit : 0x100u);
-          if (on && lane == __ffs(grp) - 1) atomicAdd(&ph[digit], (unsigned long long)__popc(grp));
-        } else if (w) {
-          atomicAdd(&ph[digit], w);  // the warp's own histogram: conflicts only within the warp
-        }
+        if (w) lb.add(digit, w);  // the warp's own counters: conflicts only within the warp
+        added |= (w != 0ull);
       }
+      lb.step(lane, added);
     }
   }
+  lb.flush(lane);
   __syncthreads();
   for (int b = threadIdx.x; b < 256; b += kTThreads) {
     unsigned long long t = 0;
@@ -717,13 +766,11 @@ __global__ void __launch_bounds__(kTThreads, 2) truncate_kernel(const __grid_con
     if (ok && do_p) {
       // pass: fixed-point masses and counts of the first digit over the top-k set
       __syncthreads();
-      for (int b = lane; b < 256; b += 32) {
-        sm.ph[warp][b] = 0ull;
-        sm.pc[warp][b] = 0u;
-      }
-      __syncwarp();
-      unsigned long long* ph = sm.ph[warp];
+      for (int b = lane; b < 256; b += 32) sm.pc[warp][b] = 0u;
+      Limbs lb(sm, warp);
+      lb.zero(lane);
       chunk_walk<E>(zin, V, al, [&](int i, bool valid, const float (&x)[PV]) {
+        bool added = false;
 #pragma unroll
         for (int j = 0; j < PV; ++j) {
           if (j >= per) break;
@@ -733,10 +780,15 @@ __global__ void __launch_bounds__(kTThreads, 2) truncate_kernel(const __grid_con
           if (on) {
             atomicAdd(&sm.pc[warp][d], 1u);
             const unsigned long long w = fixed_mass(x[j], M, s);
-            if (w) atomicAdd(&ph[d], w);
+            if (w) {
+              lb.add(d, w);
+              added = true;
+            }
           }
         }
+        lb.step(lane, added);
       });
+      lb.flush(lane);
       const unsigned long long z = reduce_first<false>(sm);
       unsigned long long tau = (unsigned long long)ceil((double)P.top_p * (double)z);
       if (tau == 0ull) tau = 1ull;
