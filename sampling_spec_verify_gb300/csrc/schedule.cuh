@@ -7,9 +7,11 @@
 //
 // For a fixed B the best tau takes the B - R largest survivals; a row's
 // survivals are non-increasing (products of acceptances), so the taken ones
-// form a prefix of every row.  One CTA: sort all survivals (bitonic, in shared
-// memory, descending, ties in (row, position) order), prefix sums in fp64,
-// Theta for every B, the argmax (smaller B on ties), and the per-row counts.
+// form a prefix of every row.  One CTA: the rows are already sorted runs, so
+// they are merged pairwise (log2 R rounds; every element finds its place by a
+// binary search in the partner run) into one order, survival descending with
+// ties in (row, position) order; prefix sums in fp64, Theta for every B, the
+// argmax (smaller B on ties), and the per-row counts.
 #pragma once
 
 #include <cstdint>
@@ -29,21 +31,27 @@ struct SchedParams {
   uint32_t* status;
 };
 
+// Element a precedes element b in the merged order.
+__device__ __forceinline__ bool sched_before(const float* val, int a, int b) {
+  const float va = val[a], vb = val[b];
+  return va > vb || (va == vb && a < b);
+}
+
 __global__ void __launch_bounds__(kSThreads, 1) schedule_kernel(const __grid_constant__ SchedParams P) {
-  extern __shared__ __align__(16) unsigned long long keys[];  // [N] then int lens[R]
+  extern __shared__ __align__(16) unsigned char sched_smem[];  // val[n], idx[2][n]
   __shared__ double wsum[kSThreads / 32];
   __shared__ double wbest[kSThreads / 32];
   __shared__ int wbestm[kSThreads / 32];
   __shared__ int bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int R = P.R, L = P.L, n = R * L;
-  int N = 1;
-  while (N < n) N <<= 1;
-  int* lens = reinterpret_cast<int*>(keys + N);
+  float* val = reinterpret_cast<float*>(sched_smem);
+  int* idx0 = reinterpret_cast<int*>(val + n);
+  int* idx1 = idx0 + n;
   if (tid == 0) bad = 0;
   __syncthreads();
 
-  // ---- keys: running minimum along each row (survival bits << 32 | ~index) ----
+  // ---- running minimum along each row: every row is a sorted run ----
   for (int r = tid; r < R; r += kSThreads) {
     float run = INFINITY;
     int nan = 0;
@@ -54,37 +62,53 @@ __global__ void __launch_bounds__(kSThreads, 1) schedule_kernel(const __grid_con
         nan = 1;
       }
       run = fminf(run, fmaxf(a, 0.0f));
-      const uint32_t idx = (uint32_t)(r * L + j);
-      keys[idx] = ((unsigned long long)__float_as_uint(run) << 32) | (unsigned long long)(~idx);
+      val[r * L + j] = run;
+      idx0[r * L + j] = r * L + j;
     }
-    lens[r] = 0;
     if (nan) bad = 1;
   }
-  for (int i = n + tid; i < N; i += kSThreads) keys[i] = 0ull;  // below every real key
   __syncthreads();
 
-  // ---- bitonic sort, descending; thread work is over pairs (i, i + j), i's bit j clear ----
-  for (int k = 2; k <= N; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int q = tid; q < (N >> 1); q += kSThreads) {
-        const int i = ((q & ~(j - 1)) << 1) | (q & (j - 1));
-        const int p = i + j;
-        const unsigned long long a = keys[i], b = keys[p];
-        const bool desc = (i & k) == 0;
-        if (desc ? (a < b) : (a > b)) {
-          keys[i] = b;
-          keys[p] = a;
+  // ---- pairwise merges of runs of width w: log2(R) rounds ----
+  int* src = idx0;
+  int* dst = idx1;
+  for (int w = L; w < n; w <<= 1) {
+    for (int p = tid; p < n; p += kSThreads) {
+      const int run = p / w;
+      const int start = run * w;
+      const int e = src[p];
+      const int pstart = (run & 1) ? start - w : start + w;  // the partner run
+      int out = p;
+      if (pstart < n) {
+        const int plen = min(w, n - pstart);
+        // elements of the partner run that precede e (all keys are distinct)
+        int lo = 0, hi = plen;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (sched_before(val, src[pstart + mid], e))
+            lo = mid + 1;
+          else
+            hi = mid;
         }
+        out = min(start, pstart) + (p - start) + lo;
       }
-      __syncthreads();
+      dst[out] = e;
     }
+    __syncthreads();
+    int* t = src;
+    src = dst;
+    dst = t;
   }
+  const int* order = src;  // merged order: survival descending, ties in (row, position) order
+  int* lens = dst;          // free now (R <= n): per-row counts of taken survivals
+  for (int r = tid; r < R; r += kSThreads) lens[r] = 0;
+  __syncthreads();
 
   // ---- prefix sums over sorted positions: thread t owns [t*C, (t+1)*C) ----
   const int C = (n + kSThreads - 1) / kSThreads;
   const int lo = min(tid * C, n), hi = min(lo + C, n);
   double part = 0.0;
-  for (int i = lo; i < hi; ++i) part += (double)__uint_as_float((uint32_t)(keys[i] >> 32));
+  for (int i = lo; i < hi; ++i) part += (double)val[order[i]];
   // block exclusive scan of the thread sums
   double incl = part;
 #pragma unroll
@@ -115,7 +139,7 @@ __global__ void __launch_bounds__(kSThreads, 1) schedule_kernel(const __grid_con
     best_m = 0;
   }
   for (int i = lo; i < hi; ++i) {
-    run += (double)__uint_as_float((uint32_t)(keys[i] >> 32));
+    run += (double)val[order[i]];
     const int m = i + 1;
     const double th = ((double)R + run) * (double)P.sps[R + m];
     if (th > best) {
@@ -161,9 +185,9 @@ __global__ void __launch_bounds__(kSThreads, 1) schedule_kernel(const __grid_con
   // ---- lengths: taken positions per row; tau ----
   double taken = 0.0;
   for (int i = tid; i < mstar; i += kSThreads) {
-    const uint32_t idx = ~(uint32_t)(keys[i] & 0xFFFFFFFFull);
-    atomicAdd(&lens[idx / (uint32_t)L], 1);
-    taken += (double)__uint_as_float((uint32_t)(keys[i] >> 32));
+    const int e = order[i];
+    atomicAdd(&lens[e / L], 1);
+    taken += (double)val[e];
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) taken += __shfl_xor_sync(kFull, taken, o);
