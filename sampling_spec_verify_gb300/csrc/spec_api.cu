@@ -299,26 +299,33 @@ RaggedWs ragged_ws(int B, long long units) {
   w.cnt = w.part + part_bytes(units);
   w.rej = w.cnt + align256((size_t)B * sizeof(uint32_t));
   w.uinfo = w.rej + align256((size_t)B * sizeof(uint32_t));
-  w.bad = w.uinfo + align256((size_t)units * sizeof(uint32_t));
+  w.bad = w.uinfo + align256((size_t)units * sizeof(uint2));
   w.total = w.bad + 256;
   return w;
 }
 
-// One thread per row: checks the row's offsets and writes its packed unit
-// words; any bad row sets the flag that makes the sweep return at once.
-__global__ void ragged_units_kernel(const int32_t* roff, int B, int units, uint32_t* uinfo, uint32_t* bad,
+// One thread per row: checks the row's offsets and writes its units' entries
+// {flattened target row, packed word}; any bad row sets the flag that makes
+// the sweep return at once.
+__global__ void ragged_units_kernel(const int32_t* roff, int B, int units, uint2* uinfo, uint32_t* bad,
                                     uint32_t* status) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const int s0 = roff[b], s1 = roff[b + 1];
   const int l = s1 - s0 - 1;
-  const bool ok = s0 >= 0 && s1 > s0 && l <= kMaxK && s1 <= units && (b > 0 || s0 == 0) && (b < B - 1 || s1 == units);
+  const int d0 = s0 - b;  // drafted positions of the rows before b (valid offsets)
+  const bool ok = s0 >= 0 && s1 > s0 && l <= kMaxK && s1 <= units && (b > 0 || s0 == 0) &&
+                  (b < B - 1 || s1 == units) && d0 >= 0 && d0 + l <= units - B;
   if (!ok) {
     atomicOr(bad, 1u);
     if (status) atomicOr(status, SPEC_DEV_BAD_OFFSETS);
     return;
   }
-  for (int k = 0; k <= l; ++k) uinfo[s0 + k] = ssv::pack_unit((uint32_t)b, (uint32_t)k, k == l);
+  // drafted positions first, in flattened order, then every row's bonus: the
+  // last units read the target only and usually skip their draw
+  for (int k = 0; k < l; ++k)
+    uinfo[d0 + k] = make_uint2((uint32_t)(s0 + k), ssv::pack_unit((uint32_t)b, (uint32_t)k, false));
+  uinfo[units - B + b] = make_uint2((uint32_t)(s0 + l), ssv::pack_unit((uint32_t)b, (uint32_t)l, true));
 }
 
 bool dims_ok(int B, int K, int V) { return B >= 0 && K >= 0 && K <= kMaxK && V >= 1; }
@@ -727,7 +734,7 @@ spec_status_t spec_verify_ragged(const void* target_logits, const void* draft_lo
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(workspace);
-  uint32_t* uinfo = reinterpret_cast<uint32_t*>(w + ws.uinfo);
+  uint2* uinfo = reinterpret_cast<uint2*>(w + ws.uinfo);
   uint32_t* bad = reinterpret_cast<uint32_t*>(w + ws.bad);
   ragged_units_kernel<<<(B + 255) / 256, 256, 0, st>>>(row_offsets, B, units, uinfo, bad, dev_status);
   cudaError_t e = cudaGetLastError();

@@ -118,7 +118,7 @@ struct SweepParams {
   float* row_loss;
   uint32_t* row_cnt;
   uint32_t* rej;  // [B] sampling verify: kRejBase - (earliest rejected position seen), 0 if none
-  const uint32_t* uinfo;   // ragged: [units] packed unit words
+  const uint2* uinfo;      // ragged: [units] {flattened target row, packed unit word}, drafts first
   const int32_t* roff;     // ragged: [B + 1] first flattened target row of every row
   const uint32_t* ragbad;  // ragged: nonzero when the offsets were rejected (nothing runs)
   int relax_k;             // relaxed: top-k rank bound (<= 0: none)
@@ -591,8 +591,9 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
   auto decode = [&](int u) {
     Unit x;
     if constexpr (kRagged) {
-      x.u = u;
-      const uint32_t w = __ldg(P.uinfo + u);
+      const uint2 w2 = __ldg(P.uinfo + u);
+      x.u = (int)w2.x;  // the unit's flattened target row (its record index)
+      const uint32_t w = w2.y;
       x.b = (int)(w >> 8);
       x.k = (int)(w & 0x7Fu);
       x.bonus = (w & 0x80u) != 0u;
@@ -636,8 +637,8 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
     if constexpr (MODE == kVerifyGreedy) x.has_draft = !x.bonus && P.alpha != nullptr;
     if constexpr (MODE == kArgmax) x.has_draft = false;
     if constexpr (kRagged) {
-      x.tg = reinterpret_cast<const Raw*>(P.target) + (long long)u * V;
-      x.dg = x.has_draft ? reinterpret_cast<const Raw*>(P.draft) + (long long)(u - x.b) * V : nullptr;
+      x.tg = reinterpret_cast<const Raw*>(P.target) + (long long)x.u * V;
+      x.dg = x.has_draft ? reinterpret_cast<const Raw*>(P.draft) + (long long)(x.u - x.b) * V : nullptr;
     } else {
       x.tg = reinterpret_cast<const Raw*>(P.target) + ((long long)x.b * P.KT + x.k) * V;
       x.dg = x.has_draft ? reinterpret_cast<const Raw*>(P.draft) + ((long long)x.b * K + x.k) * V : nullptr;
@@ -737,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
     uf_ = 0.0f;
     if constexpr (kVerifyMode) {
       const Unit x = decode(u);
-      const long long di = kRagged ? (long long)(u - x.b) : (long long)x.b * K + x.k;  // drafted position
+      const long long di = kRagged ? (long long)(x.u - x.b) : (long long)x.b * K + x.k;  // drafted position
       if (!x.bonus) y_ = P.draft_tokens[di];
       if constexpr (kSample) {
         if (!x.bonus) ua_ = P.u_accept[di];
@@ -754,6 +755,7 @@ __global__ void __launch_bounds__(kThreads, 4) sweep_kernel(const SweepParams P)
     if (u >= P.units) break;
     const int stg = (nst == 2) ? (it & 1) : 0;
     const uint32_t par = (nst == 2) ? ((uint32_t)(it >> 1) & 1u) : ((uint32_t)it & 1u);
+
     if (nst == 2) {
       if (u + G < P.units) issue(u + G, stg ^ 1);
       prefetch(u + 2 * G);
