@@ -56,7 +56,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--single", choices=["verify", "greedy", "overlap", "e2e", "diag", "truncate", "ragged",
-                                         "schedule", "relaxed"], default=None,
+                                         "schedule", "relaxed", "tree"], default=None,
                     help="run only `--calls` calls of one entry point (an L2 flush before each): the "
                          "profiling target, prints no JSON")
     ap.add_argument("--shape", default="32,4,151936", help="B,K,V of --single")
@@ -508,6 +508,9 @@ def run_single(args):
             ssv.verify_ragged(t.reshape(-1, Vs), d.reshape(-1, Vs), offs, y.reshape(-1), ua.reshape(-1), uf, 1.0)
         elif args.single == "relaxed":  # top-k 8, log-probability gap 3
             ssv.verify_relaxed(t, d, y, uf, 1.0, 8, 3.0)
+        elif args.single == "tree":  # every row's K drafts as a chain-shaped tree over its K+1 slots
+            par = torch.arange(-1, Ks - 1, dtype=torch.int32, device=dev).repeat(Bs, 1)
+            ssv.tree_verify_greedy(t, par, y)
         elif args.single == "schedule":  # 1024 requests x 16 positions of prefix survivals
             g = torch.Generator(device=dev).manual_seed(SEED)
             a = torch.cumprod(torch.rand((1024, 16), generator=g, device=dev) * 0.7 + 0.3, dim=1)
