@@ -288,6 +288,8 @@ def verify_relaxed(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torc
     _need(draft, "draft", dtype=target.dtype, shape=(B, K, V), device=dev)
     _need(draft_tokens, "draft_tokens", dtype=torch.int32, shape=(B, K), device=dev)
     _need(u_final, "u_final", dtype=torch.float32, shape=(B,), device=dev)
+    if K == 0:
+        draft = draft_tokens = None  # an empty tensor may have no storage
     out = VerifyOutput(torch.empty((B, K + 1), dtype=torch.int32, device=dev),
                        torch.empty((B,), dtype=torch.int32, device=dev),
                        torch.empty((B, K), dtype=torch.float32, device=dev) if want_alpha else None,

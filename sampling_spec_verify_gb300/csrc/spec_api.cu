@@ -784,9 +784,8 @@ spec_status_t spec_verify_relaxed(const void* target_logits, const void* draft_l
   if (!dims_ok(B, K, V) || !dtype_ok(dtype)) return SPEC_ERR_INVALID_ARG;
   if (!(temperature > 0.0f) || !std::isfinite(temperature) || !(delta >= 0.0f)) return SPEC_ERR_INVALID_ARG;
   if (B == 0) return SPEC_OK;
-  if (!target_logits || !draft_logits || !u_final || !out_tokens || !n_accepted || !workspace)
-    return SPEC_ERR_INVALID_ARG;
-  if (K > 0 && !draft_tokens) return SPEC_ERR_INVALID_ARG;
+  if (!target_logits || !u_final || !out_tokens || !n_accepted || !workspace) return SPEC_ERR_INVALID_ARG;
+  if (K > 0 && (!draft_logits || !draft_tokens)) return SPEC_ERR_INVALID_ARG;
   const VerifyWs ws = verify_ws(B, K);
   if (workspace_bytes < ws.total || !aligned16(workspace)) return SPEC_ERR_INVALID_ARG;
   const long long units = (long long)B * (K + 1);
@@ -809,7 +808,7 @@ spec_status_t spec_verify_relaxed(const void* target_logits, const void* draft_l
   P.L = sh.L;
   P.nst = sh.nst;
   P.rows = 2;
-  P.aligned = aligned16(target_logits) && aligned16(draft_logits) && ((long long)V * es) % 16 == 0;
+  P.aligned = aligned16(target_logits) && (!draft_logits || aligned16(draft_logits)) && ((long long)V * es) % 16 == 0;
   P.s = (float)(1.4426950408889634 / (double)temperature);
   P.inv_t = (float)(1.0 / (double)temperature);
   P.relax_k = top_k;
