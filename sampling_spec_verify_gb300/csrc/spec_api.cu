@@ -288,7 +288,8 @@ DiagWs diag_ws(int B, int K) {
 }
 
 // Ragged verify workspace: records and partials per unit, row counters and
-// row words, then the packed unit words and the offsets-rejected flag.
+// row words, then the unit entries {flattened row, packed word} and the
+// offsets-rejected flag.
 struct RaggedWs {
   size_t rec = 0, part = 0, cnt = 0, rej = 0, uinfo = 0, bad = 0, total = 0;
 };
