@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--shape", default="32,4,151936", help="B,K,V of --single")
     ap.add_argument("--temperature", type=float, default=1.0, help="T of --single verify")
     ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--sweep", action="store_true",
+                    help="time verify at B in {1,8,32,64,128,256} x K in {1,2,4,7,16}, V=151936 (one line per point)")
     return ap.parse_args()
 
 
@@ -576,8 +578,49 @@ def run_single(args):
     print("ok", args.single, Bs, Ks, Vs, T)
 
 
+def run_sweep():
+    """Verify at every point of the shape grid: N(0, 2^2) target logits,
+    draft = target + N(0, 0.5^2), bf16, T = 1, drafted tokens from the
+    draft; CUDA events around one call after a 512 MB L2 flush, median of 11."""
+    import sampling_spec_verify_gb300 as ssv
+    dev = torch.device("cuda")
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    peak, _ = hbm_peak()
+    for Bs in (1, 8, 32, 64, 128, 256):
+        for Ks in (1, 2, 4, 7, 16):
+            g = torch.Generator(device=dev).manual_seed(Bs * 100 + Ks)
+            t = (torch.randn((Bs, Ks + 1, V), device=dev, generator=g) * 2).to(torch.bfloat16)
+            d = (t[:, :Ks].float() + 0.5 * torch.randn((Bs, Ks, V), device=dev, generator=g)).to(torch.bfloat16)
+            gum = -torch.log(-torch.log(torch.rand((Bs, Ks, V), device=dev, generator=g).clamp_min(1e-20)))
+            y = torch.argmax(d.float() + gum, dim=2).to(torch.int32)
+            del gum
+            ua = torch.rand((Bs, Ks), device=dev, generator=g)
+            uf = torch.rand((Bs,), device=dev, generator=g)
+            o = ssv.verify(t, d, y, ua, uf, 1.0)
+            ts = []
+            for i in range(13):
+                flush.zero_()
+                a, b = torch.cuda.Event(True), torch.cuda.Event(True)
+                a.record()
+                ssv.verify(t, d, y, ua, uf, 1.0, out=o)
+                b.record()
+                torch.cuda.synchronize()
+                if i >= 2:
+                    ts.append(a.elapsed_time(b) * 1e3)
+            us = statistics.median(ts)
+            by = Bs * (2 * Ks + 1) * V * 2
+            print(json.dumps({"B": Bs, "K": Ks, "V": V, "us": round(us, 1), "rows_per_s": round(Bs * Ks / us * 1e6),
+                              "GB_s": round(by / us / 1e3), "frac_of_measured_hbm": round(by / us / 1e3 / peak, 3)}),
+                  flush=True)
+            del t, d, y, o
+            torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
+    if args.sweep:
+        run_sweep()
+        return
     if args.single:
         run_single(args)
         return
