@@ -10,8 +10,14 @@
 //
 // One CTA per row; every pass streams the row through L2 (the first one from
 // HBM).  Keys are order-preserving 16-bit (bf16) or 32-bit (fp32) images of
-// the logits, selected 8 bits at a time.  Warp w always walks the same
-// contiguous chunk of the row, so per-warp counts give ordered compaction.
+// the logits.  Warp w always walks the same contiguous chunk of the row, so
+// per-warp counts give ordered compaction.
+// bf16 rows take the value-histogram path first: the maximum pass also counts
+// every bf16 value (one bin per value, three merged bins for the extremes);
+// both cuts are read off the histogram, the top-p masses as count x mass of
+// each value; the write pass keeps every element of the last cut's key, marks
+// them in a bitmap and drops the ones past the kept count.  Two passes in
+// all, unless a cut falls in a merged bin: then the row takes the radix path:
 //  1. maximum and NaN check;
 //  2. top-k: for bf16, per-warp counts of the 256 keys just below the
 //     maximum's (one bin per key), which hold the top_k-th key in the usual
@@ -62,6 +68,9 @@ struct TruncSmem {
   unsigned long long bc;
   int bin;
   int tie;
+  uint32_t wc[kTWarps];           // per-warp counts of a tie walk
+  int xbin;                       // crossing bin of the value histogram
+  unsigned long long xabove;      // weight above it
 };
 
 // Per-warp 32-bit limb counters, kept in the candidate arrays' storage while a
@@ -636,6 +645,189 @@ __device__ int crossing_bin(unsigned long long need, TruncSmem& sm, unsigned lon
   return bin;
 }
 
+// ---- bf16 value histogram: both cuts from one counting pass ---------------------
+// A bf16 row holds few distinct values, so the pass that finds the maximum
+// also counts every value: one bin per bf16 value for 2^-24 <= |x| < 2^16
+// (both signs, full 7-bit mantissa), plus three merged bins: x <= -2^16,
+// |x| < 2^-24 (zeros included) and x >= 2^16.  Bins ascend with the value,
+// so the ranking order is the bins' order, top down.  Every element of a
+// one-value bin has the same fixed-point mass, so a bin's mass is count x
+// mass, the same integer the per-element sums give.  The merged bins only
+// take part while that stays exact: the small-magnitude bin when |M| >= 2
+// (every x there then gives fl(x - M) = -M), the large negative bin when
+// its masses are provably zero, and no cut may fall in a merged bin.
+// Otherwise the row takes the radix path.
+constexpr int kFLo = 103;                        // biased exponent of 2^-24
+constexpr int kFHi = 142;                        // biased exponent of 2^15
+constexpr int kNF = (kFHi - kFLo + 1) * 128;     // one-value bins per sign
+constexpr int kNB = 2 * kNF + 3;                 // with the three merged bins
+constexpr int kBinTiny = kNF + 1;                // |x| < 2^-24
+constexpr int kTieSteps = 128;                   // per-warp step counts a tie walk keeps
+static_assert(kNB * sizeof(uint32_t) <= sizeof(unsigned long long) * kTWarps * 256 + sizeof(uint32_t) * kTWarps * 256,
+              "the value histogram fits in the radix histograms' storage");
+static_assert(kTWarps * kTieSteps * sizeof(uint16_t) <= sizeof(int) * kTCap, "step counts fit in the candidate storage");
+
+__device__ __forceinline__ uint32_t* value_hist(TruncSmem& sm) { return reinterpret_cast<uint32_t*>(&sm.ph[0][0]); }
+
+// Bin of a bf16 value held in a float.
+__device__ __forceinline__ int value_bin(float x) {
+  const uint32_t u = __float_as_uint(x) >> 16;
+  const uint32_t mag = u & 0x7FFFu;
+  if (mag < (uint32_t)(kFLo << 7)) return kBinTiny;
+  if (mag > (uint32_t)((kFHi << 7) | 0x7F)) return (u & 0x8000u) ? 0 : kNB - 1;
+  const int f = (int)mag - (kFLo << 7);
+  return (u & 0x8000u) ? kNF - f : kNF + 2 + f;
+}
+
+// The value of a one-value bin.
+__device__ __forceinline__ float bin_value(int b) {
+  const bool neg = b <= kNF;
+  const int f = neg ? kNF - b : b - (kNF + 2);
+  return __uint_as_float((((uint32_t)((kFLo << 7) + f)) | (neg ? 0x8000u : 0u)) << 16);
+}
+
+// Top-down crossing over the value histogram: thread t owns kNB / kTThreads
+// consecutive bins, walked downward, and thread order is descending bin
+// order.  wt(b) is bin b's weight; need_of(total) the weight to reach.
+// Returns the bin where the running weight first reaches it (-1: never);
+// *above gets the weight of the bins above, *need the target.
+template <class Wt, class Need>
+__device__ int value_crossing(Wt wt, Need need_of, TruncSmem& sm, unsigned long long* above,
+                              unsigned long long* need) {
+  constexpr int C = (kNB + kTThreads - 1) / kTThreads;
+  const int hi = kNB - (int)threadIdx.x * C;  // exclusive
+  const int lo = max(hi - C, 0);
+  unsigned long long t = 0;
+  for (int b = hi - 1; b >= lo; --b) t += wt(b);
+  unsigned long long total;
+  const unsigned long long incl = block_incl_scan_u64(t, sm, &total);
+  const unsigned long long nd = need_of(total);
+  if (threadIdx.x == 0) sm.xbin = -1;
+  __syncthreads();
+  const unsigned long long excl = incl - t;
+  if (excl < nd && nd <= incl) {
+    unsigned long long run = excl;
+    for (int b = hi - 1; b >= lo; --b) {
+      const unsigned long long w = wt(b);
+      if (run + w >= nd) {
+        sm.xbin = b;
+        sm.xabove = run;
+        break;
+      }
+      run += w;
+    }
+  }
+  __syncthreads();
+  const int b = sm.xbin;
+  *above = b >= 0 ? sm.xabove : 0ull;
+  *need = nd;
+  __syncthreads();  // xbin / xabove reuse
+  return b;
+}
+
+// Index of the need-th (1-based) eligible element of key thr, in index order;
+// V if there are fewer.  Every warp counts the tied elements of its chunk,
+// step by step (the chunk_walk order); the warp holding the need-th one
+// reloads only the step that holds it.
+template <class E, class Elig>
+__device__ int tie_walk(const typename E::Raw* row, int V, bool aligned, uint32_t thr, unsigned long long need,
+                        Elig elig, TruncSmem& sm) {
+  constexpr int KB = 8 * E::ES;
+  constexpr int PV = E::PV;
+  constexpr int kStep = 32 * kTUnroll;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int per = aligned ? PV : 1;
+  const int nitem = aligned ? V / PV : V;
+  const int cw = (nitem + kTWarps - 1) / kTWarps;
+  const int lo = min(warp * cw, nitem), hi = min(lo + cw, nitem);
+  uint16_t* ws = reinterpret_cast<uint16_t*>(sm.cand_idx) + warp * kTieSteps;
+  auto load = [&](int i, float (&x)[PV]) {
+#pragma unroll
+    for (int j = 0; j < PV; ++j) x[j] = -INFINITY;
+    if (i < hi) {
+      if (aligned)
+        E::unpack(__ldcg(reinterpret_cast<const uint4*>(row) + i), x);
+      else
+        x[0] = E::to_f32(__ldcg(row + i));
+    }
+  };
+  auto tied = [&](int i, const float (&x)[PV]) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < PV; ++j) {
+      if (j >= per) break;
+      const uint32_t key = order_key<KB>(x[j]);
+      if (i < hi && key == thr && elig(aligned ? i * PV + j : i, key)) m |= 1u << j;
+    }
+    return m;
+  };
+  uint32_t c = 0;
+  int step = 0;
+  for (int base = lo; base < hi; base += kStep, ++step) {
+    float x[kTUnroll][PV];
+#pragma unroll
+    for (int u = 0; u < kTUnroll; ++u) load(base + u * 32 + lane, x[u]);
+    uint32_t cs = 0;
+#pragma unroll
+    for (int u = 0; u < kTUnroll; ++u) cs += __popc(tied(base + u * 32 + lane, x[u]));
+    cs = __reduce_add_sync(kFull, cs);
+    if (lane == 0 && step < kTieSteps) ws[step] = (uint16_t)cs;
+    c += cs;
+  }
+  if (lane == 0) sm.wc[warp] = c;
+  if (threadIdx.x == 0) sm.tie = V;
+  __syncthreads();
+  unsigned long long run = 0;
+  int cwarp = -1;
+  for (int w = 0; w < kTWarps; ++w) {
+    if (run + sm.wc[w] >= need) {
+      cwarp = w;
+      break;
+    }
+    run += sm.wc[w];
+  }
+  if (warp == cwarp) {
+    unsigned long long k = need - run;  // rank inside this warp's chunk
+    const int nsteps = (hi - lo + kStep - 1) / kStep;
+    int s0 = 0;
+    if (nsteps <= kTieSteps) {  // skip whole steps by their recorded counts
+      while (s0 < nsteps && (unsigned long long)ws[s0] < k) {
+        k -= ws[s0];
+        ++s0;
+      }
+    }
+    for (int base = lo + s0 * kStep; base < hi && k > 0; base += 32) {
+      float x[PV];
+      const int i = base + lane;
+      load(i, x);
+      const uint32_t m = tied(i, x);
+      const int cc = __popc(m);
+      int incl = cc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const unsigned long long tot = (unsigned long long)__shfl_sync(kFull, incl, 31);
+      if (tot >= k) {
+        const unsigned long long ex = (unsigned long long)(incl - cc);
+        if (ex < k && k <= (unsigned long long)incl) {
+          uint32_t mm = m;
+          for (unsigned long long r = k - ex; r > 1; --r) mm &= mm - 1u;
+          const int j = __ffs(mm) - 1;
+          sm.tie = aligned ? i * PV + j : i;
+        }
+        break;
+      }
+      k -= tot;
+    }
+  }
+  __syncthreads();
+  const int t = sm.tie;
+  __syncthreads();  // tie / wc / step counts reuse
+  return t;
+}
+
 template <class E>
 __global__ void __launch_bounds__(kTThreads, 2) truncate_kernel(const __grid_constant__ TruncParams P) {
   extern __shared__ __align__(16) unsigned char tsm_raw[];
@@ -654,16 +846,22 @@ __global__ void __launch_bounds__(kTThreads, 2) truncate_kernel(const __grid_con
     const Raw* zin = reinterpret_cast<const Raw*>(P.in) + (long long)row * V;
     Raw* zout = reinterpret_cast<Raw*>(P.out) + (long long)row * V;
 
-    // ---- pass 1: maximum and NaN check ----
+    // ---- pass 1: maximum and NaN check (bf16: and the value histogram) ----
+    constexpr bool kHist = KB == 16;
+    const bool vh = kHist && (do_k || do_p);
     __syncthreads();  // the previous row is done with the shared state
+    if (vh)
+      for (int b = threadIdx.x; b < kNB; b += kTThreads) value_hist(sm)[b] = 0u;
+    __syncthreads();
     float mx = -INFINITY;
     int nan = 0;
-    chunk_walk<E>(zin, V, al, [&](int, bool, const float (&x)[PV]) {
+    chunk_walk<E>(zin, V, al, [&](int, bool valid, const float (&x)[PV]) {
 #pragma unroll
       for (int j = 0; j < PV; ++j) {
         if (j >= per) break;
         mx = fmaxf(mx, x[j]);
         nan |= (x[j] != x[j]);
+        if (kHist && vh && valid) atomicAdd(value_hist(sm) + value_bin(x[j]), 1u);
       }
     });
 #pragma unroll
@@ -687,7 +885,103 @@ __global__ void __launch_bounds__(kTThreads, 2) truncate_kernel(const __grid_con
     int tie1 = V;
     bool ok = !bad;
     bool done_k = !do_k;
-    if (ok && do_k && KB == 16) {
+    // ---- top-p over the top-k set: key thr2, ties kept up to index tie2 ----
+    uint32_t thr2 = 0;
+    int tie2 = V;
+    bool done_p = !do_p;
+
+    // ---- bf16: both cuts from the value histogram ----
+    // The last active cut leaves one key thrF of which only the first nF
+    // tied elements (index order) stay: the write pass keeps every element
+    // of that key and marks them in a bitmap, then drops the ones after the
+    // nF-th.  Rows too long for the bitmap find the index with a tie walk.
+    uint32_t thrF = 0;
+    unsigned long long nF = 0;
+    bool fix = false;
+    if constexpr (kHist) if (vh && ok) {
+      const uint32_t* H = value_hist(sm);
+      bool fast = H[kNB - 1] == 0u;  // no value at or above 2^16
+      int b1 = -1;                   // the top-k cut's bin; bins below it are dropped
+      unsigned long long keep1 = 0;  // kept elements of bin b1
+      int bF = -1;
+      if (fast && do_k) {
+        unsigned long long above = 0, need = 0;
+        const int b = value_crossing([&](int bb) { return (unsigned long long)H[bb]; },
+                                     [&](unsigned long long) { return (unsigned long long)P.top_k; }, sm, &above,
+                                     &need);
+        if (b <= 0 || b == kBinTiny) {
+          fast = false;  // a cut among merged values
+        } else {
+          thr1 = order_key<KB>(bin_value(b));
+          const unsigned long long rem = need - above, nt = H[b];
+          b1 = b;
+          keep1 = rem < nt ? rem : nt;
+          bF = b;
+          thrF = thr1;
+          nF = keep1;
+        }
+      }
+      if (fast && do_p) {
+        // merged bins with a mass: |x| < 2^-24 needs fl(x - M) = -M; x <= -2^16 needs zero mass
+        if (H[kBinTiny] != 0u && !(fabsf(M) >= 2.0f)) fast = false;
+        if (H[0] != 0u && !(__fmul_rn(__fsub_rn(-65536.0f, M), s) <= -60.0f)) fast = false;
+      }
+      if (fast && do_p) {
+        auto mass = [&](int bb) -> unsigned long long {
+          unsigned long long c = H[bb];
+          if (do_k) {
+            if (bb < b1) return 0ull;
+            if (bb == b1) c = keep1;
+          }
+          if (c == 0ull || bb == 0) return 0ull;
+          return c * fixed_mass(bb == kBinTiny ? 0.0f : bin_value(bb), M, s);
+        };
+        unsigned long long above = 0, tau = 0;
+        const int c = value_crossing(mass,
+                                     [&](unsigned long long z) {
+                                       const unsigned long long t =
+                                           (unsigned long long)ceil((double)P.top_p * (double)z);
+                                       return t == 0ull ? 1ull : t;
+                                     },
+                                     sm, &above, &tau);
+        if (c <= 0 || c == kBinTiny) {
+          fast = false;
+        } else {
+          // c >= b1: the top-p cut lies inside the top-k set
+          const float xc = bin_value(c);
+          thr2 = order_key<KB>(xc);
+          // tied tokens share one mass: keep the first ceil(rest / w) of them
+          const unsigned long long w = fixed_mass(xc, M, s);
+          const unsigned long long rest = tau - above;
+          const unsigned long long nk = w ? (rest + w - 1) / w : 1ull;
+          const unsigned long long avail = (do_k && c == b1) ? keep1 : (unsigned long long)H[c];
+          bF = c;
+          thrF = thr2;
+          nF = nk < avail ? nk : avail;
+        }
+      }
+      if (fast) {
+        done_k = true;
+        done_p = true;
+        if (nF < (unsigned long long)H[bF]) {
+          if ((V + 31) / 32 <= kTCap) {
+            fix = true;
+          } else {
+            const int t = tie_walk<E>(zin, V, al, thrF, nF, [](int, uint32_t) { return true; }, sm);
+            if (do_p) tie2 = t;
+            else tie1 = t;
+          }
+        }
+      } else {  // the radix path recomputes both cuts
+        thr1 = 0;
+        tie1 = V;
+        thr2 = 0;
+        tie2 = V;
+        thrF = 0;
+        nF = 0;
+      }
+    }
+    if (ok && !done_k && KB == 16) {
       // bf16: per-warp counts of the 256 keys just below the maximum's, one
       // bin per key (bin 255 - d for key kM - d); the top_k-th key usually
       // lies among them, and elements further down cost no atomic
@@ -760,10 +1054,7 @@ __global__ void __launch_bounds__(kTThreads, 2) truncate_kernel(const __grid_con
     }
     auto kept1 = [&](int v, uint32_t key) { return key > thr1 || (key == thr1 && v <= tie1); };
 
-    // ---- top-p over the top-k set: key thr2, ties kept up to index tie2 ----
-    uint32_t thr2 = 0;
-    int tie2 = V;
-    if (ok && do_p) {
+    if (ok && !done_p) {
       // pass: fixed-point masses and counts of the first digit over the top-k set
       __syncthreads();
       for (int b = lane; b < 256; b += 32) sm.pc[warp][b] = 0u;
@@ -828,11 +1119,18 @@ __global__ void __launch_bounds__(kTThreads, 2) truncate_kernel(const __grid_con
     // a row with NaN or infinite logits (or none finite) is copied unchanged
     if ((bad || !ok) && threadIdx.x == 0 && P.status) atomicOr(P.status, kBadLogits);
     const bool cut = ok && (do_k || do_p);
+    uint32_t* tie_bits = reinterpret_cast<uint32_t*>(sm.cand_idx);  // one bit per index of the row
     auto keep = [&](int v, float x) {
       if (!cut) return true;
       const uint32_t key = order_key<KB>(x);
-      return kept1(v, key) && (!do_p || key > thr2 || (key == thr2 && v <= tie2));
+      const bool k = kept1(v, key) && (!do_p || key > thr2 || (key == thr2 && v <= tie2));
+      if (fix && k && key == thrF) atomicOr(tie_bits + (v >> 5), 1u << (v & 31));
+      return k;
     };
+    if (fix) {
+      for (int w = threadIdx.x; w < (V + 31) / 32; w += kTThreads) tie_bits[w] = 0u;
+      __syncthreads();
+    }
 
     // ---- write pass ----
     if (al) {
@@ -870,6 +1168,44 @@ __global__ void __launch_bounds__(kTThreads, 2) truncate_kernel(const __grid_con
       for (int v = threadIdx.x; v < V; v += kTThreads) {
         const Raw r = __ldcg(zin + v);
         zout[v] = keep(v, E::to_f32(r)) ? r : E::kNegInf;
+      }
+    }
+    if (fix) {
+      // the nF-th marked index in index order; every later marked element is dropped
+      __syncthreads();
+      const int nw = (V + 31) / 32;
+      const int per_t = (nw + kTThreads - 1) / kTThreads;
+      const int w0 = min((int)threadIdx.x * per_t, nw), w1 = min(w0 + per_t, nw);
+      unsigned long long c = 0;
+      for (int w = w0; w < w1; ++w) c += __popc(tie_bits[w]);
+      unsigned long long total;
+      const unsigned long long incl = block_incl_scan_u64(c, sm, &total);
+      if (threadIdx.x == 0) sm.tie = V;
+      __syncthreads();
+      const unsigned long long ex = incl - c;
+      if (ex < nF && nF <= incl) {
+        unsigned long long k = nF - ex;
+        for (int w = w0; w < w1; ++w) {
+          const uint32_t m = tie_bits[w];
+          const unsigned long long pc = (unsigned long long)__popc(m);
+          if (pc >= k) {
+            uint32_t mm = m;
+            for (unsigned long long r = k; r > 1; --r) mm &= mm - 1u;
+            sm.tie = w * 32 + __ffs(mm) - 1;
+            break;
+          }
+          k -= pc;
+        }
+      }
+      __syncthreads();
+      const int tF = sm.tie;
+      for (int w = w0; w < w1; ++w) {
+        uint32_t m = tie_bits[w];
+        while (m) {
+          const int v = w * 32 + __ffs(m) - 1;
+          m &= m - 1u;
+          if (v > tF) zout[v] = E::kNegInf;
+        }
       }
     }
     __syncthreads();  // shared state is reused by the next row

@@ -104,6 +104,37 @@ def test_ties_at_both_cuts(ssv):
     _check_rows(zb, out, 1.0, 30, 0.93)
 
 
+@pytest.mark.parametrize("k,p", [(50, 1.0), (0, 0.9), (50, 0.9), (3000, 0.95), (8000, 0.999)])
+def test_value_histogram_limits(ssv, k, p):
+    """bf16 rows at the limits of the one-pass value histogram, each against
+    the oracle: dropped (-inf) logits, values at or above 2^16, zeros beside
+    a small maximum, a top-k cut among -inf, ties, zeros beside a large
+    maximum, mostly tiny values, and a wide range."""
+    V = 8192
+    g = torch.Generator().manual_seed(5)
+    z = torch.randn(8, V, generator=g) * 2
+    z[0, ::3] = -float("inf")                     # an already truncated row
+    z[1, :100] = 70000.0                          # at and above 2^16
+    z[1, 100:200] = 65536.0
+    z[2] = torch.log_softmax(z[2], 0)             # log-probabilities: maximum near 0
+    z[2, ::5] = 0.0                               # zeros beside it
+    z[3, 40:] = -float("inf")                     # fewer finite logits than some top_k
+    z[4] = torch.round(z[4] * 4) / 4              # heavy ties
+    z[5, ::2] = 0.0                               # zeros beside a maximum above 2
+    z[6] = torch.randn(V, generator=g) * 1e-6     # magnitudes around 2^-20
+    z[7] = z[7] * 300                             # a wide range
+    zb = z.to(torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = ssv.truncate_logits(zb.to(DEV), 1.0, k, p, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    _check_rows(zb, out, 1.0, k, p)
+    if p == 1.0:  # top-k of a top-k row keeps it
+        again = ssv.truncate_logits(out, 1.0, k, 1.0)
+        torch.cuda.synchronize()
+        assert torch.equal(again, out)
+
+
 def test_full_size_verify_batch_and_verify_on_truncated(ssv):
     """The verify batch (B=32, K=4, V=151936): truncate target and draft
     identically, draw the drafted tokens from the truncated q, verify, and
