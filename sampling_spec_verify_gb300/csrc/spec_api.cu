@@ -682,14 +682,14 @@ spec_status_t spec_schedule_lengths(const float* survival, int R, int L, const f
   if ((long long)sps_len < (long long)R * (1 + L) + 1) return SPEC_ERR_INVALID_ARG;
   if (!survival || !sps || !lengths) return SPEC_ERR_INVALID_ARG;
   if ((long long)R * L > ssv::kSchedMaxItems) return SPEC_ERR_UNSUPPORTED;
-  const size_t smem = (size_t)R * L * (sizeof(float) + 2 * sizeof(int));
+  const size_t smem = ssv::sched_smem_bytes(R * L);
   static std::atomic<uint64_t> prepared{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return SPEC_ERR_CUDA;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(prepared.load(std::memory_order_acquire) & bit)) {
-    const size_t most = (size_t)ssv::kSchedMaxItems * (sizeof(float) + 2 * sizeof(int));
+    const size_t most = ssv::sched_smem_bytes(ssv::kSchedMaxItems);
     e = cudaFuncSetAttribute(ssv::schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
     if (e != cudaSuccess) return SPEC_ERR_CUDA;
     prepared.fetch_or(bit, std::memory_order_release);

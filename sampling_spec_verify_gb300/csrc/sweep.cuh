@@ -347,13 +347,13 @@ __device__ __forceinline__ void complete_row(const SweepParams& P, int b, int S,
     const VerifyRecord* rr = P.rec + base;
     // acc: 1 accepted, 0 rejected, 2 rejected with an empty residual
     int nacc = K, acc_first = 1;
-    for (int base = 0; base < K; base += 32) {
-      const int kk = base + lane;
+    for (int k0 = 0; k0 < K; k0 += 32) {
+      const int kk = k0 + lane;
       const int a = (kk < K) ? __ldcg(&rr[kk].acc) : 1;
       const unsigned m = __ballot_sync(kFull, (a & 1) == 0);
       if (m) {
         const int l = __ffs(m) - 1;
-        nacc = base + l;
+        nacc = k0 + l;
         acc_first = __shfl_sync(kFull, a, l);
         break;
       }
