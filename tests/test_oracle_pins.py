@@ -581,6 +581,26 @@ def test_truncation_worked_example():
     assert near and _kept(out) in ([0], [0, 1])
 
 
+def test_truncation_masked_logits():
+    # z = (1, -inf, 0, -inf, 2) at T = 1: masked tokens have p = 0, so
+    # p = (e, 0, 1, 0, e^2) / (e^2 + e + 1) = (0.244728, 0, 0.090031, 0, 0.665241);
+    # ranking 4, 0, 2, then the masked tokens 1, 3 by index; preceding masses
+    # along it 0, 0.665241, 0.909969, 1, 1.
+    z = np.array([1.0, -np.inf, 0.0, -np.inf, 2.0])
+    cases = [
+        (2, 1.0, [0, 4]),
+        (0, 0.5, [4]),          # 0.665 >= 0.5
+        (0, 0.7, [0, 4]),       # 0.665 < 0.7 <= 0.910
+        (0, 0.95, [0, 2, 4]),   # 0.910 < 0.95; the masked tokens add no mass
+        (4, 0.95, [0, 2, 4]),   # top-4 takes masked token 1 too; it stays -inf
+    ]
+    for k, tp, want in cases:
+        out, near = so.truncate_logits(z, 1.0, k, tp)
+        assert _kept(out) == want, (k, tp)
+        assert not near
+        assert (out[want] == z[want]).all() and np.isneginf(np.delete(out, want)).all()
+
+
 def test_truncation_closed_forms():
     z = np.zeros(10)  # uniform: the preceding mass of rank i is i / 10
     for tp, n in ((0.35, 4), (0.05, 1), (0.5, 5), (0.95, 10)):
