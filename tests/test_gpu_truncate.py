@@ -104,7 +104,7 @@ def test_ties_at_both_cuts(ssv):
     _check_rows(zb, out, 1.0, 30, 0.93)
 
 
-@pytest.mark.parametrize("k,p", [(50, 1.0), (0, 0.9), (50, 0.9), (3000, 0.95), (8000, 0.999)])
+@pytest.mark.parametrize("k,p", [(50, 1.0), (3000, 1.0), (0, 0.9), (50, 0.9), (3000, 0.95), (8000, 0.999)])
 def test_value_histogram_limits(ssv, k, p):
     """bf16 rows at the limits of the one-pass value histogram, each against
     the oracle: dropped (-inf) logits, values at or above 2^16, zeros beside
