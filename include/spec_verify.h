@@ -406,6 +406,22 @@ spec_status_t spec_schedule_lengths(const float* survival, int R, int L,
                                     uint32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Failure-path self-test of the bounded wait.
+ *
+ * Launches one warp that waits, with the same bounded mbarrier wait the
+ * sweep uses on its bulk copies, for a phase of a fresh shared-memory
+ * mbarrier that nothing ever completes.  No copy is in flight.  After
+ * limit_ns nanoseconds of wall time the wait gives up, and the kernel ORs
+ * SPEC_DEV_TIMEOUT into *dev_status and returns.  Tests use it to check that
+ * a wait that runs out is reported on the status word and that the context
+ * stays usable afterwards.
+ * limit_ns   in [1, 10^10] (10 s).
+ * dev_status [1] uint32, device (required).
+ * Returns SPEC_ERR_INVALID_ARG for a limit out of range or a NULL status.
+ */
+spec_status_t spec_selftest_bounded_wait(uint64_t limit_ns, uint32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Launch shape the library picks for a verify sweep over `units` (row,
  * position) pairs of V logits (for benchmarks and diagnostics): CTAs per
  * cluster, threads per CTA, dynamic shared memory per CTA, the number of

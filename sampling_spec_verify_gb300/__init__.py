@@ -36,7 +36,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "SpecError", "lib", "verify", "verify_ragged", "verify_relaxed", "tree_mask", "tree_verify_greedy", "overlap", "e2e_tv_fwd_bwd", "diagnostics", "truncate_logits", "schedule_lengths", "launch_shape",
+    "SpecError", "lib", "verify", "verify_ragged", "verify_relaxed", "tree_mask", "tree_verify_greedy", "overlap", "e2e_tv_fwd_bwd", "diagnostics", "truncate_logits", "schedule_lengths", "selftest_bounded_wait", "launch_shape",
     "set_launch_override", "VerifyOutput", "OverlapOutput", "E2EOutput", "DiagOutput", "TreeOutput", "HostVerifier",
     "DEV_BAD_TOKEN", "DEV_BAD_LOGITS", "DEV_BAD_UNIFORM", "DEV_TIMEOUT", "DEV_EMPTY_RESIDUAL", "DEV_BAD_OFFSETS",
     "SPEC_OK", "SPEC_ERR_INVALID_ARG", "SPEC_ERR_UNSUPPORTED", "SPEC_ERR_CUDA",
@@ -107,6 +107,8 @@ def lib():
     L.spec_tree_verify_workspace_bytes.argtypes = [i32, i32, i32]
     L.spec_tree_verify_greedy.restype = i32
     L.spec_tree_verify_greedy.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.spec_selftest_bounded_wait.restype = i32
+    L.spec_selftest_bounded_wait.argtypes = [ctypes.c_uint64, vp, vp]
     L.spec_launch_shape.restype = i32
     L.spec_launch_shape.argtypes = [i32, i32, i32] + [ctypes.POINTER(i32)] * 5
     L.spec_set_launch_override.restype = None
@@ -533,6 +535,22 @@ def schedule_lengths(survival: torch.Tensor, sps: torch.Tensor, *, status: Optio
 # ---------------------------------------------------------------------------
 # host-buffer convenience: one verify step from pinned host memory
 # ---------------------------------------------------------------------------
+
+def selftest_bounded_wait(limit_ns: int = 2_000_000, *, status: Optional[torch.Tensor] = None,
+                          device="cuda", stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Failure-path self-test of the library's bounded wait (see
+    spec_selftest_bounded_wait in the C header): one warp waits on an
+    mbarrier that nothing completes and gives up after ``limit_ns``.  Returns
+    the int32 status word, which holds DEV_TIMEOUT once the stream has run the
+    test."""
+    L = lib()
+    if status is None:
+        status = torch.zeros((1,), dtype=torch.int32, device=torch.device(device))
+    _need(status, "status", dtype=torch.int32, shape=(1,))
+    sh, _ = _stream_handle(stream, status.device)
+    _check(L.spec_selftest_bounded_wait(int(limit_ns), _ptr(status), sh), "spec_selftest_bounded_wait")
+    return status
+
 
 class HostVerifier:
     """Runs verify steps whose inputs and outputs live in (pinned) host

@@ -333,6 +333,17 @@ bool dims_ok(int B, int K, int V) { return B >= 0 && K >= 0 && K <= kMaxK && V >
 
 bool dtype_ok(spec_dtype_t dt) { return dt == SPEC_F32 || dt == SPEC_BF16; }
 
+// One warp waits on a fresh mbarrier that nothing arrives at: phase 0 never
+// completes, so the bounded wait runs out and reports it.
+__global__ void bounded_wait_selftest_kernel(uint64_t limit_ns, uint32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t a = ssv::smem_addr(&bar);
+  if (threadIdx.x == 0) ssv::mbar_init(a, 1u);
+  __syncthreads();
+  const bool done = ssv::mbar_wait_bounded(a, 0u, limit_ns);
+  if (!done && threadIdx.x == 0) atomicOr(status, ssv::kTimeout);
+}
+
 }  // namespace
 
 extern "C" {
@@ -672,6 +683,12 @@ spec_status_t spec_truncate_logits(const void* logits, void* out, spec_dtype_t d
     ssv::truncate_kernel<Bf16><<<grid, ssv::kTThreads, smem, st>>>(P);
   else
     ssv::truncate_kernel<F32><<<grid, ssv::kTThreads, smem, st>>>(P);
+  return from_cuda(cudaGetLastError());
+}
+
+spec_status_t spec_selftest_bounded_wait(uint64_t limit_ns, uint32_t* dev_status, void* stream) {
+  if (!dev_status || limit_ns == 0 || limit_ns > 10000000000ull) return SPEC_ERR_INVALID_ARG;
+  bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, dev_status);
   return from_cuda(cudaGetLastError());
 }
 

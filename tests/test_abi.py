@@ -35,7 +35,7 @@ def test_header_declares_the_boundary():
                  "spec_diagnostics", "spec_diagnostics_workspace_bytes", "spec_truncate_logits",
                  "spec_schedule_lengths", "spec_verify_ragged", "spec_verify_ragged_workspace_bytes",
                  "spec_verify_relaxed", "spec_tree_mask", "spec_tree_verify_greedy",
-                 "spec_tree_verify_workspace_bytes"):
+                 "spec_tree_verify_workspace_bytes", "spec_selftest_bounded_wait"):
         assert want in names
 
 
@@ -137,3 +137,7 @@ def test_argument_validation_without_gpu(L):
     assert L.spec_tree_verify_greedy(fake, 1, 2, 3, 10, fake, fake, fake, fake, fake, None, ws, 8, None) == 1
     assert L.spec_tree_verify_greedy(None, 1, 0, 3, 10, None, None, None, None, None, None, None, 0, None) == 0
     assert L.spec_tree_verify_workspace_bytes(2, 3, 10) >= 2 * 4 * 4
+    # bounded-wait self-test: a limit in [1 ns, 10 s] and a status word
+    assert L.spec_selftest_bounded_wait(0, fake, None) == 1
+    assert L.spec_selftest_bounded_wait(10_000_000_001, fake, None) == 1
+    assert L.spec_selftest_bounded_wait(1_000_000, None, None) == 1
