@@ -49,7 +49,7 @@ extern "C" {
 typedef enum {
   SPEC_OK = 0,
   SPEC_ERR_INVALID_ARG = 1, /* a pointer, size, dtype or temperature is invalid */
-  SPEC_ERR_UNSUPPORTED = 2, /* valid request beyond this build's limits */
+  SPEC_ERR_UNSUPPORTED = 2, /* valid request beyond the library's limits */
   SPEC_ERR_CUDA = 3         /* the CUDA runtime reported an error */
 } spec_status_t;
 
