@@ -685,6 +685,19 @@ def test_schedule_hand_example():
     assert not r.near
 
 
+def test_schedule_tie_rules():
+    # Equal survivals are taken in (row, position) order: R = 2, L = 1,
+    # a = [[0.5], [0.5]], SPS(2..4) = 1, 1, 0.5: B = 2 -> 2, B = 3 -> 2.5,
+    # B = 4 -> 1.5, so one survival is taken, and it is row 0's.
+    r = so.schedule_lengths([[0.5], [0.5]], [0, 0, 1.0, 1.0, 0.5])
+    assert r.lengths.tolist() == [1, 0] and r.batch == 3 and r.theta == 2.5
+    # Equal throughputs keep the smaller batch: SPS(2..4) = 1.25, 1, 0.5 gives
+    # B = 2 -> 2.5 and B = 3 -> 2.5 exactly (binary fractions), so B = 2.
+    r = so.schedule_lengths([[0.5], [0.5]], [0, 0, 1.25, 1.0, 0.5])
+    assert r.lengths.tolist() == [0, 0] and r.batch == 2 and r.theta == 2.5
+    assert r.near  # another B reaches the same throughput
+
+
 def _survivals(rng, R, L):
     c = rng.uniform(0.3, 1.0, size=(R, L))
     return np.cumprod(c, axis=1)
