@@ -226,9 +226,10 @@ spec_status_t spec_verify_ragged(const void* target_logits,
 /* ------------------------------------------------------------------------ */
 /* Allocation-free verify.  The pages have no counterpart: this entry point
  * exists for callers that cannot allocate device memory when they run a
- * verify step -- code inside a CUDA stream capture (where cudaMalloc is not
- * allowed), runtimes whose pool owns all device memory, plugin hosts that
- * provide buffers but no allocator.
+ * verify step -- runtimes whose pool owns all device memory from start-up,
+ * plugin hosts that provide buffers but no allocator, and latency-critical
+ * decode loops that cannot take the device-wide synchronisation of
+ * cudaMalloc / cudaFree.
  *
  * Same arguments and results as spec_verify, without the workspace: the
  * scratch is a fixed device array of SPEC_NOALLOC_SCRATCH_BYTES inside the
@@ -238,8 +239,8 @@ spec_status_t spec_verify_ragged(const void* target_logits,
  * allocates or frees memory; each clears the part of the array it uses with
  * cudaMemsetAsync on `stream`.
  *  - The first call on a device looks up the array's device address (once per
- *    device, with that device current); make that first call before any
- *    stream capture.
+ *    device, with that device current; a failed lookup is retried by the next
+ *    call); make that first call before any stream capture.
  *  - Every call on a device shares the one array: calls that may overlap on
  *    the GPU (different streams without ordering between them) race and give
  *    wrong results.  Serialise them. */

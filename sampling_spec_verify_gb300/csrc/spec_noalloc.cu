@@ -1,16 +1,17 @@
 // Allocation-free variant of spec_verify.
 //
 // Some callers cannot allocate device memory at the point where they need a
-// verify step: code running while a CUDA stream is being captured into a
-// graph (cudaMalloc is not allowed there), runtimes that hand every byte of
-// device memory to their own pool at start-up and forbid raw allocations
-// afterwards, and plugin hosts that give a plugin its input and output
-// buffers but no allocator.  spec_verify_noalloc serves them: it takes the
-// same inputs and outputs as spec_verify but no workspace; its scratch space
-// is the fixed-size device array below, which every GPU that loads this
-// library holds until the process exits.
+// verify step: runtimes that hand every byte of device memory to their own
+// pool at start-up and forbid raw allocations afterwards, plugin hosts that
+// give a plugin its input and output buffers but no allocator, and
+// latency-critical decode loops that cannot take the implicit device-wide
+// synchronisation of cudaMalloc / cudaFree.  spec_verify_noalloc serves them:
+// it takes the same inputs and outputs as spec_verify but no workspace; its
+// scratch space is the fixed-size device array below, which every GPU that
+// loads this library holds until the process exits.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -23,25 +24,34 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SPEC_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
-std::once_flag g_scratch_once[kMaxDevices];
+std::atomic<void*> g_scratch_ptr[kMaxDevices];  // null until a lookup on that device succeeds
+std::mutex g_scratch_mu;
 
 // Device address of the scratch array on the current device.  The host-side
 // symbol is only a stand-in: a kernel must be given this address instead.
-// Looked up once per device, with that device current.
+// Looked up with that device current; only a successful lookup is kept, so a
+// failed one (which also clears the error it left pending) is retried on the
+// next call.
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::call_once(g_scratch_once[dev], [dev]() {
-    void* p = nullptr;
-    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    g_scratch_ptr[dev] = (g_scratch_err[dev] == cudaSuccess) ? p : nullptr;
-  });
-  *out = g_scratch_ptr[dev];
-  return g_scratch_err[dev];
+  void* p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> g(g_scratch_mu);
+    p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+    if (p == nullptr) {
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+      }
+      g_scratch_ptr[dev].store(p, std::memory_order_release);
+    }
+  }
+  *out = p;
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -52,11 +62,15 @@ extern "C" spec_status_t spec_verify_noalloc(const void* target_logits, const vo
                                              const float* u_final, int32_t* out_tokens, int32_t* n_accepted,
                                              float* alpha_out, uint32_t* dev_status, void* stream) {
   const size_t need = spec_verify_workspace_bytes(B, K, V);
-  if (need == 0) return SPEC_ERR_INVALID_ARG;
+  // An empty batch, or dimensions spec_verify rejects: nothing needs scratch,
+  // and spec_verify gives the same answer it gives any caller (its argument
+  // checks, then SPEC_OK for B == 0).
+  if (B <= 0 || need == 0)
+    return spec_verify(target_logits, draft_logits, dtype, B, K, V, temperature, draft_tokens, u_accept, u_final,
+                       out_tokens, n_accepted, alpha_out, dev_status, nullptr, 0, stream);
   if (need > (size_t)SPEC_NOALLOC_SCRATCH_BYTES) return SPEC_ERR_UNSUPPORTED;
-  if (B == 0) return SPEC_OK;
   void* scratch = nullptr;
-  if (scratch_address(&scratch) != cudaSuccess || scratch == nullptr) return SPEC_ERR_CUDA;
+  if (scratch_address(&scratch) != cudaSuccess) return SPEC_ERR_CUDA;
   // The array keeps whatever the previous call left; the counters must start
   // at zero, so clear the part this call uses (on the caller's stream).
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -179,13 +179,17 @@ def test_entropy_mix_full_size(ssv, T):
     ref = oracle_verify(w)
     flagged = assert_verify(out, ref)
     print(f"T={T}: flagged rows {flagged} / {w.shape[0]}, mean accepted {ref.n_accepted.mean():.3f}")
+    assert flagged <= 2, flagged
     assert int(out.status.item()) == 0
 
 
 def test_zipf_full_size(ssv):
+    """The Zipf workload (B=128, K=7, V=129280 bf16, T=1) runs the row-grouped
+    kernel with draw skipping: every row against the oracle."""
     w = synth.zipf(seed=1236)
     out = ssv.verify(*to_dev(w), w.temperature)
     torch.cuda.synchronize()
+    assert int(out.status.item()) == 0
     B, K, V = w.shape
     n = out.n_accepted.cpu().numpy()
     a = out.alpha.cpu().numpy()
@@ -193,19 +197,23 @@ def test_zipf_full_size(ssv):
     # draft == target bitwise: every draft accepted, alpha 1
     assert (n[same] == K).all()
     np.testing.assert_allclose(a[same], 1.0, rtol=0, atol=2e-6)
-    rows = list(w.low_rows[:16]) + list(same[:8])
-    ref = oracle_verify(w, rows=rows)
-    assert_verify(out, ref, rows=rows)
+    ref = oracle_verify(w)
+    flagged = assert_verify(out, ref)
+    # a near tie has probability of order 1e-6 per evaluated position
+    assert flagged <= 2, flagged
 
 
 def test_sweep_points_sampled_rows(ssv):
+    """Points of the B x K grid at V=151936: every row up to B=64, sampled rows
+    at B=256."""
     for B, K in ((1, 1), (8, 2), (64, 7), (64, 16), (256, 4)):
         w = synth.sweep(B, K, seed=1238 + B + K)
         out = ssv.verify(*to_dev(w), w.temperature)
         torch.cuda.synchronize()
-        rows = sorted(set([0, B // 2, B - 1]))
+        rows = list(range(B)) if B <= 64 else sorted(set(range(0, B, 8)) | {B - 1})
         ref = oracle_verify(w, rows=rows)
-        assert_verify(out, ref, rows=rows)
+        flagged = assert_verify(out, ref, rows=rows)
+        assert flagged <= 2, (B, K, flagged)
         n = out.n_accepted.cpu().numpy()
         assert (n >= 0).all() and (n <= K).all()
         del w, out
@@ -272,8 +280,9 @@ def test_e2e_full_size(ssv):
     g = e.grad.cpu().numpy()
     # the gradient of each softmax row sums to zero
     assert np.abs(g.sum(axis=2)).max() < 1e-6
-    amb = _check_grad(g, w, 1.0, 1.0, [0, 131, 255])
-    print(f"ambiguous indicator elements in sampled rows: {amb}")
+    rows = list(range(0, B, 8))  # 32 of the 256 rows, element by element
+    amb = _check_grad(g, w, 1.0, 1.0, rows)
+    print(f"ambiguous indicator elements in {len(rows)} rows: {amb}")
 
 
 # ---------------------------------------------------------------------------

@@ -127,6 +127,39 @@ def test_inverse_cdf_near_flag():
     assert not so.inverse_cdf(w, 0.25)[1]
 
 
+def _near_case(u0, u1=0.0):
+    """Two drafted positions over two tokens, every ratio exact in binary:
+    p_k = (1/4, 3/4), q_k = (1/2, 1/2), token 0 drafted at both, so
+    p(y)/q(y) = 1/2 exactly (q/p = 2, p(y) = 1/4)."""
+    p = [np.array([0.25, 0.75])] * 3
+    q = [np.array([0.5, 0.5])] * 2
+    return so.accept_and_correct(p, q, [0, 0], [u0, u1], 0.3)
+
+
+def test_accept_near_flag_threshold_and_operand():
+    # the acceptance test (Speculative Decoding 与 MTP, sections 2 and 3)
+    # compares u with p(y)/q(y) = 1/2;
+    # the oracle flags |u - p/q| < 1e-6 at every evaluated position
+    for du in (5e-7, -5e-7):
+        _, n, near, _, _ = _near_case(0.5 + du)
+        assert near, du
+        assert n == (2 if du < 0 else 0)  # u <= p/q accepts (u = 0 accepts the second)
+    for du in (5e-6, -5e-6):
+        assert not _near_case(0.5 + du)[2], du
+    # equality is a near tie and accepts (u <= p/q)
+    _, n, near, _, _ = _near_case(0.5, 0.9)
+    assert near and n == 1
+    # the operand is p/q: u near p(y) = 1/4 or near 1 (q/p = 2 is out of reach) raises no flag
+    for u in (0.25, 0.25 + 1e-7, 1.0 - 1e-7):
+        assert not _near_case(u)[2], u
+    # positions after the first rejection are not evaluated: no flag there
+    _, n, near, _, _ = _near_case(0.9, 0.5)
+    assert n == 0 and not near
+    # an evaluated later position does flag
+    _, n, near, _, _ = _near_case(0.1, 0.5 + 2e-7)
+    assert n == 1 and near
+
+
 # ---------------------------------------------------------------------------
 # worked examples printed on the pages
 # ---------------------------------------------------------------------------

@@ -1,12 +1,14 @@
 """The allocation-free verify entry point.
 
 spec_verify_noalloc is for callers that cannot allocate device memory when
-they run a verify step (inside a stream capture, under a runtime whose pool
-owns all device memory, in a plugin host that only hands out buffers).  It
-keeps its scratch in a fixed device array inside the library.  Here it is
-called through the C ABI and must give the same results as spec_verify with
-a caller-provided workspace, on two calls in a row (the second call reuses
-the array the first one left behind).
+they run a verify step (under a runtime whose pool owns all device memory, in
+a plugin host that only hands out buffers, in a decode loop that cannot take
+cudaMalloc's device-wide synchronisation).  It keeps its scratch in a fixed
+device array inside the library.  Here it is called through the C ABI and
+must give the same results as spec_verify with a caller-provided workspace,
+on two calls in a row (the second call reuses the array the first one left
+behind), agree with the fp64 oracle, and answer an empty batch as
+spec_verify does.
 """
 
 import ctypes
@@ -15,6 +17,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from sampling_spec_verify_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -62,6 +65,27 @@ def test_noalloc_matches_workspace_entry_point():
         assert torch.equal(n, ref.n_accepted)
         np.testing.assert_allclose(a.cpu().numpy(), ref.alpha.cpu().numpy(), rtol=RTOL, atol=ATOL)
         assert int(st.item()) == 0
+        # and the fp64 oracle, on every row it does not flag as a near tie
+        orc = oracle.verify(synth.f64(w.target), synth.f64(w.draft), w.draft_tokens.numpy(), w.u_accept.numpy(),
+                            w.u_final.numpy(), w.temperature)
+        ok = ~orc.flagged
+        assert (tok.cpu().numpy()[ok] == orc.tokens[ok]).all()
+        assert (n.cpu().numpy()[ok] == orc.n_accepted[ok]).all()
+        np.testing.assert_allclose(a.cpu().numpy(), orc.alpha, rtol=RTOL, atol=ATOL)
+
+
+def test_noalloc_empty_batch_like_spec_verify():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sampling_spec_verify_gb300 as ssv
+    L = ssv.lib()
+    fn = _entry(L)
+    # B = 0: nothing to do, SPEC_OK, as spec_verify answers (no pointer is touched)
+    assert fn(None, None, 1, 0, 4, 1000, 1.0, None, None, None, None, None, None, None, None) == 0
+    # invalid dimensions and temperature are rejected like spec_verify rejects them
+    assert fn(None, None, 1, 0, 4, 0, 1.0, None, None, None, None, None, None, None, None) == 1
+    assert fn(None, None, 1, 0, 4, 1000, -1.0, None, None, None, None, None, None, None, None) == 1
+    assert fn(None, None, 1, -1, 4, 1000, 1.0, None, None, None, None, None, None, None, None) == 1
 
 
 def test_noalloc_rejects_sizes_beyond_its_array():
@@ -70,7 +94,9 @@ def test_noalloc_rejects_sizes_beyond_its_array():
     import sampling_spec_verify_gb300 as ssv
     L = ssv.lib()
     fn = _entry(L)
-    fake = ctypes.c_void_p(0x1000)
-    # 100,000 rows at K = 7 need far more than the fixed scratch array
-    rc = fn(fake, fake, 1, 100000, 7, 1024, 1.0, fake, fake, fake, fake, fake, None, None, None)
+    # 100,000 rows at K = 7 need far more than the fixed scratch array.  Every
+    # pointer is null: were the size check ever to let this through,
+    # spec_verify's own null checks would answer SPEC_ERR_INVALID_ARG before
+    # any launch.
+    rc = fn(None, None, 1, 100000, 7, 1024, 1.0, None, None, None, None, None, None, None, None)
     assert rc == 2  # SPEC_ERR_UNSUPPORTED
