@@ -1,17 +1,25 @@
 #!/usr/bin/env python
 """Throughput benchmark of the verify / overlap / E2E-TV hot path.
 
-One *step* is one pass of the whole hot path over one batch of the
-entropy-mix workload (B=32 rows, K=4 drafted positions, V=151936, bf16
-logits, per-row sigma in {1, 2, 4}, draft = target + N(0, 0.7^2)):
+One *step* is one pass of the whole hot path over one batch of the Zipf
+workload (B=128 rows, K=7 drafted positions, V=129280, bf16 logits
+-1.1 ln(rank) + N(0, 0.3^2) with a random rank permutation per row; the draft
+equals the target except in 20% of rows, whose draft rows are permuted):
 
-  verify at T=1.0, verify at T=0.7 (both with per-position overlap),
-  greedy verify at T=0, and the E2E-TV loss + draft-logit gradient at T=1.0.
+  sampling verify at T=1 with the per-position overlap (acceptance,
+  first rejection, residual / bonus draw), greedy verify at T=0 (drafted
+  tokens from a greedy drafter), and the E2E-TV loss + draft-logit gradient
+  at T=1 over the batch's K drafted positions.
 
 Metric: verified draft positions ("rows") per second, B*K per verify call,
-three verify calls per step; the E2E-TV call adds time but no rows.  Inputs
-are resident in HBM and rotated over 8 copies of the batch (700 MB, above
-the 129 MB L2), so every call reads its logits from HBM.
+two verify calls per step; the E2E-TV call adds time but no rows.  Every call
+reads at least 265 MB of logits, and inputs alternate between two resident
+copies of the batch, so every call reads its logits from HBM, not L2.
+
+Extra keys time the other workloads of the same path: the entropy-mix step
+(B=32, K=4, V=151936), the E2E-TV training batch (B=256, K=7, V=151936), the
+per-call latency of the small case (B=1, K=4, V=1024 fp32, 1000 seeded calls)
+and the fp64 oracle per workload on the host cores.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 
@@ -26,9 +34,11 @@ import ctypes
 import hashlib
 import json
 import os
+import shutil
 import statistics
 import subprocess
 import sys
+import tempfile
 import threading
 import time
 
@@ -38,27 +48,43 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-B, K, V = 32, 4, 151936
-SEED = 1235
-TEMPS = (1.0, 0.7, 0.0)
-N_ROT = 8
+# headline workload: Zipf logits, B=128, K=7, V=129280
+B, K, V = 128, 7, 129280
+SEED = 1236
+N_ROT = 2
 METRIC = "verify rows/s (B*K*V logits) and achieved HBM GB/s vs 8 TB/s roofline"
-WORKLOAD = "entropy-mix verify step: B=32, K=4, V=151936 bf16, T in {1.0, 0.7, 0 greedy} + E2E-TV fwd+bwd at T=1"
-L2_NOTE = "inputs rotated over 8 resident copies of the batch (700 MB > 129 MB L2)"
+WORKLOAD = ("zipf verify step: B=128, K=7, V=129280 bf16 (Zipf logits, 20% of rows permuted); "
+            "sampling verify T=1 with overlap + greedy verify T=0 + E2E-TV fwd+bwd T=1")
+L2_NOTE = "inputs alternate between 2 resident copies of the batch (each call reads >= 265 MB > 129 MB L2)"
+CALLS = ("verify", "greedy", "e2e")
+# ex2 results per SM per clock, measured on this GPU with a probe kernel
+# (a dependent-free stream of ex2.approx.ftz.f32)
+EX2_PER_SM_CLK = 31.4
+
+# the entropy-mix workload (extra key)
+B2, K2, V2 = 32, 4, 151936
+SEED2 = 1235
+TEMPS2 = (1.0, 0.7, 0.0)
+# the E2E-TV training batch (extra key)
+B4, K4, V4 = 256, 7, 151936
+SEED4 = 1237
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--no-extras", action="store_true", help="skip the extra workloads")
+    ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--single", choices=["verify", "greedy", "overlap", "e2e", "diag", "truncate", "ragged",
                                          "schedule", "relaxed", "tree"], default=None,
                     help="run only `--calls` calls of one entry point (an L2 flush before each): the "
                          "profiling target, prints no JSON")
+    ap.add_argument("--workload", choices=["entropy", "zipf"], default="entropy",
+                    help="inputs of --single: entropy mix, or the Zipf workload")
     ap.add_argument("--shape", default="32,4,151936", help="B,K,V of --single")
     ap.add_argument("--temperature", type=float, default=1.0, help="T of --single verify")
     ap.add_argument("--calls", type=int, default=3)
@@ -122,7 +148,7 @@ class ClockSampler:
             ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
         except Exception:
             ident = None
-        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
         if ident:
             cmd[1:1] = ["-i", ident]
         try:
@@ -160,10 +186,12 @@ class ClockSampler:
                 return None
         sm = [num(p[0]) for p in win if num(p[0]) is not None]
         mx = [num(p[1]) for p in win if num(p[1]) is not None]
+        pw = [num(p[2]) for p in win if num(p[2]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for p in win for i in range(4) if p[3 + i].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(win)}
+                "power_w_median": statistics.median(pw) if pw else None, "reasons": reasons,
+                "samples": len(win)}
 
 
 # ---------------------------------------------------------------------------
@@ -171,12 +199,14 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 def kernel_source_hash():
-    """Hash of the sweep kernel's device code (the kernel the ncu traffic
-    record describes); other kernels' sources do not change it."""
+    """Hash of the sweep kernels' device code (the kernels the ncu traffic
+    records describe); other kernels' sources do not change it."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "sampling_spec_verify_gb300", "csrc")
-    for name in ("ptx.cuh", "sweep.cuh"):
-        h.update(open(os.path.join(d, name), "rb").read())
+    for name in ("ptx.cuh", "sweep.cuh", "pipe.cuh"):
+        path = os.path.join(d, name)
+        if os.path.exists(path):
+            h.update(open(path, "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -200,121 +230,225 @@ def hbm_peak():
         return 6800.0, "fallback"
 
 
-# ---------------------------------------------------------------------------
-# workload
-# ---------------------------------------------------------------------------
-
-def make_batches(seed):
-    from sampling_spec_verify_gb300 import synth
-    # same logits for every temperature; tokens drafted from q at that T
-    return {T: synth.entropy_mix(seed=seed, temperature=T) for T in TEMPS}
-
-
-def algorithmic_bytes():
-    s = 2
+def algorithmic_bytes(b, k, v, s=2):
     return {
-        "verify": B * (K + 1) * V * s + B * K * V * s,
-        "greedy": B * (K + 1) * V * s,
-        "e2e": B * K * V * (s + s + 4),
+        "verify": b * (k + 1) * v * s + b * k * v * s,   # target [B, K+1, V] + draft [B, K, V]
+        "greedy": b * (k + 1) * v * s,                   # target only (no overlap requested)
+        "e2e": b * k * v * (s + s + 4),                  # read target and draft, write fp32 gradient
     }
+
+
+def exps_per_verify(b, k, v):
+    """ex2 evaluations of one sampling verify with overlap, draws left out:
+    two per drafted element pair for the normalisers, one for min(p, q), one
+    per bonus-row element."""
+    return 3 * b * k * v + b * v
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+def make_headline(seed):
+    from sampling_spec_verify_gb300 import synth
+    w = synth.zipf(seed=seed, B=B, K=K, V=V)
+    return w, synth.greedy_tokens(w.draft)
 
 
 # ---------------------------------------------------------------------------
 # CPU baseline: the fp64 oracle as it stands, on host cores
 # ---------------------------------------------------------------------------
+# Pool workers read batch rows from files the parent writes once (a sample of
+# each workload's rows), so no worker regenerates a whole batch.
 
-def oracle_step(batches, rows):
+_ROWS = None
+
+
+def _save_rows(d, name, w, rows, extra=None):
+    arrs = {"target": w.target[rows].contiguous(), "draft": w.draft[rows].contiguous()}
+    for k_, t in arrs.items():
+        if t.dtype == torch.bfloat16:
+            np.save(os.path.join(d, f"{name}_{k_}.npy"), t.view(torch.int16).numpy())
+        else:
+            np.save(os.path.join(d, f"{name}_{k_}_f32.npy"), t.numpy())
+    small = {"y": w.draft_tokens[rows].numpy(), "ua": w.u_accept[rows].numpy(), "uf": w.u_final[rows].numpy(),
+             "T": np.float64(w.temperature)}
+    if extra:
+        small.update({k_: v_[rows].numpy() for k_, v_ in extra.items()})
+    np.savez(os.path.join(d, f"{name}_small.npz"), **small)
+
+
+def _load_rows(d, name):
+    from sampling_spec_verify_gb300 import synth
+    out = {}
+    for k_ in ("target", "draft"):
+        p16 = os.path.join(d, f"{name}_{k_}.npy")
+        if os.path.exists(p16):
+            out[k_] = synth.f64(torch.from_numpy(np.load(p16)).view(torch.bfloat16))
+        else:
+            out[k_] = synth.f64(torch.from_numpy(np.load(os.path.join(d, f"{name}_{k_}_f32.npy"))))
+    z = np.load(os.path.join(d, f"{name}_small.npz"))
+    out.update({k_: z[k_] for k_ in z.files})
+    return out
+
+
+def _pool_init(d):
+    global _ROWS
+    torch.set_num_threads(1)
+    _ROWS = {n: _load_rows(d, n) for n in ("zipf", "entropy", "e2e")}
+
+
+def oracle_headline_row(r, i):
+    """The oracle on batch row i of the headline step: sampling verify at T=1,
+    greedy verify at T=0, E2E-TV loss and gradient at T=1."""
+    import oracle
+    zt, zd = r["target"][i:i + 1], r["draft"][i:i + 1]
+    oracle.verify(zt, zd, r["y"][i:i + 1], r["ua"][i:i + 1], r["uf"][i:i + 1], 1.0)
+    oracle.verify(zt, None, r["y0"][i:i + 1], r["ua"][i:i + 1], r["uf"][i:i + 1], 0.0)
+    kk = zd.shape[1]
+    oracle.e2e_tv_loss(zt[:, :kk], zd, 1.0)
+    oracle.e2e_tv_grad(zt[:, :kk], zd, 1.0)
+
+
+def oracle_task(task):
+    """One oracle task in a pool worker: (workload, row) -> rows verified."""
     import oracle
     from sampling_spec_verify_gb300 import synth
-    w = batches[1.0]
-    zt, zd = synth.f64(w.target[rows]), synth.f64(w.draft[rows])
-    for T in TEMPS:
-        x = batches[T]
-        oracle.verify(zt, zd if T > 0 else None, x.draft_tokens[rows].numpy(), x.u_accept[rows].numpy(),
-                      x.u_final[rows].numpy(), T)
-    oracle.e2e_tv_loss(zt[:, :K], zd, 1.0)
-    oracle.e2e_tv_grad(zt[:, :K], zd, 1.0)
-
-
-_POOL_BATCHES = None
-
-
-def _pool_init(seed):
-    global _POOL_BATCHES
-    torch.set_num_threads(1)
-    _POOL_BATCHES = make_batches(seed)
-
-
-def _pool_rows(rows):
-    oracle_step(_POOL_BATCHES, rows)
-    return len(rows)
+    name, i = task
+    if name == "zipf":
+        r = _ROWS["zipf"]
+        i %= r["y"].shape[0]
+        oracle_headline_row(r, i)
+        return 2 * r["y"].shape[1]
+    if name == "entropy":  # one row of the entropy step's T=1 verify
+        r = _ROWS["entropy"]
+        i %= r["y"].shape[0]
+        oracle.verify(r["target"][i:i + 1], r["draft"][i:i + 1], r["y"][i:i + 1], r["ua"][i:i + 1],
+                      r["uf"][i:i + 1], float(r["T"]))
+        return r["y"].shape[1]
+    if name == "e2e":  # one row of the E2E-TV batch: loss and gradient
+        r = _ROWS["e2e"]
+        i %= r["target"].shape[0]
+        oracle.e2e_tv_loss(r["target"][i:i + 1], r["draft"][i:i + 1], 1.0)
+        oracle.e2e_tv_grad(r["target"][i:i + 1], r["draft"][i:i + 1], 1.0)
+        return r["target"].shape[1]
+    if name == "small":  # one call of the small case (B=1, K=4, V=1024 fp32)
+        w = synth.small(seed=i % 1000)
+        oracle.verify(synth.f64(w.target), synth.f64(w.draft), w.draft_tokens.numpy(), w.u_accept.numpy(),
+                      w.u_final.numpy(), w.temperature)
+        return 4
+    raise ValueError(name)
 
 
 def _single_threaded_children():
     # pool workers inherit the environment: one BLAS / OpenMP thread each
-    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ[k] = "1"
+    for k_ in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k_] = "1"
 
 
-def oracle_pool_rate(budget_s=12.0):
-    """The oracle as it stands, one batch row per task, over a process pool
-    of one worker per host core (spawned, so it is safe after CUDA starts).
-    Returns (rows of the step per second, workers, rows done, seconds)."""
-    import multiprocessing as mp
-    n = os.cpu_count() or 1
-    _single_threaded_children()
-    ctx = mp.get_context("spawn")
-    with ctx.Pool(n, initializer=_pool_init, initargs=(SEED,)) as pool:
-        pool.map(_pool_rows, [[i % B] for i in range(n)], chunksize=1)  # every worker ready
-        done, b = 0, 0
+class OraclePool:
+    """The oracle as it stands over a spawned process pool of one
+    single-threaded worker per host core (spawned, so it is safe after CUDA
+    starts), plus a one-process timer."""
+
+    def __init__(self, row_dir):
+        import multiprocessing as mp
+        self.n = os.cpu_count() or 1
+        self.dir = row_dir
+        _single_threaded_children()
+        self.pool = mp.get_context("spawn").Pool(self.n, initializer=_pool_init, initargs=(row_dir,))
+        self.pool.map(oracle_task, [("small", i) for i in range(self.n)], chunksize=1)  # every worker ready
+
+    def rate(self, name, budget_s, start=0):
+        done, rows, i = 0, 0, start
         t0 = time.time()
         while time.time() - t0 < budget_s:
-            done += sum(pool.map(_pool_rows, [[(b + i) % B] for i in range(n)], chunksize=1))
-            b += n
+            rows += sum(self.pool.map(oracle_task, [(name, i + j) for j in range(self.n)], chunksize=1))
+            done += self.n
+            i += self.n
         dt = time.time() - t0
-    return len(TEMPS) * K * done / dt, n, done, dt
+        return rows / dt, done, dt
+
+    def single_core_rate(self, name, budget_s):
+        global _ROWS
+        if _ROWS is None:
+            _pool_init(self.dir)
+        done, rows = 0, 0
+        t0 = time.time()
+        while time.time() - t0 < budget_s:
+            rows += oracle_task((name, done))
+            done += 1
+        dt = time.time() - t0
+        return rows / dt, done, dt
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
 
 
-def cpu_baseline(batches, budget_s=12.0):
-    done_rows = 0
-    t0 = time.time()
-    b = 0
-    while True:
-        oracle_step(batches, [b % B])
-        done_rows += 1
-        b += 1
-        if time.time() - t0 > budget_s:
-            break
-    dt = time.time() - t0
-    one = len(TEMPS) * K * done_rows / dt
-    rate, n, done, dtp = oracle_pool_rate(budget_s)
-    return {"value": rate, "unit": "rows/s", "cores": n, "kind": "oracle",
-            "sample": f"{done} batch rows of the step (3 verify calls + E2E-TV) in {dtp:.1f} s over a pool of "
-                      f"{n} single-threaded numpy float64 workers, one row per task",
-            "single_core": {"value": one, "cores": 1,
-                            "sample": f"{done_rows} batch rows in {dt:.1f} s, one process"}}
+def write_oracle_rows(d, headline, y0):
+    """The rows the oracle timings use: 32 rows of the headline batch (its
+    permuted rows among them), 32 of the entropy mix and 16 of the E2E-TV
+    batch."""
+    from sampling_spec_verify_gb300 import synth
+    low = [int(x) for x in headline.low_rows[:8]]
+    rows = sorted(set(low) | set(range(32 - len(low))))[:32]
+    _save_rows(d, "zipf", headline, rows, extra={"y0": y0})
+    _save_rows(d, "entropy", synth.entropy_mix(seed=SEED2, temperature=1.0, B=B2, K=K2, V=V2), list(range(32)))
+    g = synth.gaussian(16, K4, V4, sigma=2.0, noise=0.5, dtype=torch.bfloat16, temperature=1.0, seed=SEED4,
+                       bonus=False, name="e2e", draft_tokens=False)
+    _save_rows(d, "e2e", g, list(range(16)))
+
+
+def cpu_baselines(pool, budget_s=12.0, per_cfg_s=2.5):
+    rate, done, dt = pool.rate("zipf", budget_s)
+    one, done1, dt1 = pool.single_core_rate("zipf", budget_s / 2)
+    out = {"value": rate, "unit": "rows/s", "cores": pool.n, "kind": "oracle",
+           "sample": f"{done} batch rows of the headline step (sampling verify T=1, greedy verify T=0, E2E-TV "
+                     f"loss and gradient; {2 * K} verified positions per row) in {dt:.1f} s over a pool of "
+                     f"{pool.n} single-threaded numpy float64 workers, one row per task",
+           "single_core": {"value": one, "cores": 1, "sample": f"{done1} batch rows in {dt1:.1f} s, one process"}}
+    per_cfg = {}
+    units = {"small": "rows/s (B=1, K=4, V=1024 fp32 calls; 4 rows each)",
+             "entropy": "rows/s (T=1 verify of B=32, K=4, V=151936 rows)",
+             "zipf": "rows/s (the headline step's rows)",
+             "e2e": "positions/s (E2E-TV loss + gradient, B=256, K=7, V=151936 rows)"}
+    for name in ("small", "entropy", "zipf", "e2e"):
+        r, d_, t_ = pool.rate(name, per_cfg_s)
+        r1, d1, t1 = pool.single_core_rate(name, per_cfg_s)
+        per_cfg[name] = {"unit": units[name], "pool": r, "pool_cores": pool.n, "pool_tasks": d_,
+                         "single_core": r1, "single_core_tasks": d1}
+    out["per_workload"] = per_cfg
+    return out
 
 
 def run_reference(args, ws, rank):
-    """The oracle, timed as the reference arm (rank 0 only)."""
+    """The oracle, timed as the reference arm (rank 0 only): each step is one
+    batch row of the headline step per host core."""
     if rank != 0:
         return
-    import multiprocessing as mp
-    n = os.cpu_count() or 1
-    _single_threaded_children()
-    ctx = mp.get_context("spawn")
-    budget_s = 120.0  # the timed steps stop here even if fewer than --steps ran
-    with ctx.Pool(n, initializer=_pool_init, initargs=(SEED,)) as pool:
-        # a step: one batch row per host core, the rows of the step's calls
-        for i in range(max(1, min(args.warmup, 3))):
-            pool.map(_pool_rows, [[(i * n + j) % B] for j in range(n)], chunksize=1)
-        t0 = time.time()
-        done = 0
-        while done < max(1, args.steps) and (done == 0 or time.time() - t0 < budget_s):
-            pool.map(_pool_rows, [[(done * n + j) % B] for j in range(n)], chunksize=1)
-            done += 1
-        dt = time.time() - t0
-    value = len(TEMPS) * K * done * n / max(dt, 1e-9)
+    headline, y0 = make_headline(SEED)
+    d = tempfile.mkdtemp(prefix="ssv_bench_rows_")
+    try:
+        write_oracle_rows(d, headline, y0)
+        del headline
+        pool = OraclePool(d)
+        try:
+            n = pool.n
+            for i in range(max(1, min(args.warmup, 3))):
+                pool.pool.map(oracle_task, [("zipf", i * n + j) for j in range(n)], chunksize=1)
+            budget_s = 120.0  # the timed steps stop here even if fewer than --steps ran
+            t0 = time.time()
+            done, rows = 0, 0
+            while done < max(1, args.steps) and (done == 0 or time.time() - t0 < budget_s):
+                rows += sum(pool.pool.map(oracle_task, [("zipf", done * n + j) for j in range(n)], chunksize=1))
+                done += 1
+            dt = time.time() - t0
+        finally:
+            pool.close()
+    finally:
+        shutil.rmtree(d, ignore_errors=True)
+    value = rows / max(dt, 1e-9)
     line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus, "steps": done,
             "steps_requested": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / done,
             "higher_is_better": True,
@@ -332,23 +466,27 @@ def run_reference(args, ws, rank):
 # native arm
 # ---------------------------------------------------------------------------
 
+def _P(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
 def run_native(args, ws, rank, local):
     import sampling_spec_verify_gb300 as ssv
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     L = ssv.lib()
-    batches = make_batches(SEED + rank)
-    base = batches[1.0]
+    headline, y0 = make_headline(SEED + rank)
     stream = torch.cuda.current_stream(dev)
     sh = ctypes.c_void_p(stream.cuda_stream)
 
     # resident inputs: N_ROT copies of the batch's logits
-    tgt = [base.target.to(dev) for _ in range(N_ROT)]
-    drf = [base.draft.to(dev) for _ in range(N_ROT)]
-    per_t = {T: (batches[T].draft_tokens.to(dev), batches[T].u_accept.to(dev), batches[T].u_final.to(dev))
-             for T in TEMPS}
-    outs = {T: (torch.empty((B, K + 1), dtype=torch.int32, device=dev), torch.empty((B,), dtype=torch.int32, device=dev),
-                torch.empty((B, K), dtype=torch.float32, device=dev)) for T in TEMPS}
+    tgt = [headline.target.to(dev) for _ in range(N_ROT)]
+    drf = [headline.draft.to(dev) for _ in range(N_ROT)]
+    y, ua, uf = headline.draft_tokens.to(dev), headline.u_accept.to(dev), headline.u_final.to(dev)
+    y0d = y0.to(dev)
+    tok1, n1 = torch.empty((B, K + 1), dtype=torch.int32, device=dev), torch.empty((B,), dtype=torch.int32, device=dev)
+    a1 = torch.empty((B, K), dtype=torch.float32, device=dev)
+    tok0, n0 = torch.empty((B, K + 1), dtype=torch.int32, device=dev), torch.empty((B,), dtype=torch.int32, device=dev)
     status = torch.zeros((1,), dtype=torch.int32, device=dev)
     loss = torch.empty((1,), dtype=torch.float32, device=dev)
     alpha_e = torch.empty((B, K), dtype=torch.float32, device=dev)
@@ -357,37 +495,28 @@ def run_native(args, ws, rank, local):
     wsz_e = L.spec_e2e_tv_workspace_bytes(B, K, V)
     ws_v = torch.zeros(wsz_v, dtype=torch.uint8, device=dev)
     ws_e = torch.zeros(wsz_e, dtype=torch.uint8, device=dev)
-    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
 
-    # prebuilt C-ABI argument lists: call c of the rotation reads copy c % N_ROT
-    calls = []  # (kind, args)
+    calls = []  # per rotation copy: the three C-ABI calls of a step
     for c in range(N_ROT):
-        T = TEMPS[c % 4] if c % 4 < 3 else None
         t, d = tgt[c], drf[c]
-        if T is None:
-            calls.append(("e2e", (P(t), P(d), 1, B, K, K + 1, V, 1.0, 1.0, P(loss), P(alpha_e), P(grad), P(status),
-                                  P(ws_e), wsz_e, sh)))
-        else:
-            y, ua, uf = per_t[T]
-            o = outs[T]
-            greedy = T == 0.0
-            calls.append(("greedy" if greedy else "verify",
-                          (P(t), None if greedy else P(d), 1, B, K, V, T, P(y), P(ua), P(uf), P(o[0]), P(o[1]),
-                           None if greedy else P(o[2]), P(status), P(ws_v), wsz_v, sh)))
-    fn = {"verify": L.spec_verify, "greedy": L.spec_verify, "e2e": L.spec_e2e_tv_fwd_bwd}
-    kinds_per_step = ["verify", "verify", "greedy", "e2e"]
-    launches_per_step = 5  # 3 verify kernels + E2E-TV sweep + E2E-TV gradient
+        calls.append([
+            (L.spec_verify, (_P(t), _P(d), 1, B, K, V, 1.0, _P(y), _P(ua), _P(uf), _P(tok1), _P(n1), _P(a1),
+                             _P(status), _P(ws_v), wsz_v, sh)),
+            (L.spec_verify, (_P(t), None, 1, B, K, V, 0.0, _P(y0d), None, None, _P(tok0), _P(n0), None,
+                             _P(status), _P(ws_v), wsz_v, sh)),
+            (L.spec_e2e_tv_fwd_bwd, (_P(t), _P(d), 1, B, K, K + 1, V, 1.0, 1.0, _P(loss), _P(alpha_e), _P(grad),
+                                     _P(status), _P(ws_e), wsz_e, sh)),
+        ])
 
     def step(i, ev=None):
-        for j in range(4):
-            kind, a = calls[(4 * i + j) % N_ROT]
+        for j, (fn, a) in enumerate(calls[i % N_ROT]):
             if ev is not None:
                 ev[j][0].record(stream)
-            rc = fn[kind](*a)
+            rc = fn(*a)
             if ev is not None:
                 ev[j][1].record(stream)
             if rc != 0:
-                raise RuntimeError(f"{kind} returned status {rc}")
+                raise RuntimeError(f"{CALLS[j]} returned status {rc}")
 
     for i in range(max(args.warmup, 3)):
         step(i)
@@ -395,14 +524,14 @@ def run_native(args, ws, rank, local):
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
     # ---- timed region: K steps, events around every call ----
-    n_ev = args.steps
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(4)]
-           for _ in range(n_ev)]
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in CALLS]
+           for _ in range(args.steps)]
     clocks = ClockSampler(dev.index) if rank == 0 else None
     time.sleep(0.5 if clocks else 0)
     barrier(ws)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_launch0 = ssv.kernel_launches()
     t_wall0 = time.time()
     e0.record(stream)
     for i in range(args.steps):
@@ -410,84 +539,112 @@ def run_native(args, ws, rank, local):
     e1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
+    n_launch = ssv.kernel_launches() - n_launch0
     barrier(ws)
     ms_total = e0.elapsed_time(e1)
     ms_total = max_over_ranks(ms_total, ws, dev)
     if clocks:
         time.sleep(0.3)
         clocks.stop()
-    per_kind = {k: [] for k in ("verify", "greedy", "e2e")}
-    for i in range(n_ev):
-        for j in range(4):
-            per_kind[kinds_per_step[j]].append(evs[i][j][0].elapsed_time(evs[i][j][1]))
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    per_kind = {k_: [evs[i][j][0].elapsed_time(evs[i][j][1]) for i in range(args.steps)]
+                for j, k_ in enumerate(CALLS)}
     ms_step = ms_total / args.steps
-    rows_per_step = len(TEMPS) * B * K
+    rows_per_step = 2 * B * K
     value = job_rate(ms_total, args.steps, ws, rows_per_step)
 
     # ---- end to end through the public API, host buffers ----
-    e2e = run_e2e(args, ssv, batches, dev, stream)
+    e2e = run_e2e(args, ssv, headline, y0, dev, stream)
+    del tgt, drf, grad
+    torch.cuda.empty_cache()
 
+    barrier(ws)
     if rank != 0:
         return
-    abytes = algorithmic_bytes()
+    abytes = algorithmic_bytes(B, K, V)
     peak, peak_kind = hbm_peak()
-    avg = {k: statistics.mean(v) for k, v in per_kind.items()}
-    share = {k: (sum(per_kind[k]) / max(sum(sum(v) for v in per_kind.values()), 1e-9)) for k in per_kind}
-    # dominant single kernel by time: verify (two calls per step) vs the E2E pair
-    dom = max(("verify", "greedy"), key=lambda k: sum(per_kind[k]))
+    avg = {k_: statistics.mean(v_) for k_, v_ in per_kind.items()}
+    med = {k_: statistics.median(v_) for k_, v_ in per_kind.items()}
+    share = {k_: sum(per_kind[k_]) / max(sum(sum(v_) for v_ in per_kind.values()), 1e-9) for k_ in per_kind}
+    keys = {"verify": "sweep<Bf16,verify T=1>@zipf B128K7V129280",
+            "greedy": "sweep<Bf16,greedy T=0>@zipf B128K7V129280",
+            "e2e": "e2e-tv fwd+bwd<Bf16>@zipf B128K7V129280"}
+    clk = clocks.summary(t_wall0, t_wall1) if clocks else None
+    # the dominant call by time share carries the roofline object
+    dom = max(CALLS, key=lambda k_: share[k_])
     achieved = abytes[dom] / (avg[dom] * 1e-3) / 1e9
-    key = {"verify": "sweep_kernel<Bf16,kVerify>@entropy B32K4V151936",
-           "greedy": "sweep_kernel<Bf16,kVerifyGreedy>@entropy B32K4V151936"}[dom]
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-            "traffic": measured_traffic(key), "kernel": key, "peak_kind": peak_kind,
-            "algorithmic_bytes_per_launch": abytes[dom], "avg_launch_us": 1e3 * avg[dom]}
-    per_call = {k: {"avg_us": 1e3 * avg[k], "GB_s": abytes[k] / (avg[k] * 1e-3) / 1e9,
-                    "frac_of_measured_hbm": abytes[k] / (avg[k] * 1e-3) / 1e9 / peak, "time_share": share[k]}
-                for k in per_kind}
+            "traffic": measured_traffic(keys[dom]), "kernel": keys[dom], "peak_kind": peak_kind,
+            "algorithmic_bytes_per_launch": abytes[dom], "avg_launch_us": 1e3 * avg[dom],
+            "frac_of_nominal_8tbs": achieved / 8000.0}
+    sm_mhz = (clk or {}).get("sm_mhz") or 2070.0
+    nexp = exps_per_verify(B, K, V)
+    mufu_peak = EX2_PER_SM_CLK * torch.cuda.get_device_properties(dev).multi_processor_count * sm_mhz * 1e6
+    mufu = {"kernel": keys["verify"], "ex2_per_launch": nexp, "ex2_per_s": nexp / (avg["verify"] * 1e-3),
+            "peak_ex2_per_s": mufu_peak, "frac": nexp / (avg["verify"] * 1e-3) / mufu_peak,
+            "peak_basis": f"{EX2_PER_SM_CLK} ex2 per SM per clock (probe) x SMs x median SM clock {sm_mhz} MHz"}
+    per_call = {k_: {"avg_us": 1e3 * avg[k_], "median_us": 1e3 * med[k_],
+                     "GB_s": abytes[k_] / (avg[k_] * 1e-3) / 1e9,
+                     "frac_of_measured_hbm": abytes[k_] / (avg[k_] * 1e-3) / 1e9 / peak,
+                     "algorithmic_bytes": abytes[k_], "time_share": share[k_],
+                     "traffic": measured_traffic(keys[k_])} for k_ in CALLS}
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "B": B, "K": K, "V": V, "l2": L2_NOTE, "rows_per_step": rows_per_step,
                    "parallelism": f"dp{ws} (independent batch rows per GPU)"},
-        "roofline": roof, "per_call": per_call,
-        "gpu_launches": launches_per_step * args.steps,
+        "roofline": roof, "mufu": mufu, "per_call": per_call,
+        "gpu_launches": n_launch,
         "e2e": e2e,
-        "clocks": clocks.summary(t_wall0, t_wall1) if clocks else None,
+        "clocks": clk,
     }
+    if not args.no_extras:
+        line["extra"] = run_extras(ssv, L, dev, stream, peak)
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(batches)
+        d = tempfile.mkdtemp(prefix="ssv_bench_rows_")
+        try:
+            write_oracle_rows(d, headline, y0)
+            pool = OraclePool(d)
+            try:
+                line["cpu_baseline"] = cpu_baselines(pool)
+            finally:
+                pool.close()
+        finally:
+            shutil.rmtree(d, ignore_errors=True)
     print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, ssv, batches, dev, stream):
+def run_e2e(args, ssv, w, y0, dev, stream):
     """Whole steps from pinned host memory through the public API: H2D copy of
-    the batch, the four calls, D2H of tokens / counts / overlaps / loss.  The
+    the batch, the three calls, D2H of tokens / counts / overlaps / loss.  The
     copy of step i+1's inputs runs on a copy stream into the other of two
     device input sets while step i's kernels run: every step still copies
     its own inputs and reads back its own results."""
-    base = batches[1.0]
     pin = lambda t: t.contiguous().pin_memory()  # noqa: E731
-    th, dh = pin(base.target), pin(base.draft)
-    hin = {T: (pin(batches[T].draft_tokens), pin(batches[T].u_accept), pin(batches[T].u_final)) for T in TEMPS}
+    th, dh = pin(w.target), pin(w.draft)
+    hin = (pin(w.draft_tokens), pin(w.u_accept), pin(w.u_final), pin(y0))
     sets = []
     for _ in range(2):
         sets.append({"t": torch.empty_like(th, device=dev), "d": torch.empty_like(dh, device=dev),
-                     "in": {T: tuple(torch.empty_like(x, device=dev) for x in hin[T]) for T in TEMPS}})
-    outs = {T: ssv.VerifyOutput(torch.empty((B, K + 1), dtype=torch.int32, device=dev),
-                                torch.empty((B,), dtype=torch.int32, device=dev),
-                                torch.empty((B, K), dtype=torch.float32, device=dev) if T > 0 else None,
-                                torch.zeros((1,), dtype=torch.int32, device=dev)) for T in TEMPS}
+                     "in": tuple(torch.empty_like(x, device=dev) for x in hin)})
+    o1 = ssv.VerifyOutput(torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+                          torch.empty((B,), dtype=torch.int32, device=dev),
+                          torch.empty((B, K), dtype=torch.float32, device=dev),
+                          torch.zeros((1,), dtype=torch.int32, device=dev))
+    o0 = ssv.VerifyOutput(torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+                          torch.empty((B,), dtype=torch.int32, device=dev), None,
+                          torch.zeros((1,), dtype=torch.int32, device=dev))
     eo = ssv.E2EOutput(torch.empty((1,), dtype=torch.float32, device=dev),
                        torch.empty((B, K), dtype=torch.float32, device=dev),
                        torch.empty((B, K, V), dtype=torch.float32, device=dev),
                        torch.zeros((1,), dtype=torch.int32, device=dev))
-    hout = {T: (torch.empty((B, K + 1), dtype=torch.int32).pin_memory(),
-                torch.empty((B,), dtype=torch.int32).pin_memory(),
-                torch.empty((B, K), dtype=torch.float32).pin_memory()) for T in TEMPS}
+    hout = (torch.empty((B, K + 1), dtype=torch.int32).pin_memory(), torch.empty((B,), dtype=torch.int32).pin_memory(),
+            torch.empty((B, K), dtype=torch.float32).pin_memory(),
+            torch.empty((B, K + 1), dtype=torch.int32).pin_memory(), torch.empty((B,), dtype=torch.int32).pin_memory())
     hloss = torch.empty((1,), dtype=torch.float32).pin_memory()
-    h2d = th.numel() * 2 + dh.numel() * 2 + sum(x.numel() * x.element_size() for T in TEMPS for x in hin[T])
-    d2h = 4 + sum(x.numel() * x.element_size() for T in TEMPS for x in (hout[T][:2] if T == 0 else hout[T]))
+    h2d = th.numel() * 2 + dh.numel() * 2 + sum(x.numel() * x.element_size() for x in hin)
+    d2h = 4 + sum(x.numel() * x.element_size() for x in hout)
     copy_s = torch.cuda.Stream(dev)
     free = [torch.cuda.Event(), torch.cuda.Event()]  # the kernels are done with input set j
     for ev in free:
@@ -499,23 +656,22 @@ def run_e2e(args, ssv, batches, dev, stream):
         with torch.cuda.stream(copy_s):
             st["t"].copy_(th, non_blocking=True)
             st["d"].copy_(dh, non_blocking=True)
-            for T in TEMPS:
-                for a, b_ in zip(st["in"][T], hin[T]):
-                    a.copy_(b_, non_blocking=True)
+            for a, b_ in zip(st["in"], hin):
+                a.copy_(b_, non_blocking=True)
         landed = torch.cuda.Event()
         landed.record(copy_s)
         stream.wait_event(landed)
         t, d = st["t"], st["d"]
-        for T in TEMPS:
-            y, ua, uf = st["in"][T]
-            ssv.verify(t, d if T > 0 else None, y, ua, uf, T, out=outs[T], stream=stream)
+        yy, uaa, uff, yy0 = st["in"]
+        ssv.verify(t, d, yy, uaa, uff, 1.0, out=o1, stream=stream)
+        ssv.verify(t, None, yy0, None, None, 0.0, out=o0, stream=stream)
         ssv.e2e_tv_fwd_bwd(t, d, 1.0, 1.0, K=K, out=eo, stream=stream)
         free[i & 1].record(stream)
-        for T in TEMPS:
-            hout[T][0].copy_(outs[T].tokens, non_blocking=True)
-            hout[T][1].copy_(outs[T].n_accepted, non_blocking=True)
-            if T > 0:
-                hout[T][2].copy_(outs[T].alpha, non_blocking=True)
+        hout[0].copy_(o1.tokens, non_blocking=True)
+        hout[1].copy_(o1.n_accepted, non_blocking=True)
+        hout[2].copy_(o1.alpha, non_blocking=True)
+        hout[3].copy_(o0.tokens, non_blocking=True)
+        hout[4].copy_(o0.n_accepted, non_blocking=True)
         hloss.copy_(eo.loss, non_blocking=True)
 
     for i in range(3):
@@ -528,16 +684,116 @@ def run_e2e(args, ssv, batches, dev, stream):
     torch.cuda.synchronize()
     dt = time.perf_counter() - t0
     # the last step's results, read on the host, check the pipeline
-    ref_tok = outs[1.0].tokens.cpu()
-    assert torch.equal(hout[1.0][0], ref_tok)
-    return {"value": len(TEMPS) * B * K * n / dt, "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
+    assert torch.equal(hout[0], o1.tokens.cpu())
+    return {"value": 2 * B * K * n / dt, "unit": "rows/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "steps": n, "ms_per_step": 1e3 * dt / n,
             "overlap": "step i+1's H2D copy runs on a second stream during step i's kernels (two input sets)"}
 
 
+# ---------------------------------------------------------------------------
+# extra workloads (rank 0, after the timed region)
+# ---------------------------------------------------------------------------
+
+def _time_calls(stream, fns, reps):
+    """CUDA events around each call; returns per-call lists of ms."""
+    ts = [[] for _ in fns]
+    for r in range(reps):
+        for j, f in enumerate(fns):
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            f(r)
+            b_.record(stream)
+            ts[j].append((a, b_))
+    torch.cuda.synchronize()
+    return [[a.elapsed_time(b_) for a, b_ in t] for t in ts]
+
+
+def run_extras(ssv, L, dev, stream, peak):
+    from sampling_spec_verify_gb300 import synth
+    out = {}
+    # -- the entropy-mix step: verify T=1 and T=0.7 with overlap, greedy, E2E-TV (rotated over 8 copies) --
+    bat = {T: synth.entropy_mix(seed=SEED2, temperature=T, B=B2, K=K2, V=V2) for T in TEMPS2}
+    base = bat[1.0]
+    nrot = 8
+    tg = [base.target.to(dev) for _ in range(nrot)]
+    dr = [base.draft.to(dev) for _ in range(nrot)]
+    inp = {T: (bat[T].draft_tokens.to(dev), bat[T].u_accept.to(dev), bat[T].u_final.to(dev)) for T in TEMPS2}
+    o = {T: ssv.verify(tg[0], dr[0] if T > 0 else None, *inp[T], T) for T in TEMPS2}
+    eo = ssv.e2e_tv_fwd_bwd(tg[0], dr[0], 1.0, 1.0, K=K2)
+    fns = [lambda r, T=T: ssv.verify(tg[r % nrot], dr[r % nrot] if T > 0 else None, *inp[T], T, out=o[T],
+                                      stream=stream) for T in TEMPS2]
+    fns.append(lambda r: ssv.e2e_tv_fwd_bwd(tg[r % nrot], dr[r % nrot], 1.0, 1.0, K=K2, out=eo, stream=stream))
+    for r in range(5):
+        for f in fns:
+            f(r)
+    t = _time_calls(stream, fns, 400)
+    ab = algorithmic_bytes(B2, K2, V2)
+    names = ["verify_t1", "verify_t07", "greedy", "e2e"]
+    kinds = ["verify", "verify", "greedy", "e2e"]
+    step_ms = sum(statistics.mean(x) for x in t)
+    out["entropy_mix_b32k4"] = {
+        "workload": "entropy mix B=32, K=4, V=151936 bf16; verify T=1 and T=0.7 with overlap, greedy T=0, "
+                    "E2E-TV fwd+bwd T=1; 8 rotated copies (700 MB > L2)",
+        "rows_per_s": 3 * B2 * K2 / (step_ms * 1e-3),
+        "calls": {n_: {"avg_us": 1e3 * statistics.mean(x), "GB_s": ab[k_] / (statistics.mean(x) * 1e-3) / 1e9,
+                       "frac_of_measured_hbm": ab[k_] / (statistics.mean(x) * 1e-3) / 1e9 / peak}
+                  for n_, k_, x in zip(names, kinds, t)}}
+    del tg, dr, o, eo, bat, base
+    torch.cuda.empty_cache()
+
+    # -- E2E-TV training batch, B=256, K=7, V=151936 (2 rotated copies, 2.18 GB per call) --
+    w4 = synth.e2e(seed=SEED4, B=B4, K=K4, V=V4)
+    t4 = [w4.target.to(dev) for _ in range(2)]
+    d4 = [w4.draft.to(dev) for _ in range(2)]
+    del w4
+    e4 = ssv.e2e_tv_fwd_bwd(t4[0], d4[0], 1.0, 1.0)
+    f4 = [lambda r: ssv.e2e_tv_fwd_bwd(t4[r & 1], d4[r & 1], 1.0, 1.0, out=e4, stream=stream)]
+    for r in range(3):
+        f4[0](r)
+    x = _time_calls(stream, f4, 30)[0]
+    by = algorithmic_bytes(B4, K4, V4)["e2e"]
+    out["e2e_tv_b256k7"] = {"workload": "E2E-TV fwd+bwd B=256, K=7, V=151936 bf16 logits, fp32 gradient, T=1",
+                            "avg_us": 1e3 * statistics.mean(x), "median_us": 1e3 * statistics.median(x),
+                            "algorithmic_bytes": by, "GB_s": by / (statistics.mean(x) * 1e-3) / 1e9,
+                            "frac_of_measured_hbm": by / (statistics.mean(x) * 1e-3) / 1e9 / peak}
+    del t4, d4, e4
+    torch.cuda.empty_cache()
+
+    # -- the small case: 1000 seeded calls of B=1, K=4, V=1024 fp32, one at a time --
+    ws_ = [synth.small(seed=s_) for s_ in range(1000)]
+    args_ = [(w.target.to(dev), w.draft.to(dev), w.draft_tokens.to(dev), w.u_accept.to(dev), w.u_final.to(dev))
+             for w in ws_]
+    os_ = ssv.verify(*args_[0], 1.0)
+    wsp = torch.zeros(L.spec_verify_workspace_bytes(1, 4, 1024), dtype=torch.uint8, device=dev)
+    for a in args_[:20]:
+        ssv.verify(*a, 1.0, out=os_, workspace=wsp, stream=stream)
+    torch.cuda.synchronize()
+    dev_us, wall_us = [], []
+    for a in args_:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record(stream)
+        ssv.verify(*a, 1.0, out=os_, workspace=wsp, stream=stream)
+        e1.record(stream)
+        e1.synchronize()
+        wall_us.append(1e6 * (time.perf_counter() - t0))
+        dev_us.append(1e3 * e0.elapsed_time(e1))
+    q = lambda v, p: float(np.percentile(np.asarray(v), p))  # noqa: E731
+    out["small_b1k4_latency"] = {
+        "workload": "B=1, K=4, V=1024 fp32, T=1; 1000 seeded calls, one at a time",
+        "device_us": {"median": q(dev_us, 50), "p99": q(dev_us, 99)},
+        "host_wall_us": {"median": q(wall_us, 50), "p99": q(wall_us, 99),
+                         "note": "Python binding call + launch + kernel + event synchronise"}}
+    return out
+
+
+# ---------------------------------------------------------------------------
+# single calls and the shape sweep (profiling targets)
+# ---------------------------------------------------------------------------
+
 def run_single(args):
-    """A few calls of one entry point on the entropy-mix workload at --shape,
-    each after a 512 MB L2 flush, for ncu captures of one launch."""
+    """A few calls of one entry point at --shape, each after a 512 MB L2
+    flush, for ncu captures of one launch."""
     import sampling_spec_verify_gb300 as ssv
     from sampling_spec_verify_gb300 import synth
     Bs, Ks, Vs = (int(v) for v in args.shape.split(","))
@@ -545,9 +801,14 @@ def run_single(args):
     T = 0.0 if args.single == "greedy" else (
         1.0 if args.single in ("overlap", "e2e", "diag", "truncate", "ragged", "schedule", "relaxed")
         else args.temperature)
-    w = synth.entropy_mix(seed=SEED, temperature=T, B=Bs, K=Ks, V=Vs)
+    if args.workload == "zipf":
+        w = synth.zipf(seed=SEED, B=Bs, K=Ks, V=Vs)
+        y = (synth.greedy_tokens(w.draft) if T == 0.0 else w.draft_tokens).to(dev)
+    else:
+        w = synth.entropy_mix(seed=SEED2, temperature=T, B=Bs, K=Ks, V=Vs)
+        y = w.draft_tokens.to(dev)
     t, d = w.target.to(dev), w.draft.to(dev)
-    y, ua, uf = w.draft_tokens.to(dev), w.u_accept.to(dev), w.u_final.to(dev)
+    ua, uf = w.u_accept.to(dev), w.u_final.to(dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     for _ in range(args.calls):
         flush.zero_()
@@ -575,7 +836,7 @@ def run_single(args):
         else:
             ssv.e2e_tv_fwd_bwd(t, d, 1.0, 1.0, K=Ks)
     torch.cuda.synchronize()
-    print("ok", args.single, Bs, Ks, Vs, T)
+    print("ok", args.single, args.workload, Bs, Ks, Vs, T)
 
 
 def run_sweep():
@@ -586,12 +847,13 @@ def run_sweep():
     dev = torch.device("cuda")
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     peak, _ = hbm_peak()
+    Vs = 151936
     for Bs in (1, 8, 32, 64, 128, 256):
         for Ks in (1, 2, 4, 7, 16):
             g = torch.Generator(device=dev).manual_seed(Bs * 100 + Ks)
-            t = (torch.randn((Bs, Ks + 1, V), device=dev, generator=g) * 2).to(torch.bfloat16)
-            d = (t[:, :Ks].float() + 0.5 * torch.randn((Bs, Ks, V), device=dev, generator=g)).to(torch.bfloat16)
-            gum = -torch.log(-torch.log(torch.rand((Bs, Ks, V), device=dev, generator=g).clamp_min(1e-20)))
+            t = (torch.randn((Bs, Ks + 1, Vs), device=dev, generator=g) * 2).to(torch.bfloat16)
+            d = (t[:, :Ks].float() + 0.5 * torch.randn((Bs, Ks, Vs), device=dev, generator=g)).to(torch.bfloat16)
+            gum = -torch.log(-torch.log(torch.rand((Bs, Ks, Vs), device=dev, generator=g).clamp_min(1e-20)))
             y = torch.argmax(d.float() + gum, dim=2).to(torch.int32)
             del gum
             ua = torch.rand((Bs, Ks), device=dev, generator=g)
@@ -608,8 +870,8 @@ def run_sweep():
                 if i >= 2:
                     ts.append(a.elapsed_time(b) * 1e3)
             us = statistics.median(ts)
-            by = Bs * (2 * Ks + 1) * V * 2
-            print(json.dumps({"B": Bs, "K": Ks, "V": V, "us": round(us, 1), "rows_per_s": round(Bs * Ks / us * 1e6),
+            by = Bs * (2 * Ks + 1) * Vs * 2
+            print(json.dumps({"B": Bs, "K": Ks, "V": Vs, "us": round(us, 1), "rows_per_s": round(Bs * Ks / us * 1e6),
                               "GB_s": round(by / us / 1e3), "frac_of_measured_hbm": round(by / us / 1e3 / peak, 3)}),
                   flush=True)
             del t, d, y, o

@@ -69,6 +69,12 @@ int spec_abi_version(void);
 /* Human-readable name of a status code (static string). */
 const char* spec_status_string(spec_status_t status);
 
+/* Number of kernels this library has launched in this process, over every
+ * device and stream: counted on the host when a launch is enqueued without
+ * error (library memsets are not counted).  For measurement: read it before
+ * and after a timed region.  Never fails. */
+unsigned long long spec_kernel_launches(void);
+
 /* ------------------------------------------------------------------------ */
 /* Batched verify step.
  *

@@ -36,7 +36,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "SpecError", "lib", "verify", "verify_ragged", "verify_relaxed", "tree_mask", "tree_verify_greedy", "overlap", "e2e_tv_fwd_bwd", "diagnostics", "truncate_logits", "schedule_lengths", "selftest_bounded_wait", "launch_shape",
+    "SpecError", "lib", "verify", "verify_ragged", "verify_relaxed", "tree_mask", "tree_verify_greedy", "overlap", "e2e_tv_fwd_bwd", "diagnostics", "truncate_logits", "schedule_lengths", "selftest_bounded_wait", "launch_shape", "kernel_launches",
     "set_launch_override", "VerifyOutput", "OverlapOutput", "E2EOutput", "DiagOutput", "TreeOutput", "HostVerifier",
     "DEV_BAD_TOKEN", "DEV_BAD_LOGITS", "DEV_BAD_UNIFORM", "DEV_TIMEOUT", "DEV_EMPTY_RESIDUAL", "DEV_BAD_OFFSETS",
     "SPEC_OK", "SPEC_ERR_INVALID_ARG", "SPEC_ERR_UNSUPPORTED", "SPEC_ERR_CUDA",
@@ -73,6 +73,8 @@ def lib():
     L = ctypes.CDLL(LIB_PATH)
     vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.spec_abi_version.restype = i32
+    L.spec_kernel_launches.restype = ctypes.c_ulonglong
+    L.spec_kernel_launches.argtypes = []
     L.spec_status_string.restype = ctypes.c_char_p
     L.spec_status_string.argtypes = [i32]
     L.spec_verify_workspace_bytes.restype = sz
@@ -170,6 +172,11 @@ def _workspace(nbytes: int, device, stream) -> torch.Tensor:
 def _check(status: int, what: str):
     if status != SPEC_OK:
         raise SpecError(status, what)
+
+
+def kernel_launches() -> int:
+    """Kernels the library has launched in this process (host-side count)."""
+    return int(lib().spec_kernel_launches())
 
 
 def set_launch_override(cluster_ctas: int = 0, stages: int = 0) -> None:

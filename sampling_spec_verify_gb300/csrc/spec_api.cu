@@ -33,6 +33,15 @@ constexpr int kStaticSmemReserve = 4096;
 std::atomic<int> g_cluster_override{0};
 std::atomic<int> g_stage_override{0};
 
+// Kernels launched by this library (counted on the host when a launch is
+// enqueued without error).
+std::atomic<unsigned long long> g_launches{0};
+
+cudaError_t counted(cudaError_t e) {
+  if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
+
 struct DevInfo {
   int sms = 0;
   int smem_optin = 0;
@@ -213,7 +222,7 @@ cudaError_t launch_sweep(const SweepParams& P0, const Shape& sh, cudaStream_t st
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fn, P);
+  return counted(cudaLaunchKernelEx(&cfg, fn, P));
 }
 
 template <int MODE>
@@ -228,7 +237,7 @@ cudaError_t launch_grad(const ssv::GradParams& G, cudaStream_t stream) {
   gx = gx < 1 ? 1 : gx;
   const int gy = G.units < 65535 ? G.units : 65535;
   ssv::e2e_grad_kernel<E><<<dim3(gx, gy, 1), 256, 0, stream>>>(G);
-  return cudaGetLastError();
+  return counted(cudaGetLastError());
 }
 
 // Workspace layouts (all offsets 256-byte aligned).
@@ -349,6 +358,8 @@ __global__ void bounded_wait_selftest_kernel(uint64_t limit_ns, uint32_t* status
 extern "C" {
 
 int spec_abi_version(void) { return 2; }
+
+unsigned long long spec_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* spec_status_string(spec_status_t s) {
   switch (s) {
@@ -683,13 +694,13 @@ spec_status_t spec_truncate_logits(const void* logits, void* out, spec_dtype_t d
     ssv::truncate_kernel<Bf16><<<grid, ssv::kTThreads, smem, st>>>(P);
   else
     ssv::truncate_kernel<F32><<<grid, ssv::kTThreads, smem, st>>>(P);
-  return from_cuda(cudaGetLastError());
+  return from_cuda(counted(cudaGetLastError()));
 }
 
 spec_status_t spec_selftest_bounded_wait(uint64_t limit_ns, uint32_t* dev_status, void* stream) {
   if (!dev_status || limit_ns == 0 || limit_ns > 10000000000ull) return SPEC_ERR_INVALID_ARG;
   bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_ns, dev_status);
-  return from_cuda(cudaGetLastError());
+  return from_cuda(counted(cudaGetLastError()));
 }
 
 spec_status_t spec_schedule_lengths(const float* survival, int R, int L, const float* sps, int sps_len,
@@ -721,7 +732,7 @@ spec_status_t spec_schedule_lengths(const float* survival, int R, int L, const f
   P.objective = objective;
   P.status = dev_status;
   ssv::schedule_kernel<<<1, ssv::kSThreads, smem, static_cast<cudaStream_t>(stream)>>>(P);
-  return from_cuda(cudaGetLastError());
+  return from_cuda(counted(cudaGetLastError()));
 }
 
 size_t spec_verify_ragged_workspace_bytes(int B, int units, int V) {
@@ -755,7 +766,7 @@ spec_status_t spec_verify_ragged(const void* target_logits, const void* draft_lo
   uint2* uinfo = reinterpret_cast<uint2*>(w + ws.uinfo);
   uint32_t* bad = reinterpret_cast<uint32_t*>(w + ws.bad);
   ragged_units_kernel<<<(B + 255) / 256, 256, 0, st>>>(row_offsets, B, units, uinfo, bad, dev_status);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = counted(cudaGetLastError());
   if (e != cudaSuccess) return SPEC_ERR_CUDA;
   SweepParams P = {};
   P.target = target_logits;
@@ -858,7 +869,7 @@ spec_status_t spec_tree_mask(const int32_t* parent, int B, int N, uint8_t* mask,
   const unsigned grid = (unsigned)((n + 255) / 256);
   ssv::tree_mask_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(parent, B, N, mask, depth,
                                                                              dev_status);
-  return from_cuda(cudaGetLastError());
+  return from_cuda(counted(cudaGetLastError()));
 }
 
 size_t spec_tree_verify_workspace_bytes(int B, int N, int V) {
@@ -905,7 +916,7 @@ spec_status_t spec_tree_verify_greedy(const void* target_logits, spec_dtype_t dt
   if (e != cudaSuccess) return SPEC_ERR_CUDA;
   ssv::tree_walk_kernel<<<(B + 127) / 128, 128, 0, st>>>(am, parent, node_tokens, B, N, path, out_tokens,
                                                           n_accepted, dev_status);
-  e = cudaGetLastError();
+  e = counted(cudaGetLastError());
   if (e != cudaSuccess) return SPEC_ERR_CUDA;
   // the argmax array is the only workspace written: leave it zero
   return from_cuda(cudaMemsetAsync(am, 0, (size_t)units * sizeof(int32_t), st));

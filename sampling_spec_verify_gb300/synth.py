@@ -154,6 +154,12 @@ def zipf(seed=0, B=128, K=7, V=129280, temperature=1.0, low_frac=0.2, bonus=True
     return w
 
 
+def greedy_tokens(draft: torch.Tensor) -> torch.Tensor:
+    """The tokens a greedy (T == 0) drafter proposes: argmax z_d per position,
+    first index on ties."""
+    return _gumbel_draft(None, draft, 0.0)
+
+
 def e2e(seed=0, B=256, K=7, V=151936):
     """E2E-TV training batch: target and draft logits [B, K, V] (no bonus row)."""
     return gaussian(B, K, V, sigma=2.0, noise=0.5, dtype=torch.bfloat16,

@@ -53,6 +53,8 @@ def test_status_strings_and_version(L):
     assert L.spec_status_string(0) == b"ok"
     assert L.spec_status_string(1) == b"invalid argument"
     assert L.spec_status_string(99) == b"unknown status"
+    # no kernel is launched without a GPU; the counter answers all the same
+    assert L.spec_kernel_launches() == 0
 
 
 def test_workspace_sizes(L):
