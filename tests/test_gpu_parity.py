@@ -44,6 +44,32 @@ def oracle_verify(w, T=None, rows=None, with_draft=True):
                          w.draft_tokens.numpy(), w.u_accept.numpy(), w.u_final.numpy(), T, rows=rows)
 
 
+def flag_budget(w, ref, rows=None):
+    """Upper tail of the number of rows the oracle may flag, from the exact
+    flag probabilities of each row.  Over a uniform u', a draw from weights w
+    is flagged when u' lies within 1e-6 of either end of the chosen token's
+    CDF interval [C_{v-1}, C_v) / Z, with probability sum_v min(w_v / Z, 2e-6);
+    each evaluated acceptance adds at most 2e-6 (|u - p/q| < 1e-6).  A
+    threshold or operand gone wrong in the oracle flags far more rows than
+    this bound allows."""
+    eps = oracle.spec_oracle.NEAR_TIE
+    T = w.temperature
+    B, K, _ = w.shape
+    rows = range(B) if rows is None else rows
+    e = 0.0
+    for i, b in enumerate(rows):
+        n = int(ref.n_accepted[i])
+        zt = synth.f64(w.target[b])
+        p = oracle.softmax_t(zt[n], T)
+        if n < K:
+            r = oracle.residual(p, oracle.softmax_t(synth.f64(w.draft[b, n]), T))
+            wts = r if r.sum() > 0 else p
+        else:
+            wts = p
+        e += float(np.minimum(wts / wts.sum(), 2 * eps).sum()) + 2 * eps * (min(n + 1, K))
+    return e + 4.0 * np.sqrt(e) + 3.0
+
+
 def assert_verify(out, ref, rows=None, check_alpha=True):
     tok = out.tokens.cpu().numpy()
     n = out.n_accepted.cpu().numpy()
@@ -178,8 +204,10 @@ def test_entropy_mix_full_size(ssv, T):
     torch.cuda.synchronize()
     ref = oracle_verify(w)
     flagged = assert_verify(out, ref)
-    print(f"T={T}: flagged rows {flagged} / {w.shape[0]}, mean accepted {ref.n_accepted.mean():.3f}")
-    assert flagged <= 2, flagged
+    budget = flag_budget(w, ref) if T > 0 else 0
+    print(f"T={T}: flagged rows {flagged} / {w.shape[0]} (bound {budget:.1f}), mean accepted "
+          f"{ref.n_accepted.mean():.3f}")
+    assert flagged <= budget, (flagged, budget)
     assert int(out.status.item()) == 0
 
 
@@ -199,8 +227,9 @@ def test_zipf_full_size(ssv):
     np.testing.assert_allclose(a[same], 1.0, rtol=0, atol=2e-6)
     ref = oracle_verify(w)
     flagged = assert_verify(out, ref)
-    # a near tie has probability of order 1e-6 per evaluated position
-    assert flagged <= 2, flagged
+    budget = flag_budget(w, ref)
+    print(f"zipf: flagged rows {flagged} / {B} (bound {budget:.1f})")
+    assert flagged <= budget, (flagged, budget)
 
 
 def test_sweep_points_sampled_rows(ssv):
@@ -213,7 +242,8 @@ def test_sweep_points_sampled_rows(ssv):
         rows = list(range(B)) if B <= 64 else sorted(set(range(0, B, 8)) | {B - 1})
         ref = oracle_verify(w, rows=rows)
         flagged = assert_verify(out, ref, rows=rows)
-        assert flagged <= 2, (B, K, flagged)
+        budget = flag_budget(w, ref, rows)
+        assert flagged <= budget, (B, K, flagged, budget)
         n = out.n_accepted.cpu().numpy()
         assert (n >= 0).all() and (n <= K).all()
         del w, out
