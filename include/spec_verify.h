@@ -429,20 +429,32 @@ spec_status_t spec_schedule_lengths(const float* survival, int R, int L,
 spec_status_t spec_selftest_bounded_wait(uint64_t limit_ns, uint32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------ */
-/* Launch shape the library picks for a verify sweep over `units` (row,
- * position) pairs of V logits (for benchmarks and diagnostics): CTAs per
- * cluster, threads per CTA, dynamic shared memory per CTA, the number of
- * persistent clusters launched and the shared-memory stages per CTA.  Needs a current CUDA device.  Returns
+/* Launch shape the library picks for a sampling verify sweep over `units`
+ * (row, position) pairs of V logits with rows on 16-byte boundaries (for
+ * benchmarks and diagnostics): CTAs per cluster, threads per CTA (320 for
+ * the two-pass sweep, 256 for the single-read sweep), dynamic shared memory
+ * per CTA, the number of persistent clusters launched and the shared-memory
+ * stages per CTA.  Needs a current CUDA device.  Returns
  * SPEC_ERR_UNSUPPORTED if V does not fit.  Any output pointer may be NULL. */
 spec_status_t spec_launch_shape(spec_dtype_t dtype, int units, int V,
                                 int* cluster_ctas, int* threads,
                                 int* smem_bytes, int* clusters, int* stages);
 
-/* Forces the CTAs per cluster (1..16) and the shared-memory stages per CTA
- * (1 or 2) of later launches in this process, for launch-shape sweeps in
+/* Forces the CTAs per cluster (1..16) and caps the shared-memory stages per
+ * CTA (1 or 2) of later launches in this process, for launch-shape sweeps in
  * benchmarks; 0 restores the automatic choice of either.  Process-wide; not
  * synchronised with launches in flight. */
 void spec_set_launch_override(int cluster_ctas, int stages);
+
+/* Selects the vocabulary-sweep kernel of later verify, overlap and E2E-TV
+ * calls in this process: 0 automatic (the two-pass sweep wherever rows start
+ * on 16-byte boundaries and the mode has it, else the single-read sweep),
+ * 1 the single-read sweep (rows resident in cluster shared memory between
+ * passes), 2 the two-pass sweep where it applies (pass A from HBM, pass C
+ * from L2).  Any other value means 0.  For tests and benchmarks; both give
+ * the same results within the parity bar.  Process-wide; not synchronised
+ * with launches in flight. */
+void spec_set_kernel_override(int kernel);
 
 #ifdef __cplusplus
 }

@@ -36,7 +36,7 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "SpecError", "lib", "verify", "verify_ragged", "verify_relaxed", "tree_mask", "tree_verify_greedy", "overlap", "e2e_tv_fwd_bwd", "diagnostics", "truncate_logits", "schedule_lengths", "selftest_bounded_wait", "launch_shape", "kernel_launches",
+    "SpecError", "lib", "verify", "verify_ragged", "verify_relaxed", "tree_mask", "tree_verify_greedy", "overlap", "e2e_tv_fwd_bwd", "diagnostics", "truncate_logits", "schedule_lengths", "selftest_bounded_wait", "launch_shape", "kernel_launches", "set_kernel_override",
     "set_launch_override", "VerifyOutput", "OverlapOutput", "E2EOutput", "DiagOutput", "TreeOutput", "HostVerifier",
     "DEV_BAD_TOKEN", "DEV_BAD_LOGITS", "DEV_BAD_UNIFORM", "DEV_TIMEOUT", "DEV_EMPTY_RESIDUAL", "DEV_BAD_OFFSETS",
     "SPEC_OK", "SPEC_ERR_INVALID_ARG", "SPEC_ERR_UNSUPPORTED", "SPEC_ERR_CUDA",
@@ -115,6 +115,8 @@ def lib():
     L.spec_launch_shape.argtypes = [i32, i32, i32] + [ctypes.POINTER(i32)] * 5
     L.spec_set_launch_override.restype = None
     L.spec_set_launch_override.argtypes = [i32, i32]
+    L.spec_set_kernel_override.restype = None
+    L.spec_set_kernel_override.argtypes = [i32]
     _lib = L
     return L
 
@@ -177,6 +179,12 @@ def _check(status: int, what: str):
 def kernel_launches() -> int:
     """Kernels the library has launched in this process (host-side count)."""
     return int(lib().spec_kernel_launches())
+
+
+def set_kernel_override(kernel: int = 0) -> None:
+    """Sweep kernel of later calls: 0 automatic, 1 the single-read sweep,
+    2 the two-pass sweep where it applies."""
+    lib().spec_set_kernel_override(int(kernel))
 
 
 def set_launch_override(cluster_ctas: int = 0, stages: int = 0) -> None:

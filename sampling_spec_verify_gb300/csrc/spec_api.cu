@@ -13,6 +13,7 @@
 
 #include "spec_verify.h"
 #include "sweep.cuh"
+#include "pipe.cuh"
 #include "truncate.cuh"
 #include "schedule.cuh"
 #include "tree.cuh"
@@ -32,6 +33,7 @@ constexpr int kStaticSmemReserve = 4096;
 
 std::atomic<int> g_cluster_override{0};
 std::atomic<int> g_stage_override{0};
+std::atomic<int> g_kernel_override{0};  // 0 automatic, 1 single-read sweep, 2 two-pass sweep
 
 // Kernels launched by this library (counted on the host when a launch is
 // enqueued without error).
@@ -96,7 +98,7 @@ std::map<std::tuple<const void*, int, int, int>, int> g_occ;  // (kernel, S, sme
 
 // Clusters of S CTAs with `smem` dynamic bytes each that fit on the device at once.
 template <class Fn>
-int max_active_clusters(Fn fn, int S, int smem) {
+int max_active_clusters(Fn fn, int S, int smem, int threads = ssv::kThreads) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   const auto key = std::make_tuple((const void*)fn, S, smem, dev);
@@ -107,7 +109,7 @@ int max_active_clusters(Fn fn, int S, int smem) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)S, 1, 1);
-  cfg.blockDim = dim3(ssv::kThreads, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -240,11 +242,154 @@ cudaError_t launch_grad(const ssv::GradParams& G, cudaStream_t stream) {
   return counted(cudaGetLastError());
 }
 
+// ---- the two-pass sweep (pass A from HBM, pass C from L2) -------------------------
+
+struct PShape {
+  int S = 0, G = 0, NV = 0, CV = 0, NCH = 0, WV = 0, NS = 0, rows = 0, smem = 0;
+};
+
+constexpr int kPStageTarget = 32768;  // bytes of logits per ring stage
+constexpr int kPSmemReserve = 1024;
+
+template <class Fn>
+cudaError_t prepare_pipe(Fn fn, std::atomic<uint64_t>& done_mask) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done_mask.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  DevInfo di;
+  if (!device_info(&di)) return cudaErrorInvalidDevice;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           di.smem_optin - (int)sizeof(ssv::PipeSmem) - kPSmemReserve);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  done_mask.fetch_or(bit, std::memory_order_release);
+  return cudaSuccess;
+}
+
+// Picks the cluster size S for a two-pass sweep: every S whose slices fit the
+// ring (at most kPMaxCh chunks per slice, S x chunks <= kPMaxParts, at least
+// three stages) is costed as (waves of units over the resident clusters) x
+// (the fresh bytes of one CTA's slice over its share of HBM bandwidth, plus a
+// fixed allowance per unit); slices above 320 KB pay a penalty, because the
+// pass-C copy of their first chunks no longer finds them in L2.
+template <class Fn>
+bool pick_pipe_shape(Fn fn, int es, long long units, int V, int rows, PShape* out) {
+  DevInfo di;
+  if (!device_info(&di)) return false;
+  const long long smem_avail = di.smem_optin - (long long)sizeof(ssv::PipeSmem) - kPSmemReserve;
+  const int pv = 16 / es;
+  const long long nvec_row = V / pv;
+  const int ov = g_cluster_override.load();
+  const int ovs = g_stage_override.load();
+  double best = -1.0;
+  for (int S = (ov > 0 ? ov : 1); S <= (ov > 0 ? ov : ssv::kPMaxS); ++S) {
+    const long long NV = (nvec_row + S - 1) / S;
+    const long long cvmax = kPStageTarget / (rows * 16);
+    long long NCH = (NV + cvmax - 1) / cvmax;
+    if (NCH < 1) NCH = 1;
+    long long CV = (NV + NCH - 1) / NCH;
+    if (CV < 1) CV = 1;
+    if (NCH > ssv::kPMaxCh || S * NCH > ssv::kPMaxParts) continue;
+    const long long stage = (long long)rows * CV * 16;
+    long long NS = smem_avail / stage;
+    if (NS > ssv::kPMaxNS) NS = ssv::kPMaxNS;
+    if (ovs > 0 && NS > ovs) NS = ovs;
+    if (NS < 1 || (ovs == 0 && NS < 3)) continue;
+    const int G = max_active_clusters(fn, S, (int)(NS * stage), ssv::kPThreads);
+    if (G <= 0) continue;
+    const long long Ge = units < G ? units : G;
+    const double waves = (double)((units + Ge - 1) / Ge);
+    const double bytes_cta = (double)NV * rows * 16.0;
+    double bw = 6.8e12 / (double)(Ge * S);
+    if (bw > 1.2e11) bw = 1.2e11;
+    double t = waves * (bytes_cta / bw + 0.5e-6);
+    if (bytes_cta > 320.0 * 1024.0) t *= 1.5;
+    if (best < 0 || t < best) {
+      best = t;
+      out->S = S;
+      out->G = (int)Ge;
+      out->NV = (int)NV;
+      out->CV = (int)CV;
+      out->NCH = (int)NCH;
+      out->WV = (int)((CV + ssv::kPNC - 1) / ssv::kPNC);
+      out->NS = (int)NS;
+      out->rows = rows;
+      out->smem = (int)(NS * stage);
+    }
+  }
+  return best >= 0;
+}
+
+template <class E, int MODE>
+std::atomic<uint64_t>& pipe_prepared_mask() {
+  static std::atomic<uint64_t> m{0};
+  return m;
+}
+
+template <class E, int MODE>
+spec_status_t pipe_shape_for(long long units, int V, int rows, PShape* sh) {
+  auto fn = ssv::pipe_kernel<E, MODE>;
+  if (prepare_pipe(fn, pipe_prepared_mask<E, MODE>()) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (!pick_pipe_shape(fn, E::ES, units, V, rows, sh)) return SPEC_ERR_UNSUPPORTED;
+  return SPEC_OK;
+}
+
+template <int MODE>
+spec_status_t pipe_shape_dt(spec_dtype_t dt, long long units, int V, int rows, PShape* sh) {
+  return dt == SPEC_BF16 ? pipe_shape_for<Bf16, MODE>(units, V, rows, sh)
+                         : pipe_shape_for<F32, MODE>(units, V, rows, sh);
+}
+
+template <class E, int MODE>
+cudaError_t launch_pipe(const ssv::PipeParams& P, const PShape& sh, cudaStream_t stream) {
+  auto fn = ssv::pipe_kernel<E, MODE>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(sh.G * sh.S), 1, 1);
+  cfg.blockDim = dim3(ssv::kPThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)sh.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)sh.S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return counted(cudaLaunchKernelEx(&cfg, fn, P));
+}
+
+template <int MODE>
+cudaError_t launch_pipe_dt(spec_dtype_t dt, const ssv::PipeParams& P, const PShape& sh, cudaStream_t stream) {
+  return dt == SPEC_BF16 ? launch_pipe<Bf16, MODE>(P, sh, stream) : launch_pipe<F32, MODE>(P, sh, stream);
+}
+
+// Fills the shape fields of a two-pass launch.
+void pipe_geometry(ssv::PipeParams* P, const PShape& sh) {
+  P->S = sh.S;
+  P->G = sh.G;
+  P->NV = sh.NV;
+  P->CV = sh.CV;
+  P->NCH = sh.NCH;
+  P->WV = sh.WV;
+  P->NS = sh.NS;
+  P->rows = sh.rows;
+}
+
+// The two-pass sweep serves rows that start on 16-byte boundaries.
+bool pipe_allowed(const void* a, const void* b, int V, int es) {
+  if (g_kernel_override.load() == 1) return false;
+  return ((long long)V * es) % 16 == 0 && (reinterpret_cast<uintptr_t>(a) & 15u) == 0 &&
+         (b == nullptr || (reinterpret_cast<uintptr_t>(b) & 15u) == 0);
+}
+
 // Workspace layouts (all offsets 256-byte aligned).
 size_t part_bytes(long long units) { return align256((size_t)units * ssv::kPartStride * sizeof(float)); }
 
 struct VerifyWs {
-  size_t rec = 0, part = 0, cnt = 0, rej = 0, total = 0;
+  size_t rec = 0, part = 0, cnt = 0, rej = 0, dtot = 0, dcnt = 0, total = 0;
 };
 VerifyWs verify_ws(int B, int K) {
   const long long units = (long long)B * (K + 1);
@@ -253,7 +398,9 @@ VerifyWs verify_ws(int B, int K) {
   w.part = align256((size_t)units * sizeof(VerifyRecord));
   w.cnt = w.part + part_bytes(units);
   w.rej = w.cnt + align256((size_t)B * sizeof(uint32_t));
-  w.total = w.rej + align256((size_t)B * sizeof(uint32_t));
+  w.dtot = w.rej + align256((size_t)B * sizeof(uint32_t));
+  w.dcnt = w.dtot + align256((size_t)units * ssv::kPMaxParts * sizeof(float));
+  w.total = w.dcnt + align256((size_t)units * sizeof(uint32_t));
   return w;
 }
 struct OverlapWs {
@@ -380,9 +527,24 @@ void spec_set_launch_override(int cluster_ctas, int stages) {
   g_stage_override.store(stages == 1 || stages == 2 ? stages : 0);
 }
 
+void spec_set_kernel_override(int kernel) { g_kernel_override.store(kernel == 1 || kernel == 2 ? kernel : 0); }
+
 spec_status_t spec_launch_shape(spec_dtype_t dtype, int units, int V, int* cluster_ctas, int* threads,
                                 int* smem_bytes, int* clusters, int* stages) {
   if (!dtype_ok(dtype) || units < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (g_kernel_override.load() != 1 && ((long long)V * elem_size(dtype)) % 16 == 0) {
+    PShape ps;
+    const spec_status_t r = pipe_shape_dt<ssv::kPSample>(dtype, units, V, 2, &ps);
+    if (r == SPEC_ERR_CUDA) return r;
+    if (r == SPEC_OK) {
+      if (cluster_ctas) *cluster_ctas = ps.S;
+      if (threads) *threads = ssv::kPThreads;
+      if (smem_bytes) *smem_bytes = ps.smem;
+      if (clusters) *clusters = ps.G;
+      if (stages) *stages = ps.NS;
+      return SPEC_OK;
+    }
+  }
   Shape sh;
   const spec_status_t r = shape_for_dt<ssv::kVerify>(dtype, units, V, 2, &sh);
   if (r != SPEC_OK) return r;
@@ -417,6 +579,43 @@ spec_status_t spec_verify(const void* target_logits, const void* draft_logits, s
   if (units > 0x7FFFFFFFLL) return SPEC_ERR_UNSUPPORTED;
   const int es = elem_size(dtype);
   const int rows = (greedy && !alpha_out) ? 1 : 2;  // greedy without overlap reads no draft row
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (pipe_allowed(target_logits, rows == 2 ? draft_logits : nullptr, V, es)) {
+    PShape ps;
+    const spec_status_t r = greedy ? pipe_shape_dt<ssv::kPGreedy>(dtype, units, V, rows, &ps)
+                                   : pipe_shape_dt<ssv::kPSample>(dtype, units, V, rows, &ps);
+    if (r == SPEC_ERR_CUDA) return r;
+    if (r == SPEC_OK) {
+      ssv::PipeParams P = {};
+      P.target = target_logits;
+      P.draft = draft_logits;
+      P.B = B;
+      P.K = K;
+      P.KT = K + 1;
+      P.V = V;
+      P.units = (int)units;
+      pipe_geometry(&P, ps);
+      P.grouped = (!greedy && B >= ps.G) ? 1 : 0;
+      P.s = greedy ? 0.0f : (float)(1.4426950408889634 / (double)temperature);
+      P.inv_t = greedy ? 0.0f : (float)(1.0 / (double)temperature);
+      P.draft_tokens = draft_tokens;
+      P.u_accept = u_accept;
+      P.u_final = u_final;
+      P.out_tokens = out_tokens;
+      P.n_accepted = n_accepted;
+      P.alpha = alpha_out;
+      char* w = static_cast<char*>(workspace);
+      P.rec = reinterpret_cast<VerifyRecord*>(w + ws.rec);
+      P.part = reinterpret_cast<float*>(w + ws.part);
+      P.row_cnt = reinterpret_cast<uint32_t*>(w + ws.cnt);
+      P.rej = reinterpret_cast<uint32_t*>(w + ws.rej);
+      P.dtot = reinterpret_cast<float*>(w + ws.dtot);
+      P.dcnt = reinterpret_cast<uint32_t*>(w + ws.dcnt);
+      P.status = dev_status;
+      return from_cuda(greedy ? launch_pipe_dt<ssv::kPGreedy>(dtype, P, ps, st)
+                              : launch_pipe_dt<ssv::kPSample>(dtype, P, ps, st));
+    }
+  }
   Shape sh;
   {
     // both sampling orders share one launch shape
@@ -452,7 +651,6 @@ spec_status_t spec_verify(const void* target_logits, const void* draft_logits, s
   P.row_cnt = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + ws.cnt);
   P.rej = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + ws.rej);
   P.status = dev_status;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   // At least one row per cluster: rows in groups, position-major (later
   // positions can skip draws that an earlier rejection makes unused).
   // Fewer rows: row-major order, which measured faster there.
@@ -492,6 +690,32 @@ spec_status_t spec_overlap(const void* target_logits, const void* draft_logits, 
   if (units > 0x7FFFFFFFLL) return SPEC_ERR_UNSUPPORTED;
   const int es = elem_size(dtype);
   const bool greedy = temperature == 0.0f;
+  if (!greedy && pipe_allowed(target_logits, draft_logits, V, es)) {
+    PShape ps;
+    const spec_status_t r = pipe_shape_dt<ssv::kPOverlap>(dtype, units, V, 2, &ps);
+    if (r == SPEC_ERR_CUDA) return r;
+    if (r == SPEC_OK) {
+      ssv::PipeParams P = {};
+      P.target = target_logits;
+      P.draft = draft_logits;
+      P.B = B;
+      P.K = K;
+      P.KT = KT;
+      P.V = V;
+      P.units = (int)units;
+      pipe_geometry(&P, ps);
+      P.s = (float)(1.4426950408889634 / (double)temperature);
+      P.inv_t = (float)(1.0 / (double)temperature);
+      P.alpha = alpha;
+      P.tv = tv;
+      P.surv = prefix_survival;
+      P.exp_acc = expected_accepted;
+      P.part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.part);
+      P.row_cnt = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + ws.cnt);
+      P.status = dev_status;
+      return from_cuda(launch_pipe_dt<ssv::kPOverlap>(dtype, P, ps, st));
+    }
+  }
   Shape sh;
   {
     const spec_status_t r = greedy ? shape_for_dt<ssv::kOverlapGreedy>(dtype, units, V, 2, &sh)
@@ -545,12 +769,46 @@ spec_status_t spec_e2e_tv_fwd_bwd(const void* target_logits, const void* draft_l
   const long long units = (long long)B * K;
   if (units > 0x7FFFFFFFLL) return SPEC_ERR_UNSUPPORTED;
   const int es = elem_size(dtype);
+  char* w = static_cast<char*>(workspace);
+  const bool aligned = aligned16(target_logits) && aligned16(draft_logits) && ((long long)V * es) % 16 == 0;
+  cudaError_t e = cudaSuccess;
+  bool launched = false;
+  if (pipe_allowed(target_logits, draft_logits, V, es)) {
+    PShape ps;
+    const spec_status_t r = pipe_shape_dt<ssv::kPE2E>(dtype, units, V, 2, &ps);
+    if (r == SPEC_ERR_CUDA) return r;
+    if (r == SPEC_OK) {
+      ssv::PipeParams Q = {};
+      Q.target = target_logits;
+      Q.draft = draft_logits;
+      Q.B = B;
+      Q.K = K;
+      Q.KT = KT;
+      Q.V = V;
+      Q.units = (int)units;
+      pipe_geometry(&Q, ps);
+      Q.s = (float)(1.4426950408889634 / (double)temperature);
+      Q.inv_t = (float)(1.0 / (double)temperature);
+      Q.grad_scale = grad_scale;
+      Q.alpha = alpha_out;
+      Q.loss = loss_out;
+      Q.stats = reinterpret_cast<E2EStats*>(w + ws.stats);
+      Q.part = reinterpret_cast<float*>(w + ws.part);
+      Q.part2 = reinterpret_cast<float*>(w + ws.part2);
+      Q.row_loss = reinterpret_cast<float*>(w + ws.row_loss);
+      Q.row_cnt = reinterpret_cast<uint32_t*>(w + ws.cnt);
+      Q.glob_cnt = reinterpret_cast<uint32_t*>(w + ws.glob);
+      Q.status = dev_status;
+      e = launch_pipe_dt<ssv::kPE2E>(dtype, Q, ps, st);
+      if (e != cudaSuccess) return SPEC_ERR_CUDA;
+      launched = true;
+    }
+  }
   Shape sh;
-  {
+  if (!launched) {
     const spec_status_t r = shape_for_dt<ssv::kE2E>(dtype, units, V, 2, &sh);
     if (r != SPEC_OK) return r;
   }
-  char* w = static_cast<char*>(workspace);
   SweepParams P = {};
   P.target = target_logits;
   P.draft = draft_logits;
@@ -563,7 +821,7 @@ spec_status_t spec_e2e_tv_fwd_bwd(const void* target_logits, const void* draft_l
   P.L = sh.L;
   P.nst = sh.nst;
   P.rows = 2;
-  P.aligned = aligned16(target_logits) && aligned16(draft_logits) && ((long long)V * es) % 16 == 0;
+  P.aligned = aligned;
   P.s = (float)(1.4426950408889634 / (double)temperature);
   P.inv_t = (float)(1.0 / (double)temperature);
   P.grad_scale = grad_scale;
@@ -576,8 +834,10 @@ spec_status_t spec_e2e_tv_fwd_bwd(const void* target_logits, const void* draft_l
   P.row_cnt = reinterpret_cast<uint32_t*>(w + ws.cnt);
   P.glob_cnt = reinterpret_cast<uint32_t*>(w + ws.glob);
   P.status = dev_status;
-  cudaError_t e = launch_sweep_dt<ssv::kE2E>(dtype, P, sh, st);
-  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  if (!launched) {
+    e = launch_sweep_dt<ssv::kE2E>(dtype, P, sh, st);
+    if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  }
   ssv::GradParams G = {};
   G.target = target_logits;
   G.draft = draft_logits;

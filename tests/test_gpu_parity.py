@@ -478,6 +478,9 @@ def test_deterministic_and_workspace_left_zero(ssv):
 
 
 def test_unaligned_rows_match_aligned(ssv):
+    """Rows off 16-byte boundaries take the single-read sweep, aligned rows
+    the two-pass sweep: both match the oracle and each other within the
+    parity bar."""
     B, K, V = 3, 3, 4096
     w = synth.gaussian(B, K, V, sigma=2.0, noise=0.6, dtype=torch.bfloat16, temperature=1.0, seed=12)
     t, d, y, ua, uf = to_dev(w)
@@ -491,8 +494,12 @@ def test_unaligned_rows_match_aligned(ssv):
     d2.copy_(d)
     out = ssv.verify(t2, d2, y, ua, uf, 1.0)
     torch.cuda.synchronize()
-    assert torch.equal(out.tokens, ref.tokens) and torch.equal(out.n_accepted, ref.n_accepted)
-    np.testing.assert_allclose(out.alpha.cpu().numpy(), ref.alpha.cpu().numpy(), rtol=1e-6, atol=1e-7)
+    orc = oracle_verify(w)
+    assert_verify(out, orc)
+    assert_verify(ref, orc)
+    ok = ~orc.flagged
+    assert (out.tokens.cpu().numpy()[ok] == ref.tokens.cpu().numpy()[ok]).all()
+    np.testing.assert_allclose(out.alpha.cpu().numpy(), ref.alpha.cpu().numpy(), rtol=RTOL, atol=ATOL)
 
 
 def test_host_verifier_round_trip(ssv):
