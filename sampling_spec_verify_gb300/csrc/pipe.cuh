@@ -9,41 +9,44 @@
 //   * a producer warp, whose elected lane streams chunks into a ring of NS
 //     shared-memory stages with 1-D bulk (TMA) copies, each stage completing
 //     on its own mbarrier;
-//   * eight consumer warps, which share every chunk (warp w takes a
-//     contiguous sub-segment, lane l every 32nd vector of it);
-//   * a draw warp, which runs the inverse-CDF draws of rejected and bonus
-//     positions from L2-resident data, off the consumers' path.
+//   * sixteen consumer warps, which share every chunk (warp w takes a
+//     contiguous sub-segment, lane l every 32nd vector of it) and touch
+//     nothing but shared memory on their hot path;
+//   * a completion warp, which takes each finished unit from an in-order job
+//     ring in shared memory and does all of the unit's global-memory work:
+//     per-CTA partials, records, arrivals on the row counters, the row's
+//     completion, and the inverse-CDF draws of rejected and bonus positions.
 // A unit's chunks are loaded twice: once for pass A (softmax normalisers,
-// from HBM) and once more for pass C (overlap, residual weights; the copy
-// hits L2, because the second load comes a few chunks after the first).  The
-// ring interleaves the pass-A chunks of unit u+1 with the pass-C chunks of
-// unit u, so a stage is never held while the cluster exchanges unit u's
+// from HBM) and once more for pass C (overlap, residual weights; the second
+// copy hits L2, because it comes a few chunks after the first).  The ring
+// interleaves the pass-A chunks of unit u+1 with the pass-C chunks of unit
+// u, so a stage is never held while the cluster exchanges unit u's
 // normalisers: every consumer warp pushes its (max, sum) pairs with st.async
 // into every CTA's mailbox, completing on that CTA's mbarrier, and every warp
-// combines all S x 8 pairs itself in one fixed order, so every warp of the
-// cluster takes the same decision with no block or cluster barrier.
+// combines all the cluster's pairs itself in one fixed order, so every warp
+// of the cluster takes the same decision with no block or cluster barrier.
 //
 // Draws: each warp's per-chunk residual totals are summed per (CTA, chunk);
-// the CTA whose arrival completes a drawing unit hands it to its draw warp,
-// which locates the (CTA, chunk) holding u' * total, recomputes that
-// chunk's weights from global memory in the same order and with the same
-// arithmetic, and walks to the token.
+// the CTA whose completion warp brings a drawing unit's counter to S does the
+// draw: it locates the (CTA, chunk) holding u' * total, recomputes that
+// chunk's weights from global memory in the consumers' order and arithmetic,
+// and walks to the token.
 #pragma once
 
 #include "sweep.cuh"
 
 namespace ssv {
 
-constexpr int kPNC = 8;                     // consumer warps
+constexpr int kPNC = 16;                    // consumer warps
 constexpr int kPProd = kPNC;                // producer warp
-constexpr int kPDraw = kPNC + 1;            // draw warp
-constexpr int kPThreads = (kPNC + 2) * 32;  // 320
+constexpr int kPDone = kPNC + 1;            // completion warp
+constexpr int kPThreads = (kPNC + 2) * 32;  // 576
 constexpr int kPNX = 4;                     // exchange slots (units in flight)
 constexpr int kPMaxS = 16;
 constexpr int kPMaxNS = 8;
 constexpr int kPMaxCh = 32;     // chunks per slice
 constexpr int kPMaxParts = 64;  // S x chunks per slice: draw totals per unit
-constexpr int kPQ = 16;         // draw job ring
+constexpr int kPQ = 8;          // units between the consumers and the completion warp
 
 enum PMode : int { kPSample = 0, kPGreedy = 1, kPOverlap = 2, kPE2E = 3 };
 
@@ -85,6 +88,16 @@ struct PipeParams {
   uint32_t* glob_cnt;
   uint32_t* status;
 };
+
+// Dynamic shared memory of a launch: the ring, then the mailbox, then the
+// per-chunk draw totals of the units between the consumers and the
+// completion warp.
+__host__ __device__ constexpr size_t pipe_stage_bytes(int rows, int CV) { return (size_t)rows * CV * 16; }
+__host__ __device__ constexpr size_t pipe_mbox_bytes(int S) { return (size_t)kPNX * S * (kPNC + 1) * 16; }
+__host__ __device__ constexpr size_t pipe_wt_bytes(int NCH) { return (size_t)kPQ * NCH * kPNC * 4; }
+__host__ __device__ constexpr size_t pipe_dyn_bytes(int NS, int rows, int CV, int S, int NCH) {
+  return NS * pipe_stage_bytes(rows, CV) + pipe_mbox_bytes(S) + pipe_wt_bytes(NCH);
+}
 
 struct PUnit {
   int b, k, rec;
@@ -140,33 +153,27 @@ __device__ __forceinline__ PUnit pdecode(const PipeParams& P, int u) {
   return x;
 }
 
-struct DrawJob {
-  int rec;
-  int b;
-  int resid;  // 1: residual max(0, p - q); 0: target p
-  int pad;
-  long long trow, drow;
-  float c1t, c1d, ratio, ufin;
+// A unit's decision, handed from the consumers to the completion warp.
+struct UnitJob {
+  int mode_c;  // 0 overlap only, 1 residual draw, 2 target draw, 3 invalid logits
+  int acc;     // accepted (verify), or the greedy decision
+  int draw;    // this unit draws (it may still be unused)
+  int am_t, am_d;  // greedy: target / draft arg-maxima
+  float c1t, c1d, cd2, izt, ratio, ufin;
 };
 
 struct PipeSmem {
   uint64_t full[kPMaxNS];
   uint64_t empty[kPMaxNS];
   uint64_t xbar[kPNX];
-  alignas(16) float mbox[kPNX][kPMaxS][kPNC + 1][4];  // [slot][sender CTA][sender warp | aux][field]
-  float wa[kPNX][kPNC];           // warp overlap partials
-  float wg[kPNX][kPNC];           // warp E2E S-mass partials
-  float wt[kPNX][kPMaxCh][kPNC];  // warp draw totals per chunk
-  uint32_t cnt[kPNX];             // warps done with a unit
-  DrawJob q[kPQ];
-  uint32_t q_ticket[kPQ];  // ticket t + 1 once job t is in its slot
-  uint32_t q_res;          // jobs reserved
-  uint32_t q_head;         // jobs taken by the draw warp
-  uint32_t finished;       // consumer warps done
-  float dsum[kPMaxParts];  // draw warp: recomputed totals (empty residual)
+  float wa[kPQ][kPNC];  // warp overlap partials
+  float wg[kPQ][kPNC];  // warp E2E S-mass partials
+  uint32_t cnt[kPQ];    // warps done with a unit
+  UnitJob job[kPQ];
+  uint32_t ticket[kPQ];    // p + 1 once unit p's job is in slot p % kPQ
+  uint32_t done_head;      // units the completion warp has finished
+  float dsum[kPMaxParts];  // completion warp: draw totals of one unit
 };
-
-static_assert(offsetof(PipeSmem, mbox) % 16 == 0, "mailbox must be 16-byte aligned");
 
 __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d, uint32_t bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
@@ -192,6 +199,27 @@ __device__ __forceinline__ void st_volatile_u32(uint32_t* p, uint32_t v) {
   *reinterpret_cast<volatile uint32_t*>(p) = v;
 }
 
+// Waits (lane 0 polling, the warp following) until *ctr >= want; gives up
+// after the wait limit and reports it.
+__device__ __forceinline__ void wait_counter(const uint32_t* ctr, uint32_t want, int lane, uint32_t* status) {
+  int ok = 1;
+  if (lane == 0) {
+    if (ld_volatile_u32(ctr) < want) {
+      const uint64_t t0 = global_timer_ns();
+      while (ld_volatile_u32(ctr) < want) {
+        __nanosleep(32);
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          ok = 0;
+          break;
+        }
+      }
+    }
+    __threadfence_block();
+  }
+  ok = __shfl_sync(kFull, ok, 0);
+  if (!ok && lane == 0 && status) atomicOr(status, kTimeout);
+}
+
 // (m, z) stands for z * 2^fl(m s).  Merges (mi, zi) into (m, z) with the same
 // rescaling as the warp combine.
 __device__ __forceinline__ void mz_merge(float& m, float& z, float mi, float zi, float s) {
@@ -207,9 +235,10 @@ __device__ __forceinline__ void mz_merge(float& m, float& z, float mi, float zi,
   }
 }
 
-// (m, z) of one lane's vectors of a chunk: m the maximum of its first vector,
-// z the sum of 2^(x s - fl(m s)); a sum not below 2^100 (a value far above
-// the offset, an infinity or a NaN) is summed again with a running maximum.
+// (m, z) of one lane's vectors i0, i0+32, ... < i1 of a chunk: m the maximum
+// of its first vector, z the sum of 2^(x s - fl(m s)) (two vectors per step,
+// two accumulators); a sum not below 2^100 (a value far above the offset, an
+// infinity or a NaN) is summed again with a running maximum.
 template <class E>
 __device__ __forceinline__ void lane_chunk_mz(const uint4* base, int i0, int i1, float s, float& m, float& z) {
   constexpr int PV = E::PV;
@@ -217,22 +246,37 @@ __device__ __forceinline__ void lane_chunk_mz(const uint4* base, int i0, int i1,
   z = 0.0f;
   if (i0 >= i1) return;
   const f32x2 S2 = f2(s, s);
-  m = E::vmax(base[i0]);
+  const uint4 first = base[i0];
+  m = E::vmax(first);
   const float c = __fmul_rn(m, s);
   const f32x2 C2 = f2(-c, -c);
-  f32x2 acc = f2(0.0f, 0.0f);
-  for (int i = i0; i < i1; i += 32) {
+  f32x2 acc0 = f2(0.0f, 0.0f), acc1 = f2(0.0f, 0.0f);
+  {
     f32x2 ep[PV / 2];
-    exp_pairs<E>(base[i], S2, C2, ep);
-    acc = f2_add(acc, psum(ep));
+    exp_pairs<E>(first, S2, C2, ep);
+    acc0 = psum(ep);
   }
-  z = f2_hsum(acc);
+  int i = i0 + 32;
+  for (; i + 32 < i1; i += 64) {
+    const uint4 w0 = base[i], w1 = base[i + 32];
+    f32x2 e0[PV / 2], e1[PV / 2];
+    exp_pairs<E>(w0, S2, C2, e0);
+    exp_pairs<E>(w1, S2, C2, e1);
+    acc1 = f2_add(acc1, psum(e0));
+    acc0 = f2_add(acc0, psum(e1));
+  }
+  if (i < i1) {
+    f32x2 e0[PV / 2];
+    exp_pairs<E>(base[i], S2, C2, e0);
+    acc1 = f2_add(acc1, psum(e0));
+  }
+  z = f2_hsum(f2_add(acc0, acc1));
   if (!(z < 0x1p100f) || !(c > -INFINITY)) {
     m = -INFINITY;
     z = 0.0f;
     float cm = 0.0f;
-    for (int i = i0; i < i1; i += 32) {
-      const uint4 w = base[i];
+    for (int q = i0; q < i1; q += 32) {
+      const uint4 w = base[q];
       const float vm = E::vmax(w);
       if (vm > m) {
         const float cn = __fmul_rn(vm, s);
@@ -249,25 +293,60 @@ __device__ __forceinline__ void lane_chunk_mz(const uint4* base, int i0, int i1,
   }
 }
 
+// Overlap terms of one lane's vector pairs: sum of 2^min(x_t, x_d') (and,
+// for E2E-TV, of the terms with x_d' < x_t), two vectors per step.
+template <class E, bool kE2EM>
+__device__ __forceinline__ void lane_overlap(const uint4* st, const uint4* sd, int i0, int i1, f32x2 S2, f32x2 CT,
+                                             f32x2 CD, f32x2& a2, f32x2& g2) {
+  constexpr int PV = E::PV;
+  auto one = [&](const uint4& wt, const uint4& wd, f32x2& aa, f32x2& gg) {
+    f32x2 pt[PV / 2], pd[PV / 2], ep[PV / 2], gp[PV / 2];
+    E::pairs(wt, pt);
+    E::pairs(wd, pd);
+#pragma unroll
+    for (int h = 0; h < PV / 2; ++h) {
+      float t0, t1, d0, d1;
+      f2_split(f2_fma(pt[h], S2, CT), t0, t1);
+      f2_split(f2_fma(pd[h], S2, CD), d0, d1);
+      const float e0 = ex2(fminf(t0, d0)), e1 = ex2(fminf(t1, d1));
+      ep[h] = f2(e0, e1);
+      if constexpr (kE2EM) gp[h] = f2(d0 < t0 ? e0 : 0.0f, d1 < t1 ? e1 : 0.0f);
+    }
+    aa = f2_add(aa, psum(ep));
+    if constexpr (kE2EM) gg = f2_add(gg, psum(gp));
+  };
+  f32x2 b2 = f2(0.0f, 0.0f), h2 = f2(0.0f, 0.0f);
+  int i = i0;
+  for (; i + 32 < i1; i += 64) {
+    const uint4 t0 = st[i], d0 = sd[i], t1 = st[i + 32], d1 = sd[i + 32];
+    one(t0, d0, a2, g2);
+    one(t1, d1, b2, h2);
+  }
+  if (i < i1) one(st[i], sd[i], a2, g2);
+  a2 = f2_add(a2, b2);
+  if constexpr (kE2EM) g2 = f2_add(g2, h2);
+}
+
 // Total of the draw weights of one warp sub-segment [v0, v1) of a chunk
 // (vector indices into `tv` / `dv`), one vector per lane per step, steps
-// summed in order: the arithmetic pass C' and the draw warp both use.
-// With thr >= 0 it also walks to the first element whose running sum
-// exceeds thr (returned in *pick as a vector * PV + element offset from
-// v0's element, or the last positive weight if none does).
+// summed in order: the arithmetic of pass C' and of the draw.  With pick
+// non-null it also walks to the first element whose running sum exceeds thr
+// (returned as a vector * PV + element offset from v0's first element, or
+// the last positive weight if none does).
 template <class E, bool kResid>
 __device__ __forceinline__ float seg_weights(const uint4* tv, const uint4* dv, int v0, int v1, f32x2 S2, f32x2 CT,
-                                             f32x2 CD, f32x2 NR, int lane, float thr, int* pick) {
+                                             f32x2 CD, f32x2 NR, int lane, float thr, int* pick,
+                                             f32x2* min_mass = nullptr) {
   constexpr int PV = E::PV;
   float R = 0.0f;
   int found = -1, ilast = -1;
+  f32x2 mm = f2(0.0f, 0.0f);
   for (int base = v0; base < v1; base += 32) {
     const int i = base + lane;
     float w[PV];
     float ws = 0.0f;
     if (i < v1) {
-      f32x2 dummy = f2(0.0f, 0.0f);
-      ws = draw_weights<E, kResid>(tv[i], kResid ? dv[i] : tv[i], S2, CT, CD, NR, w, dummy);
+      ws = draw_weights<E, kResid>(tv[i], kResid ? dv[i] : tv[i], S2, CT, CD, NR, w, mm);
     } else {
 #pragma unroll
       for (int e = 0; e < PV; ++e) w[e] = 0.0f;
@@ -302,6 +381,7 @@ __device__ __forceinline__ float seg_weights(const uint4* tv, const uint4* dv, i
     }
     R = __shfl_sync(kFull, run, 31);
   }
+  if (min_mass) *min_mass = f2_add(*min_mass, mm);
   if (pick != nullptr) {
     if (found < 0 && ilast >= 0) {  // no crossing (rounding): the last positive weight
       int pk = -1;
@@ -480,21 +560,21 @@ __device__ __forceinline__ void parrive_row(const PipeParams& P, int b, int lane
   if (last) pcomplete_row<MODE>(P, b, lane);
 }
 
-// ---- the draw warp's work: one inverse-CDF draw of a unit ------------------------
+// ---- the draw of one unit (completion warp) ------------------------------------------
 
 template <class E, int MODE>
-__device__ void pdraw(const PipeParams& P, PipeSmem& sm, const DrawJob& J, int lane) {
+__device__ void pdraw(const PipeParams& P, PipeSmem& sm, const PUnit& x, const UnitJob& J, int lane) {
   constexpr int PV = E::PV;
   const int S = P.S, NCH = P.NCH, CV = P.CV, WV = P.WV;
   const int nvec_row = P.V / PV;
   const int nparts = S * NCH;
-  const uint4* tv = reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::Raw*>(P.target) + J.trow * P.V);
-  const uint4* dv = reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::Raw*>(P.draft) + J.drow * P.V);
+  const uint4* tv = reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::Raw*>(P.target) + x.trow * P.V);
+  const uint4* dv = reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::Raw*>(P.draft) + x.drow * P.V);
   const f32x2 S2 = f2(P.s, P.s);
   const f32x2 CT = f2(-J.c1t, -J.c1t);
   const f32x2 CD = f2(-J.c1d, -J.c1d);
   const f32x2 NR = f2(-J.ratio, -J.ratio);
-  float* dt = P.dtot + (long long)J.rec * kPMaxParts;
+  float* dt = P.dtot + (long long)x.rec * kPMaxParts;
   auto chunk_range = [&](int jj, int& c0, int& cv) {
     const int r = jj / NCH, c = jj - r * NCH;
     const int s0 = min(r * P.NV, nvec_row);
@@ -502,9 +582,9 @@ __device__ void pdraw(const PipeParams& P, PipeSmem& sm, const DrawJob& J, int l
     c0 = min(s0 + c * CV, s1);
     cv = min(c0 + CV, s1) - c0;
   };
-  bool resid = J.resid != 0;
+  bool resid = (J.mode_c == 1);
   bool emptied = false;
-  // per-(CTA, chunk) totals in prefix order, summed in order by lane 0
+  // per-(CTA, chunk) totals in prefix order, summed in order
   for (int i = lane; i < nparts; i += 32) sm.dsum[i] = __ldcg(dt + i);
   __syncwarp();
   float total = 0.0f;
@@ -522,9 +602,10 @@ __device__ void pdraw(const PipeParams& P, PipeSmem& sm, const DrawJob& J, int l
         const int a0 = min(w * WV, cv), a1 = min(a0 + WV, cv);
         t = __fadd_rn(t, seg_weights<E, false>(tv, dv, c0 + a0, c0 + a1, S2, CT, CD, NR, lane, -1.0f, nullptr));
       }
+      __syncwarp();
       if (lane == 0) sm.dsum[jj] = t;
+      __syncwarp();
     }
-    __syncwarp();
     total = 0.0f;
     for (int i = 0; i < nparts; ++i) total = __fadd_rn(total, sm.dsum[i]);
   }
@@ -583,13 +664,92 @@ __device__ void pdraw(const PipeParams& P, PipeSmem& sm, const DrawJob& J, int l
     }
   }
   if (lane == 0) {
-    P.rec[J.rec].token = token;
-    if (emptied) P.rec[J.rec].pad0 = 1u;
-    P.dcnt[J.rec] = 0u;
+    P.rec[x.rec].token = token;
+    if (emptied) P.rec[x.rec].pad0 = 1u;
+    P.dcnt[x.rec] = 0u;
   }
   for (int i = lane; i < nparts; i += 32) dt[i] = 0.0f;
   __syncwarp();
-  parrive_row<MODE>(P, J.b, lane);
+  parrive_row<MODE>(P, x.b, lane);
+}
+
+// The completion warp's work for unit p: the CTA's partials, the record, the
+// draw and the arrival.
+template <class E, int MODE>
+__device__ void pfinish_unit(const PipeParams& P, PipeSmem& sm, const float* wt, int p, int cl, uint32_t rank,
+                             int lane) {
+  const int slot = p % kPQ;
+  const UnitJob J = sm.job[slot];
+  const PUnit x = pdecode<MODE>(P, cl + p * P.G);
+  const float nanv = __int_as_float(0x7FC00000);
+  if constexpr (MODE == kPGreedy) {
+    if (rank == 0) {
+      if (lane == 0) {
+        VerifyRecord r;
+        r.acc = J.acc;
+        r.token = J.am_t;
+        r.pad0 = r.pad1 = 0u;
+        P.rec[x.rec] = r;
+        if (x.has_draft) P.part[(long long)x.rec * kPartStride] = (J.am_t >= 0 && J.am_t == J.am_d) ? 1.0f : 0.0f;
+      }
+      __syncwarp();
+      parrive_row<MODE>(P, x.b, lane);
+    }
+    return;
+  } else {
+    if (lane == 0) {
+      if (x.has_draft && (MODE != kPSample || P.alpha != nullptr)) {
+        float A = 0.0f;
+        for (int w = 0; w < kPNC; ++w) A = __fadd_rn(A, sm.wa[slot][w]);
+        P.part[(long long)x.rec * kPartStride + rank] = (J.mode_c == 3) ? nanv : __fmul_rn(A, J.izt);
+      }
+      if constexpr (MODE == kPE2E) {
+        float M2 = 0.0f;
+        for (int w = 0; w < kPNC; ++w) M2 = __fadd_rn(M2, sm.wg[slot][w]);
+        P.part2[(long long)x.rec * kPartStride + rank] = (J.mode_c == 3) ? nanv : __fmul_rn(M2, J.izt);
+        if (rank == 0) {
+          E2EStats e2;
+          e2.c1t = J.c1t;
+          e2.cd = J.cd2;
+          e2.izt = J.izt;
+          e2.smass = e2.alpha = e2.b1 = e2.b0 = e2.pad = 0.0f;
+          P.stats[x.rec] = e2;
+        }
+      }
+      if constexpr (MODE == kPSample) {
+        if (rank == 0) {
+          P.rec[x.rec].acc = x.bonus ? 1 : J.acc;
+          if (!J.draw) P.rec[x.rec].token = -1;
+        }
+      }
+    }
+    if constexpr (MODE == kPSample) {
+      if (J.draw) {
+        // per-chunk totals of this CTA, warps in order
+        const int NCH = P.NCH;
+        float* dt = P.dtot + (long long)x.rec * kPMaxParts + (long long)rank * NCH;
+        for (int c = lane; c < NCH; c += 32) {
+          float t = 0.0f;
+          for (int w = 0; w < kPNC; ++w) t = __fadd_rn(t, wt[(slot * NCH + c) * kPNC + w]);
+          dt[c] = t;
+        }
+        __syncwarp();
+        int drawer = 0;
+        if (lane == 0) {
+          __threadfence();
+          drawer = (atomicAdd(&P.dcnt[x.rec], 1u) == (uint32_t)(P.S - 1)) ? 1 : 0;
+          if (drawer) __threadfence();
+        }
+        drawer = __shfl_sync(kFull, drawer, 0);
+        if (drawer) {
+          pdraw<E, MODE>(P, sm, x, J, lane);  // writes the token, then arrives
+          return;
+        }
+      }
+    }
+    __syncwarp();
+    parrive_row<MODE>(P, x.b, lane);
+  }
 }
 
 // ---- the kernel ------------------------------------------------------------------
@@ -615,25 +775,25 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
   const int nvec_row = P.V / PV;
   const int sv0 = min((int)rank * P.NV, nvec_row);
   const int sv1 = min(sv0 + P.NV, nvec_row);
-  const size_t stage_bytes = (size_t)P.rows * (size_t)CV * 16u;
+  const size_t stage_bytes = pipe_stage_bytes(P.rows, CV);
   auto stage_t = [&](int st) { return reinterpret_cast<uint4*>(dyn_smem + st * stage_bytes); };
+  // mailbox [slot][sender CTA][sender warp | aux][4] and per-chunk draw totals [job slot][chunk][warp]
+  float* mbox = reinterpret_cast<float*>(dyn_smem + NS * stage_bytes);
+  float* wt = reinterpret_cast<float*>(dyn_smem + NS * stage_bytes + pipe_mbox_bytes(S));
+  auto mb_at = [&](int slot, int r, int w) { return mbox + ((slot * S + r) * (kPNC + 1) + w) * 4; };
   const uint32_t xbytes = (uint32_t)(S * (kPNC + 1) * 16);
-  const int per_row = (kSampleM || kGreedyM) ? P.K + 1 : P.K;
-  (void)per_row;
 
   if (tid == 0) {
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_addr(&sm.full[i]), 1);
       mbar_init(smem_addr(&sm.empty[i]), kPNC);
     }
-    for (int i = 0; i < kPNX; ++i) {
-      mbar_init(smem_addr(&sm.xbar[i]), 1);
+    for (int i = 0; i < kPNX; ++i) mbar_init(smem_addr(&sm.xbar[i]), 1);
+    for (int i = 0; i < kPQ; ++i) {
       sm.cnt[i] = 0;
+      sm.ticket[i] = 0;
     }
-    for (int i = 0; i < kPQ; ++i) sm.q_ticket[i] = 0;
-    sm.q_res = 0;
-    sm.q_head = 0;
-    sm.finished = 0;
+    sm.done_head = 0;
     fence_mbar_init();
     // arm the first exchange slots
     for (int i = 0; i < kPNX && i < nit; ++i) mbar_arrive_expect_tx(smem_addr(&sm.xbar[i]), xbytes);
@@ -682,43 +842,16 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
         mbar_wait_bounded(smem_addr(&sm.full[jj % NS]), (uint32_t)(jj / NS) & 1u, kWaitLimitNs);
     }
     __syncwarp();
-  } else if (warp == kPDraw) {
-    // ===================== draw warp =====================
-    if constexpr (kSampleM) {
-      uint32_t h = 0;
-      uint64_t t0 = global_timer_ns();
-      for (;;) {
-        // lane 0 polls; the warp follows its reading
-        int state = 0;  // 1: a job is ready, 2: no more jobs, 3: gave up
-        if (lane == 0) {
-          if (ld_volatile_u32(&sm.q_ticket[h % kPQ]) == h + 1u) {
-            state = 1;
-          } else if (ld_volatile_u32(&sm.finished) == (uint32_t)kPNC && ld_volatile_u32(&sm.q_res) == h) {
-            state = 2;
-          } else if (global_timer_ns() - t0 > kWaitLimitNs) {
-            state = 3;
-          }
-          __threadfence_block();
-        }
-        state = __shfl_sync(kFull, state, 0);
-        if (state == 0) {
-          __nanosleep(64);
-          continue;
-        }
-        if (state != 1) {
-          if (state == 3 && lane == 0 && P.status) atomicOr(P.status, kTimeout);
-          break;
-        }
-        const DrawJob J = sm.q[h % kPQ];
-        __syncwarp();
-        if (lane == 0) {
-          st_volatile_u32(&sm.q_ticket[h % kPQ], 0u);
-          __threadfence_block();
-          st_volatile_u32(&sm.q_head, h + 1u);
-        }
-        ++h;
-        pdraw<E, MODE>(P, sm, J, lane);
-        t0 = global_timer_ns();
+  } else if (warp == kPDone) {
+    // ===================== completion warp =====================
+    for (int p = 0; p < nit; ++p) {
+      const uint32_t slot = (uint32_t)(p % kPQ);
+      wait_counter(&sm.ticket[slot], (uint32_t)p + 1u, lane, P.status);
+      pfinish_unit<E, MODE>(P, sm, wt, p, cl, rank, lane);
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        st_volatile_u32(&sm.done_head, (uint32_t)p + 1u);
       }
     }
     __syncwarp();
@@ -729,7 +862,6 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
     int j = 0;  // ring position
 
     // pass-A state of the unit being read
-    PUnit ax = {};
     float amt = -INFINITY, azt = 0.0f, amd = -INFINITY, azd = 0.0f;  // sampling: (m, z) pairs
     float gbt = -INFINITY, gbd = -INFINITY;                          // greedy: best values
     int git = 0x7FFFFFFF, gid = 0x7FFFFFFF;                          // greedy: their indices
@@ -739,12 +871,10 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
     uint32_t a_rejw = 0;
     bool a_ok = true;
     // a unit whose pass A has ended, until the end of the phase
-    PUnit tx = {};
     int t_y = -1;
     float t_ua = 0.0f, t_uf = 0.0f, t_zty = 0.0f, t_zdy = 0.0f;
     bool t_okA = true;
     // the unit waiting for its exchange and pass C
-    PUnit cx = {};
     int c_y = -1;
     float c_ua = 0.0f, c_uf = 0.0f, c_zty = 0.0f, c_zdy = 0.0f;
     bool c_okA = true;
@@ -762,8 +892,8 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
       const int st = j % NS;
       const uint32_t par = (uint32_t)(j / NS) & 1u;
       ++j;
+      const PUnit ax = pdecode<MODE>(P, cl + p * G);
       if (c == 0) {
-        ax = pdecode<MODE>(P, cl + p * G);
         amt = -INFINITY;
         azt = 0.0f;
         amd = -INFINITY;
@@ -853,11 +983,10 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
           warp_argmax_redux(gbt, git);
           warp_argmax_redux(gbd, gid);
           const bool nn = __any_sync(kFull, gnan);
-          f0 = gbt;
+          f0 = nn ? __int_as_float(0x7FC00000) : gbt;  // a NaN anywhere poisons the unit
           f1 = __int_as_float(git);
-          f2_ = nn ? __int_as_float(0x7FC00000) : gbd;  // a NaN anywhere poisons the draft value
+          f2_ = nn ? __int_as_float(0x7FC00000) : gbd;
           f3 = __int_as_float(gid);
-          if (nn) f0 = __int_as_float(0x7FC00000);
         } else {
           warp_combine_mz2(amt, azt, amd, azd, s);
           f0 = amt;
@@ -868,16 +997,15 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
         const uint32_t rjw = __shfl_sync(kFull, a_rejw, 0);
         const float aok = __all_sync(kFull, a_ok) ? 0.0f : 1.0f;
         if (lane < S) {
-          const uint32_t a = map_rank(smem_addr(&sm.mbox[slot][rank][warp][0]), (uint32_t)lane);
+          const uint32_t a = map_rank(smem_addr(mb_at(slot, (int)rank, warp)), (uint32_t)lane);
           const uint32_t bar = map_rank(smem_addr(&sm.xbar[slot]), (uint32_t)lane);
           st_async_v4(a, f0, f1, f2_, f3, bar);
           if (warp == 0) {
-            const uint32_t ax_ = map_rank(smem_addr(&sm.mbox[slot][rank][kPNC][0]), (uint32_t)lane);
+            const uint32_t ax_ = map_rank(smem_addr(mb_at(slot, (int)rank, kPNC)), (uint32_t)lane);
             st_async_v4(ax_, __uint_as_float(rjw), aok, 0.0f, 0.0f, bar);
           }
         }
         // hand the unit over; pass C takes it at the end of this phase
-        tx = ax;
         t_okA = __all_sync(kFull, a_ok);
         t_y = __shfl_sync(kFull, a_y, 0);
         t_ua = __shfl_sync(kFull, a_ua, 0);
@@ -887,21 +1015,24 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
         if constexpr (kSampleM) {
           // gathered logits of the drafted token (read from L2 while pass C of
           // the previous unit runs)
-          if (lane == 0 && !tx.bonus && t_y >= 0 && t_y < P.V) {
-            t_zty = E::to_f32(__ldg(reinterpret_cast<const Raw*>(P.target) + tx.trow * P.V + t_y));
-            t_zdy = E::to_f32(__ldg(reinterpret_cast<const Raw*>(P.draft) + tx.drow * P.V + t_y));
+          if (lane == 0 && !ax.bonus && t_y >= 0 && t_y < P.V) {
+            t_zty = E::to_f32(__ldg(reinterpret_cast<const Raw*>(P.target) + ax.trow * P.V + t_y));
+            t_zdy = E::to_f32(__ldg(reinterpret_cast<const Raw*>(P.draft) + ax.drow * P.V + t_y));
           }
         }
       }
     };
 
     auto C_begin = [&](int p) {
+      const PUnit cx = pdecode<MODE>(P, cl + p * G);
       const int slot = p % kPNX;
       const uint32_t xpar = (uint32_t)(p / kPNX) & 1u;
       if (!mbar_wait_bounded(smem_addr(&sm.xbar[slot]), xpar, kWaitLimitNs)) {
         if (lane == 0 && P.status) atomicOr(P.status, kTimeout);
       }
       if (warp == 0 && lane == 0 && p + kPNX < nit) mbar_arrive_expect_tx(smem_addr(&sm.xbar[slot]), xbytes);
+      // the completion warp must be done with the unit whose job slot this one takes
+      if (p >= kPQ) wait_counter(&sm.done_head, (uint32_t)(p - kPQ + 1), lane, P.status);
       const int ne = S * (kPNC + 1);
       const bool tok_ok = cx.bonus || (c_y >= 0 && c_y < P.V);
       uint32_t flags = 0;
@@ -916,7 +1047,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
         for (int e = lane; e < ne; e += 32) {
           const int r = e / (kPNC + 1), w = e - r * (kPNC + 1);
           if (w == kPNC) continue;
-          const float* mm = sm.mbox[slot][r][w];
+          const float* mm = mb_at(slot, r, w);
           const float a = mm[0], d = mm[2];
           const int ia = __float_as_int(mm[1]), id = __float_as_int(mm[3]);
           nn |= (a != a) || (d != d);
@@ -944,7 +1075,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
         for (int e = lane; e < ne; e += 32) {
           const int r = e / (kPNC + 1), w = e - r * (kPNC + 1);
           if (w == kPNC) continue;
-          const float* mm = sm.mbox[slot][r][w];
+          const float* mm = mb_at(slot, r, w);
           mz_merge(mt, zt, mm[0], mm[1], s);
           mz_merge(md, zd, mm[2], mm[3], s);
         }
@@ -960,7 +1091,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
         mode_c = 0;
         acc = 1;
         if constexpr (kSampleM) {
-          const uint32_t seen = __float_as_uint(sm.mbox[slot][0][kPNC][0]);
+          const uint32_t seen = __float_as_uint(mb_at(slot, 0, kPNC)[0]);
           if (cx.b != lrow) {
             lrow = cx.b;
             lrej = false;
@@ -988,11 +1119,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
             if (rank == 0 && warp == 0 && lane == 0) atomicMax(&P.rej[cx.b], kRejBase - (uint32_t)cx.k);
             lrej = true;
           }
-          if (mode_c == 2) {
-            draw = !earlier;
-          } else if (mode_c == 1) {
-            draw = !earlier;
-          }
+          draw = (mode_c == 1 || mode_c == 2) && !earlier;
           need_a = cx.has_draft && P.alpha != nullptr && mode_c != 3;
         } else {
           if (!valid) {
@@ -1010,7 +1137,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
       const int st = j % NS;
       const uint32_t par = (uint32_t)(j / NS) & 1u;
       ++j;
-      const int slot = p % kPNX;
+      const int qs = p % kPQ;
       const bool ok = mbar_wait_bounded(smem_addr(&sm.full[st]), par, kWaitLimitNs);
       if (!ok && lane == 0 && P.status) atomicOr(P.status, kTimeout);
       const int v0 = min(sv0 + c * CV, sv1);
@@ -1019,178 +1146,77 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
       const uint4* stt = stage_t(st);
       const uint4* sdd = stt + CV;
       const f32x2 CT = f2(-c1t, -c1t);
+      float R = 0.0f;
       if (ok) {
         if (mode_c == 0 && need_a) {
           // overlap (and E2E S-mass) terms: one exp per element of min(log p, log q)
-          const f32x2 CD = f2(-cd2, -cd2);
-          for (int i = w0 + lane; i < w1; i += 32) {
-            f32x2 pt[PV / 2], pd[PV / 2], ep[PV / 2], gp[PV / 2];
-            E::pairs(stt[i], pt);
-            E::pairs(sdd[i], pd);
-#pragma unroll
-            for (int h = 0; h < PV / 2; ++h) {
-              float t0, t1, d0, d1;
-              f2_split(f2_fma(pt[h], S2, CT), t0, t1);
-              f2_split(f2_fma(pd[h], S2, CD), d0, d1);
-              const float e0 = ex2(fminf(t0, d0)), e1 = ex2(fminf(t1, d1));
-              ep[h] = f2(e0, e1);
-              if constexpr (MODE == kPE2E) gp[h] = f2(d0 < t0 ? e0 : 0.0f, d1 < t1 ? e1 : 0.0f);
-            }
-            a2 = f2_add(a2, psum(ep));
-            if constexpr (MODE == kPE2E) g2 = f2_add(g2, psum(gp));
-          }
+          lane_overlap<E, MODE == kPE2E>(stt, sdd, w0 + lane, w1, S2, CT, f2(-cd2, -cd2), a2, g2);
         } else if constexpr (kSampleM) {
           if (mode_c == 1 && (draw || need_a)) {
             // residual weights; the overlap from the same arithmetic
             const f32x2 CDd = f2(-c1d, -c1d);
             const f32x2 NR = f2(-ratio, -ratio);
             if (draw) {
-              float R = 0.0f;
-              for (int base = w0; base < w1; base += 32) {
-                const int i = base + lane;
-                float w[PV];
-                float ws = 0.0f;
-                if (i < w1) ws = draw_weights<E, true>(stt[i], sdd[i], S2, CT, CDd, NR, w, a2);
-                R = __fadd_rn(R, __shfl_sync(kFull, warp_incl_scan(ws, lane), 31));
-              }
-              if (lane == 0) sm.wt[slot][c][warp] = R;
+              R = seg_weights<E, true>(stt, sdd, w0, w1, S2, CT, CDd, NR, lane, -1.0f, nullptr, &a2);
             } else {
+              // the same per-chunk association as the drawing branch, so
+              // that alpha does not depend on whether the draw was skipped
+              f32x2 mm = f2(0.0f, 0.0f);
               for (int i = w0 + lane; i < w1; i += 32) {
                 float w[PV];
-                draw_weights<E, true>(stt[i], sdd[i], S2, CT, CDd, NR, w, a2);
+                draw_weights<E, true>(stt[i], sdd[i], S2, CT, CDd, NR, w, mm);
               }
+              a2 = f2_add(a2, mm);
             }
           } else if (mode_c == 2 && draw) {
-            float R = 0.0f;
             const f32x2 Z2 = f2(0.0f, 0.0f);
-            for (int base = w0; base < w1; base += 32) {
-              const int i = base + lane;
-              float w[PV];
-              float ws = 0.0f;
-              f32x2 dummy = Z2;
-              if (i < w1) ws = draw_weights<E, false>(stt[i], stt[i], S2, CT, CT, Z2, w, dummy);
-              R = __fadd_rn(R, __shfl_sync(kFull, warp_incl_scan(ws, lane), 31));
-            }
-            if (lane == 0) sm.wt[slot][c][warp] = R;
+            R = seg_weights<E, false>(stt, stt, w0, w1, S2, CT, CT, Z2, lane, -1.0f, nullptr);
           }
         }
-      } else if (draw && lane == 0) {
-        sm.wt[slot][c][warp] = 0.0f;
       }
+      if (draw && lane == 0) wt[(qs * NCH + c) * kPNC + warp] = R;
       __syncwarp();
       if (lane == 0) mbar_arrive_cta(smem_addr(&sm.empty[st]));
     };
 
     auto C_end = [&](int p) {
-      const int slot = p % kPNX;
+      const int qs = p % kPQ;
+      UnitJob J;
+      J.mode_c = mode_c;
+      J.acc = acc;
+      J.draw = draw ? 1 : 0;
+      J.am_t = am_t;
+      J.am_d = am_d;
+      J.c1t = c1t;
+      J.c1d = c1d;
+      J.cd2 = cd2;
+      J.izt = izt;
+      J.ratio = ratio;
+      J.ufin = c_uf;
       if constexpr (kGreedyM) {
-        if (rank == 0 && warp == 0) {
-          if (lane == 0) {
-            VerifyRecord r;
-            r.acc = acc;
-            r.token = am_t;
-            r.pad0 = r.pad1 = 0u;
-            P.rec[cx.rec] = r;
-            if (cx.has_draft)
-              P.part[(long long)cx.rec * kPartStride] = (am_t >= 0 && am_t == am_d) ? 1.0f : 0.0f;
-          }
-          __syncwarp();
-          parrive_row<MODE>(P, cx.b, lane);
+        // every warp decided alike: warp 0 hands the unit over
+        if (warp == 0 && lane == 0) {
+          sm.job[qs] = J;
+          __threadfence_block();
+          st_volatile_u32(&sm.ticket[qs], (uint32_t)p + 1u);
         }
-        return;
       } else {
         const float a = warp_sum(f2_hsum(a2));
         float g = 0.0f;
         if constexpr (MODE == kPE2E) g = warp_sum(f2_hsum(g2));
-        int last = 0;
         if (lane == 0) {
-          sm.wa[slot][warp] = a;
-          sm.wg[slot][warp] = g;
+          sm.wa[qs][warp] = a;
+          sm.wg[qs][warp] = g;
           __threadfence_block();
-          last = (atomicAdd(&sm.cnt[slot], 1u) == (uint32_t)(kPNC - 1)) ? 1 : 0;
-          if (last) {
+          if (atomicAdd(&sm.cnt[qs], 1u) == (uint32_t)(kPNC - 1)) {
+            // the last warp of the CTA hands the unit to the completion warp
             __threadfence_block();
-            sm.cnt[slot] = 0u;
+            sm.cnt[qs] = 0u;
+            sm.job[qs] = J;
+            __threadfence_block();
+            st_volatile_u32(&sm.ticket[qs], (uint32_t)p + 1u);
           }
         }
-        last = __shfl_sync(kFull, last, 0);
-        if (!last) return;
-        // this warp finishes the CTA's share of the unit
-        const float nanv = __int_as_float(0x7FC00000);
-        if (lane == 0) {
-          if (cx.has_draft && (!kSampleM || P.alpha != nullptr)) {
-            float A = 0.0f;
-            for (int w = 0; w < kPNC; ++w) A = __fadd_rn(A, sm.wa[slot][w]);
-            P.part[(long long)cx.rec * kPartStride + rank] = (mode_c == 3) ? nanv : __fmul_rn(A, izt);
-          }
-          if constexpr (MODE == kPE2E) {
-            float M2 = 0.0f;
-            for (int w = 0; w < kPNC; ++w) M2 = __fadd_rn(M2, sm.wg[slot][w]);
-            P.part2[(long long)cx.rec * kPartStride + rank] = (mode_c == 3) ? nanv : __fmul_rn(M2, izt);
-            if (rank == 0) {
-              E2EStats e2;
-              e2.c1t = c1t;
-              e2.cd = cd2;
-              e2.izt = izt;
-              e2.smass = e2.alpha = e2.b1 = e2.b0 = e2.pad = 0.0f;
-              P.stats[cx.rec] = e2;
-            }
-          }
-          if constexpr (kSampleM) {
-            if (rank == 0) {
-              P.rec[cx.rec].acc = cx.bonus ? 1 : acc;
-              if (!draw) P.rec[cx.rec].token = -1;
-            }
-          }
-        }
-        if constexpr (kSampleM) {
-          if (draw) {
-            // per-chunk totals of this CTA, warps in order
-            float* dt = P.dtot + (long long)cx.rec * kPMaxParts + (long long)rank * NCH;
-            for (int c = lane; c < NCH; c += 32) {
-              float t = 0.0f;
-              for (int w = 0; w < kPNC; ++w) t = __fadd_rn(t, sm.wt[slot][c][w]);
-              dt[c] = t;
-            }
-            __syncwarp();
-            int drawer = 0;
-            if (lane == 0) {
-              __threadfence();
-              drawer = (atomicAdd(&P.dcnt[cx.rec], 1u) == (uint32_t)(S - 1)) ? 1 : 0;
-              if (drawer) {
-                __threadfence();
-                // hand the draw to this CTA's draw warp
-                const uint32_t t = atomicAdd(&sm.q_res, 1u);
-                const uint64_t w0t = global_timer_ns();
-                while (t - ld_volatile_u32(&sm.q_head) >= (uint32_t)kPQ) {
-                  __nanosleep(64);
-                  if (global_timer_ns() - w0t > kWaitLimitNs) {
-                    if (P.status) atomicOr(P.status, kTimeout);
-                    break;
-                  }
-                }
-                DrawJob J;
-                J.rec = cx.rec;
-                J.b = cx.b;
-                J.resid = (mode_c == 1) ? 1 : 0;
-                J.pad = 0;
-                J.trow = cx.trow;
-                J.drow = cx.drow;
-                J.c1t = c1t;
-                J.c1d = c1d;
-                J.ratio = ratio;
-                J.ufin = c_uf;
-                sm.q[t % kPQ] = J;
-                __threadfence_block();
-                st_volatile_u32(&sm.q_ticket[t % kPQ], t + 1u);
-              }
-            }
-            drawer = __shfl_sync(kFull, drawer, 0);
-            if (drawer) return;  // the draw warp arrives for this CTA once the token is written
-          }
-        }
-        __syncwarp();
-        parrive_row<MODE>(P, cx.b, lane);
       }
     };
 
@@ -1209,7 +1235,6 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
         C_end(p - 1);
       }
       // unit p goes on to pass C in the next phase
-      cx = tx;
       c_y = t_y;
       c_ua = t_ua;
       c_uf = t_uf;
@@ -1218,10 +1243,6 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
       c_okA = t_okA;
     }
     __syncwarp();
-    if (lane == 0) {
-      __threadfence_block();
-      atomicAdd(&sm.finished, 1u);
-    }
   }
   __syncthreads();
   cluster_sync();  // no CTA leaves while a peer may still read or write its shared memory

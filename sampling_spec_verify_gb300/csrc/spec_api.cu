@@ -294,11 +294,13 @@ bool pick_pipe_shape(Fn fn, int es, long long units, int V, int rows, PShape* ou
     if (CV < 1) CV = 1;
     if (NCH > ssv::kPMaxCh || S * NCH > ssv::kPMaxParts) continue;
     const long long stage = (long long)rows * CV * 16;
-    long long NS = smem_avail / stage;
+    const long long fixed = (long long)(ssv::pipe_mbox_bytes(S) + ssv::pipe_wt_bytes((int)NCH));
+    long long NS = (smem_avail - fixed) / stage;
     if (NS > ssv::kPMaxNS) NS = ssv::kPMaxNS;
     if (ovs > 0 && NS > ovs) NS = ovs;
     if (NS < 1 || (ovs == 0 && NS < 3)) continue;
-    const int G = max_active_clusters(fn, S, (int)(NS * stage), ssv::kPThreads);
+    const int G = max_active_clusters(fn, S, (int)ssv::pipe_dyn_bytes((int)NS, rows, (int)CV, S, (int)NCH),
+                                      ssv::kPThreads);
     if (G <= 0) continue;
     const long long Ge = units < G ? units : G;
     const double waves = (double)((units + Ge - 1) / Ge);
@@ -317,7 +319,7 @@ bool pick_pipe_shape(Fn fn, int es, long long units, int V, int rows, PShape* ou
       out->WV = (int)((CV + ssv::kPNC - 1) / ssv::kPNC);
       out->NS = (int)NS;
       out->rows = rows;
-      out->smem = (int)(NS * stage);
+      out->smem = (int)ssv::pipe_dyn_bytes((int)NS, rows, (int)CV, S, (int)NCH);
     }
   }
   return best >= 0;
