@@ -293,6 +293,46 @@ __device__ __forceinline__ void lane_chunk_mz(const uint4* base, int i0, int i1,
   }
 }
 
+// Adds one lane's vectors i0, i0+32, ... < i1 of a chunk to its running pair
+// (m, z) of the unit: the offset fl(m s) is fixed by the lane's first vector
+// of the unit, and later chunks add 2^(x s - fl(m s)) to z (two vectors per
+// step, two accumulators).  A chunk whose sum is not below 2^100 (a value far
+// above the offset, an infinity or a NaN), or a lane with no offset yet,
+// takes lane_chunk_mz's careful path and is merged with rescaling.
+template <class E>
+__device__ __forceinline__ void lane_chunk_add(const uint4* base, int i0, int i1, float s, float& m, float& z) {
+  constexpr int PV = E::PV;
+  if (i0 >= i1) return;
+  if (m > -INFINITY) {
+    const f32x2 S2 = f2(s, s);
+    const float c = __fmul_rn(m, s);
+    const f32x2 C2 = f2(-c, -c);
+    f32x2 acc0 = f2(0.0f, 0.0f), acc1 = f2(0.0f, 0.0f);
+    int i = i0;
+    for (; i + 32 < i1; i += 64) {
+      const uint4 w0 = base[i], w1 = base[i + 32];
+      f32x2 e0[PV / 2], e1[PV / 2];
+      exp_pairs<E>(w0, S2, C2, e0);
+      exp_pairs<E>(w1, S2, C2, e1);
+      acc0 = f2_add(acc0, psum(e0));
+      acc1 = f2_add(acc1, psum(e1));
+    }
+    if (i < i1) {
+      f32x2 e0[PV / 2];
+      exp_pairs<E>(base[i], S2, C2, e0);
+      acc0 = f2_add(acc0, psum(e0));
+    }
+    const float zc = f2_hsum(f2_add(acc0, acc1));
+    if (zc < 0x1p100f) {  // false for NaN and infinities
+      z = __fadd_rn(z, zc);
+      return;
+    }
+  }
+  float mc, zc;
+  lane_chunk_mz<E>(base, i0, i1, s, mc, zc);
+  mz_merge(m, z, mc, zc, s);
+}
+
 // Overlap terms of one lane's vector pairs: sum of 2^min(x_t, x_d') (and,
 // for E2E-TV, of the terms with x_d' < x_t), two vectors per step.
 template <class E, bool kE2EM>
@@ -806,19 +846,19 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
     if (lane == 0) {
       const uint64_t polA = kHasC ? l2_evict_normal_policy() : l2_evict_first_policy();
       const uint64_t polC = l2_evict_first_policy();
-      int j = 0;
-      auto issue = [&](int it, int c, bool second) {
-        const int st = j % NS;
+      int j = 0;             // items issued
+      int st = 0;            // ring stage of item j
+      uint32_t epar = 0u;    // phase parity of empty[st] to wait for (from item NS on)
+      auto issue = [&](const PUnit& x, int c, bool second) {
         if (j >= NS) {
-          if (!mbar_wait_bounded(smem_addr(&sm.empty[st]), (uint32_t)((j / NS) - 1) & 1u, kWaitLimitNs) && P.status)
+          if (!mbar_wait_bounded(smem_addr(&sm.empty[st]), epar, kWaitLimitNs) && P.status)
             atomicOr(P.status, kTimeout);
         }
-        const PUnit x = pdecode<MODE>(P, cl + it * G);
         const int v0 = min(sv0 + c * CV, sv1);
         const int v1 = min(v0 + CV, sv1);
         const uint32_t nb = (uint32_t)(v1 - v0) * 16u;
         const uint32_t bar = smem_addr(&sm.full[st]);
-        fence_proxy_async_smem();
+        fence_proxy_async_smem();  // the consumers' reads of this stage come first
         mbar_arrive_expect_tx(bar, x.has_draft ? 2u * nb : nb);
         if (nb) {
           uint4* dst = stage_t(st);
@@ -830,11 +870,18 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
           }
         }
         ++j;
+        if (++st == NS) {
+          st = 0;
+          if (j > NS) epar ^= 1u;
+        }
       };
+      PUnit xa = {}, xc = {};
       for (int p = 0; p <= nit; ++p) {
+        xc = xa;
+        if (p < nit) xa = pdecode<MODE>(P, cl + p * G);
         for (int c = 0; c < NCH; ++c) {
-          if (p < nit) issue(p, c, false);
-          if (kHasC && p >= 1) issue(p - 1, c, true);
+          if (p < nit) issue(xa, c, false);
+          if (kHasC && p >= 1) issue(xc, c, true);
         }
       }
       // no copy may still be in flight when the CTA exits
@@ -859,9 +906,17 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
     // ===================== consumer warps =====================
     const f32x2 S2 = f2(P.s, P.s);
     const float s = P.s;
-    int j = 0;  // ring position
+    int st = 0;           // ring stage of the next item
+    uint32_t fpar = 0u;   // phase parity of full[st]
+    auto advance = [&]() {
+      if (++st == NS) {
+        st = 0;
+        fpar ^= 1u;
+      }
+    };
 
     // pass-A state of the unit being read
+    PUnit ax = {};
     float amt = -INFINITY, azt = 0.0f, amd = -INFINITY, azd = 0.0f;  // sampling: (m, z) pairs
     float gbt = -INFINITY, gbd = -INFINITY;                          // greedy: best values
     int git = 0x7FFFFFFF, gid = 0x7FFFFFFF;                          // greedy: their indices
@@ -875,6 +930,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
     float t_ua = 0.0f, t_uf = 0.0f, t_zty = 0.0f, t_zdy = 0.0f;
     bool t_okA = true;
     // the unit waiting for its exchange and pass C
+    PUnit cx = {};
     int c_y = -1;
     float c_ua = 0.0f, c_uf = 0.0f, c_zty = 0.0f, c_zdy = 0.0f;
     bool c_okA = true;
@@ -889,11 +945,8 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
     bool lrej = false;
 
     auto A_item = [&](int p, int c) {
-      const int st = j % NS;
-      const uint32_t par = (uint32_t)(j / NS) & 1u;
-      ++j;
-      const PUnit ax = pdecode<MODE>(P, cl + p * G);
       if (c == 0) {
+        ax = pdecode<MODE>(P, cl + p * G);
         amt = -INFINITY;
         azt = 0.0f;
         amd = -INFINITY;
@@ -912,7 +965,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
           }
         }
       }
-      const bool ok = mbar_wait_bounded(smem_addr(&sm.full[st]), par, kWaitLimitNs);
+      const bool ok = mbar_wait_bounded(smem_addr(&sm.full[st]), fpar, kWaitLimitNs);
       if (!ok) {
         a_ok = false;
         if (lane == 0 && P.status) atomicOr(P.status, kTimeout);
@@ -964,17 +1017,13 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
             gid = (v0 + jd) * PV + e;
           }
         } else {
-          float m, z;
-          lane_chunk_mz<E>(stt, w0 + lane, w1, s, m, z);
-          mz_merge(amt, azt, m, z, s);
-          if (ax.has_draft) {
-            lane_chunk_mz<E>(sdd, w0 + lane, w1, s, m, z);
-            mz_merge(amd, azd, m, z, s);
-          }
+          lane_chunk_add<E>(stt, w0 + lane, w1, s, amt, azt);
+          if (ax.has_draft) lane_chunk_add<E>(sdd, w0 + lane, w1, s, amd, azd);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive_cta(smem_addr(&sm.empty[st]));
+      advance();
       if (c == NCH - 1) {
         // this warp's share of the unit: to every CTA of the cluster
         const int slot = p % kPNX;
@@ -1024,7 +1073,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
     };
 
     auto C_begin = [&](int p) {
-      const PUnit cx = pdecode<MODE>(P, cl + p * G);
+      cx = pdecode<MODE>(P, cl + p * G);
       const int slot = p % kPNX;
       const uint32_t xpar = (uint32_t)(p / kPNX) & 1u;
       if (!mbar_wait_bounded(smem_addr(&sm.xbar[slot]), xpar, kWaitLimitNs)) {
@@ -1134,11 +1183,8 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
     };
 
     auto C_item = [&](int p, int c) {
-      const int st = j % NS;
-      const uint32_t par = (uint32_t)(j / NS) & 1u;
-      ++j;
       const int qs = p % kPQ;
-      const bool ok = mbar_wait_bounded(smem_addr(&sm.full[st]), par, kWaitLimitNs);
+      const bool ok = mbar_wait_bounded(smem_addr(&sm.full[st]), fpar, kWaitLimitNs);
       if (!ok && lane == 0 && P.status) atomicOr(P.status, kTimeout);
       const int v0 = min(sv0 + c * CV, sv1);
       const int cv = min(v0 + CV, sv1) - v0;
@@ -1177,6 +1223,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
       if (draw && lane == 0) wt[(qs * NCH + c) * kPNC + warp] = R;
       __syncwarp();
       if (lane == 0) mbar_arrive_cta(smem_addr(&sm.empty[st]));
+      advance();
     };
 
     auto C_end = [&](int p) {
