@@ -235,114 +235,80 @@ __device__ __forceinline__ void mz_merge(float& m, float& z, float mi, float zi,
   }
 }
 
-// (m, z) of one lane's vectors i0, i0+32, ... < i1 of a chunk: m the maximum
-// of its first vector, z the sum of 2^(x s - fl(m s)) (two vectors per step,
-// two accumulators); a sum not below 2^100 (a value far above the offset, an
-// infinity or a NaN) is summed again with a running maximum.
-template <class E>
-__device__ __forceinline__ void lane_chunk_mz(const uint4* base, int i0, int i1, float s, float& m, float& z) {
-  constexpr int PV = E::PV;
-  m = -INFINITY;
-  z = 0.0f;
-  if (i0 >= i1) return;
-  const f32x2 S2 = f2(s, s);
-  const uint4 first = base[i0];
-  m = E::vmax(first);
-  const float c = __fmul_rn(m, s);
-  const f32x2 C2 = f2(-c, -c);
-  f32x2 acc0 = f2(0.0f, 0.0f), acc1 = f2(0.0f, 0.0f);
-  {
-    f32x2 ep[PV / 2];
-    exp_pairs<E>(first, S2, C2, ep);
-    acc0 = psum(ep);
+// A lane's VPL vectors idx0, idx0+32, ... of a chunk of cv vectors, loaded
+// at once; vectors past the chunk read as -inf (they add nothing).
+template <class E, int VPL>
+__device__ __forceinline__ bool load_lane(const uint4* base, int idx0, int cv, uint4 (&w)[VPL]) {
+  const uint32_t ninf = (E::ES == 2) ? 0xFF80FF80u : 0xFF800000u;
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    const int i = idx0 + 32 * v;
+    w[v] = (i < cv) ? base[i] : make_uint4(ninf, ninf, ninf, ninf);
   }
-  int i = i0 + 32;
-  for (; i + 32 < i1; i += 64) {
-    const uint4 w0 = base[i], w1 = base[i + 32];
-    f32x2 e0[PV / 2], e1[PV / 2];
-    exp_pairs<E>(w0, S2, C2, e0);
-    exp_pairs<E>(w1, S2, C2, e1);
-    acc1 = f2_add(acc1, psum(e0));
-    acc0 = f2_add(acc0, psum(e1));
-  }
-  if (i < i1) {
-    f32x2 e0[PV / 2];
-    exp_pairs<E>(base[i], S2, C2, e0);
-    acc1 = f2_add(acc1, psum(e0));
-  }
-  z = f2_hsum(f2_add(acc0, acc1));
-  if (!(z < 0x1p100f) || !(c > -INFINITY)) {
-    m = -INFINITY;
-    z = 0.0f;
-    float cm = 0.0f;
-    for (int q = i0; q < i1; q += 32) {
-      const uint4 w = base[q];
-      const float vm = E::vmax(w);
-      if (vm > m) {
-        const float cn = __fmul_rn(vm, s);
-        z = (m > -INFINITY) ? __fmul_rn(z, ex2(__fadd_rn(cm, -cn))) : 0.0f;
-        cm = cn;
-        m = vm;
-      }
-      if (m > -INFINITY) {
-        f32x2 ep[PV / 2];
-        exp_pairs<E>(w, S2, f2(-cm, -cm), ep);
-        z = __fadd_rn(z, f2_hsum(psum(ep)));
-      }
-    }
-  }
+  return idx0 < cv;
 }
 
-// Adds one lane's vectors i0, i0+32, ... < i1 of a chunk to its running pair
-// (m, z) of the unit: the offset fl(m s) is fixed by the lane's first vector
-// of the unit, and later chunks add 2^(x s - fl(m s)) to z (two vectors per
-// step, two accumulators).  A chunk whose sum is not below 2^100 (a value far
-// above the offset, an infinity or a NaN), or a lane with no offset yet,
-// takes lane_chunk_mz's careful path and is merged with rescaling.
-template <class E>
-__device__ __forceinline__ void lane_chunk_add(const uint4* base, int i0, int i1, float s, float& m, float& z) {
+// Adds a lane's vectors of one chunk to its running pair (m, z) of the unit:
+// the offset fl(m s) is fixed by the lane's first vector of the unit and
+// later chunks add 2^(x s - fl(m s)) to z.  A chunk whose sum is not below
+// 2^100 (a value far above the offset, an infinity or a NaN) is summed again
+// with a running maximum and merged with rescaling.
+template <class E, int VPL>
+__device__ __forceinline__ void lane_item_add(const uint4 (&w)[VPL], float s, float& m, float& z) {
   constexpr int PV = E::PV;
-  if (i0 >= i1) return;
-  if (m > -INFINITY) {
-    const f32x2 S2 = f2(s, s);
-    const float c = __fmul_rn(m, s);
+  const f32x2 S2 = f2(s, s);
+  float m0 = m, z0 = z;
+  if (!(m0 > -INFINITY)) {
+    m0 = E::vmax(w[0]);
+    z0 = 0.0f;
+  }
+  if (m0 > -INFINITY) {
+    const float c = __fmul_rn(m0, s);
     const f32x2 C2 = f2(-c, -c);
-    f32x2 acc0 = f2(0.0f, 0.0f), acc1 = f2(0.0f, 0.0f);
-    int i = i0;
-    for (; i + 32 < i1; i += 64) {
-      const uint4 w0 = base[i], w1 = base[i + 32];
-      f32x2 e0[PV / 2], e1[PV / 2];
-      exp_pairs<E>(w0, S2, C2, e0);
-      exp_pairs<E>(w1, S2, C2, e1);
-      acc0 = f2_add(acc0, psum(e0));
-      acc1 = f2_add(acc1, psum(e1));
+    f32x2 acc = f2(0.0f, 0.0f);
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+      f32x2 e[PV / 2];
+      exp_pairs<E>(w[v], S2, C2, e);
+      acc = f2_add(acc, psum(e));
     }
-    if (i < i1) {
-      f32x2 e0[PV / 2];
-      exp_pairs<E>(base[i], S2, C2, e0);
-      acc0 = f2_add(acc0, psum(e0));
-    }
-    const float zc = f2_hsum(f2_add(acc0, acc1));
+    const float zc = f2_hsum(acc);
     if (zc < 0x1p100f) {  // false for NaN and infinities
-      z = __fadd_rn(z, zc);
+      m = m0;
+      z = __fadd_rn(z0, zc);
       return;
     }
   }
-  float mc, zc;
-  lane_chunk_mz<E>(base, i0, i1, s, mc, zc);
+  float mc = -INFINITY, zc = 0.0f, cm = 0.0f;
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    const float vm = E::vmax(w[v]);
+    if (vm > mc) {
+      const float cn = __fmul_rn(vm, s);
+      zc = (mc > -INFINITY) ? __fmul_rn(zc, ex2(__fadd_rn(cm, -cn))) : 0.0f;
+      cm = cn;
+      mc = vm;
+    }
+    if (mc > -INFINITY) {
+      f32x2 ep[PV / 2];
+      exp_pairs<E>(w[v], S2, f2(-cm, -cm), ep);
+      zc = __fadd_rn(zc, f2_hsum(psum(ep)));
+    }
+  }
   mz_merge(m, z, mc, zc, s);
 }
 
-// Overlap terms of one lane's vector pairs: sum of 2^min(x_t, x_d') (and,
-// for E2E-TV, of the terms with x_d' < x_t), two vectors per step.
-template <class E, bool kE2EM>
-__device__ __forceinline__ void lane_overlap(const uint4* st, const uint4* sd, int i0, int i1, f32x2 S2, f32x2 CT,
-                                             f32x2 CD, f32x2& a2, f32x2& g2) {
+// Overlap terms of a lane's vector pairs of one chunk: the sum of
+// 2^min(x_t, x_d') (and, for E2E-TV, of the terms with x_d' < x_t).
+template <class E, int VPL, bool kE2EM>
+__device__ __forceinline__ void lane_item_overlap(const uint4 (&wt)[VPL], const uint4 (&wd)[VPL], f32x2 S2, f32x2 CT,
+                                                  f32x2 CD, f32x2& a2, f32x2& g2) {
   constexpr int PV = E::PV;
-  auto one = [&](const uint4& wt, const uint4& wd, f32x2& aa, f32x2& gg) {
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
     f32x2 pt[PV / 2], pd[PV / 2], ep[PV / 2], gp[PV / 2];
-    E::pairs(wt, pt);
-    E::pairs(wd, pd);
+    E::pairs(wt[v], pt);
+    E::pairs(wd[v], pd);
 #pragma unroll
     for (int h = 0; h < PV / 2; ++h) {
       float t0, t1, d0, d1;
@@ -352,19 +318,9 @@ __device__ __forceinline__ void lane_overlap(const uint4* st, const uint4* sd, i
       ep[h] = f2(e0, e1);
       if constexpr (kE2EM) gp[h] = f2(d0 < t0 ? e0 : 0.0f, d1 < t1 ? e1 : 0.0f);
     }
-    aa = f2_add(aa, psum(ep));
-    if constexpr (kE2EM) gg = f2_add(gg, psum(gp));
-  };
-  f32x2 b2 = f2(0.0f, 0.0f), h2 = f2(0.0f, 0.0f);
-  int i = i0;
-  for (; i + 32 < i1; i += 64) {
-    const uint4 t0 = st[i], d0 = sd[i], t1 = st[i + 32], d1 = sd[i + 32];
-    one(t0, d0, a2, g2);
-    one(t1, d1, b2, h2);
+    a2 = f2_add(a2, psum(ep));
+    if constexpr (kE2EM) g2 = f2_add(g2, psum(gp));
   }
-  if (i < i1) one(st[i], sd[i], a2, g2);
-  a2 = f2_add(a2, b2);
-  if constexpr (kE2EM) g2 = f2_add(g2, h2);
 }
 
 // Total of the draw weights of one warp sub-segment [v0, v1) of a chunk
@@ -794,7 +750,7 @@ __device__ void pfinish_unit(const PipeParams& P, PipeSmem& sm, const float* wt,
 
 // ---- the kernel ------------------------------------------------------------------
 
-template <class E, int MODE>
+template <class E, int MODE, int VPL>
 __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) {
   extern __shared__ __align__(128) uint8_t dyn_smem[];
   __shared__ __align__(16) PipeSmem sm;
@@ -811,7 +767,9 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
   const int cl = blockIdx.x / S;
   const int G = P.G;
   const int nit = (P.units > cl) ? (P.units - cl + G - 1) / G : 0;
-  const int NS = P.NS, NCH = P.NCH, CV = P.CV, WV = P.WV;
+  constexpr int WV = 32 * VPL;    // vectors per consumer warp per chunk
+  constexpr int CV = kPNC * WV;   // vectors per chunk (per row)
+  const int NS = P.NS, NCH = P.NCH;
   const int nvec_row = P.V / PV;
   const int sv0 = min((int)rank * P.NV, nvec_row);
   const int sv1 = min(sv0 + P.NV, nvec_row);
@@ -972,53 +930,72 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
       }
       const int v0 = min(sv0 + c * CV, sv1);
       const int cv = min(v0 + CV, sv1) - v0;
-      const int w0 = min(warp * WV, cv), w1 = min(w0 + WV, cv);
+      const int idx0 = warp * WV + lane;
       const uint4* stt = stage_t(st);
       const uint4* sdd = stt + CV;
       if (ok) {
         if constexpr (kGreedyM) {
           // packed maxima per vector; the winning vector is unpacked below
-          float bt = -INFINITY, bd = -INFINITY;
-          int jt = -1, jd = -1;
-          for (int i = w0 + lane; i < w1; i += 32) {
+          uint4 w[VPL];
+          load_lane<E, VPL>(stt, idx0, cv, w);
+          float bt = -INFINITY;
+          uint4 wb = w[0];
+          int jt = -1;
+#pragma unroll
+          for (int v = 0; v < VPL; ++v) {
             bool nn;
-            float vm = E::vmax_nan(stt[i], nn);
+            const float vm = E::vmax_nan(w[v], nn);
             gnan |= nn;
             if (vm > bt) {
               bt = vm;
-              jt = i;
-            }
-            if (ax.has_draft) {
-              vm = E::vmax_nan(sdd[i], nn);
-              gnan |= nn;
-              if (vm > bd) {
-                bd = vm;
-                jd = i;
-              }
+              jt = idx0 + 32 * v;
+              wb = w[v];
             }
           }
           // earlier chunks hold smaller indices: a later chunk wins only if larger
           if (jt >= 0 && bt > gbt) {
             float xv[PV];
-            E::unpack(stt[jt], xv);
+            E::unpack(wb, xv);
             int e = PV - 1;
             for (int q = PV - 1; q >= 0; --q)
               if (xv[q] == bt) e = q;
             gbt = bt;
             git = (v0 + jt) * PV + e;
           }
-          if (jd >= 0 && bd > gbd) {
-            float xv[PV];
-            E::unpack(sdd[jd], xv);
-            int e = PV - 1;
-            for (int q = PV - 1; q >= 0; --q)
-              if (xv[q] == bd) e = q;
-            gbd = bd;
-            gid = (v0 + jd) * PV + e;
+          if (ax.has_draft) {
+            load_lane<E, VPL>(sdd, idx0, cv, w);
+            float bd = -INFINITY;
+            int jd = -1;
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+              bool nn;
+              const float vm = E::vmax_nan(w[v], nn);
+              gnan |= nn;
+              if (vm > bd) {
+                bd = vm;
+                jd = idx0 + 32 * v;
+                wb = w[v];
+              }
+            }
+            if (jd >= 0 && bd > gbd) {
+              float xv[PV];
+              E::unpack(wb, xv);
+              int e = PV - 1;
+              for (int q = PV - 1; q >= 0; --q)
+                if (xv[q] == bd) e = q;
+              gbd = bd;
+              gid = (v0 + jd) * PV + e;
+            }
           }
         } else {
-          lane_chunk_add<E>(stt, w0 + lane, w1, s, amt, azt);
-          if (ax.has_draft) lane_chunk_add<E>(sdd, w0 + lane, w1, s, amd, azd);
+          uint4 w[VPL];
+          if (load_lane<E, VPL>(stt, idx0, cv, w)) {
+            lane_item_add<E, VPL>(w, s, amt, azt);
+            if (ax.has_draft) {
+              load_lane<E, VPL>(sdd, idx0, cv, w);
+              lane_item_add<E, VPL>(w, s, amd, azd);
+            }
+          }
         }
       }
       __syncwarp();
@@ -1196,7 +1173,11 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
       if (ok) {
         if (mode_c == 0 && need_a) {
           // overlap (and E2E S-mass) terms: one exp per element of min(log p, log q)
-          lane_overlap<E, MODE == kPE2E>(stt, sdd, w0 + lane, w1, S2, CT, f2(-cd2, -cd2), a2, g2);
+          uint4 wt_[VPL], wd_[VPL];
+          if (load_lane<E, VPL>(stt, w0 + lane, w1, wt_)) {
+            load_lane<E, VPL>(sdd, w0 + lane, w1, wd_);
+            lane_item_overlap<E, VPL, MODE == kPE2E>(wt_, wd_, S2, CT, f2(-cd2, -cd2), a2, g2);
+          }
         } else if constexpr (kSampleM) {
           if (mode_c == 1 && (draw || need_a)) {
             // residual weights; the overlap from the same arithmetic

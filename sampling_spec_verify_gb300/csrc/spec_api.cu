@@ -248,7 +248,6 @@ struct PShape {
   int S = 0, G = 0, NV = 0, CV = 0, NCH = 0, WV = 0, NS = 0, rows = 0, smem = 0;
 };
 
-constexpr int kPStageTarget = 32768;  // bytes of logits per ring stage
 constexpr int kPSmemReserve = 1024;
 
 template <class Fn>
@@ -269,6 +268,10 @@ cudaError_t prepare_pipe(Fn fn, std::atomic<uint64_t>& done_mask) {
   return cudaSuccess;
 }
 
+// Vectors per lane per row of a chunk: 2 when a stage holds target and draft
+// rows, 4 when it holds the target alone (32 KB of logits per stage either way).
+constexpr int pipe_vpl(int rows) { return rows == 2 ? 2 : 4; }
+
 // Picks the cluster size S for a two-pass sweep: every S whose slices fit the
 // ring (at most kPMaxCh chunks per slice, S x chunks <= kPMaxParts, at least
 // three stages) is costed as (waves of units over the resident clusters) x
@@ -282,16 +285,15 @@ bool pick_pipe_shape(Fn fn, int es, long long units, int V, int rows, PShape* ou
   const long long smem_avail = di.smem_optin - (long long)sizeof(ssv::PipeSmem) - kPSmemReserve;
   const int pv = 16 / es;
   const long long nvec_row = V / pv;
+  const int vpl = pipe_vpl(rows);
+  const long long CV = (long long)ssv::kPNC * 32 * vpl;
   const int ov = g_cluster_override.load();
   const int ovs = g_stage_override.load();
   double best = -1.0;
   for (int S = (ov > 0 ? ov : 1); S <= (ov > 0 ? ov : ssv::kPMaxS); ++S) {
     const long long NV = (nvec_row + S - 1) / S;
-    const long long cvmax = kPStageTarget / (rows * 16);
-    long long NCH = (NV + cvmax - 1) / cvmax;
+    long long NCH = (NV + CV - 1) / CV;
     if (NCH < 1) NCH = 1;
-    long long CV = (NV + NCH - 1) / NCH;
-    if (CV < 1) CV = 1;
     if (NCH > ssv::kPMaxCh || S * NCH > ssv::kPMaxParts) continue;
     const long long stage = (long long)rows * CV * 16;
     const long long fixed = (long long)(ssv::pipe_mbox_bytes(S) + ssv::pipe_wt_bytes((int)NCH));
@@ -316,7 +318,7 @@ bool pick_pipe_shape(Fn fn, int es, long long units, int V, int rows, PShape* ou
       out->NV = (int)NV;
       out->CV = (int)CV;
       out->NCH = (int)NCH;
-      out->WV = (int)((CV + ssv::kPNC - 1) / ssv::kPNC);
+      out->WV = 32 * vpl;
       out->NS = (int)NS;
       out->rows = rows;
       out->smem = (int)ssv::pipe_dyn_bytes((int)NS, rows, (int)CV, S, (int)NCH);
@@ -325,29 +327,36 @@ bool pick_pipe_shape(Fn fn, int es, long long units, int V, int rows, PShape* ou
   return best >= 0;
 }
 
-template <class E, int MODE>
+template <class E, int MODE, int VPL>
 std::atomic<uint64_t>& pipe_prepared_mask() {
   static std::atomic<uint64_t> m{0};
   return m;
 }
 
-template <class E, int MODE>
+template <class E, int MODE, int VPL>
 spec_status_t pipe_shape_for(long long units, int V, int rows, PShape* sh) {
-  auto fn = ssv::pipe_kernel<E, MODE>;
-  if (prepare_pipe(fn, pipe_prepared_mask<E, MODE>()) != cudaSuccess) return SPEC_ERR_CUDA;
+  auto fn = ssv::pipe_kernel<E, MODE, VPL>;
+  if (prepare_pipe(fn, pipe_prepared_mask<E, MODE, VPL>()) != cudaSuccess) return SPEC_ERR_CUDA;
   if (!pick_pipe_shape(fn, E::ES, units, V, rows, sh)) return SPEC_ERR_UNSUPPORTED;
   return SPEC_OK;
 }
 
+// Only greedy verify stages the target alone (rows == 1).
 template <int MODE>
 spec_status_t pipe_shape_dt(spec_dtype_t dt, long long units, int V, int rows, PShape* sh) {
-  return dt == SPEC_BF16 ? pipe_shape_for<Bf16, MODE>(units, V, rows, sh)
-                         : pipe_shape_for<F32, MODE>(units, V, rows, sh);
+  if constexpr (MODE == ssv::kPGreedy) {
+    if (rows == 1)
+      return dt == SPEC_BF16 ? pipe_shape_for<Bf16, MODE, 4>(units, V, rows, sh)
+                             : pipe_shape_for<F32, MODE, 4>(units, V, rows, sh);
+  }
+  if (rows != 2) return SPEC_ERR_UNSUPPORTED;
+  return dt == SPEC_BF16 ? pipe_shape_for<Bf16, MODE, 2>(units, V, rows, sh)
+                         : pipe_shape_for<F32, MODE, 2>(units, V, rows, sh);
 }
 
-template <class E, int MODE>
+template <class E, int MODE, int VPL>
 cudaError_t launch_pipe(const ssv::PipeParams& P, const PShape& sh, cudaStream_t stream) {
-  auto fn = ssv::pipe_kernel<E, MODE>;
+  auto fn = ssv::pipe_kernel<E, MODE, VPL>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(sh.G * sh.S), 1, 1);
   cfg.blockDim = dim3(ssv::kPThreads, 1, 1);
@@ -365,7 +374,12 @@ cudaError_t launch_pipe(const ssv::PipeParams& P, const PShape& sh, cudaStream_t
 
 template <int MODE>
 cudaError_t launch_pipe_dt(spec_dtype_t dt, const ssv::PipeParams& P, const PShape& sh, cudaStream_t stream) {
-  return dt == SPEC_BF16 ? launch_pipe<Bf16, MODE>(P, sh, stream) : launch_pipe<F32, MODE>(P, sh, stream);
+  if constexpr (MODE == ssv::kPGreedy) {
+    if (sh.rows == 1)
+      return dt == SPEC_BF16 ? launch_pipe<Bf16, MODE, 4>(P, sh, stream) : launch_pipe<F32, MODE, 4>(P, sh, stream);
+  }
+  if (sh.rows != 2) return cudaErrorInvalidValue;
+  return dt == SPEC_BF16 ? launch_pipe<Bf16, MODE, 2>(P, sh, stream) : launch_pipe<F32, MODE, 2>(P, sh, stream);
 }
 
 // Fills the shape fields of a two-pass launch.
