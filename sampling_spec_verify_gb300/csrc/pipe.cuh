@@ -47,6 +47,10 @@ constexpr int kPMaxNS = 8;
 constexpr int kPMaxCh = 32;     // chunks per slice
 constexpr int kPMaxParts = 64;  // S x chunks per slice: draw totals per unit
 constexpr int kPQ = 8;          // units between the consumers and the completion warp
+// Unit-scalar slots: the producer may run up to a full ring (kPMaxNS items,
+// one phase per item at worst) ahead of the consumers, which read a unit's
+// slot until the phase after it.
+constexpr int kPUS = 16;
 
 enum PMode : int { kPSample = 0, kPGreedy = 1, kPOverlap = 2, kPE2E = 3 };
 
@@ -162,6 +166,15 @@ struct UnitJob {
   float c1t, c1d, cd2, izt, ratio, ufin;
 };
 
+// Per-unit inputs of the decision, loaded by the producer warp so that the
+// consumer warps issue no global-memory operation.
+struct UnitScalars {
+  int y;          // drafted token
+  float ua, uf;   // acceptance and final uniforms
+  uint32_t rejw;  // rank 0: the row's earliest-rejection word when the unit started
+  float zty, zdy; // target and draft logits of the drafted token
+};
+
 struct PipeSmem {
   uint64_t full[kPMaxNS];
   uint64_t empty[kPMaxNS];
@@ -173,6 +186,7 @@ struct PipeSmem {
   uint32_t ticket[kPQ];    // p + 1 once unit p's job is in slot p % kPQ
   uint32_t done_head;      // units the completion warp has finished
   float dsum[kPMaxParts];  // completion warp: draw totals of one unit
+  UnitScalars us[kPUS];    // written by the producer at the start of a unit's phase
 };
 
 __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d, uint32_t bar) {
@@ -833,10 +847,56 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
           if (j > NS) epar ^= 1u;
         }
       };
+      // Unit scalars, one phase ahead: loads issued in phase q-1 land in
+      // shared memory at the start of phase q, before the release of that
+      // phase's first full barrier publishes them.
+      constexpr bool kScal = (kSampleM || kGreedyM);
+      int ny = -1;
+      float nua = 0.0f, nuf = 0.0f, pzt = 0.0f, pzd = 0.0f;
+      uint32_t nrej = 0u;
+      auto load_scalars = [&](int q) {  // issue the loads of unit q (no wait)
+        const PUnit x = pdecode<MODE>(P, cl + q * G);
+        const long long di = (long long)x.b * P.K + x.k;
+        ny = x.bonus ? -1 : __ldg(P.draft_tokens + di);
+        if constexpr (kSampleM) {
+          nua = x.bonus ? 0.0f : __ldg(P.u_accept + di);
+          nuf = __ldg(P.u_final + x.b);
+          nrej = (rank == 0) ? __ldcg(P.rej + x.b) : 0u;
+        }
+      };
+      if constexpr (kScal) {
+        if (nit > 0) load_scalars(0);
+      }
       PUnit xa = {}, xc = {};
       for (int p = 0; p <= nit; ++p) {
         xc = xa;
         if (p < nit) xa = pdecode<MODE>(P, cl + p * G);
+        if constexpr (kScal) {
+          if (p >= 1) {  // gathered logits of unit p-1 (loaded during phase p-1)
+            sm.us[(p - 1) % kPUS].zty = pzt;
+            sm.us[(p - 1) % kPUS].zdy = pzd;
+          }
+          if (p < nit) {
+            UnitScalars u;
+            u.y = ny;
+            u.ua = nua;
+            u.uf = nuf;
+            u.rejw = nrej;
+            u.zty = 0.0f;
+            u.zdy = 0.0f;
+            sm.us[p % kPUS] = u;
+            // this unit's gathered logits, then the next unit's scalars
+            pzt = 0.0f;
+            pzd = 0.0f;
+            if constexpr (kSampleM) {
+              if (!xa.bonus && ny >= 0 && ny < P.V) {
+                pzt = E::to_f32(__ldg(reinterpret_cast<const Raw*>(P.target) + xa.trow * P.V + ny));
+                pzd = E::to_f32(__ldg(reinterpret_cast<const Raw*>(P.draft) + xa.drow * P.V + ny));
+              }
+            }
+            if (p + 1 < nit) load_scalars(p + 1);
+          }
+        }
         for (int c = 0; c < NCH; ++c) {
           if (p < nit) issue(xa, c, false);
           if (kHasC && p >= 1) issue(xc, c, true);
@@ -879,18 +939,13 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
     float gbt = -INFINITY, gbd = -INFINITY;                          // greedy: best values
     int git = 0x7FFFFFFF, gid = 0x7FFFFFFF;                          // greedy: their indices
     bool gnan = false;
-    int a_y = -1;
-    float a_ua = 0.0f, a_uf = 0.0f;
-    uint32_t a_rejw = 0;
     bool a_ok = true;
     // a unit whose pass A has ended, until the end of the phase
-    int t_y = -1;
-    float t_ua = 0.0f, t_uf = 0.0f, t_zty = 0.0f, t_zdy = 0.0f;
     bool t_okA = true;
     // the unit waiting for its exchange and pass C
     PUnit cx = {};
     int c_y = -1;
-    float c_ua = 0.0f, c_uf = 0.0f, c_zty = 0.0f, c_zdy = 0.0f;
+    float c_ua = 0.0f, c_uf = 0.0f;
     bool c_okA = true;
     // decision of that unit
     int mode_c = 0;  // 0: overlap only, 1: residual, 2: target draw, 3: invalid
@@ -913,15 +968,6 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
         git = gid = 0x7FFFFFFF;
         gnan = false;
         a_ok = true;
-        if (lane == 0) {
-          const long long di = (long long)ax.b * P.K + ax.k;
-          if constexpr (kSampleM || kGreedyM) a_y = ax.bonus ? -1 : __ldg(P.draft_tokens + di);
-          if constexpr (kSampleM) {
-            a_ua = ax.bonus ? 0.0f : __ldg(P.u_accept + di);
-            a_uf = __ldg(P.u_final + ax.b);
-            a_rejw = (rank == 0 && warp == 0) ? __ldcg(P.rej + ax.b) : 0u;
-          }
-        }
       }
       const bool ok = mbar_wait_bounded(smem_addr(&sm.full[st]), fpar, kWaitLimitNs);
       if (!ok) {
@@ -1020,7 +1066,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
           f2_ = amd;
           f3 = azd;
         }
-        const uint32_t rjw = __shfl_sync(kFull, a_rejw, 0);
+        const uint32_t rjw = sm.us[p % kPUS].rejw;  // published by the first chunk's full barrier
         const float aok = __all_sync(kFull, a_ok) ? 0.0f : 1.0f;
         if (lane < S) {
           const uint32_t a = map_rank(smem_addr(mb_at(slot, (int)rank, warp)), (uint32_t)lane);
@@ -1033,19 +1079,6 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
         }
         // hand the unit over; pass C takes it at the end of this phase
         t_okA = __all_sync(kFull, a_ok);
-        t_y = __shfl_sync(kFull, a_y, 0);
-        t_ua = __shfl_sync(kFull, a_ua, 0);
-        t_uf = __shfl_sync(kFull, a_uf, 0);
-        t_zty = 0.0f;
-        t_zdy = 0.0f;
-        if constexpr (kSampleM) {
-          // gathered logits of the drafted token (read from L2 while pass C of
-          // the previous unit runs)
-          if (lane == 0 && !ax.bonus && t_y >= 0 && t_y < P.V) {
-            t_zty = E::to_f32(__ldg(reinterpret_cast<const Raw*>(P.target) + ax.trow * P.V + t_y));
-            t_zdy = E::to_f32(__ldg(reinterpret_cast<const Raw*>(P.draft) + ax.drow * P.V + t_y));
-          }
-        }
       }
     };
 
@@ -1060,6 +1093,16 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
       // the completion warp must be done with the unit whose job slot this one takes
       if (p >= kPQ) wait_counter(&sm.done_head, (uint32_t)(p - kPQ + 1), lane, P.status);
       const int ne = S * (kPNC + 1);
+      // the unit's scalars (published before this phase's first full barrier)
+      float c_zty = 0.0f, c_zdy = 0.0f;
+      if constexpr (kSampleM || kGreedyM) {
+        const UnitScalars& u = sm.us[p % kPUS];
+        c_y = u.y;
+        c_ua = u.ua;
+        c_uf = u.uf;
+        c_zty = u.zty;
+        c_zdy = u.zdy;
+      }
       const bool tok_ok = cx.bonus || (c_y >= 0 && c_y < P.V);
       uint32_t flags = 0;
       a2 = f2(0.0f, 0.0f);
@@ -1127,7 +1170,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
             mode_c = 2;
           } else {
             // u * q(y) <= p(y), with p(y), q(y) formed like the per-element values
-            const float zty = __shfl_sync(kFull, c_zty, 0), zdy = __shfl_sync(kFull, c_zdy, 0);
+            const float zty = c_zty, zdy = c_zdy;
             const float py = __fmul_rn(ex2(fmaf(zty, s, -c1t)), izt);
             const float qy = __fmul_rn(ex2(fmaf(zdy, s, -c1d)), izd);
             acc = (tok_ok && __fmul_rn(c_ua, qy) <= py) ? 1 : 0;
@@ -1263,11 +1306,6 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
         C_end(p - 1);
       }
       // unit p goes on to pass C in the next phase
-      c_y = t_y;
-      c_ua = t_ua;
-      c_uf = t_uf;
-      c_zty = t_zty;
-      c_zdy = t_zdy;
       c_okA = t_okA;
     }
     __syncwarp();
