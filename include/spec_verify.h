@@ -241,7 +241,7 @@ spec_status_t spec_verify_ragged(const void* target_logits,
  * scratch is a fixed device array of SPEC_NOALLOC_SCRATCH_BYTES inside the
  * library, held by every GPU that loads the library until the process exits.
  * Sizes whose spec_verify_workspace_bytes(B, K, V) exceeds it are rejected with
- * SPEC_ERR_UNSUPPORTED (at K = 4 that is about 2,500 rows).  No call
+ * SPEC_ERR_UNSUPPORTED (at K = 4 that is 393 rows, at K = 7 245 rows).  No call
  * allocates or frees memory; each clears the part of the array it uses with
  * cudaMemsetAsync on `stream`.
  *  - The first call on a device looks up the array's device address (once per
@@ -250,7 +250,7 @@ spec_status_t spec_verify_ragged(const void* target_logits,
  *  - Every call on a device shares the one array: calls that may overlap on
  *    the GPU (different streams without ordering between them) race and give
  *    wrong results.  Serialise them. */
-#define SPEC_NOALLOC_SCRATCH_BYTES (1u << 20)
+#define SPEC_NOALLOC_SCRATCH_BYTES (4u << 20)
 
 spec_status_t spec_verify_noalloc(const void* target_logits,
                                   const void* draft_logits, spec_dtype_t dtype,

@@ -45,7 +45,8 @@ constexpr int kPNX = 4;                     // exchange slots (units in flight)
 constexpr int kPMaxS = 16;
 constexpr int kPMaxNS = 8;
 constexpr int kPMaxCh = 32;     // chunks per slice
-constexpr int kPMaxParts = 64;  // S x chunks per slice: draw totals per unit
+constexpr int kPMaxParts = 32;  // S x chunks per slice
+constexpr int kPSegs = kPMaxParts * 16;  // draw totals per unit: one per (CTA, chunk, consumer warp)
 constexpr int kPQ = 8;          // units between the consumers and the completion warp
 // Unit-scalar slots: the producer may run up to a full ring (kPMaxNS items,
 // one phase per item at worst) ahead of the consumers, which read a unit's
@@ -84,7 +85,7 @@ struct PipeParams {
   E2EStats* stats;
   float* part;     // [units][kPartStride] overlap partials, one per CTA
   float* part2;    // [units][kPartStride] E2E S-mass partials
-  float* dtot;     // [units][kPMaxParts] draw totals per (CTA, chunk)
+  float* dtot;     // [units][kPSegs] draw totals per (CTA, chunk, consumer warp)
   uint32_t* dcnt;  // [units] CTAs done with a drawing unit
   float* row_loss;
   uint32_t* row_cnt;
@@ -185,7 +186,6 @@ struct PipeSmem {
   UnitJob job[kPQ];
   uint32_t ticket[kPQ];    // p + 1 once unit p's job is in slot p % kPQ
   uint32_t done_head;      // units the completion warp has finished
-  float dsum[kPMaxParts];  // completion warp: draw totals of one unit
   UnitScalars us[kPUS];    // written by the producer at the start of a unit's phase
 };
 
@@ -249,10 +249,30 @@ __device__ __forceinline__ void mz_merge(float& m, float& z, float mi, float zi,
   }
 }
 
+// The values of a 16-byte vector as float2 pairs in element order (exact
+// widening of bf16; fp32 as is).
+template <class E>
+__device__ __forceinline__ void pairs2(const uint4& w, float2 (&p)[E::PV / 2]) {
+  if constexpr (E::ES == 2) {
+    p[0] = make_float2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u));
+    p[1] = make_float2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+    p[2] = make_float2(__uint_as_float(w.z << 16), __uint_as_float(w.z & 0xFFFF0000u));
+    p[3] = make_float2(__uint_as_float(w.w << 16), __uint_as_float(w.w & 0xFFFF0000u));
+  } else {
+    p[0] = make_float2(__uint_as_float(w.x), __uint_as_float(w.y));
+    p[1] = make_float2(__uint_as_float(w.z), __uint_as_float(w.w));
+  }
+}
+
 // A lane's VPL vectors idx0, idx0+32, ... of a chunk of cv vectors, loaded
 // at once; vectors past the chunk read as -inf (they add nothing).
 template <class E, int VPL>
 __device__ __forceinline__ bool load_lane(const uint4* base, int idx0, int cv, uint4 (&w)[VPL]) {
+  if (idx0 + 32 * (VPL - 1) < cv) {  // every vector present: all but a slice's last chunk
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) w[v] = base[idx0 + 32 * v];
+    return true;
+  }
   const uint32_t ninf = (E::ES == 2) ? 0xFF80FF80u : 0xFF800000u;
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
@@ -270,7 +290,6 @@ __device__ __forceinline__ bool load_lane(const uint4* base, int idx0, int cv, u
 template <class E, int VPL>
 __device__ __forceinline__ void lane_item_add(const uint4 (&w)[VPL], float s, float& m, float& z) {
   constexpr int PV = E::PV;
-  const f32x2 S2 = f2(s, s);
   float m0 = m, z0 = z;
   if (!(m0 > -INFINITY)) {
     m0 = E::vmax(w[0]);
@@ -278,21 +297,26 @@ __device__ __forceinline__ void lane_item_add(const uint4 (&w)[VPL], float s, fl
   }
   if (m0 > -INFINITY) {
     const float c = __fmul_rn(m0, s);
-    const f32x2 C2 = f2(-c, -c);
-    f32x2 acc = f2(0.0f, 0.0f);
+    const float2 S2 = make_float2(s, s), C2 = make_float2(-c, -c);
+    float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int v = 0; v < VPL; ++v) {
-      f32x2 e[PV / 2];
-      exp_pairs<E>(w[v], S2, C2, e);
-      acc = f2_add(acc, psum(e));
+      float2 p[PV / 2];
+      pairs2<E>(w[v], p);
+#pragma unroll
+      for (int h = 0; h < PV / 2; ++h) {
+        const float2 x = __ffma2_rn(p[h], S2, C2);
+        acc = __fadd2_rn(acc, make_float2(ex2(x.x), ex2(x.y)));
+      }
     }
-    const float zc = f2_hsum(acc);
+    const float zc = __fadd_rn(acc.x, acc.y);
     if (zc < 0x1p100f) {  // false for NaN and infinities
       m = m0;
       z = __fadd_rn(z0, zc);
       return;
     }
   }
+  const f32x2 S2 = f2(s, s);
   float mc = -INFINITY, zc = 0.0f, cm = 0.0f;
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
@@ -315,25 +339,22 @@ __device__ __forceinline__ void lane_item_add(const uint4 (&w)[VPL], float s, fl
 // Overlap terms of a lane's vector pairs of one chunk: the sum of
 // 2^min(x_t, x_d') (and, for E2E-TV, of the terms with x_d' < x_t).
 template <class E, int VPL, bool kE2EM>
-__device__ __forceinline__ void lane_item_overlap(const uint4 (&wt)[VPL], const uint4 (&wd)[VPL], f32x2 S2, f32x2 CT,
-                                                  f32x2 CD, f32x2& a2, f32x2& g2) {
+__device__ __forceinline__ void lane_item_overlap(const uint4 (&wt)[VPL], const uint4 (&wd)[VPL], float s, float ct,
+                                                  float cd, float2& a2, float2& g2) {
   constexpr int PV = E::PV;
+  const float2 S2 = make_float2(s, s), CT = make_float2(-ct, -ct), CD = make_float2(-cd, -cd);
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
-    f32x2 pt[PV / 2], pd[PV / 2], ep[PV / 2], gp[PV / 2];
-    E::pairs(wt[v], pt);
-    E::pairs(wd[v], pd);
+    float2 pt[PV / 2], pd[PV / 2];
+    pairs2<E>(wt[v], pt);
+    pairs2<E>(wd[v], pd);
 #pragma unroll
     for (int h = 0; h < PV / 2; ++h) {
-      float t0, t1, d0, d1;
-      f2_split(f2_fma(pt[h], S2, CT), t0, t1);
-      f2_split(f2_fma(pd[h], S2, CD), d0, d1);
-      const float e0 = ex2(fminf(t0, d0)), e1 = ex2(fminf(t1, d1));
-      ep[h] = f2(e0, e1);
-      if constexpr (kE2EM) gp[h] = f2(d0 < t0 ? e0 : 0.0f, d1 < t1 ? e1 : 0.0f);
+      const float2 x = __ffma2_rn(pt[h], S2, CT), y = __ffma2_rn(pd[h], S2, CD);
+      const float e0 = ex2(fminf(x.x, y.x)), e1 = ex2(fminf(x.y, y.y));
+      a2 = __fadd2_rn(a2, make_float2(e0, e1));
+      if constexpr (kE2EM) g2 = __fadd2_rn(g2, make_float2(y.x < x.x ? e0 : 0.0f, y.y < x.y ? e1 : 0.0f));
     }
-    a2 = f2_add(a2, psum(ep));
-    if constexpr (kE2EM) g2 = f2_add(g2, psum(gp));
   }
 }
 
@@ -573,104 +594,101 @@ __device__ __forceinline__ void parrive_row(const PipeParams& P, int b, int lane
 // ---- the draw of one unit (completion warp) ------------------------------------------
 
 template <class E, int MODE>
-__device__ void pdraw(const PipeParams& P, PipeSmem& sm, const PUnit& x, const UnitJob& J, int lane) {
+__device__ void pdraw(const PipeParams& P, const PUnit& x, const UnitJob& J, int lane) {
   constexpr int PV = E::PV;
   const int S = P.S, NCH = P.NCH, CV = P.CV, WV = P.WV;
   const int nvec_row = P.V / PV;
-  const int nparts = S * NCH;
+  const int nseg = S * NCH * kPNC;  // warp sub-segments in prefix order (CTA, chunk, warp)
   const uint4* tv = reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::Raw*>(P.target) + x.trow * P.V);
   const uint4* dv = reinterpret_cast<const uint4*>(reinterpret_cast<const typename E::Raw*>(P.draft) + x.drow * P.V);
   const f32x2 S2 = f2(P.s, P.s);
   const f32x2 CT = f2(-J.c1t, -J.c1t);
   const f32x2 CD = f2(-J.c1d, -J.c1d);
   const f32x2 NR = f2(-J.ratio, -J.ratio);
-  float* dt = P.dtot + (long long)x.rec * kPMaxParts;
-  auto chunk_range = [&](int jj, int& c0, int& cv) {
-    const int r = jj / NCH, c = jj - r * NCH;
+  float* dt = P.dtot + (long long)x.rec * kPSegs;
+  // vectors [v0, v1) of sub-segment j of the row
+  auto seg_range = [&](int j, int& v0, int& v1) {
+    const int w = j % kPNC, rc = j / kPNC;
+    const int r = rc / NCH, c = rc - r * NCH;
     const int s0 = min(r * P.NV, nvec_row);
     const int s1 = min(s0 + P.NV, nvec_row);
-    c0 = min(s0 + c * CV, s1);
-    cv = min(c0 + CV, s1) - c0;
+    const int c0 = min(s0 + c * CV, s1);
+    const int cv = min(c0 + CV, s1) - c0;
+    v0 = c0 + min(w * WV, cv);
+    v1 = c0 + min(w * WV + WV, cv);
   };
   bool resid = (J.mode_c == 1);
   bool emptied = false;
-  // per-(CTA, chunk) totals in prefix order, summed in order
-  for (int i = lane; i < nparts; i += 32) sm.dsum[i] = __ldcg(dt + i);
-  __syncwarp();
-  float total = 0.0f;
-  for (int i = 0; i < nparts; ++i) total = __fadd_rn(total, sm.dsum[i]);
+  // lane l takes the contiguous block [l * E, (l + 1) * E) of the totals
+  const int E_ = (nseg + 31) / 32;
+  auto block_sum = [&]() {
+    float t = 0.0f;
+    for (int i = 0; i < E_; ++i) {
+      const int j = lane * E_ + i;
+      if (j < nseg) t = __fadd_rn(t, __ldcg(dt + j));
+    }
+    return t;
+  };
+  float bt = block_sum();
+  float incl = warp_incl_scan(bt, lane);
+  float total = __shfl_sync(kFull, incl, 31);
   if (!(total > 0.0f) && resid) {
     // no residual mass (rounding only): draw from p, recomputing every
-    // chunk's target-weight total in the consumers' order
+    // sub-segment's target-weight total with the consumers' arithmetic
     resid = false;
     emptied = true;
-    for (int jj = 0; jj < nparts; ++jj) {
-      int c0, cv;
-      chunk_range(jj, c0, cv);
-      float t = 0.0f;
-      for (int w = 0; w < kPNC; ++w) {
-        const int a0 = min(w * WV, cv), a1 = min(a0 + WV, cv);
-        t = __fadd_rn(t, seg_weights<E, false>(tv, dv, c0 + a0, c0 + a1, S2, CT, CD, NR, lane, -1.0f, nullptr));
-      }
-      __syncwarp();
-      if (lane == 0) sm.dsum[jj] = t;
-      __syncwarp();
+    for (int j = 0; j < nseg; ++j) {
+      int v0, v1;
+      seg_range(j, v0, v1);
+      const float t = seg_weights<E, false>(tv, dv, v0, v1, S2, CT, CD, NR, lane, -1.0f, nullptr);
+      if (lane == 0) dt[j] = t;
     }
-    total = 0.0f;
-    for (int i = 0; i < nparts; ++i) total = __fadd_rn(total, sm.dsum[i]);
+    __syncwarp();
+    __threadfence();
+    bt = block_sum();
+    incl = warp_incl_scan(bt, lane);
+    total = __shfl_sync(kFull, incl, 31);
   }
   int token = -1;
   if (total > 0.0f) {
     const float thr = __fmul_rn(J.ufin, total);
-    int jsel = -1, jlast = -1;
-    float cum = 0.0f, before = 0.0f;
-    for (int i = 0; i < nparts; ++i) {
-      const float t = sm.dsum[i];
+    // first positive sub-segment whose running total passes thr
+    const float up = __shfl_up_sync(kFull, incl, 1);
+    float cum = (lane == 0) ? 0.0f : up;
+    int hit = -1, lastp = -1;
+    float before = 0.0f;
+    for (int i = 0; i < E_; ++i) {
+      const int j = lane * E_ + i;
+      const float t = (j < nseg) ? __ldcg(dt + j) : 0.0f;
       const float nc = __fadd_rn(cum, t);
       if (t > 0.0f) {
-        jlast = i;
-        if (jsel < 0 && nc > thr) {
-          jsel = i;
+        lastp = j;
+        if (hit < 0 && nc > thr) {
+          hit = j;
           before = cum;
         }
       }
       cum = nc;
     }
-    float thr_c = INFINITY;
-    if (jsel >= 0) {
-      thr_c = __fadd_rn(thr, -before);
-    } else {
-      jsel = jlast;
-    }
-    int c0, cv;
-    chunk_range(jsel, c0, cv);
-    // the consumers' warp order inside the chunk
-    float cw = 0.0f;
-    int wsel = -1, wlast = -1;
+    const unsigned hm = __ballot_sync(kFull, hit >= 0);
+    int jsel;
     float thr_w = INFINITY;
-    for (int w = 0; w < kPNC && wsel < 0; ++w) {
-      const int a0 = min(w * WV, cv), a1 = min(a0 + WV, cv);
-      const float t = resid ? seg_weights<E, true>(tv, dv, c0 + a0, c0 + a1, S2, CT, CD, NR, lane, -1.0f, nullptr)
-                            : seg_weights<E, false>(tv, dv, c0 + a0, c0 + a1, S2, CT, CD, NR, lane, -1.0f, nullptr);
-      const float nc = __fadd_rn(cw, t);
-      if (t > 0.0f) {
-        wlast = w;
-        if (nc > thr_c) {
-          wsel = w;
-          thr_w = __fadd_rn(thr_c, -cw);
-        }
-      }
-      cw = nc;
+    if (hm) {
+      const int l = __ffs(hm) - 1;
+      jsel = __shfl_sync(kFull, hit, l);
+      thr_w = __fadd_rn(thr, -__shfl_sync(kFull, before, l));
+    } else {  // no crossing (rounding): the last positive weight
+      const unsigned pm = __ballot_sync(kFull, lastp >= 0);
+      jsel = pm ? __shfl_sync(kFull, lastp, 31 - __clz(pm)) : -1;
     }
-    if (wsel < 0) wsel = wlast;  // no crossing (rounding): the last positive weight
-    if (wsel >= 0) {
-      const int a0 = min(wsel * WV, cv), a1 = min(a0 + WV, cv);
-      int pk = -1;
+    if (jsel >= 0) {
+      int v0, v1, pk = -1;
+      seg_range(jsel, v0, v1);
       if (resid)
-        seg_weights<E, true>(tv, dv, c0 + a0, c0 + a1, S2, CT, CD, NR, lane, thr_w, &pk);
+        seg_weights<E, true>(tv, dv, v0, v1, S2, CT, CD, NR, lane, thr_w, &pk);
       else
-        seg_weights<E, false>(tv, dv, c0 + a0, c0 + a1, S2, CT, CD, NR, lane, thr_w, &pk);
-      if (pk >= 0) token = (c0 + a0) * PV + pk;
+        seg_weights<E, false>(tv, dv, v0, v1, S2, CT, CD, NR, lane, thr_w, &pk);
+      if (pk >= 0) token = v0 * PV + pk;
     }
   }
   if (lane == 0) {
@@ -678,7 +696,7 @@ __device__ void pdraw(const PipeParams& P, PipeSmem& sm, const PUnit& x, const U
     if (emptied) P.rec[x.rec].pad0 = 1u;
     P.dcnt[x.rec] = 0u;
   }
-  for (int i = lane; i < nparts; i += 32) dt[i] = 0.0f;
+  for (int i = lane; i < nseg; i += 32) dt[i] = 0.0f;
   __syncwarp();
   parrive_row<MODE>(P, x.b, lane);
 }
@@ -735,14 +753,10 @@ __device__ void pfinish_unit(const PipeParams& P, PipeSmem& sm, const float* wt,
     }
     if constexpr (MODE == kPSample) {
       if (J.draw) {
-        // per-chunk totals of this CTA, warps in order
+        // this CTA's per-warp totals, (chunk, warp) order
         const int NCH = P.NCH;
-        float* dt = P.dtot + (long long)x.rec * kPMaxParts + (long long)rank * NCH;
-        for (int c = lane; c < NCH; c += 32) {
-          float t = 0.0f;
-          for (int w = 0; w < kPNC; ++w) t = __fadd_rn(t, wt[(slot * NCH + c) * kPNC + w]);
-          dt[c] = t;
-        }
+        float* dt = P.dtot + (long long)x.rec * kPSegs + (long long)rank * NCH * kPNC;
+        for (int i = lane; i < NCH * kPNC; i += 32) dt[i] = wt[slot * NCH * kPNC + i];
         __syncwarp();
         int drawer = 0;
         if (lane == 0) {
@@ -752,7 +766,7 @@ __device__ void pfinish_unit(const PipeParams& P, PipeSmem& sm, const float* wt,
         }
         drawer = __shfl_sync(kFull, drawer, 0);
         if (drawer) {
-          pdraw<E, MODE>(P, sm, x, J, lane);  // writes the token, then arrives
+          pdraw<E, MODE>(P, x, J, lane);  // writes the token, then arrives
           return;
         }
       }
@@ -852,7 +866,8 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
       // phase's first full barrier publishes them.
       constexpr bool kScal = (kSampleM || kGreedyM);
       int ny = -1;
-      float nua = 0.0f, nuf = 0.0f, pzt = 0.0f, pzd = 0.0f;
+      float nua = 0.0f, nuf = 0.0f;
+      Raw pzt = E::kNegInf, pzd = E::kNegInf;  // raw logits, converted a phase later
       uint32_t nrej = 0u;
       auto load_scalars = [&](int q) {  // issue the loads of unit q (no wait)
         const PUnit x = pdecode<MODE>(P, cl + q * G);
@@ -873,8 +888,8 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
         if (p < nit) xa = pdecode<MODE>(P, cl + p * G);
         if constexpr (kScal) {
           if (p >= 1) {  // gathered logits of unit p-1 (loaded during phase p-1)
-            sm.us[(p - 1) % kPUS].zty = pzt;
-            sm.us[(p - 1) % kPUS].zdy = pzd;
+            sm.us[(p - 1) % kPUS].zty = E::to_f32(pzt);
+            sm.us[(p - 1) % kPUS].zdy = E::to_f32(pzd);
           }
           if (p < nit) {
             UnitScalars u;
@@ -886,12 +901,12 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
             u.zdy = 0.0f;
             sm.us[p % kPUS] = u;
             // this unit's gathered logits, then the next unit's scalars
-            pzt = 0.0f;
-            pzd = 0.0f;
+            pzt = E::kNegInf;
+            pzd = E::kNegInf;
             if constexpr (kSampleM) {
               if (!xa.bonus && ny >= 0 && ny < P.V) {
-                pzt = E::to_f32(__ldg(reinterpret_cast<const Raw*>(P.target) + xa.trow * P.V + ny));
-                pzd = E::to_f32(__ldg(reinterpret_cast<const Raw*>(P.draft) + xa.drow * P.V + ny));
+                pzt = __ldg(reinterpret_cast<const Raw*>(P.target) + xa.trow * P.V + ny);
+                pzd = __ldg(reinterpret_cast<const Raw*>(P.draft) + xa.drow * P.V + ny);
               }
             }
             if (p + 1 < nit) load_scalars(p + 1);
@@ -952,7 +967,8 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
     bool draw = false, need_a = false;
     int acc = 1, am_t = -1, am_d = -1;
     float c1t = 0.0f, c1d = 0.0f, cd2 = 0.0f, izt = 0.0f, ratio = 0.0f;
-    f32x2 a2 = f2(0.0f, 0.0f), g2 = f2(0.0f, 0.0f);
+    f32x2 a2 = f2(0.0f, 0.0f);                                // draw-path overlap terms
+    float2 ao = make_float2(0.0f, 0.0f), go = make_float2(0.0f, 0.0f);  // overlap path (and E2E S-mass)
     // rejection seen earlier in the current row (this cluster's own decisions)
     int lrow = -1;
     bool lrej = false;
@@ -1106,7 +1122,8 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
       const bool tok_ok = cx.bonus || (c_y >= 0 && c_y < P.V);
       uint32_t flags = 0;
       a2 = f2(0.0f, 0.0f);
-      g2 = f2(0.0f, 0.0f);
+      ao = make_float2(0.0f, 0.0f);
+      go = make_float2(0.0f, 0.0f);
       draw = false;
       need_a = false;
       if constexpr (kGreedyM) {
@@ -1219,7 +1236,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
           uint4 wt_[VPL], wd_[VPL];
           if (load_lane<E, VPL>(stt, w0 + lane, w1, wt_)) {
             load_lane<E, VPL>(sdd, w0 + lane, w1, wd_);
-            lane_item_overlap<E, VPL, MODE == kPE2E>(wt_, wd_, S2, CT, f2(-cd2, -cd2), a2, g2);
+            lane_item_overlap<E, VPL, MODE == kPE2E>(wt_, wd_, s, c1t, cd2, ao, go);
           }
         } else if constexpr (kSampleM) {
           if (mode_c == 1 && (draw || need_a)) {
@@ -1272,9 +1289,10 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
           st_volatile_u32(&sm.ticket[qs], (uint32_t)p + 1u);
         }
       } else {
-        const float a = warp_sum(f2_hsum(a2));
+        // a unit takes either the overlap path or the draw path
+        const float a = warp_sum(__fadd_rn(__fadd_rn(ao.x, ao.y), f2_hsum(a2)));
         float g = 0.0f;
-        if constexpr (MODE == kPE2E) g = warp_sum(f2_hsum(g2));
+        if constexpr (MODE == kPE2E) g = warp_sum(__fadd_rn(go.x, go.y));
         if (lane == 0) {
           sm.wa[qs][warp] = a;
           sm.wg[qs][warp] = g;

@@ -415,7 +415,7 @@ VerifyWs verify_ws(int B, int K) {
   w.cnt = w.part + part_bytes(units);
   w.rej = w.cnt + align256((size_t)B * sizeof(uint32_t));
   w.dtot = w.rej + align256((size_t)B * sizeof(uint32_t));
-  w.dcnt = w.dtot + align256((size_t)units * ssv::kPMaxParts * sizeof(float));
+  w.dcnt = w.dtot + align256((size_t)units * ssv::kPSegs * sizeof(float));
   w.total = w.dcnt + align256((size_t)units * sizeof(uint32_t));
   return w;
 }
