@@ -431,8 +431,9 @@ spec_status_t spec_selftest_bounded_wait(uint64_t limit_ns, uint32_t* dev_status
 /* ------------------------------------------------------------------------ */
 /* Launch shape the library picks for a sampling verify sweep over `units`
  * (row, position) pairs of V logits with rows on 16-byte boundaries (for
- * benchmarks and diagnostics): CTAs per cluster, threads per CTA (320 for
- * the two-pass sweep, 256 for the single-read sweep), dynamic shared memory
+ * benchmarks and diagnostics): CTAs per cluster, threads per CTA (576 for
+ * the two-pass sweep: sixteen consumer warps, a copy warp and a completion
+ * warp; 256 for the single-read sweep), dynamic shared memory
  * per CTA, the number of persistent clusters launched and the shared-memory
  * stages per CTA.  Needs a current CUDA device.  Returns
  * SPEC_ERR_UNSUPPORTED if V does not fit.  Any output pointer may be NULL. */
@@ -441,7 +442,8 @@ spec_status_t spec_launch_shape(spec_dtype_t dtype, int units, int V,
                                 int* smem_bytes, int* clusters, int* stages);
 
 /* Forces the CTAs per cluster (1..16) and caps the shared-memory stages per
- * CTA (1 or 2) of later launches in this process, for launch-shape sweeps in
+ * CTA (the two-pass sweep's ring stages, at least 1; the single-read sweep's
+ * 1 or 2) of later launches in this process, for launch-shape sweeps in
  * benchmarks; 0 restores the automatic choice of either.  Process-wide; not
  * synchronised with launches in flight. */
 void spec_set_launch_override(int cluster_ctas, int stages);

@@ -268,16 +268,20 @@ cudaError_t prepare_pipe(Fn fn, std::atomic<uint64_t>& done_mask) {
   return cudaSuccess;
 }
 
-// Vectors per lane per row of a chunk: 2 when a stage holds target and draft
-// rows, 4 when it holds the target alone (32 KB of logits per stage either way).
-constexpr int pipe_vpl(int rows) { return rows == 2 ? 2 : 4; }
+// Vectors per lane per row of a chunk: 4 (a stage of 64 KB when it holds target
+// and draft rows, 32 KB when it holds the target alone).  Fewer, larger items
+// beat a deeper ring: each item costs a barrier wait, a warp sync and an
+// arrival per consumer warp.
+constexpr int kPipeVpl = 4;
+constexpr int pipe_vpl(int) { return kPipeVpl; }
 
 // Picks the cluster size S for a two-pass sweep: every S whose slices fit the
 // ring (at most kPMaxCh chunks per slice, S x chunks <= kPMaxParts, at least
 // three stages) is costed as (waves of units over the resident clusters) x
 // (the fresh bytes of one CTA's slice over its share of HBM bandwidth, plus a
-// fixed allowance per unit); slices above 320 KB pay a penalty, because the
-// pass-C copy of their first chunks no longer finds them in L2.
+// fixed allowance per unit); slices above 640 KB pay a penalty, because the
+// pass-C copy of their first chunks no longer finds them in L2 (a unit's
+// slices of all resident CTAs are in flight between its two passes).
 template <class Fn>
 bool pick_pipe_shape(Fn fn, int es, long long units, int V, int rows, PShape* out) {
   DevInfo di;
@@ -309,8 +313,8 @@ bool pick_pipe_shape(Fn fn, int es, long long units, int V, int rows, PShape* ou
     const double bytes_cta = (double)NV * rows * 16.0;
     double bw = 6.8e12 / (double)(Ge * S);
     if (bw > 1.2e11) bw = 1.2e11;
-    double t = waves * (bytes_cta / bw + 0.5e-6);
-    if (bytes_cta > 320.0 * 1024.0) t *= 1.5;
+    double t = waves * (bytes_cta / bw + 1.0e-6);
+    if (bytes_cta > 640.0 * 1024.0) t *= 1.5;
     if (best < 0 || t < best) {
       best = t;
       out->S = S;
@@ -344,14 +348,9 @@ spec_status_t pipe_shape_for(long long units, int V, int rows, PShape* sh) {
 // Only greedy verify stages the target alone (rows == 1).
 template <int MODE>
 spec_status_t pipe_shape_dt(spec_dtype_t dt, long long units, int V, int rows, PShape* sh) {
-  if constexpr (MODE == ssv::kPGreedy) {
-    if (rows == 1)
-      return dt == SPEC_BF16 ? pipe_shape_for<Bf16, MODE, 4>(units, V, rows, sh)
-                             : pipe_shape_for<F32, MODE, 4>(units, V, rows, sh);
-  }
-  if (rows != 2) return SPEC_ERR_UNSUPPORTED;
-  return dt == SPEC_BF16 ? pipe_shape_for<Bf16, MODE, 2>(units, V, rows, sh)
-                         : pipe_shape_for<F32, MODE, 2>(units, V, rows, sh);
+  if (rows != 2 && !(MODE == ssv::kPGreedy && rows == 1)) return SPEC_ERR_UNSUPPORTED;
+  return dt == SPEC_BF16 ? pipe_shape_for<Bf16, MODE, kPipeVpl>(units, V, rows, sh)
+                         : pipe_shape_for<F32, MODE, kPipeVpl>(units, V, rows, sh);
 }
 
 template <class E, int MODE, int VPL>
@@ -374,12 +373,9 @@ cudaError_t launch_pipe(const ssv::PipeParams& P, const PShape& sh, cudaStream_t
 
 template <int MODE>
 cudaError_t launch_pipe_dt(spec_dtype_t dt, const ssv::PipeParams& P, const PShape& sh, cudaStream_t stream) {
-  if constexpr (MODE == ssv::kPGreedy) {
-    if (sh.rows == 1)
-      return dt == SPEC_BF16 ? launch_pipe<Bf16, MODE, 4>(P, sh, stream) : launch_pipe<F32, MODE, 4>(P, sh, stream);
-  }
-  if (sh.rows != 2) return cudaErrorInvalidValue;
-  return dt == SPEC_BF16 ? launch_pipe<Bf16, MODE, 2>(P, sh, stream) : launch_pipe<F32, MODE, 2>(P, sh, stream);
+  if (sh.rows != 2 && !(MODE == ssv::kPGreedy && sh.rows == 1)) return cudaErrorInvalidValue;
+  return dt == SPEC_BF16 ? launch_pipe<Bf16, MODE, kPipeVpl>(P, sh, stream)
+                         : launch_pipe<F32, MODE, kPipeVpl>(P, sh, stream);
 }
 
 // Fills the shape fields of a two-pass launch.

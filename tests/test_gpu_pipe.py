@@ -62,11 +62,11 @@ def _run(ssv, kernel, S, nst, fn):
 
 # B, K, V, dtype, T, S (0 = automatic), stages cap (0 = automatic)
 SHAPES = [
-    (4, 3, 151936, torch.bfloat16, 1.0, 1, 0),    # one CTA per row: 19 chunks per slice
-    (6, 4, 151936, torch.bfloat16, 0.7, 2, 0),    # CTA pairs: 10 chunks each
-    (5, 7, 129280, torch.bfloat16, 1.0, 3, 2),    # uneven slices, a two-stage ring
+    (4, 3, 151936, torch.bfloat16, 1.0, 1, 0),    # one CTA per row: 10 chunks per slice
+    (6, 4, 151936, torch.bfloat16, 0.7, 2, 0),    # CTA pairs: 5 chunks each
+    (5, 7, 129280, torch.bfloat16, 1.0, 3, 2),    # uneven slices of 3 chunks, a two-stage ring
     (9, 2, 40000, torch.bfloat16, 1.0, 16, 0),    # 16 CTAs, short slices
-    (3, 5, 24000, torch.float32, 1.3, 4, 1),      # fp32, a one-stage ring
+    (3, 5, 24000, torch.float32, 1.3, 1, 1),      # fp32, 3 chunks through a one-stage ring
     (2, 4, 8, torch.bfloat16, 1.0, 16, 0),        # V below one vector per CTA: empty slices
     (3, 0, 5000, torch.bfloat16, 1.0, 0, 0),      # K = 0: the bonus draw only
     (2, 33, 1024, torch.float32, 0.9, 0, 0),      # K + 1 above one warp
