@@ -279,9 +279,11 @@ constexpr int pipe_vpl(int) { return kPipeVpl; }
 // ring (at most kPMaxCh chunks per slice, S x chunks <= kPMaxParts, at least
 // three stages) is costed as (waves of units over the resident clusters) x
 // (the fresh bytes of one CTA's slice over its share of HBM bandwidth, plus a
-// fixed allowance per unit); slices above 640 KB pay a penalty, because the
-// pass-C copy of their first chunks no longer finds them in L2 (a unit's
-// slices of all resident CTAs are in flight between its two passes).
+// fixed allowance per unit); slices above 320 KB pay a penalty: every
+// resident CTA holds one unit slice in L2 between its two passes, and beyond
+// about 48 MB in all (152 x 320 KB) the pass-C copies start to miss L2 and
+// read HBM again (measured: one-CTA slices of 517 KB read 25% more DRAM
+// bytes than the logits hold, two-CTA slices of 258 KB read them once).
 template <class Fn>
 bool pick_pipe_shape(Fn fn, int es, long long units, int V, int rows, PShape* out) {
   DevInfo di;
@@ -314,7 +316,7 @@ bool pick_pipe_shape(Fn fn, int es, long long units, int V, int rows, PShape* ou
     double bw = 6.8e12 / (double)(Ge * S);
     if (bw > 1.2e11) bw = 1.2e11;
     double t = waves * (bytes_cta / bw + 1.0e-6);
-    if (bytes_cta > 640.0 * 1024.0) t *= 1.5;
+    if (bytes_cta > 320.0 * 1024.0) t *= 1.5;
     if (best < 0 || t < best) {
       best = t;
       out->S = S;
