@@ -431,9 +431,9 @@ spec_status_t spec_selftest_bounded_wait(uint64_t limit_ns, uint32_t* dev_status
 /* ------------------------------------------------------------------------ */
 /* Launch shape the library picks for a sampling verify sweep over `units`
  * (row, position) pairs of V logits with rows on 16-byte boundaries (for
- * benchmarks and diagnostics): CTAs per cluster, threads per CTA (576 for
- * the two-pass sweep: sixteen consumer warps, a copy warp and a completion
- * warp; 256 for the single-read sweep), dynamic shared memory
+ * benchmarks and diagnostics): CTAs per cluster, threads per CTA (608 for
+ * the two-pass sweep: sixteen consumer warps, a copy warp, a decision warp
+ * and a completion warp; 256 for the single-read sweep), dynamic shared memory
  * per CTA, the number of persistent clusters launched and the shared-memory
  * stages per CTA.  Needs a current CUDA device.  Returns
  * SPEC_ERR_UNSUPPORTED if V does not fit.  Any output pointer may be NULL. */

@@ -12,6 +12,9 @@
 //   * sixteen consumer warps, which share every chunk (warp w takes a
 //     contiguous sub-segment, lane l every 32nd vector of it) and touch
 //     nothing but shared memory on their hot path;
+//   * a decision warp, which combines the cluster's per-warp pass-A
+//     partials of each unit once per CTA and publishes the unit's decision
+//     (normalisers, acceptance, what pass C computes) in shared memory;
 //   * a completion warp, which takes each finished unit from an in-order job
 //     ring in shared memory and does all of the unit's global-memory work:
 //     per-CTA partials, records, arrivals on the row counters, the row's
@@ -22,9 +25,9 @@
 // interleaves the pass-A chunks of unit u+1 with the pass-C chunks of unit
 // u, so a stage is never held while the cluster exchanges unit u's
 // normalisers: every consumer warp pushes its (max, sum) pairs with st.async
-// into every CTA's mailbox, completing on that CTA's mbarrier, and every warp
-// combines all the cluster's pairs itself in one fixed order, so every warp
-// of the cluster takes the same decision with no block or cluster barrier.
+// into every CTA's mailbox, completing on that CTA's mbarrier, and each CTA's
+// decision warp combines all the cluster's pairs in one fixed order, so every
+// CTA of the cluster takes the same decision with no cluster barrier.
 //
 // Draws: each warp's per-chunk residual totals are summed per (CTA, chunk);
 // the CTA whose completion warp brings a drawing unit's counter to S does the
@@ -40,7 +43,8 @@ namespace ssv {
 constexpr int kPNC = 16;                    // consumer warps
 constexpr int kPProd = kPNC;                // producer warp
 constexpr int kPDone = kPNC + 1;            // completion warp
-constexpr int kPThreads = (kPNC + 2) * 32;  // 576
+constexpr int kPDec = kPNC + 2;             // decision warp
+constexpr int kPThreads = (kPNC + 3) * 32;  // 608
 constexpr int kPNX = 4;                     // exchange slots (units in flight)
 constexpr int kPMaxS = 16;
 constexpr int kPMaxNS = 8;
@@ -163,6 +167,7 @@ struct UnitJob {
   int mode_c;  // 0 overlap only, 1 residual draw, 2 target draw, 3 invalid logits
   int acc;     // accepted (verify), or the greedy decision
   int draw;    // this unit draws (it may still be unused)
+  int need_a;  // pass C sums the overlap
   int am_t, am_d;  // greedy: target / draft arg-maxima
   float c1t, c1d, cd2, izt, ratio, ufin;
 };
@@ -186,7 +191,10 @@ struct PipeSmem {
   UnitJob job[kPQ];
   uint32_t ticket[kPQ];    // p + 1 once unit p's job is in slot p % kPQ
   uint32_t done_head;      // units the completion warp has finished
+  uint32_t us_done;        // units whose scalars (gathered logits included) are in `us`
   UnitScalars us[kPUS];    // written by the producer at the start of a unit's phase
+  uint64_t dbar[kPNX];     // a unit's decision is in `dec`
+  UnitJob dec[kPNX];       // written by the decision warp, read by the consumer warps
 };
 
 __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d, uint32_t bar) {
@@ -814,12 +822,16 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
       mbar_init(smem_addr(&sm.full[i]), 1);
       mbar_init(smem_addr(&sm.empty[i]), kPNC);
     }
-    for (int i = 0; i < kPNX; ++i) mbar_init(smem_addr(&sm.xbar[i]), 1);
+    for (int i = 0; i < kPNX; ++i) {
+      mbar_init(smem_addr(&sm.xbar[i]), 1);
+      mbar_init(smem_addr(&sm.dbar[i]), 1);
+    }
     for (int i = 0; i < kPQ; ++i) {
       sm.cnt[i] = 0;
       sm.ticket[i] = 0;
     }
     sm.done_head = 0;
+    sm.us_done = 0;
     fence_mbar_init();
     // arm the first exchange slots
     for (int i = 0; i < kPNX && i < nit; ++i) mbar_arrive_expect_tx(smem_addr(&sm.xbar[i]), xbytes);
@@ -890,6 +902,8 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
           if (p >= 1) {  // gathered logits of unit p-1 (loaded during phase p-1)
             sm.us[(p - 1) % kPUS].zty = E::to_f32(pzt);
             sm.us[(p - 1) % kPUS].zdy = E::to_f32(pzd);
+            __threadfence_block();
+            st_volatile_u32(&sm.us_done, (uint32_t)p);
           }
           if (p < nit) {
             UnitScalars u;
@@ -922,6 +936,163 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
         mbar_wait_bounded(smem_addr(&sm.full[jj % NS]), (uint32_t)(jj / NS) & 1u, kWaitLimitNs);
     }
     __syncwarp();
+  } else if (warp == kPDec) {
+    // ===================== decision warp =====================
+    // Takes each unit's decision once for the CTA, as soon as the cluster's
+    // pass-A partials are in: the combined normalisers, the acceptance test
+    // and what pass C does.  Every CTA of the cluster combines the same
+    // partials in the same order, so all take the same decision.
+    constexpr bool kScal = (kSampleM || kGreedyM);
+    const float s = P.s;
+    int lrow = -1;  // rejection seen earlier in the current row (this cluster's own decisions)
+    bool lrej = false;
+    for (int p = 0; p < nit; ++p) {
+      const PUnit cx = pdecode<MODE>(P, cl + p * G);
+      const int slot = p % kPNX;
+      const uint32_t xpar = (uint32_t)(p / kPNX) & 1u;
+      const bool xok = mbar_wait_bounded(smem_addr(&sm.xbar[slot]), xpar, kWaitLimitNs);
+      if (lane == 0 && p + kPNX < nit) mbar_arrive_expect_tx(smem_addr(&sm.xbar[slot]), xbytes);
+      if constexpr (kScal) wait_counter(&sm.us_done, (uint32_t)p + 1u, lane, P.status);
+      const int ne = S * (kPNC + 1);
+      // the unit's scalars
+      int c_y = -1;
+      float c_ua = 0.0f, c_uf = 0.0f, c_zty = 0.0f, c_zdy = 0.0f;
+      if constexpr (kSampleM || kGreedyM) {
+        const UnitScalars u = sm.us[p % kPUS];
+        c_y = u.y;
+        c_ua = u.ua;
+        c_uf = u.uf;
+        c_zty = u.zty;
+        c_zdy = u.zdy;
+      }
+      const bool tok_ok = cx.bonus || (c_y >= 0 && c_y < P.V);
+      uint32_t flags = 0;
+      int mode_c = 0, acc = 1, am_t = -1, am_d = -1;
+      bool draw = false, need_a = false;
+      float c1t = 0.0f, c1d = 0.0f, cd2 = 0.0f, izt = 0.0f, ratio = 0.0f;
+      if constexpr (kGreedyM) {
+        float v1 = -INFINITY, v2 = -INFINITY;
+        int i1 = 0x7FFFFFFF, i2 = 0x7FFFFFFF;
+        bool nn = false;
+        for (int e = lane; e < ne; e += 32) {
+          const int r = e / (kPNC + 1), w = e - r * (kPNC + 1);
+          if (w == kPNC) continue;
+          const float* mm = mb_at(slot, r, w);
+          const float a = mm[0], d = mm[2];
+          const int ia = __float_as_int(mm[1]), id = __float_as_int(mm[3]);
+          nn |= (a != a) || (d != d);
+          if (a > v1 || (a == v1 && ia < i1)) {
+            v1 = a;
+            i1 = ia;
+          }
+          if (d > v2 || (d == v2 && id < i2)) {
+            v2 = d;
+            i2 = id;
+          }
+        }
+        warp_argmax_redux(v1, i1);
+        warp_argmax_redux(v2, i2);
+        nn = __any_sync(kFull, nn);
+        const bool bad = nn || !(v1 < INFINITY) || i1 == 0x7FFFFFFF ||
+                         (cx.has_draft && (!(v2 < INFINITY) || i2 == 0x7FFFFFFF));
+        if (bad) flags |= kBadLogits;
+        am_t = bad ? -1 : i1;
+        am_d = i2;
+        acc = (!cx.bonus && tok_ok && c_y == am_t) ? 1 : 0;
+        if (!cx.bonus && !tok_ok) flags |= kBadToken;
+      } else {
+        float mt = -INFINITY, zt = 0.0f, md = -INFINITY, zd = 0.0f;
+        for (int e = lane; e < ne; e += 32) {
+          const int r = e / (kPNC + 1), w = e - r * (kPNC + 1);
+          if (w == kPNC) continue;
+          const float* mm = mb_at(slot, r, w);
+          mz_merge(mt, zt, mm[0], mm[1], s);
+          mz_merge(md, zd, mm[2], mm[3], s);
+        }
+        warp_combine_mz2(mt, zt, md, zd, s);
+        const float Zt = zt, Zd = zd;
+        c1t = __fmul_rn(mt, s);
+        c1d = __fmul_rn(md, s);
+        const bool valid = (Zt > 0.0f && Zt < INFINITY) && (!cx.has_draft || (Zd > 0.0f && Zd < INFINITY));
+        izt = __frcp_rn(Zt);
+        const float izd = __frcp_rn(Zd);
+        cd2 = (cx.has_draft && valid) ? __fadd_rn(c1d, __log2f(__fmul_rn(Zd, izt))) : 0.0f;
+        ratio = __fmul_rn(Zt, izd);
+        mode_c = 0;
+        acc = 1;
+        if constexpr (kSampleM) {
+          const uint32_t seen = __float_as_uint(mb_at(slot, 0, kPNC)[0]);
+          if (cx.b != lrow) {
+            lrow = cx.b;
+            lrej = false;
+          }
+          const bool earlier = lrej || (seen > kRejBase - (uint32_t)cx.k);
+          if (cx.bonus) {
+            mode_c = 2;
+          } else {
+            // u * q(y) <= p(y), with p(y), q(y) formed like the per-element values
+            const float zty = c_zty, zdy = c_zdy;
+            const float py = __fmul_rn(ex2(fmaf(zty, s, -c1t)), izt);
+            const float qy = __fmul_rn(ex2(fmaf(zdy, s, -c1d)), izd);
+            acc = (tok_ok && __fmul_rn(c_ua, qy) <= py) ? 1 : 0;
+            mode_c = acc ? 0 : 1;
+            if (!(c_ua >= 0.0f && c_ua < 1.0f)) flags |= kBadUniform;
+            if (!tok_ok) flags |= kBadToken;
+          }
+          if (!(c_uf >= 0.0f && c_uf < 1.0f)) flags |= kBadUniform;
+          if (!valid) {
+            flags |= kBadLogits;
+            mode_c = 3;
+            acc = 0;
+          }
+          if (!cx.bonus && (mode_c == 1 || mode_c == 3)) {
+            if (rank == 0 && lane == 0) atomicMax(&P.rej[cx.b], kRejBase - (uint32_t)cx.k);
+            lrej = true;
+          }
+          draw = (mode_c == 1 || mode_c == 2) && !earlier;
+          need_a = cx.has_draft && P.alpha != nullptr && mode_c != 3;
+        } else {
+          if (!valid) {
+            flags |= kBadLogits;
+            mode_c = 3;
+          }
+          need_a = (mode_c == 0);
+        }
+      }
+      if (!xok) flags |= kTimeout;
+      if (flags && rank == 0 && lane == 0 && P.status) atomicOr(P.status, flags);
+      UnitJob J;
+      J.mode_c = mode_c;
+      J.acc = acc;
+      J.draw = draw ? 1 : 0;
+      J.need_a = need_a ? 1 : 0;
+      J.am_t = am_t;
+      J.am_d = am_d;
+      J.c1t = c1t;
+      J.c1d = c1d;
+      J.cd2 = cd2;
+      J.izt = izt;
+      J.ratio = ratio;
+      J.ufin = c_uf;
+      if constexpr (kGreedyM) {
+        // no pass C: the unit goes straight to the completion warp, once it
+        // is done with the unit whose job slot this one takes
+        const int qs = p % kPQ;
+        if (p >= kPQ) wait_counter(&sm.done_head, (uint32_t)(p - kPQ + 1), lane, P.status);
+        if (lane == 0) {
+          sm.job[qs] = J;
+          __threadfence_block();
+          st_volatile_u32(&sm.ticket[qs], (uint32_t)p + 1u);
+          mbar_arrive_cta(smem_addr(&sm.dbar[slot]));
+        }
+      } else {
+        if (lane == 0) {
+          sm.dec[slot] = J;
+          mbar_arrive_cta(smem_addr(&sm.dbar[slot]));
+        }
+      }
+      __syncwarp();
+    }
   } else if (warp == kPDone) {
     // ===================== completion warp =====================
     for (int p = 0; p < nit; ++p) {
@@ -957,21 +1128,14 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
     bool a_ok = true;
     // a unit whose pass A has ended, until the end of the phase
     bool t_okA = true;
-    // the unit waiting for its exchange and pass C
-    PUnit cx = {};
-    int c_y = -1;
-    float c_ua = 0.0f, c_uf = 0.0f;
+    // the unit in pass C
     bool c_okA = true;
-    // decision of that unit
+    // its decision, as the decision warp took it
     int mode_c = 0;  // 0: overlap only, 1: residual, 2: target draw, 3: invalid
     bool draw = false, need_a = false;
-    int acc = 1, am_t = -1, am_d = -1;
-    float c1t = 0.0f, c1d = 0.0f, cd2 = 0.0f, izt = 0.0f, ratio = 0.0f;
+    float c1t = 0.0f, c1d = 0.0f, cd2 = 0.0f, ratio = 0.0f;
     f32x2 a2 = f2(0.0f, 0.0f);                                // draw-path overlap terms
     float2 ao = make_float2(0.0f, 0.0f), go = make_float2(0.0f, 0.0f);  // overlap path (and E2E S-mass)
-    // rejection seen earlier in the current row (this cluster's own decisions)
-    int lrow = -1;
-    bool lrej = false;
 
     auto A_item = [&](int p, int c) {
       if (c == 0) {
@@ -1099,124 +1263,24 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
     };
 
     auto C_begin = [&](int p) {
-      cx = pdecode<MODE>(P, cl + p * G);
       const int slot = p % kPNX;
-      const uint32_t xpar = (uint32_t)(p / kPNX) & 1u;
-      if (!mbar_wait_bounded(smem_addr(&sm.xbar[slot]), xpar, kWaitLimitNs)) {
+      if (!mbar_wait_bounded(smem_addr(&sm.dbar[slot]), (uint32_t)(p / kPNX) & 1u, kWaitLimitNs)) {
         if (lane == 0 && P.status) atomicOr(P.status, kTimeout);
       }
-      if (warp == 0 && lane == 0 && p + kPNX < nit) mbar_arrive_expect_tx(smem_addr(&sm.xbar[slot]), xbytes);
       // the completion warp must be done with the unit whose job slot this one takes
       if (p >= kPQ) wait_counter(&sm.done_head, (uint32_t)(p - kPQ + 1), lane, P.status);
-      const int ne = S * (kPNC + 1);
-      // the unit's scalars (published before this phase's first full barrier)
-      float c_zty = 0.0f, c_zdy = 0.0f;
-      if constexpr (kSampleM || kGreedyM) {
-        const UnitScalars& u = sm.us[p % kPUS];
-        c_y = u.y;
-        c_ua = u.ua;
-        c_uf = u.uf;
-        c_zty = u.zty;
-        c_zdy = u.zdy;
-      }
-      const bool tok_ok = cx.bonus || (c_y >= 0 && c_y < P.V);
-      uint32_t flags = 0;
+      const UnitJob& D = sm.dec[slot];
+      mode_c = D.mode_c;
+      draw = D.draw != 0;
+      need_a = D.need_a != 0;
+      c1t = D.c1t;
+      c1d = D.c1d;
+      cd2 = D.cd2;
+      ratio = D.ratio;
       a2 = f2(0.0f, 0.0f);
       ao = make_float2(0.0f, 0.0f);
       go = make_float2(0.0f, 0.0f);
-      draw = false;
-      need_a = false;
-      if constexpr (kGreedyM) {
-        float v1 = -INFINITY, v2 = -INFINITY;
-        int i1 = 0x7FFFFFFF, i2 = 0x7FFFFFFF;
-        bool nn = false;
-        for (int e = lane; e < ne; e += 32) {
-          const int r = e / (kPNC + 1), w = e - r * (kPNC + 1);
-          if (w == kPNC) continue;
-          const float* mm = mb_at(slot, r, w);
-          const float a = mm[0], d = mm[2];
-          const int ia = __float_as_int(mm[1]), id = __float_as_int(mm[3]);
-          nn |= (a != a) || (d != d);
-          if (a > v1 || (a == v1 && ia < i1)) {
-            v1 = a;
-            i1 = ia;
-          }
-          if (d > v2 || (d == v2 && id < i2)) {
-            v2 = d;
-            i2 = id;
-          }
-        }
-        warp_argmax_redux(v1, i1);
-        warp_argmax_redux(v2, i2);
-        nn = __any_sync(kFull, nn);
-        const bool bad = nn || !(v1 < INFINITY) || i1 == 0x7FFFFFFF ||
-                         (cx.has_draft && (!(v2 < INFINITY) || i2 == 0x7FFFFFFF));
-        if (bad) flags |= kBadLogits;
-        am_t = bad ? -1 : i1;
-        am_d = i2;
-        acc = (!cx.bonus && tok_ok && c_y == am_t) ? 1 : 0;
-        if (!cx.bonus && !tok_ok) flags |= kBadToken;
-      } else {
-        float mt = -INFINITY, zt = 0.0f, md = -INFINITY, zd = 0.0f;
-        for (int e = lane; e < ne; e += 32) {
-          const int r = e / (kPNC + 1), w = e - r * (kPNC + 1);
-          if (w == kPNC) continue;
-          const float* mm = mb_at(slot, r, w);
-          mz_merge(mt, zt, mm[0], mm[1], s);
-          mz_merge(md, zd, mm[2], mm[3], s);
-        }
-        warp_combine_mz2(mt, zt, md, zd, s);
-        const float Zt = zt, Zd = zd;
-        c1t = __fmul_rn(mt, s);
-        c1d = __fmul_rn(md, s);
-        const bool valid = (Zt > 0.0f && Zt < INFINITY) && (!cx.has_draft || (Zd > 0.0f && Zd < INFINITY));
-        izt = __frcp_rn(Zt);
-        const float izd = __frcp_rn(Zd);
-        cd2 = (cx.has_draft && valid) ? __fadd_rn(c1d, __log2f(__fmul_rn(Zd, izt))) : 0.0f;
-        ratio = __fmul_rn(Zt, izd);
-        mode_c = 0;
-        acc = 1;
-        if constexpr (kSampleM) {
-          const uint32_t seen = __float_as_uint(mb_at(slot, 0, kPNC)[0]);
-          if (cx.b != lrow) {
-            lrow = cx.b;
-            lrej = false;
-          }
-          const bool earlier = lrej || (seen > kRejBase - (uint32_t)cx.k);
-          if (cx.bonus) {
-            mode_c = 2;
-          } else {
-            // u * q(y) <= p(y), with p(y), q(y) formed like the per-element values
-            const float zty = c_zty, zdy = c_zdy;
-            const float py = __fmul_rn(ex2(fmaf(zty, s, -c1t)), izt);
-            const float qy = __fmul_rn(ex2(fmaf(zdy, s, -c1d)), izd);
-            acc = (tok_ok && __fmul_rn(c_ua, qy) <= py) ? 1 : 0;
-            mode_c = acc ? 0 : 1;
-            if (!(c_ua >= 0.0f && c_ua < 1.0f)) flags |= kBadUniform;
-            if (!tok_ok) flags |= kBadToken;
-          }
-          if (!(c_uf >= 0.0f && c_uf < 1.0f)) flags |= kBadUniform;
-          if (!valid) {
-            flags |= kBadLogits;
-            mode_c = 3;
-            acc = 0;
-          }
-          if (!cx.bonus && (mode_c == 1 || mode_c == 3)) {
-            if (rank == 0 && warp == 0 && lane == 0) atomicMax(&P.rej[cx.b], kRejBase - (uint32_t)cx.k);
-            lrej = true;
-          }
-          draw = (mode_c == 1 || mode_c == 2) && !earlier;
-          need_a = cx.has_draft && P.alpha != nullptr && mode_c != 3;
-        } else {
-          if (!valid) {
-            flags |= kBadLogits;
-            mode_c = 3;
-          }
-          need_a = (mode_c == 0);
-        }
-      }
-      if (!c_okA) flags |= kTimeout;
-      if (flags && rank == 0 && warp == 0 && lane == 0 && P.status) atomicOr(P.status, flags);
+      if (!c_okA && lane == 0 && P.status) atomicOr(P.status, kTimeout);
     };
 
     auto C_item = [&](int p, int c) {
@@ -1269,47 +1333,41 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
 
     auto C_end = [&](int p) {
       const int qs = p % kPQ;
-      UnitJob J;
-      J.mode_c = mode_c;
-      J.acc = acc;
-      J.draw = draw ? 1 : 0;
-      J.am_t = am_t;
-      J.am_d = am_d;
-      J.c1t = c1t;
-      J.c1d = c1d;
-      J.cd2 = cd2;
-      J.izt = izt;
-      J.ratio = ratio;
-      J.ufin = c_uf;
-      if constexpr (kGreedyM) {
-        // every warp decided alike: warp 0 hands the unit over
-        if (warp == 0 && lane == 0) {
-          sm.job[qs] = J;
+      // this warp's overlap (and E2E S-mass) terms of the unit: one path or the other
+      const float a = warp_sum(__fadd_rn(__fadd_rn(ao.x, ao.y), f2_hsum(a2)));
+      float g = 0.0f;
+      if constexpr (MODE == kPE2E) g = warp_sum(__fadd_rn(go.x, go.y));
+      if (lane == 0) {
+        sm.wa[qs][warp] = a;
+        sm.wg[qs][warp] = g;
+        __threadfence_block();
+        if (atomicAdd(&sm.cnt[qs], 1u) == (uint32_t)(kPNC - 1)) {
+          // the last warp of the CTA hands the unit to the completion warp
+          // (the decision slot is not reused before every warp has pushed
+          // the pass-A partials of unit p + kPNX)
+          __threadfence_block();
+          sm.cnt[qs] = 0u;
+          sm.job[qs] = sm.dec[p % kPNX];
           __threadfence_block();
           st_volatile_u32(&sm.ticket[qs], (uint32_t)p + 1u);
-        }
-      } else {
-        // a unit takes either the overlap path or the draw path
-        const float a = warp_sum(__fadd_rn(__fadd_rn(ao.x, ao.y), f2_hsum(a2)));
-        float g = 0.0f;
-        if constexpr (MODE == kPE2E) g = warp_sum(__fadd_rn(go.x, go.y));
-        if (lane == 0) {
-          sm.wa[qs][warp] = a;
-          sm.wg[qs][warp] = g;
-          __threadfence_block();
-          if (atomicAdd(&sm.cnt[qs], 1u) == (uint32_t)(kPNC - 1)) {
-            // the last warp of the CTA hands the unit to the completion warp
-            __threadfence_block();
-            sm.cnt[qs] = 0u;
-            sm.job[qs] = J;
-            __threadfence_block();
-            st_volatile_u32(&sm.ticket[qs], (uint32_t)p + 1u);
-          }
         }
       }
     };
 
     for (int p = 0; p <= nit; ++p) {
+      if constexpr (!kHasC) {
+        // Unit p's partials go to mailbox slot p % kPNX of every CTA, which
+        // must have read unit p - kPNX from it.  A CTA that decided unit
+        // p - 2 had every CTA's partials of p - 2, each pushed after that
+        // CTA saw its own decision of p - 4 (this same wait).  (With pass C
+        // the wait for each decision before pass C gives the same order.)
+        if (p >= 2 && p < nit) {
+          const int q = p - 2;
+          if (!mbar_wait_bounded(smem_addr(&sm.dbar[q % kPNX]), (uint32_t)(q / kPNX) & 1u, kWaitLimitNs)) {
+            if (lane == 0 && P.status) atomicOr(P.status, kTimeout);
+          }
+        }
+      }
       for (int c = 0; c < NCH; ++c) {
         if (p < nit) A_item(p, c);
         if constexpr (kHasC) {
@@ -1319,9 +1377,8 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
           }
         }
       }
-      if (p >= 1) {
-        if constexpr (!kHasC) C_begin(p - 1);
-        C_end(p - 1);
+      if constexpr (kHasC) {
+        if (p >= 1) C_end(p - 1);
       }
       // unit p goes on to pass C in the next phase
       c_okA = t_okA;
