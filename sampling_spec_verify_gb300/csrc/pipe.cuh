@@ -52,6 +52,7 @@ constexpr int kPMaxCh = 32;     // chunks per slice
 constexpr int kPMaxParts = 32;  // S x chunks per slice
 constexpr int kPSegs = kPMaxParts * 16;  // draw totals per unit: one per (CTA, chunk, consumer warp)
 constexpr int kPQ = 8;          // units between the consumers and the completion warp
+constexpr int kPSegV = 128;     // vectors per row of a warp sub-segment, at most (32 lanes x 4)
 // Unit-scalar slots: the producer may run up to a full ring (kPMaxNS items,
 // one phase per item at worst) ahead of the consumers, which read a unit's
 // slot until the phase after it.
@@ -195,6 +196,7 @@ struct PipeSmem {
   UnitScalars us[kPUS];    // written by the producer at the start of a unit's phase
   uint64_t dbar[kPNX];     // a unit's decision is in `dec`
   UnitJob dec[kPNX];       // written by the decision warp, read by the consumer warps
+  uint4 dseg[2 * kPSegV];  // the completion warp's copy of the sub-segment a draw walks
 };
 
 __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d, uint32_t bar) {
@@ -602,7 +604,7 @@ __device__ __forceinline__ void parrive_row(const PipeParams& P, int b, int lane
 // ---- the draw of one unit (completion warp) ------------------------------------------
 
 template <class E, int MODE>
-__device__ void pdraw(const PipeParams& P, const PUnit& x, const UnitJob& J, int lane) {
+__device__ void pdraw(const PipeParams& P, const PUnit& x, const UnitJob& J, uint4* stage, int lane) {
   constexpr int PV = E::PV;
   const int S = P.S, NCH = P.NCH, CV = P.CV, WV = P.WV;
   const int nvec_row = P.V / PV;
@@ -692,11 +694,35 @@ __device__ void pdraw(const PipeParams& P, const PUnit& x, const UnitJob& J, int
     if (jsel >= 0) {
       int v0, v1, pk = -1;
       seg_range(jsel, v0, v1);
+      // the sub-segment's vectors into shared memory with one round of loads,
+      // then the walk in the consumers' order and arithmetic
+      const int nv = v1 - v0;
+      uint4* st_t = stage;
+      uint4* st_d = stage + kPSegV;
+      uint4 rt[kPSegV / 32], rd[kPSegV / 32];
+#pragma unroll
+      for (int k = 0; k < kPSegV / 32; ++k) {
+        const int i = lane + 32 * k;
+        if (i < nv) {
+          rt[k] = __ldcg(tv + v0 + i);
+          if (resid) rd[k] = __ldcg(dv + v0 + i);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kPSegV / 32; ++k) {
+        const int i = lane + 32 * k;
+        if (i < nv) {
+          st_t[i] = rt[k];
+          if (resid) st_d[i] = rd[k];
+        }
+      }
+      __syncwarp();
       if (resid)
-        seg_weights<E, true>(tv, dv, v0, v1, S2, CT, CD, NR, lane, thr_w, &pk);
+        seg_weights<E, true>(st_t, st_d, 0, nv, S2, CT, CD, NR, lane, thr_w, &pk);
       else
-        seg_weights<E, false>(tv, dv, v0, v1, S2, CT, CD, NR, lane, thr_w, &pk);
+        seg_weights<E, false>(st_t, st_t, 0, nv, S2, CT, CD, NR, lane, thr_w, &pk);
       if (pk >= 0) token = v0 * PV + pk;
+      __syncwarp();
     }
   }
   if (lane == 0) {
@@ -774,7 +800,7 @@ __device__ void pfinish_unit(const PipeParams& P, PipeSmem& sm, const float* wt,
         }
         drawer = __shfl_sync(kFull, drawer, 0);
         if (drawer) {
-          pdraw<E, MODE>(P, x, J, lane);  // writes the token, then arrives
+          pdraw<E, MODE>(P, x, J, sm.dseg, lane);  // writes the token, then arrives
           return;
         }
       }

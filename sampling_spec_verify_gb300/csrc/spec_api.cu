@@ -274,6 +274,7 @@ cudaError_t prepare_pipe(Fn fn, std::atomic<uint64_t>& done_mask) {
 // arrival per consumer warp.
 constexpr int kPipeVpl = 4;
 constexpr int pipe_vpl(int) { return kPipeVpl; }
+static_assert(32 * kPipeVpl <= ssv::kPSegV, "a draw's warp sub-segment fits the completion warp's copy of it");
 
 // Picks the cluster size S for a two-pass sweep: every S whose slices fit the
 // ring (at most kPMaxCh chunks per slice, S x chunks <= kPMaxParts, at least
