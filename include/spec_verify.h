@@ -402,7 +402,8 @@ spec_status_t spec_truncate_logits(const void* logits, void* out,
  * lengths    [R] int32 (written): l_r in [0, L].
  * objective  [2] float32 or NULL: {Theta, tau} at the choice.
  * Limits: 1 <= L <= 64 and R * L <= 16384 (SPEC_ERR_UNSUPPORTED beyond).
- * One CTA.  Survivals are summed exactly as integers in units of 2^-48 (one
+ * One cluster of 16 CTAs (distributed shared memory; no workspace).
+ * Survivals are summed exactly as integers in units of 2^-48 (one
  * rounding each, so sums of n of them are within n * 2^-49 of the real sum);
  * Theta is formed in fp64.  A choice whose Theta lies within about 1e-10
  * relative of another B's may therefore differ from exact arithmetic.

@@ -984,16 +984,16 @@ spec_status_t spec_schedule_lengths(const float* survival, int R, int L, const f
   if (R == 0) return SPEC_OK;
   if ((long long)sps_len < (long long)R * (1 + L) + 1) return SPEC_ERR_INVALID_ARG;
   if (!survival || !sps || !lengths) return SPEC_ERR_INVALID_ARG;
-  if ((long long)R * L > ssv::kSchedMaxItems) return SPEC_ERR_UNSUPPORTED;
-  const size_t smem = ssv::sched_smem_bytes(R * L);
+  if ((long long)R * L > ssv::kSchedMaxItems || L > ssv::kSchedMaxL) return SPEC_ERR_UNSUPPORTED;
+  const size_t smem = sizeof(ssv::SchedSmem);
   static std::atomic<uint64_t> prepared{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return SPEC_ERR_CUDA;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(prepared.load(std::memory_order_acquire) & bit)) {
-    const size_t most = ssv::sched_smem_bytes(ssv::kSchedMaxItems);
-    e = cudaFuncSetAttribute(ssv::schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
+    e = cudaFuncSetAttribute(ssv::schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ssv::schedule_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return SPEC_ERR_CUDA;
     prepared.fetch_or(bit, std::memory_order_release);
   }
@@ -1006,8 +1006,19 @@ spec_status_t spec_schedule_lengths(const float* survival, int R, int L, const f
   P.lengths = lengths;
   P.objective = objective;
   P.status = dev_status;
-  ssv::schedule_kernel<<<1, ssv::kSThreads, smem, static_cast<cudaStream_t>(stream)>>>(P);
-  return from_cuda(counted(cudaGetLastError()));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ssv::kSCtas, 1, 1);
+  cfg.blockDim = dim3(ssv::kSThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = ssv::kSCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return from_cuda(counted(cudaLaunchKernelEx(&cfg, ssv::schedule_kernel, P)));
 }
 
 size_t spec_verify_ragged_workspace_bytes(int B, int units, int V) {
