@@ -15,6 +15,7 @@
 #include "sweep.cuh"
 #include "pipe.cuh"
 #include "truncate.cuh"
+#include "topk.cuh"
 #include "schedule.cuh"
 #include "tree.cuh"
 
@@ -950,12 +951,30 @@ spec_status_t spec_truncate_logits(const void* logits, void* out, spec_dtype_t d
   P.status = dev_status;
   const int grid = rows < 2 * di.sms ? rows : 2 * di.sms;  // two resident CTAs per SM
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int smem = (int)sizeof(ssv::TruncSmem);
-  static std::atomic<uint64_t> prepared[2];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
   const uint64_t bit = 1ull << (dev & 63);
   const int which = dtype == SPEC_BF16 ? 1 : 0;
+  if (top_k > 0 && top_k < V && top_k <= ssv::kKMax) {
+    // a small top-k (with or without top-p over it): candidate filtering
+    const int smem = (int)sizeof(ssv::TopkSmem);
+    static std::atomic<uint64_t> prepared_k[2];
+    if (!(prepared_k[which].load(std::memory_order_acquire) & bit)) {
+      const cudaError_t e =
+          dtype == SPEC_BF16
+              ? cudaFuncSetAttribute(ssv::topk_kernel<Bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+              : cudaFuncSetAttribute(ssv::topk_kernel<F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return SPEC_ERR_CUDA;
+      prepared_k[which].fetch_or(bit, std::memory_order_release);
+    }
+    if (dtype == SPEC_BF16)
+      ssv::topk_kernel<Bf16><<<grid, ssv::kTThreads, smem, st>>>(P);
+    else
+      ssv::topk_kernel<F32><<<grid, ssv::kTThreads, smem, st>>>(P);
+    return from_cuda(counted(cudaGetLastError()));
+  }
+  const int smem = (int)sizeof(ssv::TruncSmem);
+  static std::atomic<uint64_t> prepared[2];
   if (!(prepared[which].load(std::memory_order_acquire) & bit)) {
     const cudaError_t e = dtype == SPEC_BF16
                               ? cudaFuncSetAttribute(ssv::truncate_kernel<Bf16>,
