@@ -432,7 +432,8 @@ spec_status_t spec_selftest_bounded_wait(uint64_t limit_ns, uint32_t* dev_status
 /* ------------------------------------------------------------------------ */
 /* Launch shape the library picks for a sampling verify sweep over `units`
  * (row, position) pairs of V logits with rows on 16-byte boundaries (for
- * benchmarks and diagnostics): CTAs per cluster, threads per CTA (608 for
+ * benchmarks and diagnostics; the two-pass sweep when units x 2 rows reach
+ * 200 MB, as in spec_set_kernel_override): CTAs per cluster, threads per CTA (608 for
  * the two-pass sweep: sixteen consumer warps, a copy warp, a decision warp
  * and a completion warp; 256 for the single-read sweep), dynamic shared memory
  * per CTA, the number of persistent clusters launched and the shared-memory
@@ -450,8 +451,9 @@ spec_status_t spec_launch_shape(spec_dtype_t dtype, int units, int V,
 void spec_set_launch_override(int cluster_ctas, int stages);
 
 /* Selects the vocabulary-sweep kernel of later verify, overlap and E2E-TV
- * calls in this process: 0 automatic (the two-pass sweep wherever rows start
- * on 16-byte boundaries and the mode has it, else the single-read sweep),
+ * calls in this process: 0 automatic (the two-pass sweep for calls that read
+ * at least 200 MB of logits, where rows start on 16-byte boundaries and the
+ * mode has it; else the single-read sweep),
  * 1 the single-read sweep (rows resident in cluster shared memory between
  * passes), 2 the two-pass sweep where it applies (pass A from HBM, pass C
  * from L2).  Any other value means 0.  For tests and benchmarks; both give

@@ -395,8 +395,17 @@ void pipe_geometry(ssv::PipeParams* P, const PShape& sh) {
 }
 
 // The two-pass sweep serves rows that start on 16-byte boundaries.
-bool pipe_allowed(const void* a, const void* b, int V, int es) {
-  if (g_kernel_override.load() == 1) return false;
+// The automatic choice takes the two-pass sweep for calls that stream at
+// least this many bytes of logits.  Below it the single-read sweep, whose
+// clusters hold a unit's rows in shared memory for one read, finishes first
+// (measured on GB300: at 175 MB, B=64, K=4, V=151936, single-read 67.5 µs
+// against 78.0; at 248 MB, B=64, K=7, V=129280, two-pass 79.8 against 92.1).
+constexpr double kPipeMinBytes = 200.0e6;
+
+bool pipe_allowed(const void* a, const void* b, int V, int es, long long rows_read) {
+  const int ov = g_kernel_override.load();
+  if (ov == 1) return false;
+  if (ov != 2 && (double)rows_read * (double)V * (double)es < kPipeMinBytes) return false;
   return ((long long)V * es) % 16 == 0 && (reinterpret_cast<uintptr_t>(a) & 15u) == 0 &&
          (b == nullptr || (reinterpret_cast<uintptr_t>(b) & 15u) == 0);
 }
@@ -548,7 +557,9 @@ void spec_set_kernel_override(int kernel) { g_kernel_override.store(kernel == 1 
 spec_status_t spec_launch_shape(spec_dtype_t dtype, int units, int V, int* cluster_ctas, int* threads,
                                 int* smem_bytes, int* clusters, int* stages) {
   if (!dtype_ok(dtype) || units < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
-  if (g_kernel_override.load() != 1 && ((long long)V * elem_size(dtype)) % 16 == 0) {
+  const int ov = g_kernel_override.load();
+  const bool big = (double)units * 2.0 * (double)V * (double)elem_size(dtype) >= kPipeMinBytes;  // ~2 rows per unit
+  if (ov != 1 && (ov == 2 || big) && ((long long)V * elem_size(dtype)) % 16 == 0) {
     PShape ps;
     const spec_status_t r = pipe_shape_dt<ssv::kPSample>(dtype, units, V, 2, &ps);
     if (r == SPEC_ERR_CUDA) return r;
@@ -596,7 +607,8 @@ spec_status_t spec_verify(const void* target_logits, const void* draft_logits, s
   const int es = elem_size(dtype);
   const int rows = (greedy && !alpha_out) ? 1 : 2;  // greedy without overlap reads no draft row
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (pipe_allowed(target_logits, rows == 2 ? draft_logits : nullptr, V, es)) {
+  if (pipe_allowed(target_logits, rows == 2 ? draft_logits : nullptr, V, es,
+                   (long long)B * (K + 1) + (rows == 2 ? (long long)B * K : 0))) {
     PShape ps;
     const spec_status_t r = greedy ? pipe_shape_dt<ssv::kPGreedy>(dtype, units, V, rows, &ps)
                                    : pipe_shape_dt<ssv::kPSample>(dtype, units, V, rows, &ps);
@@ -706,7 +718,7 @@ spec_status_t spec_overlap(const void* target_logits, const void* draft_logits, 
   if (units > 0x7FFFFFFFLL) return SPEC_ERR_UNSUPPORTED;
   const int es = elem_size(dtype);
   const bool greedy = temperature == 0.0f;
-  if (!greedy && pipe_allowed(target_logits, draft_logits, V, es)) {
+  if (!greedy && pipe_allowed(target_logits, draft_logits, V, es, 2 * units)) {
     PShape ps;
     const spec_status_t r = pipe_shape_dt<ssv::kPOverlap>(dtype, units, V, 2, &ps);
     if (r == SPEC_ERR_CUDA) return r;
@@ -789,7 +801,7 @@ spec_status_t spec_e2e_tv_fwd_bwd(const void* target_logits, const void* draft_l
   const bool aligned = aligned16(target_logits) && aligned16(draft_logits) && ((long long)V * es) % 16 == 0;
   cudaError_t e = cudaSuccess;
   bool launched = false;
-  if (pipe_allowed(target_logits, draft_logits, V, es)) {
+  if (pipe_allowed(target_logits, draft_logits, V, es, 2 * units)) {
     PShape ps;
     const spec_status_t r = pipe_shape_dt<ssv::kPE2E>(dtype, units, V, 2, &ps);
     if (r == SPEC_ERR_CUDA) return r;

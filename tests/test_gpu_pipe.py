@@ -86,13 +86,15 @@ def test_two_pass_against_oracle_and_single_read(ssv, B, K, V, dtype, T, S, nst)
     assert int(two.status.item()) == 0
     if K:
         np.testing.assert_allclose(two.alpha.cpu().numpy(), one.alpha.cpu().numpy(), rtol=RTOL, atol=ATOL)
-    # launch shape reported for the forced cluster size
+    # the two-pass launch shape reported for the forced cluster size
     if S:
+        ssv.set_kernel_override(2)
         ssv.set_launch_override(S, nst)
         try:
             assert ssv.launch_shape(dtype, B * (K + 1), V)[0] == S
         finally:
             ssv.set_launch_override(0, 0)
+            ssv.set_kernel_override(0)
 
 
 @pytest.mark.parametrize("S", [1, 2, 5, 16])
