@@ -226,14 +226,23 @@ __global__ void __launch_bounds__(kTThreads, 2) topk_kernel(const __grid_constan
     };
     // appends the elements of mask m (values x, element indices e0 + j * es)
     auto append = [&](uint32_t m, const float (&x)[PV], int e0, int es) {
-      const int c = __popc(m);
-      int incl = c;
+      const unsigned who = __ballot_sync(kFull, m != 0u);
+      int p;
+      if (__popc(who) == 1) {  // the usual case once the bounds are tight: one lane
+        const int l = __ffs(who) - 1;
+        p = n;
+        n += __shfl_sync(kFull, __popc(m), l);
+      } else {
+        const int c = __popc(m);
+        int incl = c;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += t;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(kFull, incl, o);
+          if (lane >= o) incl += t;
+        }
+        p = n + incl - c;
+        n += __shfl_sync(kFull, incl, 31);
       }
-      int p = n + incl - c;
       while (m) {
         const int j = __ffs(m) - 1;
         m &= m - 1u;
@@ -242,7 +251,6 @@ __global__ void __launch_bounds__(kTThreads, 2) topk_kernel(const __grid_constan
         mx = fmaxf(mx, x[j]);
         ++p;
       }
-      n += __shfl_sync(kFull, incl, 31);
       if (n > kKTrig) {
         __syncwarp();
         int need = 0;
@@ -260,32 +268,26 @@ __global__ void __launch_bounds__(kTThreads, 2) topk_kernel(const __grid_constan
       const int nvec = V / PV;
       const int cw = (nvec + kTWarps - 1) / kTWarps;
       const int lo = min(warp * cw, nvec), hi = min(lo + cw, nvec);
-      // every warp runs the first step (kTUnroll vectors per lane), then the
-      // CTA's k-th key over all lists so far becomes a common lower bound
-      for (int base = lo, step = 0; step <= 1 || base < hi; base += 32 * kTUnroll, ++step) {
-        if (step == 1) {
-          __syncwarp();
-          int tot = n;
-          tot = __shfl_sync(kFull, tot, 0);
-          if (lane == 0) sm.cnt[warp] = tot;
-          __syncthreads();
-          int all = 0;
-          for (int w = 0; w < kTWarps; ++w) all += sm.cnt[w];
-          __syncthreads();
-          if (all >= k) {
-            unsigned long long nd = 0;
-            const uint32_t t = cta_list_select<KB>(sm, wkey, n, k, &nd);
-            if (threadIdx.x == 0) atomicMax(&sm.gkey, t);
-            __syncthreads();
-            refresh();
-          }
-          if (base >= hi) break;
-        }
+      for (int base = lo, step = 0; step == 0 || base < hi; base += 32 * kTUnroll, ++step) {
         uint4 raw[kTUnroll];
 #pragma unroll
         for (int u = 0; u < kTUnroll; ++u) {
           const int i = base + u * 32 + lane;
           raw[u] = i < hi ? __ldcg(r4 + i) : make_uint4(kNegInfWord, kNegInfWord, kNegInfWord, kNegInfWord);
+        }
+        if (step == 0) {
+          // a common lower bound before any list: the k-th largest of the
+          // 512 lanes' maxima of their first vectors (distinct elements of
+          // the row, so at least k of the row's elements reach it)
+          float lm = -INFINITY;
+#pragma unroll
+          for (int u = 0; u < kTUnroll; ++u) lm = fmaxf(lm, E::vmax(raw[u]));
+          wkey[lane] = order_key<KB>(lm);
+          unsigned long long nd = 0;
+          const uint32_t t = cta_list_select<KB>(sm, wkey, 32, k, &nd);
+          if (threadIdx.x == 0) sm.gkey = t;
+          __syncthreads();
+          refresh();
         }
 #pragma unroll
         for (int u = 0; u < kTUnroll; ++u) {
