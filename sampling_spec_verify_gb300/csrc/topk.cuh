@@ -342,12 +342,15 @@ __global__ void __launch_bounds__(kTThreads, 2) topk_kernel(const __grid_constan
     bad |= !(M > -INFINITY && M < INFINITY);
 
     // ---- the CTA's k-th key over all lists, and its tie by index ----
-    // With at most k candidates every element above -inf is among the top k
-    // (the rest, -inf, stay -inf whatever the cut): all candidates are kept.
+    // With k candidates or more the k-th is selected (exactly k may pass the
+    // bounds while finite elements below them are dropped).  With fewer,
+    // no bound ever rose above -inf, so every element above -inf is a
+    // candidate and among the top k (the rest, -inf, stay -inf whatever the
+    // cut): all candidates are kept.
     uint32_t thr = 0;
     int tie = V;
     const int nset = total < k ? total : k;  // the top-k set's elements above -inf
-    if (!bad && total > k) {
+    if (!bad && total >= k) {
       unsigned long long need = 0;
       const uint32_t prefix = cta_list_select<KB>(sm, wkey, n, k, &need);
       thr = prefix;
@@ -463,7 +466,7 @@ __global__ void __launch_bounds__(kTThreads, 2) topk_kernel(const __grid_constan
     }
     // a row with NaN or infinite logits (or none finite) is copied unchanged
     if (bad && threadIdx.x == 0 && P.status) atomicOr(P.status, kBadLogits);
-    const bool cut = !bad && (total > k || do_p);
+    const bool cut = !bad && (total >= k || do_p);
     const float thr_f = key_value<KB>(thr);
 
     // ---- pass 2: write ----

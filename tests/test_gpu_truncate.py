@@ -135,6 +135,25 @@ def test_value_histogram_limits(ssv, k, p):
         assert torch.equal(again, out)
 
 
+def test_topk_exactly_k_pass_the_first_bound(ssv):
+    """A row whose k largest logits are each the largest of one lane's first
+    vectors, everything else far below: the candidate path's first bound
+    lets exactly k elements through, and only those may stay."""
+    V, k = 32768, 50                      # 4096 vectors of 8 bf16; 256 per warp
+    g = torch.Generator().manual_seed(31)
+    z = torch.randn(2, V, generator=g)
+    pos = [(w * 256 + lane) * 8 for w in (0, 1) for lane in range(32)][:k]
+    z[0, pos] = 100.0 + torch.arange(k, dtype=torch.float32)
+    z[1, pos] = 100.0                     # the same with all k tied
+    zb = z.to(torch.bfloat16)
+    out = ssv.truncate_logits(zb.to(DEV), 1.0, k, 1.0)
+    torch.cuda.synchronize()
+    kept = torch.isfinite(out.float().cpu())
+    assert kept[0].nonzero().flatten().tolist() == pos
+    assert kept[1].nonzero().flatten().tolist() == pos
+    _check_rows(zb, out, 1.0, k, 1.0)
+
+
 def test_full_size_verify_batch_and_verify_on_truncated(ssv):
     """The verify batch (B=32, K=4, V=151936): truncate target and draft
     identically, draw the drafted tokens from the truncated q, verify, and
