@@ -899,9 +899,10 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
           if (j > NS) epar ^= 1u;
         }
       };
-      // Unit scalars, one phase ahead: loads issued in phase q-1 land in
-      // shared memory at the start of phase q, before the release of that
-      // phase's first full barrier publishes them.
+      // Unit scalars, one phase ahead: loads issued in phase q-1 are stored
+      // in shared memory early in phase q (after the phase's first chunk is
+      // issued, so that no copy waits on a scalar load) and published to the
+      // decision warp through us_done.
       constexpr bool kScal = (kSampleM || kGreedyM);
       int ny = -1;
       float nua = 0.0f, nuf = 0.0f;
@@ -924,6 +925,9 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
       for (int p = 0; p <= nit; ++p) {
         xc = xa;
         if (p < nit) xa = pdecode<MODE>(P, cl + p * G);
+        // the phase's first chunk, then the scalars (whose loads it may wait on)
+        if (p < nit) issue(xa, 0, false);
+        if (kHasC && p >= 1) issue(xc, 0, true);
         if constexpr (kScal) {
           if (p >= 1) {  // gathered logits of unit p-1 (loaded during phase p-1)
             sm.us[(p - 1) % kPUS].zty = E::to_f32(pzt);
@@ -952,7 +956,7 @@ __global__ void __launch_bounds__(kPThreads, 1) pipe_kernel(const PipeParams P) 
             if (p + 1 < nit) load_scalars(p + 1);
           }
         }
-        for (int c = 0; c < NCH; ++c) {
+        for (int c = 1; c < NCH; ++c) {
           if (p < nit) issue(xa, c, false);
           if (kHasC && p >= 1) issue(xc, c, true);
         }
