@@ -199,11 +199,12 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 def kernel_source_hash():
-    """Hash of the sweep kernels' device code (the kernels the ncu traffic
-    records describe); other kernels' sources do not change it."""
+    """Hash of the sweep kernels' device code and of the host code that picks
+    their launch shapes (the kernels the ncu traffic records describe); other
+    kernels' sources do not change it."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "sampling_spec_verify_gb300", "csrc")
-    for name in ("ptx.cuh", "sweep.cuh", "pipe.cuh"):
+    for name in ("ptx.cuh", "sweep.cuh", "pipe.cuh", "spec_api.cu"):
         path = os.path.join(d, name)
         if os.path.exists(path):
             h.update(open(path, "rb").read())
