@@ -165,3 +165,15 @@ def test_two_pass_rejections_everywhere(ssv):
     ref = _oracle(w)
     _check(out, ref)
     assert (ref.n_accepted < K).sum() >= B // 2
+
+
+def test_kernel_choice_by_bytes_read(ssv):
+    """The automatic choice: the two-pass sweep (608 threads) for calls that
+    read at least 200 MB of logits, the single-read sweep (256) below."""
+    assert ssv.launch_shape(torch.bfloat16, 128 * 8, 129280)[1] == 608   # 1024 units x 2 rows: 530 MB
+    assert ssv.launch_shape(torch.bfloat16, 32 * 5, 151936)[1] == 256    # 97 MB
+    ssv.set_kernel_override(2)
+    try:
+        assert ssv.launch_shape(torch.bfloat16, 32 * 5, 151936)[1] == 608
+    finally:
+        ssv.set_kernel_override(0)
