@@ -391,7 +391,16 @@ def test_identical_and_disjoint_logits(ssv):
     np.testing.assert_allclose(out.alpha.cpu().numpy(), 0.0, atol=1e-6)
 
 
-def test_status_bits(ssv):
+@pytest.fixture(params=[1, 2], ids=["single_read", "two_pass"])
+def sweep_kernel(ssv, request):
+    """Runs a test with each sweep forced (the automatic choice takes the
+    single-read sweep at these sizes)."""
+    ssv.set_kernel_override(request.param)
+    yield request.param
+    ssv.set_kernel_override(0)
+
+
+def test_status_bits(ssv, sweep_kernel):
     B, K, V = 3, 2, 1000
     w = synth.gaussian(B, K, V, sigma=1.0, noise=0.5, dtype=torch.float32, temperature=1.0, seed=6)
     t, d, y, ua, uf = to_dev(w)
@@ -413,7 +422,7 @@ def test_status_bits(ssv):
     assert int(out.status.item()) & ssv.DEV_BAD_UNIFORM
 
 
-def test_empty_residual_reported_for_the_emitted_position(ssv):
+def test_empty_residual_reported_for_the_emitted_position(ssv, sweep_kernel):
     """EMPTY_RESIDUAL is raised only by the rejection a row emits (the
     oracle's ``residual_empty``), whatever later positions hold."""
     B, K, V = 2, 3, 1000
