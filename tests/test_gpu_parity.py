@@ -91,16 +91,21 @@ def assert_verify(out, ref, rows=None, check_alpha=True):
 # the seeded small case: 1000 calls of B=1, K=4, V=1024 fp32
 # ---------------------------------------------------------------------------
 
-def test_small_case_1000_seeded_calls(ssv):
+@pytest.mark.parametrize("kernel", [0, 2], ids=["automatic", "two_pass"])
+def test_small_case_1000_seeded_calls(ssv, kernel):
     flagged = 0
     hist = np.zeros(5, dtype=np.int64)
-    for seed in range(1000):
-        w = synth.small(seed=seed)
-        out = ssv.verify(*to_dev(w), w.temperature)
-        ref = oracle_verify(w)
-        flagged += assert_verify(out, ref)
-        assert int(out.status.item()) == 0
-        hist[int(ref.n_accepted[0])] += 1
+    ssv.set_kernel_override(kernel)
+    try:
+        for seed in range(1000):
+            w = synth.small(seed=seed)
+            out = ssv.verify(*to_dev(w), w.temperature)
+            ref = oracle_verify(w)
+            flagged += assert_verify(out, ref)
+            assert int(out.status.item()) == 0
+            hist[int(ref.n_accepted[0])] += 1
+    finally:
+        ssv.set_kernel_override(0)
     print(f"flagged rows: {flagged} / 1000; accepted-count histogram {hist.tolist()}")
     assert flagged < 10
 
