@@ -190,7 +190,6 @@ __global__ void __launch_bounds__(kTThreads, 2) topk_kernel(const __grid_constan
   constexpr int PV = E::PV;
   const int V = P.V;
   const bool al = P.aligned != 0;
-  const int per = al ? PV : 1;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int k = P.top_k;  // 0 < k < V, k <= kKMax
   const bool do_p = P.top_p < 1.0f;
