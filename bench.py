@@ -198,16 +198,42 @@ class ClockSampler:
 # ncu-measured traffic (null once the kernel sources changed)
 # ---------------------------------------------------------------------------
 
+def _code_only(text):
+    """C/C++ source without its comments, trailing blanks and empty lines
+    (string and character literals kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == "/" and i + 1 < n and text[i + 1] == "/":
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif c == "/" and i + 1 < n and text[i + 1] == "*":
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    lines = (ln.rstrip() for ln in "".join(out).splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash():
     """Hash of the sweep kernels' device code and of the host code that picks
-    their launch shapes (the kernels the ncu traffic records describe); other
-    kernels' sources do not change it."""
+    their launch shapes (the kernels the ncu traffic records describe), with
+    comments and blank lines left out; other kernels' sources do not change it."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "sampling_spec_verify_gb300", "csrc")
     for name in ("ptx.cuh", "sweep.cuh", "pipe.cuh", "spec_api.cu"):
         path = os.path.join(d, name)
         if os.path.exists(path):
-            h.update(open(path, "rb").read())
+            h.update(_code_only(open(path, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 
