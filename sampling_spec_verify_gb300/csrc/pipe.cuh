@@ -29,11 +29,13 @@
 // decision warp combines all the cluster's pairs in one fixed order, so every
 // CTA of the cluster takes the same decision with no cluster barrier.
 //
-// Draws: each warp's per-chunk residual totals are summed per (CTA, chunk);
-// the CTA whose completion warp brings a drawing unit's counter to S does the
-// draw: it locates the (CTA, chunk) holding u' * total, recomputes that
-// chunk's weights from global memory in the consumers' order and arithmetic,
-// and walks to the token.
+// Draws: every consumer warp's residual (or target) total of its
+// sub-segment of each chunk goes to the workspace, in (CTA, chunk, warp)
+// order; the CTA whose completion warp brings a drawing unit's counter to S
+// does the draw: it sums those totals, locates the sub-segment holding
+// u' * total, copies that sub-segment into shared memory with one round of
+// loads, recomputes its weights in the consumers' order and arithmetic, and
+// walks to the token.
 #pragma once
 
 #include "sweep.cuh"
